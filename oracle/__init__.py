@@ -1,0 +1,251 @@
+"""CPU oracle for the forward pass of one Mixture-of-Experts layer.
+
+TEST INFRASTRUCTURE ONLY. The test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers. The CUDA library never
+imports, links or runs anything here, and nothing here comes from it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C11, built with gcc); this module
+builds it and marshals numpy arrays through ctypes. bf16 arrays are passed as
+their raw uint16 bit patterns. See ``moe_oracle.h`` for the definition each
+function follows and the page sections it cites.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into a shared library next to this file."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    hdr = os.path.join(_HERE, "moe_oracle.h")
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC), os.path.getmtime(hdr))):
+        return _LIB_PATH
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math"]
+    if platform.machine() in ("x86_64", "AMD64"):
+        cmd.append("-mfma")  # hardware fmaf; fmaf is correctly rounded with or without it
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd += [_SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            sig = {
+                "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
+                "oracle_bf16_to_double": (ctypes.c_double, [ctypes.c_uint16]),
+                "oracle_router_logits": (None, [P, P, P, I64, I, I, P]),
+                "oracle_topk_softmax": (None, [P, I64, I, I, I, P, P]),
+                "oracle_expert_counts": (None, [P, I64, I, I, P]),
+                "oracle_permute": (None, [P, I64, I, I, P, P, P, P]),
+                "oracle_tile_schedule": (I, [P, I, I, P, I]),
+                "oracle_gate_up": (None, [P, P, P, P, P, I, I, I, P]),
+                "oracle_down": (None, [P, P, P, P, P, I, I, I, P]),
+                "oracle_combine": (None, [P, P, I64, I, I, P]),
+                "oracle_combine_bf16": (None, [P, P, I64, I, I, P]),
+                "oracle_forward_tokens": (None, [P, P, P, P, P, P, I64, I, I, I, I, I, P, I64,
+                                                 P, P, P]),
+                "oracle_num_threads": (I, []),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.dtype(dtype):
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def bf16_from_double(v: float) -> int:
+    return int(_load().oracle_bf16_from_double(float(v)))
+
+
+def bf16_to_double(b: int) -> float:
+    return float(_load().oracle_bf16_to_double(int(b)))
+
+
+def router_logits(X: np.ndarray, Wr: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
+    """L[T,E] fp32: fma chain over d ascending, + bias. X uint16 (bf16) [T,d]."""
+    X = _c(X, np.uint16)
+    Wr = _c(Wr, np.float32)
+    T, d = X.shape
+    E = Wr.shape[1]
+    assert Wr.shape[0] == d
+    if bias is not None:
+        bias = _c(bias, np.float32)
+        assert bias.shape == (E,)
+    L = np.empty((T, E), np.float32)
+    _load().oracle_router_logits(_p(X), _p(Wr), _p(bias), T, d, E, _p(L))
+    return L
+
+
+def topk_softmax(L: np.ndarray, K: int, renorm: bool = True):
+    """(idx int32 [T,K], w fp32 [T,K]) from logits L fp32 [T,E]."""
+    L = _c(L, np.float32)
+    T, E = L.shape
+    idx = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float32)
+    _load().oracle_topk_softmax(_p(L), T, E, K, int(bool(renorm)), _p(idx), _p(w))
+    return idx, w
+
+
+def expert_counts(idx: np.ndarray, E: int) -> np.ndarray:
+    idx = _c(idx, np.int32)
+    T, K = idx.shape
+    counts = np.empty(E, np.int32)
+    _load().oracle_expert_counts(_p(idx), T, K, E, _p(counts))
+    return counts
+
+
+def permute(idx: np.ndarray, E: int):
+    """(offsets [E+1], perm_token [R], perm_slot [R], row_of_slot [R]), all int32."""
+    idx = _c(idx, np.int32)
+    T, K = idx.shape
+    R = T * K
+    offsets = np.empty(E + 1, np.int32)
+    perm_token = np.empty(R, np.int32)
+    perm_slot = np.empty(R, np.int32)
+    row_of_slot = np.empty(R, np.int32)
+    _load().oracle_permute(_p(idx), T, E, K, _p(offsets), _p(perm_token), _p(perm_slot),
+                           _p(row_of_slot))
+    return offsets, perm_token, perm_slot, row_of_slot
+
+
+def tile_schedule(offsets: np.ndarray, M: int) -> np.ndarray:
+    """int32 [num_tiles, 4] = {expert, first row, rows, 0}."""
+    offsets = _c(offsets, np.int32)
+    E = offsets.shape[0] - 1
+    max_tiles = int(offsets[E]) // M + E + 1
+    tiles = np.zeros((max_tiles, 4), np.int32)
+    nt = _load().oracle_tile_schedule(_p(offsets), E, M, _p(tiles), max_tiles)
+    return tiles[:nt].copy()
+
+
+def gate_up(X, W1, W3, perm_token, offsets) -> np.ndarray:
+    """H uint16 (bf16) [R,n]."""
+    X = _c(X, np.uint16)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    perm_token = _c(perm_token, np.int32)
+    offsets = _c(offsets, np.int32)
+    E, d, n = W1.shape
+    assert W3.shape == W1.shape and X.shape[1] == d and offsets.shape[0] == E + 1
+    R = int(offsets[E])
+    H = np.empty((R, n), np.uint16)
+    _load().oracle_gate_up(_p(X), _p(W1), _p(W3), _p(perm_token), _p(offsets), E, d, n, _p(H))
+    return H
+
+
+def down(H, W2, topk_w, perm_slot, offsets) -> np.ndarray:
+    """Z float64 [R,d] = w * (H W2[e])."""
+    H = _c(H, np.uint16)
+    W2 = _c(W2, np.uint16)
+    topk_w = _c(topk_w, np.float32)
+    perm_slot = _c(perm_slot, np.int32)
+    offsets = _c(offsets, np.int32)
+    E, n, d = W2.shape
+    R = int(offsets[E])
+    assert H.shape == (R, n)
+    Z = np.empty((R, d), np.float64)
+    _load().oracle_down(_p(H), _p(W2), _p(topk_w), _p(perm_slot), _p(offsets), E, n, d, _p(Z))
+    return Z
+
+
+def combine(Z: np.ndarray, row_of_slot: np.ndarray, K: int) -> np.ndarray:
+    Z = _c(Z, np.float64)
+    row_of_slot = _c(row_of_slot, np.int32)
+    R, d = Z.shape
+    T = row_of_slot.shape[0] // K
+    Y = np.empty((T, d), np.uint16)
+    _load().oracle_combine(_p(Z), _p(row_of_slot), T, K, d, _p(Y))
+    return Y
+
+
+def combine_bf16(Z: np.ndarray, row_of_slot: np.ndarray, K: int) -> np.ndarray:
+    Z = _c(Z, np.uint16)
+    row_of_slot = _c(row_of_slot, np.int32)
+    R, d = Z.shape
+    T = row_of_slot.shape[0] // K
+    Y = np.empty((T, d), np.uint16)
+    _load().oracle_combine_bf16(_p(Z), _p(row_of_slot), T, K, d, _p(Y))
+    return Y
+
+
+def forward(X, Wr, bias, W1, W3, W2, K: int, renorm: bool = True, M: int = 128) -> dict:
+    """The whole layer through the grouped steps; returns every intermediate."""
+    E = Wr.shape[1]
+    L = router_logits(X, Wr, bias)
+    idx, w = topk_softmax(L, K, renorm)
+    counts = expert_counts(idx, E)
+    offsets, perm_token, perm_slot, row_of_slot = permute(idx, E)
+    tiles = tile_schedule(offsets, M)
+    H = gate_up(X, W1, W3, perm_token, offsets)
+    Z = down(H, W2, w, perm_slot, offsets)
+    Y = combine(Z, row_of_slot, K)
+    return dict(logits=L, idx=idx, w=w, counts=counts, offsets=offsets, perm_token=perm_token,
+                perm_slot=perm_slot, row_of_slot=row_of_slot, tiles=tiles, H=H, Z=Z, Y=Y)
+
+
+def forward_tokens(X, Wr, bias, W1, W3, W2, K: int, tokens, renorm: bool = True):
+    """(Y rows [n,d] uint16, idx rows [n,K], w rows [n,K]) for the listed tokens,
+    computed token by token from the definition."""
+    X = _c(X, np.uint16)
+    Wr = _c(Wr, np.float32)
+    if bias is not None:
+        bias = _c(bias, np.float32)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    W2 = _c(W2, np.uint16)
+    tokens = _c(np.asarray(tokens, np.int64), np.int64)
+    T, d = X.shape
+    E, _, n = W1.shape
+    nt = tokens.shape[0]
+    assert tokens.min(initial=0) >= 0 and tokens.max(initial=0) < T
+    Y = np.empty((nt, d), np.uint16)
+    idx = np.empty((nt, K), np.int32)
+    w = np.empty((nt, K), np.float32)
+    _load().oracle_forward_tokens(_p(X), _p(Wr), _p(bias), _p(W1), _p(W3), _p(W2), T, d, E, K, n,
+                                  int(bool(renorm)), _p(tokens), nt, _p(Y), _p(idx), _p(w))
+    return Y, idx, w
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact float64 values of an array of bf16 bit patterns."""
+    a = np.ascontiguousarray(a, np.uint16)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -1,0 +1,323 @@
+/*
+ * CPU oracle for the forward pass of one Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the CUDA library. It is deliberately
+ * slow and plain: each function is the definition written out, in the order the
+ * pages state it, with no blocking, fusion or reordering. The sources and the
+ * readings taken where the pages are silent are listed in moe_oracle.h.
+ *
+ * Build: plain C11, -ffp-contract=off (no implicit fused multiply-adds; the one
+ * fma that belongs to the definition is written as fmaf), no fast-math. OpenMP
+ * splits independent tokens or rows across threads; no result depends on the
+ * thread count.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+double oracle_bf16_to_double(uint16_t b) {
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static float bf16_to_float(uint16_t b) {
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* Nearest bf16 (8 significant bits, fp32 exponent range), ties to even, by
+ * scaling the magnitude so that one bf16 ulp becomes 1, rounding to an integer
+ * with nearbyint (round-half-even in the default rounding mode) and scaling
+ * back. Both scalings are by powers of two and therefore exact. */
+uint16_t oracle_bf16_from_double(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int ex;
+    frexp(a, &ex);             /* a in [2^(ex-1), 2^ex) */
+    int e_ulp = ex - 8;        /* ulp of an 8-significant-bit number there */
+    if (e_ulp < -133) e_ulp = -133; /* subnormal range: fixed ulp 2^-133 */
+    double r = nearbyint(ldexp(a, -e_ulp));
+    double res = ldexp(r, e_ulp);
+    if (res >= 0x1p128) return sign | 0x7F80; /* rounds past the largest bf16 */
+    float f = (float)res;      /* exact: res has at most 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return sign | (uint16_t)(bits >> 16);
+}
+
+/* ------------------------------------------------------------- router -- */
+
+/* Logits of one token row: for each expert e, acc = +0.0f, then for
+ * j = 0..d-1 in order acc = fmaf(x_j, Wr[j,e], acc); then acc + bias[e]. */
+static void logits_row(const uint16_t *x, const float *Wr, const float *bias,
+                       int d, int E, float *acc) {
+    for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+    for (int j = 0; j < d; ++j) {
+        float xj = bf16_to_float(x[j]);
+        const float *w = Wr + (int64_t)j * E;
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(xj, w[e], acc[e]);
+    }
+    if (bias)
+        for (int e = 0; e < E; ++e) acc[e] = acc[e] + bias[e];
+}
+
+void oracle_router_logits(const uint16_t *X, const float *Wr, const float *bias,
+                          int64_t T, int d, int E, float *L) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        logits_row(X + t * d, Wr, bias, d, E, L + t * E);
+}
+
+typedef struct {
+    float v;
+    int e;
+} scored;
+
+/* Higher score first; equal scores: lower expert index first. */
+static int by_score_then_index(const void *pa, const void *pb) {
+    const scored *a = (const scored *)pa, *b = (const scored *)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->e > b->e) - (a->e < b->e);
+}
+
+/* One row: sort all E experts by (score desc, index asc), keep the first K.
+ * p = softmax(L) in double with the maximum subtracted; w_k = p_k, divided by
+ * the sum of the kept p when renormalising. */
+static void route_row(const float *L, int E, int K, int renorm, int32_t *idx, float *w) {
+    scored *s = (scored *)malloc(sizeof(scored) * (size_t)E);
+    for (int e = 0; e < E; ++e) {
+        s[e].v = L[e];
+        s[e].e = e;
+    }
+    qsort(s, (size_t)E, sizeof(scored), by_score_then_index);
+    double m = (double)s[0].v;
+    double denom = 0.0;
+    for (int e = 0; e < E; ++e) denom += exp((double)L[e] - m);
+    double kept = 0.0;
+    for (int k = 0; k < K; ++k) kept += exp((double)s[k].v - m) / denom;
+    for (int k = 0; k < K; ++k) {
+        double p = exp((double)s[k].v - m) / denom;
+        idx[k] = s[k].e;
+        w[k] = (float)(renorm ? p / kept : p);
+    }
+    free(s);
+}
+
+void oracle_topk_softmax(const float *L, int64_t T, int E, int K, int renorm,
+                         int32_t *idx, float *w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        route_row(L + t * E, E, K, renorm, idx + t * K, w + t * K);
+}
+
+/* ------------------------------------------------- counts / permutation -- */
+
+void oracle_expert_counts(const int32_t *idx, int64_t T, int K, int E, int32_t *counts) {
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) counts[idx[t * K + k]] += 1;
+}
+
+void oracle_permute(const int32_t *idx, int64_t T, int E, int K,
+                    int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                    int32_t *row_of_slot) {
+    int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    oracle_expert_counts(idx, T, K, E, counts);
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    /* stable counting sort of the slots (t,k) by expert: visiting slots in
+     * ascending t puts each expert's rows in ascending token order */
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    for (int e = 0; e < E; ++e) cursor[e] = offsets[e];
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int32_t slot = (int32_t)(t * K + k);
+            int32_t p = cursor[idx[slot]]++;
+            perm_token[p] = (int32_t)t;
+            perm_slot[p] = slot;
+            row_of_slot[slot] = p;
+        }
+    free(cursor);
+    free(counts);
+}
+
+int oracle_tile_schedule(const int32_t *offsets, int E, int M, int32_t *tiles, int max_tiles) {
+    int nt = 0;
+    for (int e = 0; e < E; ++e) {
+        int32_t c = offsets[e + 1] - offsets[e];
+        for (int32_t r = 0; r < c; r += M) {
+            if (nt < max_tiles) {
+                tiles[4 * nt + 0] = e;
+                tiles[4 * nt + 1] = offsets[e] + r;
+                tiles[4 * nt + 2] = (c - r < M) ? (c - r) : M;
+                tiles[4 * nt + 3] = 0;
+            }
+            ++nt;
+        }
+    }
+    return nt;
+}
+
+/* ---------------------------------------------------------- expert MLP -- */
+
+static double silu(double a) { return a / (1.0 + exp(-a)); }
+
+/* h = bf16( SiLU(x W1e) * (x W3e) ), sums over i = 0..d-1 ascending in double.
+ * a1, a3: caller scratch of n doubles. */
+static void gate_up_row(const uint16_t *x, const uint16_t *W1e, const uint16_t *W3e,
+                        int d, int n, double *a1, double *a3, uint16_t *h) {
+    for (int j = 0; j < n; ++j) a1[j] = a3[j] = 0.0;
+    for (int i = 0; i < d; ++i) {
+        double xi = oracle_bf16_to_double(x[i]);
+        const uint16_t *w1 = W1e + (int64_t)i * n;
+        const uint16_t *w3 = W3e + (int64_t)i * n;
+        for (int j = 0; j < n; ++j) {
+            a1[j] = a1[j] + xi * oracle_bf16_to_double(w1[j]);
+            a3[j] = a3[j] + xi * oracle_bf16_to_double(w3[j]);
+        }
+    }
+    for (int j = 0; j < n; ++j) h[j] = oracle_bf16_from_double(silu(a1[j]) * a3[j]);
+}
+
+/* z = w * (h W2e), sums over j = 0..n-1 ascending in double. */
+static void down_row(const uint16_t *h, const uint16_t *W2e, double w, int n, int d,
+                     double *z) {
+    for (int c = 0; c < d; ++c) z[c] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double hj = oracle_bf16_to_double(h[j]);
+        const uint16_t *w2 = W2e + (int64_t)j * d;
+        for (int c = 0; c < d; ++c) z[c] = z[c] + hj * oracle_bf16_to_double(w2[c]);
+    }
+    for (int c = 0; c < d; ++c) z[c] = w * z[c];
+}
+
+/* expert owning grouped row p, from the offsets */
+static int expert_of_row(const int32_t *offsets, int E, int32_t p) {
+    int e = 0;
+    while (e + 1 < E && offsets[e + 1] <= p) ++e;
+    return e;
+}
+
+void oracle_gate_up(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                    const int32_t *perm_token, const int32_t *offsets,
+                    int E, int d, int n, uint16_t *H) {
+    int32_t R = offsets[E];
+#pragma omp parallel
+    {
+        double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
+        double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t p = 0; p < R; ++p) {
+            int e = expert_of_row(offsets, E, p);
+            const uint16_t *x = X + (int64_t)perm_token[p] * d;
+            gate_up_row(x, W1 + (int64_t)e * d * n, W3 + (int64_t)e * d * n, d, n, a1, a3,
+                        H + (int64_t)p * n);
+        }
+        free(a1);
+        free(a3);
+    }
+}
+
+void oracle_down(const uint16_t *H, const uint16_t *W2, const float *topk_w,
+                 const int32_t *perm_slot, const int32_t *offsets,
+                 int E, int n, int d, double *Z) {
+    int32_t R = offsets[E];
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t p = 0; p < R; ++p) {
+        int e = expert_of_row(offsets, E, p);
+        down_row(H + (int64_t)p * n, W2 + (int64_t)e * n * d, (double)topk_w[perm_slot[p]],
+                 n, d, Z + (int64_t)p * d);
+    }
+}
+
+/* ------------------------------------------------------------- combine -- */
+
+void oracle_combine(const double *Z, const int32_t *row_of_slot, int64_t T, int K,
+                    int d, uint16_t *Y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int c = 0; c < d; ++c) {
+            double y = 0.0;
+            for (int k = 0; k < K; ++k) y = y + Z[(int64_t)row_of_slot[t * K + k] * d + c];
+            Y[t * d + c] = oracle_bf16_from_double(y);
+        }
+}
+
+void oracle_combine_bf16(const uint16_t *Z, const int32_t *row_of_slot, int64_t T,
+                         int K, int d, uint16_t *Y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int c = 0; c < d; ++c) {
+            double y = 0.0;
+            for (int k = 0; k < K; ++k)
+                y = y + oracle_bf16_to_double(Z[(int64_t)row_of_slot[t * K + k] * d + c]);
+            Y[t * d + c] = oracle_bf16_from_double(y);
+        }
+}
+
+/* ------------------------------------------------------ whole layer -- */
+
+void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias,
+                           const uint16_t *W1, const uint16_t *W3, const uint16_t *W2,
+                           int64_t T, int d, int E, int K, int n, int renorm,
+                           const int64_t *tokens, int64_t n_tok,
+                           uint16_t *Y_rows, int32_t *idx_rows, float *w_rows) {
+    (void)T;
+#pragma omp parallel
+    {
+        float *L = (float *)malloc(sizeof(float) * (size_t)E);
+        double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
+        double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
+        uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n);
+        double *z = (double *)malloc(sizeof(double) * (size_t)d);
+        double *y = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_tok; ++i) {
+            int64_t t = tokens[i];
+            const uint16_t *x = X + t * d;
+            int32_t *idx = idx_rows + i * K;
+            float *w = w_rows + i * K;
+            logits_row(x, Wr, bias, d, E, L);
+            route_row(L, E, K, renorm, idx, w);
+            for (int c = 0; c < d; ++c) y[c] = 0.0;
+            for (int k = 0; k < K; ++k) {
+                int e = idx[k];
+                gate_up_row(x, W1 + (int64_t)e * d * n, W3 + (int64_t)e * d * n, d, n, a1, a3, h);
+                down_row(h, W2 + (int64_t)e * n * d, (double)w[k], n, d, z);
+                for (int c = 0; c < d; ++c) y[c] = y[c] + z[c];
+            }
+            for (int c = 0; c < d; ++c) Y_rows[i * d + c] = oracle_bf16_from_double(y[c]);
+        }
+        free(L);
+        free(a1);
+        free(a3);
+        free(h);
+        free(z);
+        free(y);
+    }
+}

@@ -1,0 +1,112 @@
+/*
+ * CPU oracle for the forward pass of one Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. This is the slow, plain reference the CUDA library
+ * is checked against. Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg load it. It shares no code, header, table or helper with the
+ * CUDA library, and the CUDA library never calls it.
+ *
+ * bf16 values travel as their raw 16-bit patterns (uint16_t). Every array is
+ * dense row-major; sizes are in elements.
+ *
+ * Sources (page title, section):
+ *   "混合专家模型(MoE)架构优化与SonicMoE实践" (SonicMoE page)
+ *       §1    X in R^{T x d}; the router scores E experts per token and keeps the
+ *             best K; then Gather, a two-layer expert MLP (GEMM), and Scatter back
+ *             to the tokens' positions; H = SiLU(W1 X) held at 2 bytes/element.
+ *       §2.2  SwiGLU fused into the GEMM epilogue; intermediates grouped by expert.
+ *       §3.1  expert_frequency_estimation: per-expert counts as a loop over t, k.
+ *       §3.2  the kept routing scores are renormalised (softmax renormalisation).
+ *   "Triton优化MoE模型：topk_gating算子融合实战" (top-k gating page)
+ *       §2.1  flow: logits -> softmax -> top-k -> output.
+ *       §2.2  max-subtracted softmax over a token's expert scores, then top-2.
+ *       §4.1  subtract the maximum before exp for numerical stability.
+ *   "稀疏矩阵乘法（SpMM）在MoE中的应用：利用Triton内核加速稀疏专家的计算" (SpMM page)
+ *       §2    CSR row offsets (an exclusive prefix sum of per-row counts).
+ *       §6    the outputs of the selected experts are combined with their weights.
+ *
+ * Readings where the pages are silent (each is stated where it is used):
+ *   - router logits are fp32, one fused multiply-add chain per (token, expert)
+ *     over j = 0..d-1 ascending, starting from +0.0f, then + bias[e] as a single
+ *     fp32 add;
+ *   - top-K is chosen on the logits (softmax is strictly increasing, so the same
+ *     set), ties go to the lower expert index, output in descending order;
+ *   - probabilities and weights are computed in double, rounded once to fp32;
+ *   - the gated branch is W1 (SiLU), the linear branch W3, no biases;
+ *   - H is rounded to bf16 (2 bytes/element); Z and Y sums stay in double until
+ *     the single final bf16 rounding of Y;
+ *   - rows of one expert are ordered by ascending token index.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Round a double to the nearest bf16 (ties to even) and return its bits. */
+uint16_t oracle_bf16_from_double(double v);
+/* Exact value of a bf16 bit pattern. */
+double oracle_bf16_to_double(uint16_t b);
+
+/* L[t,e] = fp32 fma chain over j ascending of X[t,j]*Wr[j,e], + bias[e]. */
+void oracle_router_logits(const uint16_t *X, const float *Wr, const float *bias,
+                          int64_t T, int d, int E, float *L);
+
+/* Top-K of each logit row (ties: lower index first), softmax in double, weights
+ * renormalised over the K kept experts when renorm != 0. idx/w are [T,K]. */
+void oracle_topk_softmax(const float *L, int64_t T, int E, int K, int renorm,
+                         int32_t *idx, float *w);
+
+/* counts[e] = number of (t,k) with idx[t,k] == e (plain double loop). */
+void oracle_expert_counts(const int32_t *idx, int64_t T, int K, int E, int32_t *counts);
+
+/* offsets[E+1] (exclusive prefix sum of counts); rows of expert e occupy
+ * offsets[e]..offsets[e+1]-1 in ascending token order. perm_token[p] = t,
+ * perm_slot[p] = t*K+k, row_of_slot[t*K+k] = p. */
+void oracle_permute(const int32_t *idx, int64_t T, int E, int K,
+                    int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                    int32_t *row_of_slot);
+
+/* Fixed-size row blocks per expert: for every expert with rows, ceil(count/M)
+ * blocks {expert, first row, rows (<= M), 0} in expert order. Writes at most
+ * max_tiles entries of tiles[.][4] and returns the number of blocks. */
+int oracle_tile_schedule(const int32_t *offsets, int E, int M, int32_t *tiles, int max_tiles);
+
+/* H[p,:] = bf16( SiLU(x W1[e]) * (x W3[e]) ), x = X[perm_token[p]], for the rows
+ * p of each expert e; sums in double over d ascending. W1/W3 are [E,d,n]. */
+void oracle_gate_up(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                    const int32_t *perm_token, const int32_t *offsets,
+                    int E, int d, int n, uint16_t *H);
+
+/* Z[p,:] = w[perm_slot[p]] * (H[p,:] W2[e]) in double; W2 is [E,n,d]. */
+void oracle_down(const uint16_t *H, const uint16_t *W2, const float *topk_w,
+                 const int32_t *perm_slot, const int32_t *offsets,
+                 int E, int n, int d, double *Z);
+
+/* Y[t,:] = bf16( sum over k ascending of Z[row_of_slot[t*K+k],:] ), double sum. */
+void oracle_combine(const double *Z, const int32_t *row_of_slot, int64_t T, int K,
+                    int d, uint16_t *Y);
+/* Same with bf16 Z rows (used to check the combine step on its own). */
+void oracle_combine_bf16(const uint16_t *Z, const int32_t *row_of_slot, int64_t T,
+                         int K, int d, uint16_t *Y);
+
+/* The layer for a list of tokens, straight from the definition, token by token:
+ * route the token, run each selected expert's SwiGLU MLP on it, weight and sum.
+ * Outputs per listed token: Y rows [n_tok,d], idx/w rows [n_tok,K]. */
+void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias,
+                           const uint16_t *W1, const uint16_t *W3, const uint16_t *W2,
+                           int64_t T, int d, int E, int K, int n, int renorm,
+                           const int64_t *tokens, int64_t n_tok,
+                           uint16_t *Y_rows, int32_t *idx_rows, float *w_rows);
+
+/* Threads the OpenMP loops use (1 when built without OpenMP). */
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ORACLE_H */

@@ -1,0 +1,54 @@
+"""Planted mistakes in a copy of the oracle must each fail a pin (CPU only).
+
+Every mutation below is a plausible slip in the oracle's C source: a reordered or
+unfused logit chain, the wrong tie-break, a dropped renormalisation, a sign error
+in SiLU, swapped gate/up branches, a dropped routing weight, truncating instead
+of rounding, a transposed weight, an unstable grouping. The test copies the
+oracle into a temporary directory, applies one mutation, rebuilds it there and
+runs the pin suite against the copy; the suite has to fail.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = [
+    ("unfused_logits", "acc[e] = fmaf(xj, w[e], acc[e]);", "acc[e] = acc[e] + xj * w[e];"),
+    ("descending_j", "for (int j = 0; j < d; ++j) {\n        float xj",
+     "for (int j = d - 1; j >= 0; --j) {\n        float xj"),
+    ("ties_to_high_index", "return (a->e > b->e) - (a->e < b->e);",
+     "return (a->e < b->e) - (a->e > b->e);"),
+    ("no_renorm", "renorm ? p / kept : p", "p"),
+    ("silu_sign", "a / (1.0 + exp(-a))", "a / (1.0 + exp(a))"),
+    ("gate_up_swapped", "silu(a1[j]) * a3[j]", "silu(a3[j]) * a1[j]"),
+    ("combine_drops_k0", "for (int k = 0; k < K; ++k) y = y + Z[", "for (int k = 1; k < K; ++k) y = y + Z["),
+    ("weight_dropped", "z[c] = w * z[c];", "z[c] = z[c];"),
+    ("bf16_truncates", "nearbyint(ldexp(a, -e_ulp))", "floor(ldexp(a, -e_ulp))"),
+    ("bias_sign", "acc[e] = acc[e] + bias[e];", "acc[e] = acc[e] - bias[e];"),
+    ("tile_rows_unclipped", "(c - r < M) ? (c - r) : M", "M"),
+    ("denominator_short", "for (int e = 0; e < E; ++e) denom +=", "for (int e = 0; e < E - 1; ++e) denom +="),
+    ("w2_transposed", "const uint16_t *w2 = W2e + (int64_t)j * d;", "const uint16_t *w2 = W2e + (int64_t)j;"),
+    ("grouping_reversed", "for (int64_t t = 0; t < T; ++t)\n        for (int k = 0; k < K; ++k) {\n            int32_t slot",
+     "for (int64_t t = T - 1; t >= 0; --t)\n        for (int k = 0; k < K; ++k) {\n            int32_t slot"),
+    ("gather_ignores_perm", "const uint16_t *x = X + (int64_t)perm_token[p] * d;",
+     "const uint16_t *x = X + (int64_t)p * d;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_fails_a_pin(tmp_path, name, old, new):
+    src = open(os.path.join(ROOT, "oracle", "moe_oracle.c")).read()
+    assert src.count(old) >= 1, "mutation site not found: " + name
+    dst = tmp_path / "oracle"
+    shutil.copytree(os.path.join(ROOT, "oracle"), dst,
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    (dst / "moe_oracle.c").write_text(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=f"{tmp_path}{os.pathsep}{ROOT}")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, capture_output=True, text=True, cwd=str(tmp_path), timeout=600)
+    assert r.returncode != 0, f"mutation {name} passed every pin:\n{r.stdout[-2000:]}"
