@@ -1,0 +1,379 @@
+"""Benchmark of the MoE-layer forward (moe_forward) on GB300.
+
+One step = one full forward of the layer over one batch of synthetic tokens:
+router -> grouping -> row gather -> gate/up GEMM + SwiGLU -> down GEMM + routing
+weight -> combine, i.e. every kernel moe_forward launches. Default workload: the
+Mixtral-shaped layer (T=4096, d=4096, E=8, K=2, n=14336, bf16, fp32 accumulate).
+
+Prints ONE JSON line on rank 0:
+  value       useful TFLOP/s (2*T*K*3*d*n per step) of all ranks together, device
+              timed with CUDA events, inputs resident in HBM
+  e2e         same metric through moe_forward_host: pinned host X -> device, layer,
+              Y -> pinned host, every step
+  roofline    the dominant kernel (gate/up GEMM) against the measured bf16 peak
+  cpu_baseline  the CPU oracle on a bounded token sample (rank 0, N=1 only)
+  clocks      nvidia-smi SM clocks / throttle reasons sampled during the timed region
+  extra       tokens/s, per-kernel times, router and combine GB/s, % of peak
+
+--impl reference times the CPU oracle (the only reference this layer has) on the
+same workload and metric. Under torchrun every rank runs its own replica (tokens
+are independent: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+STAGES = ["route", "permute", "gather", "gemm_gate_up", "gemm_down", "combine"]
+KERNELS_PER_STAGE = {"route": 1, "permute": 3, "gather": 1, "gemm_gate_up": 1, "gemm_down": 1,
+                     "combine": 1}
+KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
+METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
+# ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
+# the Mixtral-shaped workload (profiles/gemm_gate_up_mixtral.md); None until taken
+# for the kernel as it stands.
+GEMM1_TRAFFIC_BYTES = None
+
+
+def workload_desc(name, c):
+    return (f"{name}-shaped MoE layer forward T={c['T']} d={c['d']} E={c['E']} K={c['K']} "
+            f"n={c['n']}" + (" zipf-bias" if c.get("zipf") else ""))
+
+
+def useful_flops(c, tokens=None):
+    T = c["T"] if tokens is None else tokens
+    return 2.0 * T * c["K"] * 3 * c["d"] * c["n"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"],
+                    bf16_sustained=j.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.25)
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        mhz = sorted(r[0] for r in rows)
+        loaded = [r for r in rows if r[2] > 250.0] or rows
+        lm = sorted(r[0] for r in loaded)
+        return {"sm_mhz": lm[len(lm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "sm_mhz_min": mhz[0],
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(value_per_rank_units: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: units every rank processed / slowest rank's time."""
+    return value_per_rank_units * world / seconds_max
+
+
+def oracle_sample_tflops(inp_np, c, tokens):
+    """Time the CPU oracle (token-by-token definition) on `tokens`; TFLOP/s."""
+    import oracle
+    X, Wr, bias, W1, W3, W2 = inp_np
+    t0 = time.perf_counter()
+    oracle.forward_tokens(X, Wr, bias, W1, W3, W2, c["K"], tokens)
+    dt = time.perf_counter() - t0
+    return useful_flops(c, len(tokens)) / dt / 1e12, dt
+
+
+def host_inputs(inp):
+    from top_routing_grouped_02_gb300 import synth
+    bias = inp["bias"]
+    return (synth.bf16_bits(inp["X"]), inp["Wr"].cpu().numpy(),
+            None if bias is None else bias.cpu().numpy(), synth.bf16_bits(inp["W1"]),
+            synth.bf16_bits(inp["W3"]), synth.bf16_bits(inp["W2"]))
+
+
+def calibrate_sample(inp_np, c, seconds: float, rng_seed=0):
+    """Token count whose oracle run takes about `seconds`, and its TFLOP/s."""
+    import numpy as np
+    rng = np.random.default_rng(rng_seed)
+    n = 4
+    while True:
+        toks = np.sort(rng.choice(c["T"], size=min(n, c["T"]), replace=False))
+        tf, dt = oracle_sample_tflops(inp_np, c, toks)
+        if dt >= seconds * 0.5 or n >= c["T"]:
+            return n, tf, dt
+        n = min(c["T"], max(n * 2, int(n * seconds / max(dt, 1e-3))))
+
+
+def run_reference(args, c, world, rank):
+    """The reference arm: the CPU oracle as it stands, on rank 0 only."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from top_routing_grouped_02_gb300 import synth
+    oracle.build()
+    inp = synth.layer_inputs(device="cuda" if _has_cuda() else "cpu", **c)
+    inp_np = host_inputs(inp)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n, _, _ = calibrate_sample(inp_np, c, budget)
+    rng = np.random.default_rng(1)
+    for _ in range(args.warmup):
+        toks = np.sort(rng.choice(c["T"], size=n, replace=False))
+        oracle_sample_tflops(inp_np, c, toks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        toks = np.sort(rng.choice(c["T"], size=n, replace=False))
+        oracle.forward_tokens(*inp_np, c["K"], toks)
+    dt = time.perf_counter() - t0
+    value = useful_flops(c, n) * args.steps / dt / 1e12
+    sample = f"{n} of {c['T']} tokens per step (token-by-token oracle, routing included)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, c), **{k: c[k] for k in "TdEKn"}},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _has_cuda():
+    import torch
+    return torch.cuda.is_available()
+
+
+def run_gpu(args, c, world, rank, local):
+    import numpy as np
+    import torch
+    from top_routing_grouped_02_gb300 import moe, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T, d, E, K, n = c["T"], c["d"], c["E"], c["K"], c["n"]
+    inp = synth.layer_inputs(device=dev, seed=args.seed + rank, **c)
+    ws = moe.workspace(T, d, E, K, n, dev)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"],
+                        ws=ws, Y=Y, stream=stream, events=events)
+
+    for _ in range(args.warmup):
+        step()
+    st, word = moe.moe_sync_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} during warm-up")
+
+    # timed region: K steps, events between the stages of every step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    st, word = moe.moe_sync_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} in the timed region")
+    ms_total = start.elapsed_time(stop)
+    ms_max = max_over_ranks(ms_total, world)
+    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
+                                  for i in range(args.steps)])) for j, s in enumerate(STAGES)}
+    ms_step = ms_max / args.steps
+    flops = useful_flops(c)
+    value = aggregate(flops * args.steps, ms_max / 1e3, world) / 1e12
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    Xh = inp["X"].cpu().pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    Xd = torch.empty_like(inp["X"])
+    Yd = torch.empty_like(inp["X"])
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        moe.moe_forward_host(Xh, Yh, Xd, Yd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
+                             inp["bias"], ws=ws, stream=stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        moe.moe_forward_host(Xh, Yh, Xd, Yd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
+                             inp["bias"], ws=ws, stream=stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+    e2e_value = aggregate(flops * e2e_steps, e2e_s, world) / 1e12
+
+    peaks = load_peaks()
+    R = T * K
+    g1_flops = 4.0 * R * d * n
+    g1_tflops = g1_flops / (stage_ms["gemm_gate_up"] / 1e3) / 1e12
+    g2_tflops = 2.0 * R * n * d / (stage_ms["gemm_down"] / 1e3) / 1e12
+    router_bytes = T * d * 2 + d * E * 4 + R * 8 + E * 4
+    combine_bytes = (R + T) * d * 2
+    gather_bytes = 2 * R * d * 2
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, c), **{k: c[k] for k in "TdEKn"},
+                   "seed": args.seed, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "inputs larger than L2: expert weights "
+                         f"{3 * E * d * n * 2 / 1e9:.2f} GB per step, no flush"},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+        "roofline": {"kernel": "gemm_gate_up (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
+                     "achieved": round(g1_tflops, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": round(g1_tflops / peaks["bf16"], 4),
+                     "traffic": GEMM1_TRAFFIC_BYTES,
+                     "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                     "algorithmic_flops_per_launch": g1_flops},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "extra": {
+            "tokens_per_s": round(T * world / (ms_step / 1e3), 1),
+            "pct_bf16_peak_layer": round(value / world / peaks["bf16"] * 100, 2),
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "gemm_down_tflops": round(g2_tflops, 2),
+            "router_GBps": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9, 1),
+            "router_frac_hbm": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9 / peaks["hbm"], 4),
+            "combine_GBps": round(combine_bytes / (stage_ms["combine"] / 1e3) / 1e9, 1),
+            "gather_GBps": round(gather_bytes / (stage_ms["gather"] / 1e3) / 1e9, 1),
+            "hbm_peak_GBps": peaks["hbm"], "clock_samples": clocks.get("samples"),
+            "power_w_max": clocks.get("power_w_max"),
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        inp_np = host_inputs(inp)
+        ntok, tf, dt = calibrate_sample(inp_np, c, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{ntok} of {T} tokens, token-by-token oracle "
+                                          f"(routing included), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral", choices=["tiny", "mixtral", "dsv3", "sonic"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from top_routing_grouped_02_gb300 import synth
+    c = dict(synth.WORKLOADS[args.workload])
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, c, world, rank)
+    else:
+        run_gpu(args, c, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * moe.h - C ABI of libmoe.so: the forward pass of one Mixture-of-Experts layer
+ * on an NVIDIA GB300 (sm_103a).
+ *
+ * The layer (page "混合专家模型(MoE)架构优化与SonicMoE实践", §1): tokens
+ * X[T,d] are scored against E experts by a router, each token keeps its best K
+ * experts, rows are gathered per expert, each expert applies a two-layer SwiGLU
+ * MLP (W1/W3 [E,d,n] up, W2 [E,n,d] down), and the weighted expert outputs are
+ * scattered back and summed per token:
+ *
+ *   L[t,:]  = X[t,:] Wr (+ bias)                       router logits, fp32
+ *   idx, w  = top-K of softmax(L[t,:]), renormalised  (ties -> lower index)
+ *   H[p,:]  = SiLU(x W1[e]) * (x W3[e])                x = X[t_p], bf16 out
+ *   Z[p,:]  = w_p * (H[p,:] W2[e])                     bf16 out
+ *   Y[t,:]  = sum_k Z[row_of_slot[t*K+k],:]            ascending k, fp32 sum, bf16 out
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless a parameter says "host". The caller
+ *     owns every buffer, including the workspace; the library allocates no
+ *     device memory and keeps no state besides a per-device cache of the SM
+ *     count and architecture check.
+ *   - bf16 data travels as raw 16-bit patterns (moe_bf16). Matrices are dense
+ *     and row-major. Integer outputs are int32.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work on it and return; none waits for the GPU (except
+ *     moe_sync_check and moe_forward_host, which say so).
+ *   - Argument and shape errors are reported synchronously, before anything is
+ *     enqueued. A failed launch returns MOE_ERR_CUDA. Problems the kernels
+ *     detect on the device (an expert index out of range, a stalled pipeline
+ *     that gave up after its time limit) set bits in the workspace's error word,
+ *     which moe_sync_check reads.
+ *   - Supported shapes: 1 <= T, 1 <= E <= 256, 1 <= K <= min(E, 8);
+ *     d % 256 == 0 and n % 128 == 0 for the expert GEMMs (d % 8 == 0 for the
+ *     router and combine alone); T*K*max(d,n) < 2^31. Anything else returns
+ *     MOE_ERR_UNSUPPORTED_SHAPE.
+ *   - The kernels are built for sm_103a only; any other device returns MOE_ERR_ARCH.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad flag */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set above */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes < moe_workspace_bytes(...) */
+    MOE_ERR_ARCH = 4,               /* current device is not sm_103 */
+    MOE_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+    MOE_ERR_DEVICE_TIMEOUT = 6,     /* a kernel wait hit its time limit (error word) */
+    MOE_ERR_DEVICE_CHECK = 7        /* a kernel found bad input data (error word) */
+} moe_status_t;
+
+/* Bits of the device error word (first 4 bytes of the workspace). */
+#define MOE_DEVERR_TIMEOUT      0x1u  /* a pipeline wait gave up after its time limit */
+#define MOE_DEVERR_BAD_EXPERT   0x2u  /* a top-K index outside [0, E) was skipped */
+#define MOE_DEVERR_COUNT_MISMATCH 0x4u /* counts[] disagreed with the recount of topk_idx */
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_string(int status);
+
+/* Version of this ABI (major*100 + minor). */
+int moe_abi_version(void);
+
+/* Bytes of workspace the calls below need for this layer shape; 0 for an
+ * invalid shape. The workspace holds, 256-byte aligned: the device error word,
+ * counts[E], offsets[E+1], tile_base[E+1], the grouping scratch
+ * (ceil(T/32)*E counters and T*K ranks), perm_token/perm_slot/row_of_slot [T*K],
+ * topk_idx/topk_w [T*K] for moe_forward, the tile list [T*K/128+E][4], the
+ * gathered rows Xg [T*K,d] bf16, H [T*K,n] bf16 and Z [T*K,d] bf16.
+ * Before first use the caller zeroes it once (moe_workspace_init). */
+size_t moe_workspace_bytes(int T, int d, int E, int K, int n);
+
+/* Zero the workspace's error word and control words (enqueued on `stream`). */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Router from activations (page "Triton优化MoE模型：topk_gating算子融合实战",
+ * §2.1-§2.2, and the SonicMoE page §1, §3.2).
+ *   X       [T,d] bf16      token activations
+ *   Wr      [d,E] fp32      router weights
+ *   bias    [E] fp32 or NULL  added to every token's logits
+ *   renorm  1: weights renormalised over the K kept experts; 0: raw softmax probs
+ * Outputs: topk_idx [T,K] int32 (descending score; ties -> lower index),
+ *          topk_w [T,K] fp32, counts [E] int32 (tokens routed to each expert;
+ *          the call zeroes it first).
+ * Logits are fp32 fused multiply-add chains over j = 0..d-1 ascending from +0,
+ * then + bias[e]: bit-identical to that sequential definition. */
+moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias,
+                       int T, int d, int E, int K, int renorm,
+                       int32_t *topk_idx, float *topk_w, int32_t *counts, void *stream);
+
+/* Router from given logits [T,E] fp32 (softmax + top-K + counts only). Same
+ * outputs as moe_route. */
+moe_status_t moe_route_logits(const float *logits, int T, int E, int K, int renorm,
+                              int32_t *topk_idx, float *topk_w, int32_t *counts,
+                              void *stream);
+
+/* Group the routed slots by expert (SonicMoE page §1 Gather, §2.2 grouping by
+ * expert, §3.1 per-expert counts; SpMM page §2 CSR row offsets).
+ *   topk_idx [T,K] int32; counts [E] int32 or NULL (when given it is checked
+ *   against a recount on the device; a mismatch sets MOE_DEVERR_COUNT_MISMATCH).
+ * Outputs: offsets [E+1]; rows of expert e are offsets[e]..offsets[e+1]-1 in
+ *   ascending token order; perm_token [T*K] (token of each grouped row),
+ *   perm_slot [T*K] (t*K+k of each row), row_of_slot [T*K] (inverse of
+ *   perm_slot; -1 for a slot whose index was out of range);
+ *   tiles [(T*K)/128 + E][4] int32 = {expert, first row, rows<=128, 0}, expert
+ *   order, and num_tiles [1] (tile_base[E]). ws: workspace of this shape. */
+moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts,
+                         int T, int E, int K,
+                         int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                         int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/* Up-projection GEMM with the SwiGLU fused in its epilogue (SonicMoE page §1,
+ * §2.2, §4.2): for every grouped row p of expert e,
+ *   H[p,:] = bf16( SiLU(x W1[e]) * (x W3[e]) ),  x = X[perm_token[p],:].
+ * Uses offsets [E+1] and perm_token from moe_permute; H [T*K,n] bf16.
+ * ws: workspace of this shape (the gathered rows live there). */
+moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
+                              const int32_t *perm_token, const int32_t *offsets,
+                              int T, int d, int E, int K, int n, moe_bf16 *H,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* Down-projection GEMM with the routing weight applied in its epilogue:
+ *   Z[p,:] = bf16( topk_w[perm_slot[p]] * (H[p,:] W2[e]) ).
+ * H [T*K,n] bf16 grouped rows; Z [T*K,d] bf16. */
+moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
+                           const int32_t *perm_slot, const int32_t *offsets,
+                           int T, int d, int E, int K, int n, moe_bf16 *Z,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* Both expert GEMMs: moe_gemm_gate_up then moe_gemm_down. */
+moe_status_t moe_expert_mlp(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
+                            const moe_bf16 *W2, const float *topk_w,
+                            const int32_t *perm_token, const int32_t *perm_slot,
+                            const int32_t *offsets, int T, int d, int E, int K, int n,
+                            moe_bf16 *H, moe_bf16 *Z, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/* Scatter back and combine (SpMM page §6, SonicMoE page §1 Scatter):
+ *   Y[t,:] = bf16( sum over k = 0..K-1 ascending of Z[row_of_slot[t*K+k],:] ),
+ * fp32 accumulation, one rounding; rows with row_of_slot < 0 are skipped.
+ * Deterministic: no atomics. Z [T*K,d] bf16, Y [T,d] bf16. */
+moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, int K, int d,
+                         moe_bf16 *Y, void *stream);
+
+/* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
+ * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
+ * Enqueues 8 kernels and one memset; no host synchronisation. */
+moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
+                         const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
+                         int T, int d, int E, int K, int n, int renorm,
+                         moe_bf16 *Y, int32_t *topk_idx_out, float *topk_w_out,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/* moe_forward that also records CUDA events (cudaEvent_t as void*) on `stream`
+ * between its stages, for per-kernel timing: events[0] before the router,
+ * then after route, permute, gather, gate/up GEMM, down GEMM, combine
+ * (7 events). n_events < 7 records the first n_events of them. */
+moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float *bias,
+                                const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
+                                int T, int d, int E, int K, int n, int renorm,
+                                moe_bf16 *Y, int32_t *topk_idx_out, float *topk_w_out,
+                                void *ws, size_t ws_bytes, void *stream,
+                                void *const *events, int n_events);
+
+/* End to end from host memory: copies X_host [T,d] (host, ideally pinned) into
+ * X_dev, runs moe_forward, copies Y back into Y_host [T,d] (host) and waits
+ * for the stream. X_dev/Y_dev are caller-owned device buffers [T,d] bf16. */
+moe_status_t moe_forward_host(const moe_bf16 *X_host, moe_bf16 *Y_host,
+                              moe_bf16 *X_dev, moe_bf16 *Y_dev, const float *Wr,
+                              const float *bias, const moe_bf16 *W1, const moe_bf16 *W3,
+                              const moe_bf16 *W2, int T, int d, int E, int K, int n,
+                              int renorm, void *ws, size_t ws_bytes, void *stream);
+
+/* Wait for `stream`, read and clear the workspace's device error word.
+ * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK (or
+ * MOE_ERR_CUDA); *word_out (may be NULL) receives the raw bits. */
+moe_status_t moe_sync_check(void *ws, void *stream, uint32_t *word_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,144 @@
+"""Whole-layer parity on the GPU for every workload, through the C-ABI.
+
+The step-by-step entry points are checked against the oracle at full size
+(routing, grouping bit-exact; H, Z, Y within tolerance where the oracle can run
+the whole layer in seconds, on sampled tokens otherwise), and moe_forward in
+the configuration the benchmark times must reproduce the step-by-step Y bit for
+bit. Y[t] depends only on X[t] and the weights, so sampled tokens are checked
+against the oracle's token-by-token definition.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import W_ABS, bits, check_hz, check_y, layer_np
+from top_routing_grouped_02_gb300 import moe, synth
+
+pytestmark = pytest.mark.gpu
+
+# tokens the oracle evaluates one by one on the large workloads
+SAMPLE = 48
+
+
+def _steps(inp, K):
+    """The layer through the individual entry points; returns every output."""
+    T, d = inp["X"].shape
+    E, _, n = inp["W1"].shape
+    ws = moe.workspace(T, d, E, K, n)
+    idx, w, counts = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"])
+    g = moe.moe_permute(idx, E, counts=counts, ws=ws)
+    H, Z = moe.moe_expert_mlp(inp["X"], inp["W1"], inp["W3"], inp["W2"], w, g["perm_token"],
+                              g["perm_slot"], g["offsets"], K, ws=ws)
+    Y = moe.moe_combine(Z, g["row_of_slot"], K)
+    st, word = moe.moe_sync_check(ws)
+    assert st == 0, (st, word)
+    return dict(idx=idx, w=w, counts=counts, H=H, Z=Z, Y=Y, **g)
+
+
+def _forward(inp, K):
+    T, d = inp["X"].shape
+    E, _, n = inp["W1"].shape
+    ws = moe.workspace(T, d, E, K, n)
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    Y = moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"],
+                        ws=ws, topk_idx=idx, topk_w=w)
+    st, word = moe.moe_sync_check(ws)
+    assert st == 0, (st, word)
+    return Y, idx, w
+
+
+def _check_grouping(s, idx_r, E):
+    off_r, pt_r, ps_r, ros_r = oracle.permute(idx_r, E)
+    assert np.array_equal(s["offsets"].cpu().numpy(), off_r)
+    assert np.array_equal(s["perm_token"].cpu().numpy(), pt_r)
+    assert np.array_equal(s["perm_slot"].cpu().numpy(), ps_r)
+    assert np.array_equal(s["row_of_slot"].cpu().numpy(), ros_r)
+    assert np.array_equal(s["counts"].cpu().numpy(), oracle.expert_counts(idx_r, E))
+    tiles_r = oracle.tile_schedule(off_r, moe.TILE_M)
+    assert int(s["num_tiles"].item()) == len(tiles_r)
+    assert np.array_equal(s["tiles"].cpu().numpy()[:len(tiles_r)], tiles_r)
+    return off_r, pt_r, ps_r, ros_r
+
+
+def _run_workload(name, full_oracle: bool):
+    cfg = synth.WORKLOADS[name]
+    T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    s = _steps(inp, K)
+    Yf, idx_f, w_f = _forward(inp, K)
+    torch.cuda.synchronize()
+    # moe_forward (the benchmarked call) reproduces the step-by-step result exactly
+    assert torch.equal(Yf.view(torch.int16), s["Y"].view(torch.int16))
+    assert torch.equal(idx_f, s["idx"]) and torch.equal(w_f, s["w"])
+
+    X, Wr, bias, W1, W3, W2 = layer_np(inp)
+    L = oracle.router_logits(X, Wr, bias)
+    idx_r, w_r = oracle.topk_softmax(L, K, True)
+    assert np.array_equal(s["idx"].cpu().numpy(), idx_r)
+    assert float(np.abs(s["w"].cpu().numpy().astype(np.float64) - w_r).max()) <= W_ABS
+    off_r, pt_r, ps_r, ros_r = _check_grouping(s, idx_r, E)
+
+    if full_oracle:
+        H_ref = oracle.gate_up(X, W1, W3, pt_r, off_r)
+        check_hz(bits(s["H"]), H_ref, "H")
+        Z_ref = oracle.down(H_ref, W2, w_r, ps_r, off_r)
+        check_hz(bits(s["Z"]), Z_ref, "Z")
+        Y_ref = oracle.combine(Z_ref, ros_r, K)
+        check_y(bits(s["Y"]), Y_ref, "Y")
+    rng = np.random.default_rng(12345)
+    toks = np.sort(rng.choice(T, size=min(SAMPLE, T), replace=False))
+    toks[0], toks[-1] = 0, T - 1
+    Y_rows, idx_rows, w_rows = oracle.forward_tokens(X, Wr, bias, W1, W3, W2, K, toks)
+    assert np.array_equal(idx_rows, idx_r[toks])
+    check_y(bits(s["Y"])[toks], Y_rows, "Y (sampled tokens)")
+
+
+def test_tiny_workload():
+    _run_workload("tiny", full_oracle=True)
+
+
+def test_sonic_workload():
+    _run_workload("sonic", full_oracle=True)
+
+
+def test_mixtral_workload():
+    _run_workload("mixtral", full_oracle=False)
+
+
+def test_dsv3_workload():
+    _run_workload("dsv3", full_oracle=False)
+
+
+def test_forward_host_roundtrip_matches_device_call():
+    cfg = dict(synth.WORKLOADS["tiny"])
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
+    Y_dev_ref, _, _ = _forward(inp, K)
+    Xh = inp["X"].cpu().pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    Xd = torch.empty_like(inp["X"])
+    Yd = torch.empty_like(inp["X"])
+    moe.moe_forward_host(Xh, Yh, Xd, Yd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"])
+    assert torch.equal(Yh.view(torch.int16), Y_dev_ref.cpu().view(torch.int16))
+
+
+def test_forward_traced_records_stage_events():
+    cfg = dict(synth.WORKLOADS["tiny"])
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], cfg["K"], inp["bias"],
+                    events=ev)
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(6)]
+    assert all(t >= 0 for t in times)
+
+
+def test_forward_rejects_small_workspace():
+    cfg = dict(synth.WORKLOADS["tiny"])
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], cfg["K"], ws=ws)
+    assert e.value.status == 3

@@ -1,0 +1,81 @@
+"""Grouping parity on the GPU: offsets, permutation, inverse map and tile list
+bit-exact against the oracle; device-side checks of bad input."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_routing_grouped_02_gb300 import moe
+
+pytestmark = pytest.mark.gpu
+
+
+def _routing(T, E, K, skew=0.0, seed=0):
+    rng = np.random.default_rng(seed)
+    p = np.arange(1, E + 1, dtype=np.float64) ** (-skew)
+    p /= p.sum()
+    # K distinct experts per token, drawn without replacement (Gumbel top-K)
+    g = rng.gumbel(size=(T, E)) + np.log(p)
+    return np.argsort(-g, axis=1, kind="stable")[:, :K].astype(np.int32)
+
+
+def _check(idx: np.ndarray, E: int):
+    T, K = idx.shape
+    counts = oracle.expert_counts(idx, E)
+    off_r, pt_r, ps_r, ros_r = oracle.permute(idx, E)
+    tiles_r = oracle.tile_schedule(off_r, moe.TILE_M)
+    d_idx = torch.from_numpy(idx).cuda()
+    out = moe.moe_permute(d_idx, E, counts=torch.from_numpy(counts).cuda())
+    ws_status = None
+    torch.cuda.synchronize()
+    assert np.array_equal(out["offsets"].cpu().numpy(), off_r)
+    assert np.array_equal(out["perm_token"].cpu().numpy(), pt_r)
+    assert np.array_equal(out["perm_slot"].cpu().numpy(), ps_r)
+    assert np.array_equal(out["row_of_slot"].cpu().numpy(), ros_r)
+    nt = int(out["num_tiles"].item())
+    assert nt == len(tiles_r)
+    assert np.array_equal(out["tiles"].cpu().numpy()[:nt], tiles_r)
+    return ws_status
+
+
+@pytest.mark.parametrize("T,E,K,skew", [
+    (512, 8, 2, 0.0),       # tiny
+    (4096, 8, 2, 0.0),      # Mixtral-shaped
+    (8192, 256, 8, 1.1),    # DeepSeek-V3-shaped, Zipf-skewed loads
+    (16384, 128, 4, 0.0),   # SonicMoE-shaped
+    (1, 4, 4, 0.0),         # one token, every expert
+    (33, 256, 8, 3.0),      # most experts empty
+    (1000, 5, 1, 0.5),
+    (70000, 16, 2, 0.0),    # many chunks (> 2048)
+])
+def test_permute_matches_oracle(T, E, K, skew):
+    _check(_routing(T, E, K, skew, seed=T + E), E)
+
+
+def test_permute_one_expert_takes_everything_and_exact_tile_multiples():
+    T, E, K = 1024, 8, 1
+    _check(np.full((T, K), 3, np.int32), E)            # 1024 rows = 8 full tiles
+    idx = np.zeros((256, 2), np.int32)
+    idx[:, 0] = 2
+    idx[:, 1] = 5                                        # two experts, 256 rows each
+    _check(idx, E)
+
+
+def test_permute_flags_bad_expert_and_count_mismatch():
+    T, E, K = 64, 8, 2
+    idx = _routing(T, E, K, seed=3)
+    counts = oracle.expert_counts(idx, E)
+    bad = idx.copy()
+    bad[5, 1] = 11                                       # out of range
+    ws = moe.workspace(T, 0, E, K, 0)
+    out = moe.moe_permute(torch.from_numpy(bad).cuda(), E, counts=torch.from_numpy(counts).cuda(),
+                          ws=ws)
+    status, word = moe.moe_sync_check(ws)
+    assert status == 7 and (word & 0x2) and (word & 0x4)
+    ros = out["row_of_slot"].cpu().numpy()
+    assert ros[5 * K + 1] == -1
+    good = np.delete(np.arange(T * K), 5 * K + 1)
+    assert np.all(ros[good] >= 0)
+    assert int(out["offsets"][-1]) == T * K - 1
+    status, word = moe.moe_sync_check(ws)                # cleared by the previous read
+    assert status == 0 and word == 0

@@ -1,0 +1,361 @@
+// C ABI of libmoe.so: argument checking, workspace layout and the sequence of
+// kernel launches for each entry point declared in include/moe.h.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+    bool init = false;
+    bool arch_ok = false;
+    int sms = 0;
+};
+DeviceInfo g_dev[64];
+
+const DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    DeviceInfo &di = g_dev[dev];
+    if (!di.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        di.arch_ok = (major == 10 && minor == 3);
+        di.sms = sms;
+        di.init = true;
+    }
+    return &di;
+}
+
+moe_status_t check_arch() {
+    // a failed call made by someone else earlier must not be reported as ours
+    (void)cudaGetLastError();
+    const DeviceInfo *di = device_info();
+    if (di == nullptr) return MOE_ERR_CUDA;
+    return di->arch_ok ? MOE_OK : MOE_ERR_ARCH;
+}
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Router-level shape rules.
+moe_status_t check_route_shape(int T, int d, int E, int K) {
+    if (T < 1 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+    if (d < 0) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxE || K > kMaxK || K > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d != -1 && (d < 8 || d % 8 != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)T * K >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+// Expert-GEMM shape rules.
+moe_status_t check_mlp_shape(int T, int d, int E, int K, int n) {
+    moe_status_t s = check_route_shape(T, d, E, K);
+    if (s != MOE_OK) return s;
+    if (n < 1) return MOE_ERR_INVALID_ARG;
+    if (d % 256 != 0 || n % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int64_t R = (int64_t)T * K;
+    if (R * (d > n ? d : n) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+}  // namespace
+
+int sm_count() {
+    const DeviceInfo *di = device_info();
+    return (di != nullptr && di->sms > 0) ? di->sms : 1;
+}
+
+WsLayout ws_layout(int T, int d, int E, int K, int n) {
+    WsLayout L{};
+    const size_t R = (size_t)T * K;
+    L.nchunks = (T + kChunk - 1) / kChunk;
+    L.max_tiles = (int)(R / kTileM) + E;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    L.err = take(64);
+    L.counts = take(4 * (size_t)E);
+    L.offsets = take(4 * (size_t)(E + 1));
+    L.tile_base = take(4 * (size_t)(E + 1));
+    L.totals = take(4 * (size_t)E);
+    L.chunk_base = take(4 * (size_t)E * L.nchunks);
+    L.rank = take(4 * R);
+    L.perm_token = take(4 * R);
+    L.perm_slot = take(4 * R);
+    L.row_of_slot = take(4 * R);
+    L.topk_idx = take(4 * R);
+    L.topk_w = take(4 * R);
+    L.tiles = take(16 * (size_t)L.max_tiles);
+    L.num_tiles = take(4);
+    L.xg = take(2 * R * (size_t)d);
+    L.h = take(2 * R * (size_t)n);
+    L.z = take(2 * R * (size_t)d);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+        case MOE_ERR_ARCH: return "MOE_ERR_ARCH";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+int moe_abi_version(void) { return 100; }
+
+size_t moe_workspace_bytes(int T, int d, int E, int K, int n) {
+    if (T < 1 || E < 1 || K < 1 || d < 0 || n < 0 || E > kMaxE || K > kMaxK || K > E) return 0;
+    return ws_layout(T, d, E, K, n).total;
+}
+
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    if (ws == nullptr || ws_bytes < 64) return MOE_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(ws, 0, 64, as_stream(stream)));
+}
+
+moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias, int T, int d, int E,
+                       int K, int renorm, int32_t *topk_idx, float *topk_w, int32_t *counts,
+                       void *stream) {
+    if (!X || !Wr || !topk_idx || !topk_w || !counts || (renorm != 0 && renorm != 1))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, d, E, K);
+    if (s != MOE_OK) return s;
+    if (!aligned16(X)) return MOE_ERR_INVALID_ARG;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_route(reinterpret_cast<const __nv_bfloat16 *>(X), Wr, bias, T, d, E, K,
+                                  renorm, topk_idx, topk_w, counts, nullptr, as_stream(stream)));
+}
+
+moe_status_t moe_route_logits(const float *logits, int T, int E, int K, int renorm,
+                              int32_t *topk_idx, float *topk_w, int32_t *counts, void *stream) {
+    if (!logits || !topk_idx || !topk_w || !counts || (renorm != 0 && renorm != 1))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, 8, E, K);
+    if (s != MOE_OK) return s;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(
+        launch_route_logits(logits, T, E, K, renorm, topk_idx, topk_w, counts, as_stream(stream)));
+}
+
+moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts, int T, int E, int K,
+                         int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                         int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles, void *ws,
+                         size_t ws_bytes, void *stream) {
+    if (!topk_idx || !offsets || !perm_token || !perm_slot || !row_of_slot || !tiles ||
+        !num_tiles || !ws)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, 8, E, K);
+    if (s != MOE_OK) return s;
+    if (!aligned16(tiles)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, 0, E, K, 0);
+    if (ws_bytes < L.xg) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_permute(topk_idx, counts, T, E, K, offsets, perm_token, perm_slot,
+                                    row_of_slot, tiles, num_tiles, L, static_cast<char *>(ws),
+                                    as_stream(stream)));
+}
+
+moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
+                              const int32_t *perm_token, const int32_t *offsets, int T, int d,
+                              int E, int K, int n, moe_bf16 *H, void *ws, size_t ws_bytes,
+                              void *stream) {
+    if (!X || !W1 || !W3 || !perm_token || !offsets || !H || !ws) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W3) || !aligned16(H))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, K, n);
+    if (ws_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    const int R = T * K;
+    cudaStream_t st = as_stream(stream);
+    __nv_bfloat16 *xg = at<__nv_bfloat16>(ws, L.xg);
+    cudaError_t e = launch_gather_rows(reinterpret_cast<const __nv_bfloat16 *>(X), perm_token, T, R, d,
+                                       xg, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(launch_gemm_gate_up(xg, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                                         reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d,
+                                         E, n, reinterpret_cast<__nv_bfloat16 *>(H),
+                                         at<uint32_t>(ws, L.err), st));
+}
+
+moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
+                           const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
+                           int K, int n, moe_bf16 *Z, void *ws, size_t ws_bytes, void *stream) {
+    if (!H || !W2 || !topk_w || !perm_slot || !offsets || !Z || !ws) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (!aligned16(H) || !aligned16(W2) || !aligned16(Z)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < 64) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    const WsLayout L = ws_layout(T, d, E, K, n);
+    return from_cuda(launch_gemm_down(reinterpret_cast<const __nv_bfloat16 *>(H),
+                                      reinterpret_cast<const __nv_bfloat16 *>(W2), topk_w,
+                                      perm_slot, offsets, T * K, d, E, n,
+                                      reinterpret_cast<__nv_bfloat16 *>(Z),
+                                      at<uint32_t>(ws, L.err), as_stream(stream)));
+}
+
+moe_status_t moe_expert_mlp(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
+                            const moe_bf16 *W2, const float *topk_w, const int32_t *perm_token,
+                            const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
+                            int K, int n, moe_bf16 *H, moe_bf16 *Z, void *ws, size_t ws_bytes,
+                            void *stream) {
+    moe_status_t s = moe_gemm_gate_up(X, W1, W3, perm_token, offsets, T, d, E, K, n, H, ws,
+                                      ws_bytes, stream);
+    if (s != MOE_OK) return s;
+    return moe_gemm_down(H, W2, topk_w, perm_slot, offsets, T, d, E, K, n, Z, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, int K, int d,
+                         moe_bf16 *Y, void *stream) {
+    if (!Z || !row_of_slot || !Y) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, d, K, K);
+    if (s != MOE_OK) return s;
+    if (!aligned16(Z) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_combine(reinterpret_cast<const __nv_bfloat16 *>(Z), row_of_slot, T, K,
+                                    d, reinterpret_cast<__nv_bfloat16 *>(Y), as_stream(stream)));
+}
+
+moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float *bias,
+                                const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2, int T,
+                                int d, int E, int K, int n, int renorm, moe_bf16 *Y,
+                                int32_t *topk_idx_out, float *topk_w_out, void *ws,
+                                size_t ws_bytes, void *stream, void *const *events,
+                                int n_events) {
+    if (!X || !Wr || !W1 || !W3 || !W2 || !Y || !ws || (renorm != 0 && renorm != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (n_events < 0 || (n_events > 0 && events == nullptr)) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(Y))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, K, n);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    int ev = 0;
+    auto mark = [&]() -> bool {
+        if (ev < n_events) {
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[ev]), st) != cudaSuccess)
+                return false;
+        }
+        ++ev;
+        return true;
+    };
+    const int R = T * K;
+    uint32_t *err = at<uint32_t>(ws, L.err);
+    int32_t *idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
+    float *w = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
+    int32_t *counts = at<int32_t>(ws, L.counts);
+    int32_t *offsets = at<int32_t>(ws, L.offsets);
+    int32_t *perm_token = at<int32_t>(ws, L.perm_token);
+    int32_t *perm_slot = at<int32_t>(ws, L.perm_slot);
+    int32_t *row_of_slot = at<int32_t>(ws, L.row_of_slot);
+    __nv_bfloat16 *xg = at<__nv_bfloat16>(ws, L.xg);
+    __nv_bfloat16 *h = at<__nv_bfloat16>(ws, L.h);
+    __nv_bfloat16 *z = at<__nv_bfloat16>(ws, L.z);
+    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(X);
+
+    if (!mark()) return MOE_ERR_CUDA;
+    if (launch_route(x, Wr, bias, T, d, E, K, renorm, idx, w, counts, err, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_permute(idx, counts, T, E, K, offsets, perm_token, perm_slot, row_of_slot,
+                       at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.num_tiles), L,
+                       static_cast<char *>(ws), st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_gather_rows(x, perm_token, T, R, d, xg, st) != cudaSuccess || !mark())
+        return MOE_ERR_CUDA;
+    if (launch_gemm_gate_up(xg, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                            reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n, h,
+                            err, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), w, perm_slot, offsets, R,
+                         d, E, n, z, err, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_combine(z, row_of_slot, T, K, d, reinterpret_cast<__nv_bfloat16 *>(Y), st) !=
+            cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
+                         const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2, int T, int d,
+                         int E, int K, int n, int renorm, moe_bf16 *Y, int32_t *topk_idx_out,
+                         float *topk_w_out, void *ws, size_t ws_bytes, void *stream) {
+    return moe_forward_traced(X, Wr, bias, W1, W3, W2, T, d, E, K, n, renorm, Y, topk_idx_out,
+                              topk_w_out, ws, ws_bytes, stream, nullptr, 0);
+}
+
+moe_status_t moe_forward_host(const moe_bf16 *X_host, moe_bf16 *Y_host, moe_bf16 *X_dev,
+                              moe_bf16 *Y_dev, const float *Wr, const float *bias,
+                              const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2, int T,
+                              int d, int E, int K, int n, int renorm, void *ws, size_t ws_bytes,
+                              void *stream) {
+    if (!X_host || !Y_host || !X_dev || !Y_dev) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    const size_t bytes = (size_t)T * d * sizeof(moe_bf16);
+    if (cudaMemcpyAsync(X_dev, X_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    s = moe_forward(X_dev, Wr, bias, W1, W3, W2, T, d, E, K, n, renorm, Y_dev, nullptr, nullptr, ws,
+                    ws_bytes, stream);
+    if (s != MOE_OK) return s;
+    if (cudaMemcpyAsync(Y_host, Y_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return from_cuda(cudaStreamSynchronize(st));
+}
+
+moe_status_t moe_sync_check(void *ws, void *stream, uint32_t *word_out) {
+    if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (word != 0 && cudaMemset(ws, 0, sizeof word) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word_out != nullptr) *word_out = word;
+    if (word & MOE_DEVERR_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+    if (word != 0) return MOE_ERR_DEVICE_CHECK;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Internal declarations shared by the CUDA translation units of libmoe.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Rows per expert tile of the grouped GEMMs (the UMMA M dimension).
+constexpr int kTileM = 128;
+// Largest supported expert count and top-K.
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;
+// Tokens per grouping chunk (one warp, one bit per token).
+constexpr int kChunk = 32;
+
+// Byte offsets of the workspace regions for one layer shape (all 256-aligned).
+struct WsLayout {
+    size_t err;         // uint32 error word + control words (64 B)
+    size_t counts;      // int32 [E]
+    size_t offsets;     // int32 [E+1]
+    size_t tile_base;   // int32 [E+1]
+    size_t totals;      // int32 [E]   per-expert recount (grouping)
+    size_t chunk_base;  // int32 [E * nchunks]
+    size_t rank;        // int32 [R]
+    size_t perm_token;  // int32 [R]
+    size_t perm_slot;   // int32 [R]
+    size_t row_of_slot; // int32 [R]
+    size_t topk_idx;    // int32 [R]
+    size_t topk_w;      // fp32  [R]
+    size_t tiles;       // int32 [max_tiles][4]
+    size_t num_tiles;   // int32 [1]
+    size_t xg;          // bf16  [R, d]  gathered activation rows
+    size_t h;           // bf16  [R, n]
+    size_t z;           // bf16  [R, d]
+    size_t total;
+    int nchunks;
+    int max_tiles;
+};
+
+// Control words at the start of the workspace (uint32 each).
+enum : int { kWordErr = 0, kWordDone = 1 };
+
+WsLayout ws_layout(int T, int d, int E, int K, int n);
+
+// ---- launchers (each returns the CUDA error of its launch) -----------------
+cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
+                         int d, int E, int K, int renorm, int32_t *idx, float *w,
+                         int32_t *counts, uint32_t *err, cudaStream_t s);
+cudaError_t launch_route_logits(const float *logits, int T, int E, int K, int renorm,
+                                int32_t *idx, float *w, int32_t *counts, cudaStream_t s);
+cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, int E, int K,
+                           int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                           int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
+                           const WsLayout &L, char *ws, cudaStream_t s);
+cudaError_t launch_gather_rows(const __nv_bfloat16 *X, const int32_t *perm_token, int T, int R,
+                               int d, __nv_bfloat16 *Xg, cudaStream_t s);
+cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *Xg, const __nv_bfloat16 *W1,
+                                const __nv_bfloat16 *W3, const int32_t *offsets, int R, int d,
+                                int E, int n, __nv_bfloat16 *H, uint32_t *err, cudaStream_t s);
+cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
+                             const float *topk_w, const int32_t *perm_slot,
+                             const int32_t *offsets, int R, int d, int E, int n,
+                             __nv_bfloat16 *Z, uint32_t *err, cudaStream_t s);
+cudaError_t launch_combine(const __nv_bfloat16 *Z, const int32_t *row_of_slot, int T, int K,
+                           int d, __nv_bfloat16 *Y, cudaStream_t s);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+}  // namespace moe

@@ -1,0 +1,203 @@
+// Grouping of routed slots by expert: counts, CSR-style offsets, a stable
+// permutation (rows of one expert in ascending token order) and the row-tile
+// schedule of the grouped GEMMs.
+//
+// Pages: "混合专家模型(MoE)架构优化与SonicMoE实践" §1 (Gather by routing result;
+// tiles of fixed size pad experts whose row count is not a multiple of the tile),
+// §2.2 (intermediates stored grouped by expert), §3.1 (per-expert counts over
+// every (t,k) choice); "稀疏矩阵乘法（SpMM）在MoE中的应用：利用Triton内核加速稀疏专家
+// 的计算" §2 (CSR row offsets); "Оптимизация Triton ускоряет матричные вычисления
+// для моделей Mixture-of-Experts" (persistent kernel pulling tiles from a list).
+//
+// Three small kernels, all deterministic (no atomics decide a position):
+//  1. rank:    one warp per chunk of 32 tokens builds, for every expert, a
+//              32-bit mask of the chunk's tokens that chose it; a slot's rank in
+//              its chunk is the popcount of the mask below its lane, and the
+//              chunk's count per expert is the mask's popcount.
+//  2. scan:    one block per expert turns the chunk counts into exclusive
+//              prefix sums; the last block to finish (ticket counter) scans the
+//              expert totals into offsets, tile bases and the tile list.
+//  3. scatter: p = offsets[e] + chunk prefix + rank; writes perm_token,
+//              perm_slot and row_of_slot.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+rank_kernel(const int32_t *__restrict__ idx, int T, int E, int K, int nchunks,
+            int32_t *__restrict__ rank, int32_t *__restrict__ chunk_cnt,
+            uint32_t *__restrict__ ctrl) {
+    __shared__ uint32_t masks[kThreads / 32][kMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[kWordDone] = 0;  // ticket for the scan
+    const int chunk = blockIdx.x * (kThreads / 32) + warp;
+    if (chunk >= nchunks) return;
+    uint32_t *m = masks[warp];
+    for (int e = lane; e < E; e += 32) m[e] = 0u;
+    __syncwarp();
+    const int64_t t = (int64_t)chunk * kChunk + lane;
+    const bool valid = t < T;
+    int ek[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        ek[k] = -1;
+        if (k < K && valid) {
+            int e = idx[t * K + k];
+            if (e >= 0 && e < E) {
+                ek[k] = e;
+                atomicOr(&m[e], 1u << lane);
+            } else {
+                atomicOr(&ctrl[kWordErr], MOE_DEVERR_BAD_EXPERT);
+            }
+        }
+    }
+    __syncwarp();
+    const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k)
+        if (k < K && valid) rank[t * K + k] = ek[k] >= 0 ? __popc(m[ek[k]] & below) : -1;
+    for (int e = lane; e < E; e += 32) chunk_cnt[(int64_t)e * nchunks + chunk] = __popc(m[e]);
+}
+
+// Exclusive block-wide scan of one value per thread (256 threads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int ws = lane < kThreads / 32 ? warp_sums[lane] : 0;
+        int wi = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        if (lane < kThreads / 32) warp_sums[lane] = wi - ws;  // exclusive warp offsets
+        if (lane == kThreads / 32 - 1) warp_sums[kThreads / 32] = wi;
+    }
+    __syncthreads();
+    int excl = warp_sums[warp] + incl - v;
+    total = warp_sums[kThreads / 32];
+    __syncthreads();
+    return excl;
+}
+
+__global__ void __launch_bounds__(kThreads)
+scan_kernel(int32_t *__restrict__ chunk_cnt, int nchunks, int E, const int32_t *counts_in,
+            int32_t *__restrict__ totals, int32_t *__restrict__ offsets,
+            int32_t *__restrict__ tile_base, int32_t *__restrict__ tiles,
+            int32_t *__restrict__ num_tiles, uint32_t *__restrict__ ctrl) {
+    __shared__ int warp_sums[kThreads / 32 + 1];
+    __shared__ bool is_last;
+    const int e = blockIdx.x;
+    int32_t *row = chunk_cnt + (int64_t)e * nchunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += kThreads) {
+        const int c = c0 + threadIdx.x;
+        const int v = c < nchunks ? row[c] : 0;
+        int tot;
+        const int ex = block_exclusive_scan(v, warp_sums, tot);
+        if (c < nchunks) row[c] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) {
+        totals[e] = carry;
+        __threadfence();
+        const uint32_t ticket = atomicAdd(&ctrl[kWordDone], 1u);
+        is_last = (ticket == (uint32_t)E - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // last block: offsets, tile bases, tile list over all experts (E <= 256)
+    const int ee = threadIdx.x;
+    const int c = ee < E ? *((volatile int32_t *)totals + ee) : 0;
+    const int ntile = (c + kTileM - 1) / kTileM;
+    int tot_rows, tot_tiles;
+    const int off = block_exclusive_scan(c, warp_sums, tot_rows);
+    const int tb = block_exclusive_scan(ntile, warp_sums, tot_tiles);
+    if (ee < E) {
+        offsets[ee] = off;
+        tile_base[ee] = tb;
+        if (counts_in != nullptr && counts_in[ee] != c)
+            atomicOr(&ctrl[kWordErr], MOE_DEVERR_COUNT_MISMATCH);
+        for (int i = 0; i < ntile; ++i) {
+            int4 tv;
+            tv.x = ee;
+            tv.y = off + i * kTileM;
+            tv.z = min(kTileM, c - i * kTileM);
+            tv.w = 0;
+            reinterpret_cast<int4 *>(tiles)[tb + i] = tv;
+        }
+    }
+    if (ee == 0) {
+        offsets[E] = tot_rows;
+        tile_base[E] = tot_tiles;
+        num_tiles[0] = tot_tiles;
+        ctrl[kWordDone] = 0;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+scatter_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank,
+               const int32_t *__restrict__ chunk_base, const int32_t *__restrict__ offsets,
+               int T, int E, int K, int nchunks, int32_t *__restrict__ perm_token,
+               int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of_slot,
+               uint32_t *__restrict__ ctrl) {
+    const int64_t slot = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t R = (int64_t)T * K;
+    if (slot >= R) return;
+    const int e = idx[slot];
+    const int r = rank[slot];
+    if (e < 0 || e >= E || r < 0) {
+        row_of_slot[slot] = -1;
+        return;
+    }
+    const int64_t t = slot / K;
+    const int64_t p = (int64_t)offsets[e] + chunk_base[(int64_t)e * nchunks + t / kChunk] + r;
+    if (p < 0 || p >= R) {
+        atomicOr(&ctrl[kWordErr], MOE_DEVERR_BAD_EXPERT);
+        row_of_slot[slot] = -1;
+        return;
+    }
+    perm_token[p] = (int32_t)t;
+    perm_slot[p] = (int32_t)slot;
+    row_of_slot[slot] = (int32_t)p;
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, int E, int K,
+                           int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                           int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
+                           const WsLayout &L, char *ws, cudaStream_t s) {
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(ws + L.err);
+    int32_t *rank = reinterpret_cast<int32_t *>(ws + L.rank);
+    int32_t *chunk = reinterpret_cast<int32_t *>(ws + L.chunk_base);
+    int32_t *totals = reinterpret_cast<int32_t *>(ws + L.totals);
+    int32_t *tile_base = reinterpret_cast<int32_t *>(ws + L.tile_base);
+    const int nchunks = L.nchunks;
+    const int64_t R = (int64_t)T * K;
+    rank_kernel<<<(nchunks + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, s>>>(
+        idx, T, E, K, nchunks, rank, chunk, ctrl);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    scan_kernel<<<E, kThreads, 0, s>>>(chunk, nchunks, E, counts_in, totals, offsets, tile_base,
+                                       tiles, num_tiles, ctrl);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    scatter_kernel<<<(unsigned)((R + kThreads - 1) / kThreads), kThreads, 0, s>>>(
+        idx, rank, chunk, offsets, T, E, K, nchunks, perm_token, perm_slot, row_of_slot, ctrl);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

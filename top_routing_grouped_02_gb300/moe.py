@@ -1,0 +1,269 @@
+"""Thin ctypes binding over libmoe.so (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. Tensors must be contiguous CUDA tensors of the dtype each call names;
+their ``data_ptr()`` and the current torch stream are passed straight through.
+There is no fallback: if libmoe.so is missing or a call fails, a ``MoeError``
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "moe.h")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+          3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
+          6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_CHECK"}
+# kernels each entry point launches (for launch accounting)
+LAUNCHES = {"moe_route": 1, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 2,
+            "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 8}
+TILE_M = 128
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_abi_version": (_I, []),
+    "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_workspace_init": (_I, [_P, _SZ, _P]),
+    "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_route_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_permute": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_gemm_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_expert_mlp": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
+                            _P]),
+    "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ,
+                         _P]),
+    "moe_forward_traced": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                _SZ, _P, ctypes.POINTER(_P), _I]),
+    "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                              _P]),
+    "moe_sync_check": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+
+def header_symbols() -> list[str]:
+    """Entry points declared in include/moe.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(", text, re.M)))
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def moe_workspace_bytes(T: int, d: int, E: int, K: int, n: int) -> int:
+    return int(lib().moe_workspace_bytes(T, d, E, K, n))
+
+
+def workspace(T: int, d: int, E: int, K: int, n: int, device=None) -> torch.Tensor:
+    """A zeroed workspace tensor (uint8) for this layer shape."""
+    nbytes = moe_workspace_bytes(T, d, E, K, n)
+    if nbytes == 0:
+        raise ValueError("invalid layer shape")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None):
+    _check("moe_workspace_init", lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_route(X, Wr, K: int, bias=None, renorm: bool = True, stream=None):
+    """(topk_idx [T,K] int32, topk_w [T,K] fp32, counts [E] int32)."""
+    T, d = X.shape
+    E = Wr.shape[1]
+    idx = torch.empty((T, K), dtype=torch.int32, device=X.device)
+    w = torch.empty((T, K), dtype=torch.float32, device=X.device)
+    counts = torch.empty(E, dtype=torch.int32, device=X.device)
+    _check("moe_route", lib().moe_route(
+        _ptr(X, torch.bfloat16, "X"), _ptr(Wr, torch.float32, "Wr"), _ptr(bias, torch.float32, "bias"),
+        T, d, E, K, int(bool(renorm)), _ptr(idx), _ptr(w), _ptr(counts), _stream(stream)))
+    return idx, w, counts
+
+
+def moe_route_logits(logits, K: int, renorm: bool = True, stream=None):
+    T, E = logits.shape
+    idx = torch.empty((T, K), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    counts = torch.empty(E, dtype=torch.int32, device=logits.device)
+    _check("moe_route_logits", lib().moe_route_logits(
+        _ptr(logits, torch.float32, "logits"), T, E, K, int(bool(renorm)), _ptr(idx), _ptr(w),
+        _ptr(counts), _stream(stream)))
+    return idx, w, counts
+
+
+def moe_permute(topk_idx, E: int, counts=None, ws=None, stream=None) -> dict:
+    T, K = topk_idx.shape
+    R = T * K
+    dev = topk_idx.device
+    if ws is None:
+        ws = workspace(T, 0, E, K, 0, dev)
+    out = dict(
+        offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+        perm_token=torch.empty(R, dtype=torch.int32, device=dev),
+        perm_slot=torch.empty(R, dtype=torch.int32, device=dev),
+        row_of_slot=torch.empty(R, dtype=torch.int32, device=dev),
+        tiles=torch.zeros((R // TILE_M + E, 4), dtype=torch.int32, device=dev),
+        num_tiles=torch.empty(1, dtype=torch.int32, device=dev),
+    )
+    _check("moe_permute", lib().moe_permute(
+        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(counts, torch.int32, "counts"), T, E, K,
+        _ptr(out["offsets"]), _ptr(out["perm_token"]), _ptr(out["perm_slot"]),
+        _ptr(out["row_of_slot"]), _ptr(out["tiles"]), _ptr(out["num_tiles"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def moe_gemm_gate_up(X, W1, W3, perm_token, offsets, K: int, ws=None, stream=None):
+    T, d = X.shape
+    E, _, n = W1.shape
+    if ws is None:
+        ws = workspace(T, d, E, K, n, X.device)
+    H = torch.empty((T * K, n), dtype=torch.bfloat16, device=X.device)
+    _check("moe_gemm_gate_up", lib().moe_gemm_gate_up(
+        _ptr(X, torch.bfloat16, "X"), _ptr(W1, torch.bfloat16, "W1"), _ptr(W3, torch.bfloat16, "W3"),
+        _ptr(perm_token, torch.int32), _ptr(offsets, torch.int32), T, d, E, K, n, _ptr(H),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return H
+
+
+def moe_gemm_down(H, W2, topk_w, perm_slot, offsets, T: int, K: int, ws=None, stream=None):
+    E, n, d = W2.shape
+    if ws is None:
+        ws = workspace(T, d, E, K, n, H.device)
+    Z = torch.empty((T * K, d), dtype=torch.bfloat16, device=H.device)
+    _check("moe_gemm_down", lib().moe_gemm_down(
+        _ptr(H, torch.bfloat16, "H"), _ptr(W2, torch.bfloat16, "W2"), _ptr(topk_w, torch.float32),
+        _ptr(perm_slot, torch.int32), _ptr(offsets, torch.int32), T, d, E, K, n, _ptr(Z),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return Z
+
+
+def moe_expert_mlp(X, W1, W3, W2, topk_w, perm_token, perm_slot, offsets, K: int, ws=None,
+                   stream=None):
+    T, d = X.shape
+    E, _, n = W1.shape
+    if ws is None:
+        ws = workspace(T, d, E, K, n, X.device)
+    H = torch.empty((T * K, n), dtype=torch.bfloat16, device=X.device)
+    Z = torch.empty((T * K, d), dtype=torch.bfloat16, device=X.device)
+    _check("moe_expert_mlp", lib().moe_expert_mlp(
+        _ptr(X, torch.bfloat16), _ptr(W1, torch.bfloat16), _ptr(W3, torch.bfloat16),
+        _ptr(W2, torch.bfloat16), _ptr(topk_w, torch.float32), _ptr(perm_token, torch.int32),
+        _ptr(perm_slot, torch.int32), _ptr(offsets, torch.int32), T, d, E, K, n, _ptr(H), _ptr(Z),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return H, Z
+
+
+def moe_combine(Z, row_of_slot, K: int, stream=None):
+    R, d = Z.shape
+    T = row_of_slot.numel() // K
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device=Z.device)
+    _check("moe_combine", lib().moe_combine(
+        _ptr(Z, torch.bfloat16, "Z"), _ptr(row_of_slot, torch.int32), T, K, d, _ptr(Y),
+        _stream(stream)))
+    return Y
+
+
+def moe_forward(X, Wr, W1, W3, W2, K: int, bias=None, renorm: bool = True, ws=None, Y=None,
+                topk_idx=None, topk_w=None, stream=None, events=None):
+    """Y [T,d] bf16 for the whole layer. Optional topk_idx/topk_w receive the
+    routing; `events` (list of torch.cuda.Event) are recorded between stages."""
+    T, d = X.shape
+    E, _, n = W1.shape
+    if ws is None:
+        ws = workspace(T, d, E, K, n, X.device)
+    if Y is None:
+        Y = torch.empty((T, d), dtype=torch.bfloat16, device=X.device)
+    args = (_ptr(X, torch.bfloat16, "X"), _ptr(Wr, torch.float32, "Wr"),
+            _ptr(bias, torch.float32, "bias"), _ptr(W1, torch.bfloat16, "W1"),
+            _ptr(W3, torch.bfloat16, "W3"), _ptr(W2, torch.bfloat16, "W2"), T, d, E, K, n,
+            int(bool(renorm)), _ptr(Y, torch.bfloat16, "Y"), _ptr(topk_idx, torch.int32),
+            _ptr(topk_w, torch.float32), _ptr(ws), ws.numel(), _stream(stream))
+    if events:
+        for e in events:
+            if e.cuda_event == 0:  # torch creates the CUDA event on first record
+                e.record()
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check("moe_forward_traced", lib().moe_forward_traced(*args, arr, len(events)))
+    else:
+        _check("moe_forward", lib().moe_forward(*args))
+    return Y
+
+
+def moe_forward_host(X_host, Y_host, X_dev, Y_dev, Wr, W1, W3, W2, K: int, bias=None,
+                     renorm: bool = True, ws=None, stream=None):
+    """End to end from host memory (X_host/Y_host CPU bf16 tensors, ideally pinned);
+    returns after Y_host holds the result."""
+    T, d = X_host.shape
+    E, _, n = W1.shape
+    for name, t in (("X_host", X_host), ("Y_host", Y_host)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a contiguous CPU bf16 tensor")
+    if ws is None:
+        ws = workspace(T, d, E, K, n, X_dev.device)
+    _check("moe_forward_host", lib().moe_forward_host(
+        ctypes.c_void_p(X_host.data_ptr()), ctypes.c_void_p(Y_host.data_ptr()),
+        _ptr(X_dev, torch.bfloat16), _ptr(Y_dev, torch.bfloat16), _ptr(Wr, torch.float32),
+        _ptr(bias, torch.float32), _ptr(W1, torch.bfloat16), _ptr(W3, torch.bfloat16),
+        _ptr(W2, torch.bfloat16), T, d, E, K, n, int(bool(renorm)), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return Y_host
+
+
+def moe_sync_check(ws, stream=None):
+    """(status, raw error word) after waiting for the stream; clears the word."""
+    word = ctypes.c_uint32(0)
+    st = lib().moe_sync_check(_ptr(ws), _stream(stream), ctypes.byref(word))
+    return int(st), int(word.value)
