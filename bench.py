@@ -39,9 +39,9 @@ KERNELS_PER_STAGE = {"route": 1, "permute": 3, "gather": 1, "gemm_gate_up": 1, "
 KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
-# the Mixtral-shaped workload (profiles/gemm_gate_up_mixtral.md); None until taken
-# for the kernel as it stands.
-GEMM1_TRAFFIC_BYTES = None
+# the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
+# whenever the kernel changes, until it is captured again.
+GEMM1_TRAFFIC_BYTES = {"mixtral": 1.949522e9 + 0.227283e9}
 
 
 def workload_desc(name, c):
@@ -318,7 +318,7 @@ def run_gpu(args, c, world, rank, local):
         "roofline": {"kernel": "gemm_gate_up (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
                      "achieved": round(g1_tflops, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": round(g1_tflops / peaks["bf16"], 4),
-                     "traffic": GEMM1_TRAFFIC_BYTES,
+                     "traffic": (GEMM1_TRAFFIC_BYTES or {}).get(args.workload),
                      "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
                      "algorithmic_flops_per_launch": g1_flops},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
