@@ -118,6 +118,34 @@ moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts,
                          int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
                          void *ws, size_t ws_bytes, void *stream);
 
+/* moe_permute for callers that cannot allocate device memory. The pages have
+ * no counterpart of this call: it exists for code that is given only its inputs
+ * and outputs and may not call cudaMalloc, e.g. a plugin inside an inference
+ * engine that owns all device memory, or a serving loop whose memory was
+ * planned at start-up (cudaMalloc can synchronise the device and can fail once
+ * memory is fragmented). Same arguments, outputs and device checks as
+ * moe_permute, without the workspace: the grouping scratch is a 4 MiB array
+ * built into libmoe.so (every GPU that loads the library holds it until the
+ * process exits). The call allocates nothing.
+ *   - Limit: the shape's grouping scratch, moe_workspace_bytes(T, 0, E, K, 0)
+ *     (about 24*T*K + 4*E*ceil(T/32) bytes), must fit in 4 MiB, i.e. T*K up to
+ *     about 150000 slots; larger shapes return MOE_ERR_UNSUPPORTED_SHAPE before
+ *     anything is enqueued.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     the call clears what has to start at zero. Calls whose work overlaps on
+ *     the GPU (other streams, other threads) race on the array: serialise them.
+ *   - The device error word of these calls lives in the array and is not
+ *     reported through moe_sync_check; bad expert indices still show up as
+ *     row_of_slot == -1. */
+moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const int32_t *counts,
+                                 int T, int E, int K,
+                                 int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                                 int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
+                                 void *stream);
+
 /* Up-projection GEMM with the SwiGLU fused in its epilogue (SonicMoE page §1,
  * §2.2, §4.2): for every grouped row p of expert e,
  *   H[p,:] = bf16( SiLU(x W1[e]) * (x W3[e]) ),  x = X[perm_token[p],:].

@@ -47,6 +47,7 @@ _SIGS = {
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_route_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_gemm_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_expert_mlp": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
@@ -162,6 +163,29 @@ def moe_permute(topk_idx, E: int, counts=None, ws=None, stream=None) -> dict:
         _ptr(out["offsets"]), _ptr(out["perm_token"]), _ptr(out["perm_slot"]),
         _ptr(out["row_of_slot"]), _ptr(out["tiles"]), _ptr(out["num_tiles"]), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return out
+
+
+def moe_permute_noalloc(topk_idx, E: int, counts=None, out: dict | None = None, stream=None) -> dict:
+    """moe_permute without a workspace: the library uses its built-in 4 MiB
+    scratch array, so this call allocates no device memory of its own. `out`
+    may hold preallocated output tensors (same keys as moe_permute returns)."""
+    T, K = topk_idx.shape
+    R = T * K
+    dev = topk_idx.device
+    if out is None:
+        out = dict(
+            offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            perm_token=torch.empty(R, dtype=torch.int32, device=dev),
+            perm_slot=torch.empty(R, dtype=torch.int32, device=dev),
+            row_of_slot=torch.empty(R, dtype=torch.int32, device=dev),
+            tiles=torch.zeros((R // TILE_M + E, 4), dtype=torch.int32, device=dev),
+            num_tiles=torch.empty(1, dtype=torch.int32, device=dev),
+        )
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(counts, torch.int32, "counts"), T, E, K,
+        _ptr(out["offsets"]), _ptr(out["perm_token"]), _ptr(out["perm_slot"]),
+        _ptr(out["row_of_slot"]), _ptr(out["tiles"]), _ptr(out["num_tiles"]), _stream(stream)))
     return out
 
 
