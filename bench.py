@@ -34,7 +34,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 STAGES = ["route", "permute", "gather", "gemm_gate_up", "gemm_down", "combine"]
-KERNELS_PER_STAGE = {"route": 1, "permute": 3, "gather": 1, "gemm_gate_up": 1, "gemm_down": 1,
+KERNELS_PER_STAGE = {"route": 2, "permute": 3, "gather": 1, "gemm_gate_up": 1, "gemm_down": 1,
                      "combine": 1}
 KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"

@@ -74,7 +74,8 @@ int moe_abi_version(void);
  * counts[E], offsets[E+1], tile_base[E+1], the grouping scratch
  * (ceil(T/32)*E counters and T*K ranks), perm_token/perm_slot/row_of_slot [T*K],
  * topk_idx/topk_w [T*K] for moe_forward, the tile list [T*K/128+E][4], the
- * gathered rows Xg [T*K,d] bf16, H [T*K,n] bf16 and Z [T*K,d] bf16.
+ * gathered rows Xg [T*K,d] bf16, H [T*K,n] bf16, Z [T*K,d] bf16 and the router
+ * logits [T,E] fp32 (moe_forward).
  * Before first use the caller zeroes it once (moe_workspace_init). */
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n);
 
@@ -87,13 +88,14 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  *   Wr      [d,E] fp32      router weights
  *   bias    [E] fp32 or NULL  added to every token's logits
  *   renorm  1: weights renormalised over the K kept experts; 0: raw softmax probs
- * Outputs: topk_idx [T,K] int32 (descending score; ties -> lower index),
+ * Outputs: logits [T,E] fp32 (the router scores; also the call's scratch),
+ *          topk_idx [T,K] int32 (descending score; ties -> lower index),
  *          topk_w [T,K] fp32, counts [E] int32 (tokens routed to each expert;
  *          the call zeroes it first).
  * Logits are fp32 fused multiply-add chains over j = 0..d-1 ascending from +0,
  * then + bias[e]: bit-identical to that sequential definition. */
 moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias,
-                       int T, int d, int E, int K, int renorm,
+                       int T, int d, int E, int K, int renorm, float *logits,
                        int32_t *topk_idx, float *topk_w, int32_t *counts, void *stream);
 
 /* Router from given logits [T,E] fp32 (softmax + top-K + counts only). Same
@@ -181,7 +183,7 @@ moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, i
 
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
- * Enqueues 8 kernels and one memset; no host synchronisation. */
+ * Enqueues 9 kernels and one memset; no host synchronisation. */
 moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
                          const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                          int T, int d, int E, int K, int n, int renorm,

@@ -52,13 +52,14 @@ FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails va
 
 
 @pytest.mark.parametrize("call,expect", [
-    (lambda L: L.moe_route(None, FAKE, None, 16, 64, 8, 2, 1, FAKE, FAKE, FAKE, None), 1),
-    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 64, 8, 2, 2, FAKE, FAKE, FAKE, None), 1),
-    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 60, 8, 2, 1, FAKE, FAKE, FAKE, None), 2),
-    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 64, 300, 2, 1, FAKE, FAKE, FAKE, None), 2),
-    (lambda L: L.moe_route(FAKE, FAKE, None, 0, 64, 8, 2, 1, FAKE, FAKE, FAKE, None), 1),
+    (lambda L: L.moe_route(None, FAKE, None, 16, 64, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, None), 1),
+    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 64, 8, 2, 2, FAKE, FAKE, FAKE, FAKE, None), 1),
+    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 60, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, None), 2),
+    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 64, 300, 2, 1, FAKE, FAKE, FAKE, FAKE, None), 2),
+    (lambda L: L.moe_route(FAKE, FAKE, None, 0, 64, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, None), 1),
     (lambda L: L.moe_route(ctypes.c_void_p((1 << 20) + 2), FAKE, None, 16, 64, 8, 2, 1, FAKE,
-                           FAKE, FAKE, None), 1),
+                           FAKE, FAKE, FAKE, None), 1),
+    (lambda L: L.moe_route(FAKE, FAKE, None, 16, 64, 8, 2, 1, None, FAKE, FAKE, FAKE, None), 1),
     (lambda L: L.moe_route_logits(FAKE, 16, 8, 9, 1, FAKE, FAKE, FAKE, None), 2),
     (lambda L: L.moe_permute(FAKE, None, 16, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8,
                              None), 3),

@@ -69,6 +69,10 @@ ROUTE_CASES = [
     (300, 96, 64, 6, False),
     (129, 200, 16, 1, True),
     (65, 64, 200, 8, False),
+    (100, 256, 100, 4, True),     # E not a multiple of 64: partial expert tile
+    (40, 1024, 33, 2, False),     # smallest tiled E, scalar weight loads
+    (1000, 512, 32, 4, False),    # largest per-thread-chain E
+    (3000, 1000, 12, 3, False),   # chain kernel, d not a multiple of its stage
 ]
 
 
@@ -77,11 +81,14 @@ def test_route_from_activations(T, d, E, K, zipf):
     X = synth.normal("X", (T, d), 1.0, torch.bfloat16, "cuda")
     Wr = synth.normal("Wr", (d, E), 1.0 / math.sqrt(d), torch.float32, "cuda")
     bias = synth.zipf_bias(E).cuda() if zipf else None
-    idx, w, counts = moe.moe_route(X, Wr, K, bias)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx, w, counts = moe.moe_route(X, Wr, K, bias, logits=logits)
     torch.cuda.synchronize()
     Xn, Wn = bits(X), Wr.cpu().numpy()
     bn = None if bias is None else bias.cpu().numpy()
     L = oracle.router_logits(Xn, Wn, bn)
+    # the logits themselves are the sequential fp32 chain: identical bits
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), L.view(np.uint32))
     idx_r, w_r = oracle.topk_softmax(L, K, True)
     _check_routing(idx, w, counts, idx_r, w_r, E)
 
@@ -103,6 +110,20 @@ def test_route_zero_activations_and_exact_ties():
     L = oracle.router_logits(bits(Xi), Wi.numpy())
     idx_r, w_r = oracle.topk_softmax(L, K, True)
     _check_routing(idx, w, counts, idx_r, w_r, E)
+
+
+def test_route_unaligned_router_weights():
+    # Wr starting 4 bytes into an allocation: the kernels must not use 16-byte loads
+    for T, d, E, K in ((64, 128, 64, 4), (50, 256, 8, 2)):
+        X = synth.normal("X", (T, d), 1.0, torch.bfloat16, "cuda")
+        big = synth.normal("Wr", (d * E + 1,), 0.1, torch.float32, "cuda")
+        Wr = big[1:].view(d, E)
+        assert Wr.data_ptr() % 16 == 4
+        logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        moe.moe_route(X, Wr, K, logits=logits)
+        torch.cuda.synchronize()
+        L = oracle.router_logits(bits(X), Wr.cpu().numpy())
+        assert np.array_equal(logits.cpu().numpy().view(np.uint32), L.view(np.uint32))
 
 
 def test_route_rejects_bad_arguments():

@@ -108,6 +108,7 @@ WsLayout ws_layout(int T, int d, int E, int K, int n) {
     L.xg = take(2 * R * (size_t)d);
     L.h = take(2 * R * (size_t)n);
     L.z = take(2 * R * (size_t)d);
+    L.logits = take(4 * (size_t)T * E);
     L.total = off;
     return L;
 }
@@ -145,16 +146,16 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
 }
 
 moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias, int T, int d, int E,
-                       int K, int renorm, int32_t *topk_idx, float *topk_w, int32_t *counts,
-                       void *stream) {
-    if (!X || !Wr || !topk_idx || !topk_w || !counts || (renorm != 0 && renorm != 1))
+                       int K, int renorm, float *logits, int32_t *topk_idx, float *topk_w,
+                       int32_t *counts, void *stream) {
+    if (!X || !Wr || !logits || !topk_idx || !topk_w || !counts || (renorm != 0 && renorm != 1))
         return MOE_ERR_INVALID_ARG;
     moe_status_t s = check_route_shape(T, d, E, K);
     if (s != MOE_OK) return s;
     if (!aligned16(X)) return MOE_ERR_INVALID_ARG;
     if ((s = check_arch()) != MOE_OK) return s;
     return from_cuda(launch_route(reinterpret_cast<const __nv_bfloat16 *>(X), Wr, bias, T, d, E, K,
-                                  renorm, topk_idx, topk_w, counts, nullptr, as_stream(stream)));
+                                  renorm, logits, topk_idx, topk_w, counts, as_stream(stream)));
 }
 
 moe_status_t moe_route_logits(const float *logits, int T, int E, int K, int renorm,
@@ -290,7 +291,8 @@ moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float 
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(X);
 
     if (!mark()) return MOE_ERR_CUDA;
-    if (launch_route(x, Wr, bias, T, d, E, K, renorm, idx, w, counts, err, st) != cudaSuccess ||
+    if (launch_route(x, Wr, bias, T, d, E, K, renorm, at<float>(ws, L.logits), idx, w, counts,
+                     st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
     if (launch_permute(idx, counts, T, E, K, offsets, perm_token, perm_slot, row_of_slot,

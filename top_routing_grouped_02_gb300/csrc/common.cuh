@@ -38,6 +38,7 @@ struct WsLayout {
     size_t xg;          // bf16  [R, d]  gathered activation rows
     size_t h;           // bf16  [R, n]
     size_t z;           // bf16  [R, d]
+    size_t logits;      // fp32  [T, E] router logits (moe_forward only)
     size_t total;
     int nchunks;
     int max_tiles;
@@ -50,8 +51,10 @@ WsLayout ws_layout(int T, int d, int E, int K, int n);
 
 // ---- launchers (each returns the CUDA error of its launch) -----------------
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
-                         int d, int E, int K, int renorm, int32_t *idx, float *w,
-                         int32_t *counts, uint32_t *err, cudaStream_t s);
+                         int d, int E, int K, int renorm, float *logits, int32_t *idx, float *w,
+                         int32_t *counts, cudaStream_t s);
+cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const float *bias,
+                                 int T, int d, int E, float *L, cudaStream_t s);
 cudaError_t launch_route_logits(const float *logits, int T, int E, int K, int renorm,
                                 int32_t *idx, float *w, int32_t *counts, cudaStream_t s);
 cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, int E, int K,

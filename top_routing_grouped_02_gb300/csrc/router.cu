@@ -1,21 +1,29 @@
 // Router: logits -> softmax -> top-K -> renormalised weights -> per-expert counts.
 //
-// Pages: "Triton优化MoE模型：topk_gating算子融合实战" §2.1 (one fused pass: logits,
-// online softmax, local top-k, cross-warp merge, output), §2.2 (max-subtracted
-// softmax and top-2 in one kernel), §4.1 (subtract the maximum first), §4.2
-// (per-expert counts with atomics, bucketed); "混合专家模型(MoE)架构优化与SonicMoE实践"
-// §1 (E scores per token, keep the best K), §3.2 (renormalise the kept scores);
-// "Triton GPU 内核编程实战：用 Python 写高性能 AI 推理算子" §5.2 (the online softmax
-// recurrence m_new = max(m_old, .), l_new = e^(m_old-m_new) l_old + sum e^(s-m_new)).
+// Pages: "Triton优化MoE模型：topk_gating算子融合实战" §2.1 (logits, online softmax,
+// local top-k, cross-warp merge, output), §2.2 (max-subtracted softmax and top-2),
+// §4.1 (subtract the maximum first), §4.2 (per-expert counts with atomics,
+// bucketed per block); "混合专家模型(MoE)架构优化与SonicMoE实践" §1 (E scores per
+// token, keep the best K), §3.2 (renormalise the kept scores); "Triton GPU 内核编程
+// 实战：用 Python 写高性能 AI 推理算子" §5.2 (online softmax recurrence
+// m_new = max(m_old, s), l_new = e^(m_old - m_new) l_old + e^(s - m_new)).
 //
-// Logits are computed as a register-tiled SIMT product: every (token, expert)
-// accumulator is one fp32 fused multiply-add chain over j = 0..d-1 in ascending
-// order from +0.0f, followed by one fp32 add of the bias. That order is the
-// definition the results are pinned to, so the logits (and hence the top-K
-// indices) are bit-identical to a sequential evaluation. The chain cannot be
-// split across threads or tensor-core instructions without changing the
-// rounding, so the kernel keeps whole chains per thread and gets its
-// parallelism from tokens x experts.
+// Two kernels:
+//  1. logits: L[t,e] = fp32 fused multiply-add chain over j = 0..d-1 in ascending
+//     order from +0.0f, then one fp32 add of bias[e]. That order is the definition
+//     the results are pinned to, so L (and hence the top-K indices) is
+//     bit-identical to a sequential evaluation. The chain cannot be split over
+//     threads or tensor-core instructions without changing the rounding, so every
+//     chain stays in one thread and parallelism comes from tokens x experts:
+//       - E <= 32: one thread per (token, expert) chain fed from a cp.async
+//         shared-memory pipeline; bound by the latency of d dependent FMAs.
+//       - E > 32: one-warp blocks on 32-token x 64-expert tiles, 8x8 register
+//         micro-tiles fed by conflict-free float4 shared-memory reads; bound by
+//         the FP32 FMA pipe.
+//  2. select: one warp per token reads its E logits, merges (max, sum of exp)
+//     across lanes with the online recurrence, picks K by repeated warp argmax
+//     (ties -> lower index), writes indices and weights, and counts per expert in
+//     a block histogram flushed with one atomic per (block, expert).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -24,244 +32,321 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kBK = 32;  // reduction steps staged in shared memory per pass
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-// Block / thread tiling of the logit product for a padded expert count EP.
+// ---- E <= 32: one thread per (token, expert) chain --------------------------
+// Block: 128 threads = NT tokens x EP experts. Stages of JC reduction steps:
+// the block's NT rows of X (bf16) and JC rows of Wr (fp32) are copied to shared
+// memory with cp.async, 4 stages deep. Each stage is then widened once into fp32
+// x [NT][JC+4] and transposed weights w [EP][JC+4], so the chain's inner loop is
+// two conflict-free float4 reads per 4 fused multiply-adds.
+// Requires d % 8 == 0, E % 4 == 0 and a 16-byte-aligned Wr.
+constexpr int kChainThreads = 128;
+constexpr int kChainStages = 4;
+
 template <int EP>
-struct RouterTile {
-    static constexpr bool kNarrow = EP <= 32;
-    static constexpr int TE = kNarrow ? EP / 8 : 8;          // experts per thread
-    static constexpr int TX = EP / TE;                        // threads along experts
-    static constexpr int TY = kThreads / TX;                  // threads along tokens
-    static constexpr int TT = kNarrow ? 1 : (EP >= 128 ? 4 : 2);  // tokens per thread
-    static constexpr int BT = TY * TT;                        // tokens per block
-    static constexpr int WTX = kNarrow ? 8 : 4;               // warp shape (experts)
-    static constexpr int WTY = 32 / WTX;                      // warp shape (tokens)
-    static constexpr int NWX = TX / WTX;                      // warps along experts
-    static constexpr int LS = EP + 4;                         // logit row stride (smem)
-    static constexpr size_t kStageFloats = (size_t)kBK * BT + (size_t)kBK * EP;
-    static constexpr size_t kLogitFloats = (size_t)BT * LS;
-    static constexpr size_t kSmemFloats = kStageFloats > kLogitFloats ? kStageFloats : kLogitFloats;
-    static_assert(TX * TY == kThreads, "tiling");
-    static_assert(TX % WTX == 0 && TY % WTY == 0, "warp tiling");
+struct ChainCfg {
+    static constexpr int NT = kChainThreads / EP;        // tokens per block
+    static constexpr int JC = EP >= 32 ? 128 : 256;      // reduction steps per stage
+    static constexpr int RXBYTES = NT * JC * 2;          // raw X rows (bf16)
+    static constexpr int RWBYTES = JC * EP * 4;          // raw Wr rows (EP floats each)
+    static constexpr int RSTAGE = RXBYTES + RWBYTES;
+    static constexpr int LD = JC + 4;                    // widened row length (floats)
+    static constexpr int SMEM = kChainStages * RSTAGE + (NT + EP) * LD * 4;
 };
+
+template <int EP>
+__global__ void __launch_bounds__(kChainThreads)
+logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
+                    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    using C = ChainCfg<EP>;
+    extern __shared__ __align__(16) unsigned char sm[];
+    float *xf = reinterpret_cast<float *>(sm + kChainStages * C::RSTAGE);  // [NT][LD]
+    float *wt = xf + C::NT * C::LD;                                          // [EP][LD]
+    const int tid = threadIdx.x;
+    const int e = tid % EP, tl = tid / EP;
+    const int64_t t0 = (int64_t)blockIdx.x * C::NT;
+    const int nst = (d + C::JC - 1) / C::JC;
+
+    auto issue = [&](int st) {
+        unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
+        unsigned char *ws = xs + C::RXBYTES;
+        const int j0 = st * C::JC;
+        for (int q = tid; q < C::NT * (C::JC / 8); q += kChainThreads) {
+            const int r = q / (C::JC / 8), c = q % (C::JC / 8);
+            const int64_t t = t0 + r;
+            const int j = j0 + c * 8;
+            if (t < T && j < d) cp_async16(xs + r * (C::JC * 2) + c * 16, X + t * d + j);
+        }
+        for (int q = tid; q < C::JC * (EP / 4); q += kChainThreads) {
+            const int jj = q / (EP / 4), c4 = (q % (EP / 4)) * 4;
+            const int j = j0 + jj;
+            if (j < d && c4 < E) cp_async16(ws + (jj * EP + c4) * 4, Wr + (int64_t)j * E + c4);
+        }
+    };
+
+    for (int st = 0; st < kChainStages - 1; ++st) {
+        if (st < nst) issue(st);
+        cp_async_commit();
+    }
+    const int ec = e < E ? e : 0;
+    const float4 *xrow = reinterpret_cast<const float4 *>(xf + tl * C::LD);
+    const float4 *wrow = reinterpret_cast<const float4 *>(wt + ec * C::LD);
+    float acc = 0.f;
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait<kChainStages - 2>();
+        __syncthreads();  // raw stage st landed; the previous stage's compute is done
+        if (st + kChainStages - 1 < nst) issue(st + kChainStages - 1);
+        cp_async_commit();
+        {
+            const unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
+            const float *ws = reinterpret_cast<const float *>(xs + C::RXBYTES);
+            for (int q = tid; q < C::NT * (C::JC / 8); q += kChainThreads) {
+                const int r = q / (C::JC / 8), c = q % (C::JC / 8);
+                const uint4 raw = *reinterpret_cast<const uint4 *>(xs + r * (C::JC * 2) + c * 16);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                float4 *dst = reinterpret_cast<float4 *>(xf + r * C::LD + c * 8);
+                const float2 a = __bfloat1622float2(h2[0]), b = __bfloat1622float2(h2[1]);
+                const float2 c2 = __bfloat1622float2(h2[2]), d2 = __bfloat1622float2(h2[3]);
+                dst[0] = make_float4(a.x, a.y, b.x, b.y);
+                dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
+            }
+            for (int jj = tid; jj < C::JC; jj += kChainThreads) {
+#pragma unroll
+                for (int c4 = 0; c4 < EP; c4 += 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(ws + jj * EP + c4);
+                    wt[(c4 + 0) * C::LD + jj] = v.x;
+                    wt[(c4 + 1) * C::LD + jj] = v.y;
+                    wt[(c4 + 2) * C::LD + jj] = v.z;
+                    wt[(c4 + 3) * C::LD + jj] = v.w;
+                }
+            }
+        }
+        __syncthreads();
+        const int jn = min(C::JC, d - st * C::JC);  // a multiple of 8
+        if (jn == C::JC) {
+#pragma unroll 8
+            for (int v = 0; v < C::JC / 4; ++v) {
+                const float4 xv = xrow[v], wv = wrow[v];
+                acc = __fmaf_rn(xv.x, wv.x, acc);
+                acc = __fmaf_rn(xv.y, wv.y, acc);
+                acc = __fmaf_rn(xv.z, wv.z, acc);
+                acc = __fmaf_rn(xv.w, wv.w, acc);
+            }
+        } else {
+            for (int v = 0; v < jn / 4; ++v) {
+                const float4 xv = xrow[v], wv = wrow[v];
+                acc = __fmaf_rn(xv.x, wv.x, acc);
+                acc = __fmaf_rn(xv.y, wv.y, acc);
+                acc = __fmaf_rn(xv.z, wv.z, acc);
+                acc = __fmaf_rn(xv.w, wv.w, acc);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    const int64_t t = t0 + tl;
+    if (t < T && e < E) {
+        if (bias != nullptr) acc = __fadd_rn(acc, __ldg(bias + e));
+        L[t * E + e] = acc;
+    }
+}
+
+// Fallback for E <= 32 with E % 4 != 0 (or an unaligned Wr): operands straight
+// from global memory, one thread per (token, expert).
+constexpr int kSmallThreads = 64;
+
+template <int EP>
+__global__ void __launch_bounds__(kSmallThreads)
+logits_small_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
+                    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    constexpr int kTok = kSmallThreads / EP;
+    const int e = threadIdx.x % EP;
+    const int64_t t = (int64_t)blockIdx.x * kTok + threadIdx.x / EP;
+    if (t >= T) return;
+    const int ec = e < E ? e : E - 1;  // padding lanes compute a copy and store nothing
+    const uint4 *xr = reinterpret_cast<const uint4 *>(X + t * d);
+    const float *wc = Wr + ec;
+    float acc = 0.f;
+    const int nv = d / 8;
+#pragma unroll 4
+    for (int v = 0; v < nv; ++v) {
+        const uint4 raw = __ldg(xr + v);
+        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        float w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) w[u] = __ldg(wc + (int64_t)(8 * v + u) * E);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(h2[u]);
+            acc = __fmaf_rn(f.x, w[2 * u], acc);
+            acc = __fmaf_rn(f.y, w[2 * u + 1], acc);
+        }
+    }
+    if (e < E) {
+        if (bias != nullptr) acc = __fadd_rn(acc, __ldg(bias + e));
+        L[t * E + e] = acc;
+    }
+}
+
+// ---- E > 32: register-tiled product ------------------------------------------
+// One warp per block; block tile 32 tokens x 64 experts, so a launch has
+// ceil(T/32) * ceil(E/64) small blocks and the SMs stay evenly loaded. Lane
+// (ty, tx) = (lane / 8, lane % 8) owns tokens {4ty..4ty+3, 16+4ty..16+4ty+3} and
+// experts {4tx..4tx+3, 32+4tx..32+4tx+3}: per reduction step it reads two
+// float4 of x and two float4 of weights, each conflict-free (a half-warp touches
+// 2 distinct x addresses and 128 contiguous bytes of weights), then does 64 FMAs.
+// 32-step stages are double-buffered: weights by cp.async, x through registers
+// (converted to fp32 and transposed on the way into shared memory).
+constexpr int kWT = 32;  // tokens per block tile
+constexpr int kWE = 64;  // experts per block tile
+constexpr int kWK = 32;  // reduction steps per stage
+
+template <bool VEC>
+__global__ void __launch_bounds__(32)
+logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
+                    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    __shared__ __align__(16) float xs[2][kWK][kWT];
+    __shared__ __align__(16) float ws[2][kWK][kWE];
+    const int lane = threadIdx.x;
+    const int ty = lane >> 3, tx = lane & 7;
+    const int64_t t0 = (int64_t)blockIdx.x * kWT;
+    const int e0 = blockIdx.y * kWE;
+    const int nchunk = (d + kWK - 1) / kWK;
+
+    uint4 xr[4];  // token t0+lane, 32 consecutive j
+    auto load_x = [&](int c) {
+        const int j0 = c * kWK;
+        const int64_t t = t0 + lane;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (t < T && j0 + 8 * i < d)
+                xr[i] = __ldg(reinterpret_cast<const uint4 *>(X + t * d + j0 + 8 * i));
+            else
+                xr[i] = make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto store_x = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&xr[i]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                xs[buf][8 * i + 2 * u][lane] = f.x;
+                xs[buf][8 * i + 2 * u + 1][lane] = f.y;
+            }
+        }
+    };
+    // weights: 32 rows j x 64 experts = 512 x 16 B, 16 per lane
+    auto issue_w = [&](int c, int buf) {
+        const int j0 = c * kWK;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int q = lane + 32 * i;
+            const int jj = q >> 4, e4 = (q & 15) * 4;
+            const int j = j0 + jj, e = e0 + e4;
+            if (j >= d) continue;
+            const float *src = Wr + (int64_t)j * E + e;
+            if (VEC) {
+                if (e < E) cp_async16(&ws[buf][jj][e4], src);
+            } else {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (e + 0 < E) v.x = __ldg(src + 0);
+                if (e + 1 < E) v.y = __ldg(src + 1);
+                if (e + 2 < E) v.z = __ldg(src + 2);
+                if (e + 3 < E) v.w = __ldg(src + 3);
+                *reinterpret_cast<float4 *>(&ws[buf][jj][e4]) = v;
+            }
+        }
+        cp_async_commit();
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+
+    issue_w(0, 0);
+    load_x(0);
+    store_x(0);
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int c = 0; c < nchunk; ++c) {
+        const int buf = c & 1;
+        if (c + 1 < nchunk) {
+            issue_w(c + 1, buf ^ 1);
+            load_x(c + 1);
+        }
+        const int jn = min(kWK, d - c * kWK);
+        auto step = [&](int jj) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(&xs[buf][jj][4 * ty]);
+            const float4 x1 = *reinterpret_cast<const float4 *>(&xs[buf][jj][16 + 4 * ty]);
+            const float4 w0 = *reinterpret_cast<const float4 *>(&ws[buf][jj][4 * tx]);
+            const float4 w1 = *reinterpret_cast<const float4 *>(&ws[buf][jj][32 + 4 * tx]);
+            const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) acc[a][b] = __fmaf_rn(xa[a], wb[b], acc[a][b]);
+        };
+        if (jn == kWK) {
+#pragma unroll 4
+            for (int jj = 0; jj < kWK; ++jj) step(jj);
+        } else {
+            for (int jj = 0; jj < jn; ++jj) step(jj);
+        }
+        if (c + 1 < nchunk) {
+            store_x(buf ^ 1);
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const int64_t t = t0 + (a < 4 ? 4 * ty + a : 16 + 4 * ty + a - 4);
+        if (t >= T) continue;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int e = e0 + (b < 4 ? 4 * tx + b : 32 + 4 * tx + b - 4);
+            if (e < E) {
+                float v = acc[a][b];
+                if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
+                L[t * E + e] = v;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- select --
+
+constexpr int kSelThreads = 256;
 
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
     // higher score wins; equal scores: lower expert index wins
     return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
-// Softmax + top-K + weights + histogram for one token whose E logits are held
-// by the warp: lane l owns experts l, l+32, ... (NPL per lane; -inf padding).
+// One warp per token: lane l holds experts l, l+32, ... (NPL per lane).
 template <int NPL>
-__device__ __forceinline__ void select_topk_warp(float (&v)[NPL], int E, int K, int renorm,
-                                                 int64_t t, int32_t *idx_out, float *w_out,
-                                                 int *hist) {
-    const int lane = threadIdx.x & 31;
-    // online softmax statistics (max, sum of exp) per lane, merged across the warp
-    float m = -INFINITY, s = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-        int e = lane + 32 * i;
-        if (e < E) {
-            float mn = fmaxf(m, v[i]);
-            s = s * __expf(m - mn) + __expf(v[i] - mn);
-            m = mn;
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        float mo = __shfl_xor_sync(0xffffffffu, m, off);
-        float so = __shfl_xor_sync(0xffffffffu, s, off);
-        float mn = fmaxf(m, mo);
-        float a = (m == -INFINITY) ? 0.f : s * expf(m - mn);
-        float b = (mo == -INFINITY) ? 0.f : so * expf(mo - mn);
-        s = a + b;
-        m = mn;
-    }
-    bool taken[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) taken[i] = (lane + 32 * i) >= E;
-    int sel_idx[kMaxK];
-    float sel_val[kMaxK];
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        if (k < K) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < NPL; ++i) {
-                int e = lane + 32 * i;
-                if (!taken[i] && better(v[i], e, bv, bi)) {
-                    bv = v[i];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (better(ov, oi, bv, bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < NPL; ++i)
-                if (lane + 32 * i == bi) taken[i] = true;
-            sel_idx[k] = bi;
-            sel_val[k] = bv;
-        }
-    }
-    // weights: exp(L_k - max) over the kept sum (renormalised) or the full sum
-    const float mtop = sel_val[0];
-    float kept = 0.f;
-    float ex[kMaxK];
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        if (k < K) {
-            ex[k] = expf(sel_val[k] - mtop);
-            kept += ex[k];
-        }
-    }
-    const float full = s * expf(m - mtop);  // m == mtop; kept for clarity
-    const float denom = renorm ? kept : full;
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        if (k < K && lane == k) {
-            idx_out[t * K + k] = sel_idx[k];
-            w_out[t * K + k] = ex[k] / denom;
-            atomicAdd(&hist[sel_idx[k]], 1);
-        }
-    }
-}
-
-template <int EP>
-__global__ void __launch_bounds__(kThreads)
-router_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
-              const float *__restrict__ bias, int T, int d, int E, int K, int renorm,
+__global__ void __launch_bounds__(kSelThreads)
+select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
               int32_t *__restrict__ idx_out, float *__restrict__ w_out,
               int32_t *__restrict__ counts) {
-    using C = RouterTile<EP>;
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int hist[EP];
-    float *xs = smem;                    // [kBK][BT]  x values, j-major
-    float *ws = smem + kBK * C::BT;      // [kBK][EP]  router weights
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int wx = warp % C::NWX, wy = warp / C::NWX;
-    const int tx = wx * C::WTX + lane % C::WTX;
-    const int ty = wy * C::WTY + lane / C::WTX;
-    const int64_t t0 = (int64_t)blockIdx.x * C::BT;
-
-    for (int e = tid; e < EP; e += kThreads) hist[e] = 0;
-
-    float acc[C::TT][C::TE];
-#pragma unroll
-    for (int a = 0; a < C::TT; ++a)
-#pragma unroll
-        for (int b = 0; b < C::TE; ++b) acc[a][b] = 0.f;
-
-    for (int j0 = 0; j0 < d; j0 += kBK) {
-        const int jn = min(kBK, d - j0);
-        // stage x: BT tokens x jn columns (8 bf16 per 16-byte load), transposed
-        for (int q = tid; q < C::BT * (kBK / 8); q += kThreads) {
-            const int tt = q / (kBK / 8), c8 = (q % (kBK / 8)) * 8;
-            const int64_t t = t0 + tt;
-            float f[8];
-            if (t < T && c8 < jn) {
-                uint4 raw = *reinterpret_cast<const uint4 *>(X + t * d + j0 + c8);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float2 p = __bfloat1622float2(h2[u]);
-                    f[2 * u] = p.x;
-                    f[2 * u + 1] = p.y;
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) f[u] = 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) xs[(c8 + u) * C::BT + tt] = f[u];
-        }
-        // stage Wr rows j0..j0+jn-1 (zero padding for experts >= E)
-        for (int q = tid; q < kBK * EP; q += kThreads) {
-            const int jj = q / EP, e = q % EP;
-            ws[q] = (jj < jn && e < E) ? __ldg(Wr + (int64_t)(j0 + jj) * E + e) : 0.f;
-        }
-        __syncthreads();
-        if (jn == kBK) {
-#pragma unroll 8
-            for (int jj = 0; jj < kBK; ++jj) {
-                float xv[C::TT], wv[C::TE];
-#pragma unroll
-                for (int a = 0; a < C::TT; ++a) xv[a] = xs[jj * C::BT + ty * C::TT + a];
-#pragma unroll
-                for (int b = 0; b < C::TE; ++b) wv[b] = ws[jj * EP + tx * C::TE + b];
-#pragma unroll
-                for (int a = 0; a < C::TT; ++a)
-#pragma unroll
-                    for (int b = 0; b < C::TE; ++b) acc[a][b] = __fmaf_rn(xv[a], wv[b], acc[a][b]);
-            }
-        } else {
-            for (int jj = 0; jj < jn; ++jj) {
-                float xv[C::TT], wv[C::TE];
-#pragma unroll
-                for (int a = 0; a < C::TT; ++a) xv[a] = xs[jj * C::BT + ty * C::TT + a];
-#pragma unroll
-                for (int b = 0; b < C::TE; ++b) wv[b] = ws[jj * EP + tx * C::TE + b];
-#pragma unroll
-                for (int a = 0; a < C::TT; ++a)
-#pragma unroll
-                    for (int b = 0; b < C::TE; ++b) acc[a][b] = __fmaf_rn(xv[a], wv[b], acc[a][b]);
-            }
-        }
-        __syncthreads();
-    }
-
-    // logits tile -> shared memory, bias added as one fp32 add
-    float *ls = smem;  // [BT][LS]
-#pragma unroll
-    for (int a = 0; a < C::TT; ++a)
-#pragma unroll
-        for (int b = 0; b < C::TE; ++b) {
-            const int e = tx * C::TE + b;
-            float v = acc[a][b];
-            if (bias != nullptr && e < E) v = __fadd_rn(v, __ldg(bias + e));
-            ls[(ty * C::TT + a) * C::LS + e] = v;
-        }
-    __syncthreads();
-
-    constexpr int NPL = EP >= 32 ? EP / 32 : 1;
-    for (int tt = warp; tt < C::BT; tt += kThreads / 32) {
-        const int64_t t = t0 + tt;
-        if (t >= T) break;
-        float v[NPL];
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = (e < E) ? ls[tt * C::LS + e] : -INFINITY;
-        }
-        select_topk_warp<NPL>(v, E, K, renorm, t, idx_out, w_out, hist);
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kThreads)
-        if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
-}
-
-// Router from given logits: one warp per token row.
-template <int NPL>
-__global__ void __launch_bounds__(kThreads)
-router_logits_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
-                     int32_t *__restrict__ idx_out, float *__restrict__ w_out,
-                     int32_t *__restrict__ counts) {
     __shared__ int hist[kMaxE];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = tid; e < kMaxE; e += kThreads) hist[e] = 0;
+    for (int e = tid; e < kMaxE; e += kSelThreads) hist[e] = 0;
     __syncthreads();
-    const int64_t t = (int64_t)blockIdx.x * (kThreads / 32) + warp;
+    const int64_t t = (int64_t)blockIdx.x * (kSelThreads / 32) + warp;
     if (t < T) {
         float v[NPL];
 #pragma unroll
@@ -269,58 +354,160 @@ router_logits_kernel(const float *__restrict__ logits, int T, int E, int K, int 
             const int e = lane + 32 * i;
             v[i] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
         }
-        select_topk_warp<NPL>(v, E, K, renorm, t, idx_out, w_out, hist);
+        // online softmax statistics (max, sum of exp) per lane, merged over the warp
+        float m = -INFINITY, s = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            if (lane + 32 * i < E) {
+                const float mn = fmaxf(m, v[i]);
+                s = s * expf(m - mn) + expf(v[i] - mn);
+                m = mn;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+            const float so = __shfl_xor_sync(0xffffffffu, s, off);
+            const float mn = fmaxf(m, mo);
+            const float a = (m == -INFINITY) ? 0.f : s * expf(m - mn);
+            const float b = (mo == -INFINITY) ? 0.f : so * expf(mo - mn);
+            s = a + b;
+            m = mn;
+        }
+        bool taken[NPL];
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) taken[i] = (lane + 32 * i) >= E;
+        int sel_idx[kMaxK];
+        float sel_val[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k < K) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < NPL; ++i) {
+                    const int e = lane + 32 * i;
+                    if (!taken[i] && better(v[i], e, bv, bi)) {
+                        bv = v[i];
+                        bi = e;
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                    if (better(ov, oi, bv, bi)) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NPL; ++i)
+                    if (lane + 32 * i == bi) taken[i] = true;
+                sel_idx[k] = bi;
+                sel_val[k] = bv;
+            }
+        }
+        // weights: exp(L_k - max) over the kept sum (renormalised) or the full sum
+        const float mtop = sel_val[0];
+        float kept = 0.f, ex[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k < K) {
+                ex[k] = expf(sel_val[k] - mtop);
+                kept += ex[k];
+            }
+        }
+        const float denom = renorm ? kept : s * expf(m - mtop);
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k < K && lane == k) {
+                idx_out[t * K + k] = sel_idx[k];
+                w_out[t * K + k] = ex[k] / denom;
+                atomicAdd(&hist[sel_idx[k]], 1);
+            }
+        }
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kThreads)
+    for (int e = tid; e < E; e += kSelThreads)
         if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
 }
 
+cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, int32_t *idx,
+                          float *w, int32_t *counts, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = (unsigned)((T + kSelThreads / 32 - 1) / (kSelThreads / 32));
+    if (E <= 32)
+        select_kernel<1><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
+    else if (E <= 64)
+        select_kernel<2><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
+    else if (E <= 128)
+        select_kernel<4><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
+    else
+        select_kernel<8><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
+    return cudaGetLastError();
+}
+
 template <int EP>
-cudaError_t launch_router_ep(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
-                             int d, int E, int K, int renorm, int32_t *idx, float *w,
-                             int32_t *counts, cudaStream_t s) {
-    using C = RouterTile<EP>;
-    const size_t smem = C::kSmemFloats * sizeof(float);
-    cudaError_t err = cudaFuncSetAttribute(router_kernel<EP>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    const int blocks = (T + C::BT - 1) / C::BT;
-    router_kernel<EP><<<blocks, kThreads, smem, s>>>(X, Wr, bias, T, d, E, K, renorm, idx, w,
-                                                     counts);
+cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T, int d,
+                         int E, float *L, cudaStream_t s) {
+    using C = ChainCfg<EP>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(logits_chain_kernel<EP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const unsigned grid = (unsigned)((T + C::NT - 1) / C::NT);
+    logits_chain_kernel<EP><<<grid, kChainThreads, C::SMEM, s>>>(X, Wr, bias, T, d, E, L);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const float *bias,
+                                 int T, int d, int E, float *L, cudaStream_t s) {
+    const bool wr16 = (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
+    if (E <= 32 && E % 4 == 0 && wr16) {
+        if (E <= 8) return launch_chain<8>(X, Wr, bias, T, d, E, L, s);
+        if (E <= 16) return launch_chain<16>(X, Wr, bias, T, d, E, L, s);
+        return launch_chain<32>(X, Wr, bias, T, d, E, L, s);
+    }
+    if (E <= 32) {
+        auto grid = [&](int ep) {
+            return (unsigned)(((int64_t)T * ep + kSmallThreads - 1) / kSmallThreads);
+        };
+        if (E <= 8)
+            logits_small_kernel<8><<<grid(8), kSmallThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
+        else if (E <= 16)
+            logits_small_kernel<16><<<grid(16), kSmallThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
+        else
+            logits_small_kernel<32><<<grid(32), kSmallThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
+    } else {
+        const dim3 grid((unsigned)((T + kWT - 1) / kWT), (unsigned)((E + kWE - 1) / kWE));
+        if (E % 4 == 0 && wr16)
+            logits_tiled_kernel<true><<<grid, 32, 0, s>>>(X, Wr, bias, T, d, E, L);
+        else
+            logits_tiled_kernel<false><<<grid, 32, 0, s>>>(X, Wr, bias, T, d, E, L);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
-                         int d, int E, int K, int renorm, int32_t *idx, float *w,
-                         int32_t *counts, uint32_t *err, cudaStream_t s) {
-    (void)err;
-    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+                         int d, int E, int K, int renorm, float *logits, int32_t *idx, float *w,
+                         int32_t *counts, cudaStream_t s) {
+    cudaError_t e = launch_router_logits(X, Wr, bias, T, d, E, logits, s);
     if (e != cudaSuccess) return e;
-    if (E <= 8) return launch_router_ep<8>(X, Wr, bias, T, d, E, K, renorm, idx, w, counts, s);
-    if (E <= 16) return launch_router_ep<16>(X, Wr, bias, T, d, E, K, renorm, idx, w, counts, s);
-    if (E <= 32) return launch_router_ep<32>(X, Wr, bias, T, d, E, K, renorm, idx, w, counts, s);
-    if (E <= 64) return launch_router_ep<64>(X, Wr, bias, T, d, E, K, renorm, idx, w, counts, s);
-    if (E <= 128) return launch_router_ep<128>(X, Wr, bias, T, d, E, K, renorm, idx, w, counts, s);
-    return launch_router_ep<256>(X, Wr, bias, T, d, E, K, renorm, idx, w, counts, s);
+    return launch_select(logits, T, E, K, renorm, idx, w, counts, s);
 }
 
 cudaError_t launch_route_logits(const float *logits, int T, int E, int K, int renorm,
                                 int32_t *idx, float *w, int32_t *counts, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
-    if (e != cudaSuccess) return e;
-    const int blocks = (T + kThreads / 32 - 1) / (kThreads / 32);
-    if (E <= 32)
-        router_logits_kernel<1><<<blocks, kThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    else if (E <= 64)
-        router_logits_kernel<2><<<blocks, kThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    else if (E <= 128)
-        router_logits_kernel<4><<<blocks, kThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    else
-        router_logits_kernel<8><<<blocks, kThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    return cudaGetLastError();
+    return launch_select(logits, T, E, K, renorm, idx, w, counts, s);
 }
 
 }  // namespace moe

@@ -23,8 +23,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
           6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_CHECK"}
 # kernels each entry point launches (for launch accounting)
-LAUNCHES = {"moe_route": 1, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 2,
-            "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 8}
+LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 2,
+            "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 9}
 TILE_M = 128
 
 
@@ -44,7 +44,7 @@ _SIGS = {
     "moe_abi_version": (_I, []),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_workspace_init": (_I, [_P, _SZ, _P]),
-    "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_route_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
@@ -120,16 +120,20 @@ def moe_workspace_init(ws: torch.Tensor, stream=None):
     _check("moe_workspace_init", lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
 
 
-def moe_route(X, Wr, K: int, bias=None, renorm: bool = True, stream=None):
-    """(topk_idx [T,K] int32, topk_w [T,K] fp32, counts [E] int32)."""
+def moe_route(X, Wr, K: int, bias=None, renorm: bool = True, stream=None, logits=None):
+    """(topk_idx [T,K] int32, topk_w [T,K] fp32, counts [E] int32); the router
+    logits [T,E] fp32 land in `logits` (allocated when not given)."""
     T, d = X.shape
     E = Wr.shape[1]
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=X.device)
     idx = torch.empty((T, K), dtype=torch.int32, device=X.device)
     w = torch.empty((T, K), dtype=torch.float32, device=X.device)
     counts = torch.empty(E, dtype=torch.int32, device=X.device)
     _check("moe_route", lib().moe_route(
         _ptr(X, torch.bfloat16, "X"), _ptr(Wr, torch.float32, "Wr"), _ptr(bias, torch.float32, "bias"),
-        T, d, E, K, int(bool(renorm)), _ptr(idx), _ptr(w), _ptr(counts), _stream(stream)))
+        T, d, E, K, int(bool(renorm)), _ptr(logits, torch.float32, "logits"), _ptr(idx), _ptr(w),
+        _ptr(counts), _stream(stream)))
     return idx, w, counts
 
 
