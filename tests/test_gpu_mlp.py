@@ -12,6 +12,14 @@ from top_routing_grouped_02_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(params=["single", "pair"], autouse=True)
+def gemm_variant(request, monkeypatch):
+    # run every GEMM case on both kernels: one CTA per tile, and CTA pairs
+    # (cta_group::2) that the library otherwise picks only for large experts
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", "1" if request.param == "pair" else "0")
+    return request.param
+
 MLP_CASES = [
     # (T, d, E, K, n, zipf)
     (512, 256, 8, 2, 512, False),   # tiny workload

@@ -20,6 +20,13 @@
 // takes units b, b + gridDim.x, ...: CTAs running at the same time share one
 // expert's weight block through L2 while its few activation tiles stay hot.
 //
+// Two variants share the code. Single CTA: M=128 tiles, B tile 64x256 per stage
+// (48 KB stages, 4 deep). CTA pair (a cluster of 2 CTAs on one SM pair,
+// tcgen05 cta_group::2): the even CTA issues M=256 MMAs over both CTAs' 128 A
+// rows, each CTA loads half of B (32 KB stages, 6 deep), both CTAs' TMA loads
+// complete on the even CTA's barrier, MMA completion is multicast to both, and
+// both CTAs' epilogues release the accumulator to the even CTA.
+//
 // Warp roles (256 threads):
 //   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
 //               (MN-major, four 64-column boxes) per stage, 128-byte swizzle.
@@ -35,6 +42,7 @@
 // released, in-flight MMAs and TMA loads of a stopped role are drained.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -43,23 +51,40 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int BM = kTileM;  // 128 rows
+constexpr int BM = kTileM;  // 128 rows per CTA
 constexpr int BK = 64;      // reduction depth per stage (128 bytes of bf16)
 constexpr int BN = 256;     // accumulator columns per unit
-constexpr int kStages = 4;
-constexpr uint32_t kABytes = BM * BK * 2;               // 16 KB
-constexpr uint32_t kBBox = BK * 64 * 2;                 // 8 KB: 64 k-rows x 64 columns
-constexpr uint32_t kBBytes = 4 * kBBox;                 // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;     // 48 KB
-constexpr uint32_t kTmemCols = 2 * BN;                  // two accumulators
-constexpr uint32_t kIdesc = ptx::idesc_bf16(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+#ifndef MOE_GEMM_STAGES
+#define MOE_GEMM_STAGES 4
+#endif
+#ifndef MOE_GEMM_PAIR_STAGES
+#define MOE_GEMM_PAIR_STAGES 6
+#endif
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBBox = BK * 64 * 2;    // 8 KB: 64 k-rows x 64 columns
+constexpr uint32_t kTmemCols = 2 * BN;     // two accumulators
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kMaxStages = MOE_GEMM_STAGES > MOE_GEMM_PAIR_STAGES ? MOE_GEMM_STAGES
+                                                                   : MOE_GEMM_PAIR_STAGES;
+
+// Per-variant geometry. Single CTA: B tile 64 x 256 (four boxes), 48 KB stages.
+// CTA pair: each CTA holds its own 128 A rows and half of B (64 x 128, two
+// boxes), 32 KB stages, so the same shared memory holds more stages.
+template <bool PAIR>
+struct Geo {
+    static constexpr int kStages = PAIR ? MOE_GEMM_PAIR_STAGES : MOE_GEMM_STAGES;
+    static constexpr int kBBoxes = PAIR ? 2 : 4;
+    static constexpr uint32_t kStageBytes = kABytes + kBBoxes * kBBox;
+    static constexpr uint32_t kIdesc =
+        ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+    static constexpr uint32_t kTemptyCount = PAIR ? 8 : 4;  // epilogue warps signalling
+};
 
 enum Mode : int { kGateUp = 0, kDown = 1 };
 
 struct Ctl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -69,26 +94,33 @@ struct Ctl {
     int32_t scan[kThreads / 32 + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Ctl);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes + sizeof(Ctl);
+}
 
 struct GemmArgs {
-    const int32_t *offsets;  // [E+1] grouped row offsets
+    const int32_t *offsets;   // [E+1] grouped row offsets
     int E;
-    int R;                   // rows of A / out (T*K)
-    int Kdim;                // reduction length (d for gate/up, n for down)
-    int NB;                  // column blocks per row tile
-    __nv_bfloat16 *out;      // H [R, n] or Z [R, d]
-    int out_ld;              // row length of out (elements)
-    const float *topk_w;     // down only: routing weights [T*K]
-    const int32_t *perm_slot;// down only: slot of each grouped row
-    uint32_t *err;           // device error word
+    int R;                    // rows of A / out (T*K)
+    int Kdim;                 // reduction length (d for gate/up, n for down)
+    int NB;                   // column blocks per row tile
+    __nv_bfloat16 *out;       // H [R, n] or Z [R, d]
+    int out_ld;               // row length of out (elements)
+    const float *topk_w;      // down only: routing weights [T*K]
+    const int32_t *perm_slot; // down only: slot of each grouped row
+    uint32_t *err;            // device error word
 };
 
+template <bool PAIR>
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() {
+        return PAIR ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((spin & 63u) == 0 && ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, MOE_DEVERR_TIMEOUT);
             return false;
@@ -97,10 +129,12 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint
 }
 
 // Unit u -> (expert, column block, first row, rows). tile_base[e] counts the
-// 128-row tiles of experts before e; empty experts own no units.
+// work tiles of experts before e (128-row tiles, or pairs of them for a CTA
+// pair, whose CTA `rank` takes the pair's tile 2*pt + rank); empty experts own
+// no units. `rows` can be <= 0 for the second tile of an odd pair.
 __device__ __forceinline__ void decode_unit(int u, int NB, int E, const int32_t *tb,
-                                            const int32_t *off, int &e, int &nb, int &row0,
-                                            int &rows) {
+                                            const int32_t *off, int per_tile, int rank, int &e,
+                                            int &nb, int &row0, int &rows) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -110,8 +144,8 @@ __device__ __forceinline__ void decode_unit(int u, int NB, int E, const int32_t 
     const int m_e = tb[e + 1] - tb[e];
     const int local = u - tb[e] * NB;
     nb = local / m_e;
-    const int mt = local - nb * m_e;
-    row0 = off[e] + mt * BM;
+    const int pt = local - nb * m_e;
+    row0 = off[e] + (pt * per_tile + rank) * BM;
     rows = min(BM, off[e + 1] - row0);
 }
 
@@ -120,27 +154,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+    using G = Geo<PAIR>;
+    constexpr int S = G::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)kStages * kStageBytes);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)S * G::kStageBytes);
     const uint32_t smem_base = ptx::smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = args.E;
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int first_unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int unit_stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     // ---- setup: barriers, TMEM, tile bases --------------------------------
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&ctl->tfull[a]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), 4);
+            ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), G::kTemptyCount);
         }
         ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
         ptx::fence_barrier_init();
@@ -151,11 +191,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (MODE == kGateUp) ptx::prefetch_tensormap(&tmB1);
     }
     if (warp == 2) {
-        ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
+            ptx::tmem_relinquish();
+        }
     }
     {
-        // tile bases: exclusive scan of ceil(rows_e / 128) over experts
+        // work-tile bases: exclusive scan over experts of ceil(rows_e / 128)
+        // tiles (single CTA) or of ceil(tiles_e / 2) tile pairs (CTA pair)
         const int e = tid;
         int c = 0;
         bool bad = false;
@@ -164,6 +210,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ctl->offsets[e] = o0;
             bad = o0 < 0 || o1 < o0 || o1 > args.R || (e == 0 && o0 != 0);
             c = bad ? 0 : (o1 - o0 + BM - 1) / BM;
+            if (PAIR) c = (c + 1) / 2;
         }
         if (e == 0) ctl->offsets[E] = args.offsets[E];
         // offsets must be a non-decreasing split of [0, R); otherwise do no work
@@ -196,94 +243,126 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // peer barriers initialised, TMEM allocated
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const int NB = args.NB;
     const int total_units = ctl->tile_base[E] * NB;
     const int KB = args.Kdim / BK;
+    const int per_tile = PAIR ? 2 : 1;
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- TMA producer --
         uint32_t it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        for (int u = first_unit; u < total_units && ok; u += unit_stride) {
             int e, nb, row0, rows;
-            decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, e, nb, row0, rows);
+            decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, per_tile, rank, e, nb, row0, rows);
             const int wrow = e * args.Kdim;
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-                if (!bounded_wait(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, args.err)) {
+                const uint32_t s = it % S, ph = (it / S) & 1u;
+                if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, args.err)) {
                     ok = false;
                     break;
                 }
                 const uint32_t full = ptx::smem_addr(&ctl->full[s]);
-                const uint32_t sA = smem_base + s * kStageBytes, sB = sA + kABytes;
-                ptx::mbar_arrive_expect_tx(full, kStageBytes);
-                ptx::tma_load_2d(sA, &tmA, full, kb * BK, row0);
-                if (MODE == kGateUp) {
-                    ptx::tma_load_2d(sB + 0 * kBBox, &tmB0, full, nb * 128, wrow + kb * BK);
-                    ptx::tma_load_2d(sB + 1 * kBBox, &tmB0, full, nb * 128 + 64, wrow + kb * BK);
-                    ptx::tma_load_2d(sB + 2 * kBBox, &tmB1, full, nb * 128, wrow + kb * BK);
-                    ptx::tma_load_2d(sB + 3 * kBBox, &tmB1, full, nb * 128 + 64, wrow + kb * BK);
+                const uint32_t sA = smem_base + s * G::kStageBytes, sB = sA + kABytes;
+                const int ky = wrow + kb * BK;
+                if constexpr (PAIR) {
+                    // both CTAs' loads complete on the even CTA's barrier
+                    if (leader) ptx::mbar_arrive_expect_tx(full, 2 * G::kStageBytes);
+                    const uint32_t fullc = ptx::mapa(full, 0);
+                    ptx::tma_load_2d_pair(sA, &tmA, fullc, kb * BK, row0);
+                    if (MODE == kGateUp) {
+                        // even CTA: gate columns (W1), odd CTA: up columns (W3)
+                        const CUtensorMap *mb = leader ? &tmB0 : &tmB1;
+                        ptx::tma_load_2d_pair(sB, mb, fullc, nb * 128, ky);
+                        ptx::tma_load_2d_pair(sB + kBBox, mb, fullc, nb * 128 + 64, ky);
+                    } else {
+                        const int x0 = nb * BN + (int)rank * 128;
+                        ptx::tma_load_2d_pair(sB, &tmB0, fullc, x0, ky);
+                        ptx::tma_load_2d_pair(sB + kBBox, &tmB0, fullc, x0 + 64, ky);
+                    }
                 } else {
+                    ptx::mbar_arrive_expect_tx(full, G::kStageBytes);
+                    ptx::tma_load_2d(sA, &tmA, full, kb * BK, row0);
+                    if (MODE == kGateUp) {
+                        ptx::tma_load_2d(sB + 0 * kBBox, &tmB0, full, nb * 128, ky);
+                        ptx::tma_load_2d(sB + 1 * kBBox, &tmB0, full, nb * 128 + 64, ky);
+                        ptx::tma_load_2d(sB + 2 * kBBox, &tmB1, full, nb * 128, ky);
+                        ptx::tma_load_2d(sB + 3 * kBBox, &tmB1, full, nb * 128 + 64, ky);
+                    } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        ptx::tma_load_2d(sB + q * kBBox, &tmB0, full, nb * BN + q * 64,
-                                         wrow + kb * BK);
+                        for (int q = 0; q < 4; ++q)
+                            ptx::tma_load_2d(sB + q * kBBox, &tmB0, full, nb * BN + q * 64, ky);
+                    }
                 }
             }
         }
-        if (!ok) {
+        if (!ok && (!PAIR || leader)) {
             // drain the loads that may still be landing in shared memory
-            const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+            const uint32_t first = it > (uint32_t)S ? it - S : 0u;
             for (uint32_t j = first; j < it; ++j)
-                bounded_wait(ptx::smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1u, args.err);
+                bounded_wait<PAIR>(ptx::smem_addr(&ctl->full[j % S]), (j / S) & 1u, args.err);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer --
         uint32_t it = 0, uc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++uc) {
+        for (int u = first_unit; u < total_units && ok; u += unit_stride, ++uc) {
             const uint32_t a = uc & 1u, aph = (uc >> 1) & 1u;
-            if (!bounded_wait(ptx::smem_addr(&ctl->tempty[a]), aph ^ 1u, args.err)) {
+            if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->tempty[a]), aph ^ 1u, args.err)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + a * BN;
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-                if (!bounded_wait(ptx::smem_addr(&ctl->full[s]), ph, args.err)) {
+                const uint32_t s = it % S, ph = (it / S) & 1u;
+                if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->full[s]), ph, args.err)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sA = smem_base + s * kStageBytes, sB = sA + kABytes;
+                const uint32_t sA = smem_base + s * G::kStageBytes, sB = sA + kABytes;
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint64_t adesc = ptx::desc_sw128(sA + k * 32, 16, 1024);
                     const uint64_t bdesc = ptx::desc_sw128(sB + k * 2048, kBBox, 1024);
-                    ptx::tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0);
+                    if constexpr (PAIR)
+                        ptx::tc_mma_f16_pair(d_tmem, adesc, bdesc, G::kIdesc, (kb | k) != 0);
+                    else
+                        ptx::tc_mma_f16(d_tmem, adesc, bdesc, G::kIdesc, (kb | k) != 0);
                 }
-                ptx::tc_commit(ptx::smem_addr(&ctl->empty[s]));
+                if constexpr (PAIR)
+                    ptx::tc_commit_pair(ptx::smem_addr(&ctl->empty[s]), 0x3);
+                else
+                    ptx::tc_commit(ptx::smem_addr(&ctl->empty[s]));
             }
             if (!ok) break;
-            ptx::tc_commit(ptx::smem_addr(&ctl->tfull[a]));
+            if constexpr (PAIR)
+                ptx::tc_commit_pair(ptx::smem_addr(&ctl->tfull[a]), 0x3);
+            else
+                ptx::tc_commit(ptx::smem_addr(&ctl->tfull[a]));
         }
-        if (!ok) {
+        // every MMA this thread issued (and its barrier arrivals) has completed
+        if constexpr (PAIR)
+            ptx::tc_commit_pair(ptx::smem_addr(&ctl->drain), 0x1);
+        else
             ptx::tc_commit(ptx::smem_addr(&ctl->drain));
-            bounded_wait(ptx::smem_addr(&ctl->drain), 0, args.err);
-        }
+        bounded_wait<PAIR>(ptx::smem_addr(&ctl->drain), 0, args.err);
     } else if (warp >= 4) {
         // -------------------------------------------------------- epilogue --
         const int q = warp - 4;  // TMEM lanes 32q..32q+31 = tile rows
         const int r = q * 32 + lane;
+        const uint32_t tempty0 = PAIR ? ptx::mapa(ptx::smem_addr(&ctl->tempty[0]), 0)
+                                      : ptx::smem_addr(&ctl->tempty[0]);
         uint32_t uc = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++uc) {
+        for (int u = first_unit; u < total_units; u += unit_stride, ++uc) {
             int e, nb, row0, rows;
-            decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, e, nb, row0, rows);
+            decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, per_tile, rank, e, nb, row0, rows);
             const uint32_t a = uc & 1u, aph = (uc >> 1) & 1u;
-            if (!bounded_wait(ptx::smem_addr(&ctl->tfull[a]), aph, args.err)) break;
+            if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->tfull[a]), aph, args.err)) break;
             ptx::tc_fence_after();
             const bool valid = r < rows;
             const int64_t p = (int64_t)row0 + r;
@@ -340,15 +419,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->tempty[a]));
+            if (lane == 0) {
+                // the accumulator stage is free again (the even CTA's MMA waits on it)
+                const uint32_t bar = tempty0 + a * (uint32_t)sizeof(uint64_t);
+                if constexpr (PAIR) ptx::mbar_arrive_cluster(bar);
+                else ptx::mbar_arrive(bar);
+            }
         }
     }
 
     // ---- teardown -----------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // no remote arrival can still target us
     ptx::tc_fence_after();
-    if (warp == 2) ptx::tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 2) {
+        if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
 }
 
 // ------------------------------------------------------------ host side --
@@ -386,22 +474,59 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
-cudaError_t launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                        const GemmArgs &args, int max_units, cudaStream_t s) {
+template <int MODE, bool PAIR>
+cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                           const GemmArgs &args, int max_units, cudaStream_t s) {
+    constexpr size_t kSmem = smem_bytes<PAIR>();
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, PAIR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const int grid = max(1, min(sm_count(), max_units));
-    grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, args);
-    return cudaGetLastError();
+    if (!PAIR) {
+        const int grid = max(1, min(sm_count(), max_units));
+        grouped_gemm_kernel<MODE, false><<<grid, kThreads, kSmem, s>>>(a, b0, b1, args);
+        return cudaGetLastError();
+    }
+    // one cluster of 2 CTAs (an SM pair) per unit slot
+    const int pairs = max(1, min(sm_count() / 2, max_units));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, true>, a, b0, b1, args);
+}
+
+// CTA pairs halve the B bytes each SM receives per MMA and so allow a deeper
+// ring; they pay off when experts have many 128-row tiles (an expert with an odd
+// tile count wastes half of one pair, and few-tile experts are HBM-bound anyway):
+// measured faster at 8 tiles per expert on average, slower at 2 and 4.
+// MOE_GEMM_CTA_PAIR=0/1 forces a choice (tests run both kernels this way).
+bool use_pair(int R, int E) {
+    const char *env = getenv("MOE_GEMM_CTA_PAIR");
+    if (env != nullptr && (env[0] == '0' || env[0] == '1')) return env[0] == '1';
+    return (int64_t)R >= (int64_t)8 * BM * E;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                        const GemmArgs &args, cudaStream_t s) {
+    const int tiles = args.R / BM + args.E;  // upper bound of the 128-row tiles
+    if (use_pair(args.R, args.E))
+        return launch_variant<MODE, true>(a, b0, b1, args, (tiles / 2 + args.E) * args.NB, s);
+    return launch_variant<MODE, false>(a, b0, b1, args, tiles * args.NB, s);
 }
 
 }  // namespace
@@ -422,8 +547,7 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *Xg, const __nv_bfloat16 *W1
     args.out = H;
     args.out_ld = n;
     args.err = err;
-    const int max_units = (R / BM + E) * args.NB;
-    return launch_gemm<kGateUp>(ta, tb0, tb1, args, max_units, s);
+    return launch_gemm<kGateUp>(ta, tb0, tb1, args, s);
 }
 
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
@@ -444,8 +568,7 @@ cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
     args.topk_w = topk_w;
     args.perm_slot = perm_slot;
     args.err = err;
-    const int max_units = (R / BM + E) * args.NB;
-    return launch_gemm<kDown>(ta, tb0, tb0, args, max_units, s);
+    return launch_gemm<kDown>(ta, tb0, tb0, args, s);
 }
 
 }  // namespace moe

@@ -269,11 +269,12 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         cp_async_commit();
     };
 
-    float acc[8][8];
+    // accumulators paired along experts: acc[a][p] = (expert 2p, expert 2p+1)
+    float2 acc[8][4];
 #pragma unroll
     for (int a = 0; a < 8; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        for (int p = 0; p < 4; ++p) acc[a][p] = make_float2(0.f, 0.f);
 
     issue_w(0, 0);
     load_x(0);
@@ -293,11 +294,15 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
             const float4 w0 = *reinterpret_cast<const float4 *>(&ws[buf][jj][4 * tx]);
             const float4 w1 = *reinterpret_cast<const float4 *>(&ws[buf][jj][32 + 4 * tx]);
             const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float wb[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const float2 wp[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                                  make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+            // packed fp32 FMA: each component rounds exactly like __fmaf_rn
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < 8; ++a) {
+                const float2 xx = make_float2(xa[a], xa[a]);
 #pragma unroll
-                for (int b = 0; b < 8; ++b) acc[a][b] = __fmaf_rn(xa[a], wb[b], acc[a][b]);
+                for (int p = 0; p < 4; ++p) acc[a][p] = __ffma2_rn(xx, wp[p], acc[a][p]);
+            }
         };
         if (jn == kWK) {
 #pragma unroll 4
@@ -319,7 +324,7 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         for (int b = 0; b < 8; ++b) {
             const int e = e0 + (b < 4 ? 4 * tx + b : 32 + 4 * tx + b - 4);
             if (e < E) {
-                float v = acc[a][b];
+                float v = (b & 1) ? acc[a][b >> 1].y : acc[a][b >> 1].x;
                 if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
                 L[t * E + e] = v;
             }
