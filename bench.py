@@ -1,7 +1,7 @@
 """Benchmark of the MoE-layer forward (moe_forward) on GB300.
 
 One step = one full forward of the layer over one batch of synthetic tokens:
-router -> grouping -> row gather -> gate/up GEMM + SwiGLU -> down GEMM + routing
+router -> grouping -> gate/up GEMM (rows gathered in-kernel) + SwiGLU -> down GEMM + routing
 weight -> combine, i.e. every kernel moe_forward launches. Default workload: the
 Mixtral-shaped layer (T=4096, d=4096, E=8, K=2, n=14336, bf16, fp32 accumulate).
 
@@ -33,15 +33,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-STAGES = ["route", "permute", "gather", "gemm_gate_up", "gemm_down", "combine"]
-KERNELS_PER_STAGE = {"route": 2, "permute": 3, "gather": 1, "gemm_gate_up": 1, "gemm_down": 1,
-                     "combine": 1}
+STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine"]
+KERNELS_PER_STAGE = {"route": 2, "permute": 3, "gemm_gate_up": 1, "gemm_down": 1, "combine": 1}
 KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
 # the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
 # whenever the kernel changes, until it is captured again.
-GEMM1_TRAFFIC_BYTES = {"mixtral": 1.949522e9 + 0.227283e9}
+GEMM1_TRAFFIC_BYTES = None
 
 
 def workload_desc(name, c):
@@ -302,7 +301,6 @@ def run_gpu(args, c, world, rank, local):
     g2_tflops = 2.0 * R * n * d / (stage_ms["gemm_down"] / 1e3) / 1e12
     router_bytes = T * d * 2 + d * E * 4 + R * 8 + E * 4
     combine_bytes = (R + T) * d * 2
-    gather_bytes = 2 * R * d * 2
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -331,7 +329,6 @@ def run_gpu(args, c, world, rank, local):
             "router_GBps": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9, 1),
             "router_frac_hbm": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9 / peaks["hbm"], 4),
             "combine_GBps": round(combine_bytes / (stage_ms["combine"] / 1e3) / 1e9, 1),
-            "gather_GBps": round(gather_bytes / (stage_ms["gather"] / 1e3) / 1e9, 1),
             "hbm_peak_GBps": peaks["hbm"], "clock_samples": clocks.get("samples"),
             "power_w_max": clocks.get("power_w_max"),
         },

@@ -74,8 +74,8 @@ int moe_abi_version(void);
  * counts[E], offsets[E+1], tile_base[E+1], the grouping scratch
  * (ceil(T/32)*E counters and T*K ranks), perm_token/perm_slot/row_of_slot [T*K],
  * topk_idx/topk_w [T*K] for moe_forward, the tile list [T*K/128+E][4], the
- * gathered rows Xg [T*K,d] bf16, H [T*K,n] bf16, Z [T*K,d] bf16 and the router
- * logits [T,E] fp32 (moe_forward).
+ * gathered rows Xg [T*K,d] bf16 (used by the CTA-pair gate/up GEMM), H [T*K,n]
+ * bf16, Z [T*K,d] bf16 and the router logits [T,E] fp32 (moe_forward).
  * Before first use the caller zeroes it once (moe_workspace_init). */
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n);
 
@@ -151,8 +151,11 @@ moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const int32_t *counts,
 /* Up-projection GEMM with the SwiGLU fused in its epilogue (SonicMoE page §1,
  * §2.2, §4.2): for every grouped row p of expert e,
  *   H[p,:] = bf16( SiLU(x W1[e]) * (x W3[e]) ),  x = X[perm_token[p],:].
- * Uses offsets [E+1] and perm_token from moe_permute; H [T*K,n] bf16.
- * ws: workspace of this shape (the gathered rows live there). */
+ * Uses offsets [E+1] and perm_token from moe_permute; H [T*K,n] bf16. For
+ * small experts the GEMM gathers the rows of X itself; for experts of >= 8
+ * row tiles on average it gathers them into the workspace first and runs on
+ * CTA pairs. A perm_token entry outside [0,T) is skipped and flagged.
+ * ws: workspace of this shape. */
 moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
                               const int32_t *perm_token, const int32_t *offsets,
                               int T, int d, int E, int K, int n, moe_bf16 *H,
@@ -183,7 +186,7 @@ moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, i
 
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
- * Enqueues 9 kernels and one memset; no host synchronisation. */
+ * Enqueues 8 kernels and one memset; no host synchronisation. */
 moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
                          const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                          int T, int d, int E, int K, int n, int renorm,
@@ -192,8 +195,8 @@ moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
 
 /* moe_forward that also records CUDA events (cudaEvent_t as void*) on `stream`
  * between its stages, for per-kernel timing: events[0] before the router,
- * then after route, permute, gather, gate/up GEMM, down GEMM, combine
- * (7 events). n_events < 7 records the first n_events of them. */
+ * then after route, permute, gate/up GEMM, down GEMM, combine (6 events).
+ * n_events < 6 records the first n_events of them. */
 moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float *bias,
                                 const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                                 int T, int d, int E, int K, int n, int renorm,

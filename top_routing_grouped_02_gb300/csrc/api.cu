@@ -105,6 +105,7 @@ WsLayout ws_layout(int T, int d, int E, int K, int n) {
     L.topk_w = take(4 * R);
     L.tiles = take(16 * (size_t)L.max_tiles);
     L.num_tiles = take(4);
+    L.grouping_end = off;
     L.xg = take(2 * R * (size_t)d);
     L.h = take(2 * R * (size_t)n);
     L.z = take(2 * R * (size_t)d);
@@ -180,7 +181,7 @@ moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts, int T, 
     if (s != MOE_OK) return s;
     if (!aligned16(tiles)) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, 0, E, K, 0);
-    if (ws_bytes < L.xg) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < L.grouping_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_arch()) != MOE_OK) return s;
     return from_cuda(launch_permute(topk_idx, counts, T, E, K, offsets, perm_token, perm_slot,
                                     row_of_slot, tiles, num_tiles, L, static_cast<char *>(ws),
@@ -199,16 +200,12 @@ moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_b
     const WsLayout L = ws_layout(T, d, E, K, n);
     if (ws_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_arch()) != MOE_OK) return s;
-    const int R = T * K;
-    cudaStream_t st = as_stream(stream);
-    __nv_bfloat16 *xg = at<__nv_bfloat16>(ws, L.xg);
-    cudaError_t e = launch_gather_rows(reinterpret_cast<const __nv_bfloat16 *>(X), perm_token, T, R, d,
-                                       xg, st);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    return from_cuda(launch_gemm_gate_up(xg, reinterpret_cast<const __nv_bfloat16 *>(W1),
-                                         reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d,
-                                         E, n, reinterpret_cast<__nv_bfloat16 *>(H),
-                                         at<uint32_t>(ws, L.err), st));
+    return from_cuda(launch_gemm_gate_up(reinterpret_cast<const __nv_bfloat16 *>(X), perm_token, T,
+                                         reinterpret_cast<const __nv_bfloat16 *>(W1),
+                                         reinterpret_cast<const __nv_bfloat16 *>(W3), offsets,
+                                         T * K, d, E, n, reinterpret_cast<__nv_bfloat16 *>(H),
+                                         at<__nv_bfloat16>(ws, L.xg), at<uint32_t>(ws, L.err),
+                                         as_stream(stream)));
 }
 
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
@@ -285,7 +282,6 @@ moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float 
     int32_t *perm_token = at<int32_t>(ws, L.perm_token);
     int32_t *perm_slot = at<int32_t>(ws, L.perm_slot);
     int32_t *row_of_slot = at<int32_t>(ws, L.row_of_slot);
-    __nv_bfloat16 *xg = at<__nv_bfloat16>(ws, L.xg);
     __nv_bfloat16 *h = at<__nv_bfloat16>(ws, L.h);
     __nv_bfloat16 *z = at<__nv_bfloat16>(ws, L.z);
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(X);
@@ -300,11 +296,9 @@ moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float 
                        static_cast<char *>(ws), st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
-    if (launch_gather_rows(x, perm_token, T, R, d, xg, st) != cudaSuccess || !mark())
-        return MOE_ERR_CUDA;
-    if (launch_gemm_gate_up(xg, reinterpret_cast<const __nv_bfloat16 *>(W1),
+    if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
                             reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n, h,
-                            err, st) != cudaSuccess ||
+                            at<__nv_bfloat16>(ws, L.xg), err, st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
     if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), w, perm_slot, offsets, R,

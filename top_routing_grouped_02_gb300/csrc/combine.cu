@@ -1,5 +1,7 @@
-// Row movement kernels: the Gather of activation rows into expert-grouped order
-// and the Scatter/combine of weighted expert outputs back into token order.
+// Row movement: the Gather of activation rows into expert-grouped order (used
+// ahead of the CTA-pair gate/up GEMM, which loads A by TMA; the single-CTA GEMM
+// gathers rows itself) and the Scatter/combine of weighted expert outputs back
+// into token order.
 //
 // Pages: "混合专家模型(MoE)架构优化与SonicMoE实践" §1 (Gather rows by routing
 // result; Scatter results back to the tokens' original positions);

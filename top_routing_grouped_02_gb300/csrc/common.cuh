@@ -35,7 +35,8 @@ struct WsLayout {
     size_t topk_w;      // fp32  [R]
     size_t tiles;       // int32 [max_tiles][4]
     size_t num_tiles;   // int32 [1]
-    size_t xg;          // bf16  [R, d]  gathered activation rows
+    size_t grouping_end;// end of the grouping regions (what moe_permute needs)
+    size_t xg;          // bf16  [R, d]  gathered rows (CTA-pair gate/up GEMM)
     size_t h;           // bf16  [R, n]
     size_t z;           // bf16  [R, d]
     size_t logits;      // fp32  [T, E] router logits (moe_forward only)
@@ -63,9 +64,12 @@ cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, 
                            const WsLayout &L, char *ws, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16 *X, const int32_t *perm_token, int T, int R,
                                int d, __nv_bfloat16 *Xg, cudaStream_t s);
-cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *Xg, const __nv_bfloat16 *W1,
-                                const __nv_bfloat16 *W3, const int32_t *offsets, int R, int d,
-                                int E, int n, __nv_bfloat16 *H, uint32_t *err, cudaStream_t s);
+// xg: scratch [R, d] for the gathered rows (used when the CTA-pair kernel runs)
+cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_token, int T,
+                                const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                                const int32_t *offsets, int R, int d, int E, int n,
+                                __nv_bfloat16 *H, __nv_bfloat16 *xg, uint32_t *err,
+                                cudaStream_t s);
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,

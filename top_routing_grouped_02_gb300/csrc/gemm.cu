@@ -11,7 +11,7 @@
 // order for L2 reuse of expert weights; TMA loads of expert weights).
 //
 // One kernel template serves both GEMMs of the expert MLP:
-//   gate/up:  acc[128 x 256] = Xg[rows, d] . [W1[e][:, 128 cols] | W3[e][:, 128 cols]]
+//   gate/up:  acc[128 x 256] = X[perm_token[rows], d] . [W1[e][:, 128 cols] | W3[e][:, 128 cols]]
 //             H[rows, 128 cols] = bf16( SiLU(gate) * up )
 //   down:     acc[128 x 256] = H[rows, n] . W2[e][:, 256 cols]
 //             Z[rows, 256 cols] = bf16( w_row * acc )
@@ -28,8 +28,13 @@
 // both CTAs' epilogues release the accumulator to the even CTA.
 //
 // Warp roles (256 threads):
-//   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
-//               (MN-major, four 64-column boxes) per stage, 128-byte swizzle.
+//   warp 0      TMA producer: B tile 64x256 (MN-major, four 64-column boxes;
+//               two per CTA of a pair) per stage, 128-byte swizzle, and the A
+//               tile 128x64 (K-major) unless the A rows are gathered.
+//   warps 2-3   single-CTA gate/up only: gather the A tile's 128 token rows
+//               straight from X (cp.async into the same 128-byte-swizzled K-major
+//               layout), so no gathered copy of X goes through HBM. (CTA pairs
+//               load A by TMA from rows gathered beforehand: measured faster.)
 //   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma (M128 N256 K16)
 //               per stage into the current TMEM accumulator, commits the stage
 //               back to the producer and, after the last stage, the
@@ -82,6 +87,17 @@ struct Geo {
 
 enum Mode : int { kGateUp = 0, kDown = 1 };
 
+// Single-CTA gate/up A rows are gathered by warps 2 and 3 with 16-byte cp.async.
+// Each lane waits for its own copies and fences them for the async proxy, the
+// warp synchronises, and one lane arrives on the stage barrier (release); the
+// warps signal kGatherLag stages behind their issue so several stages are in
+// flight.
+constexpr int kGatherWarps = 2;
+#ifndef MOE_GEMM_GATHER_LAG
+#define MOE_GEMM_GATHER_LAG 2
+#endif
+constexpr int kGatherLag = MOE_GEMM_GATHER_LAG;
+
 struct Ctl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
@@ -100,6 +116,9 @@ constexpr size_t smem_bytes() {
 }
 
 struct GemmArgs {
+    const __nv_bfloat16 *X;     // gate/up only: token rows [T, d], gathered in-kernel
+    const int32_t *perm_token;  // gate/up only: token of each grouped row
+    int T;                      // gate/up only: number of tokens
     const int32_t *offsets;   // [E+1] grouped row offsets
     int E;
     int R;                    // rows of A / out (T*K)
@@ -112,15 +131,14 @@ struct GemmArgs {
     uint32_t *err;            // device error word
 };
 
+// Polls one of this CTA's barriers (acquire at CTA scope; arrivals from the
+// peer CTA of a pair are made with cluster-scope release).
 template <bool PAIR>
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
-    auto poll = [&]() {
-        return PAIR ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
-    };
-    if (poll()) return true;
+    if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (poll()) return true;
+        if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((spin & 63u) == 0 && ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, MOE_DEVERR_TIMEOUT);
             return false;
@@ -160,6 +178,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
     using G = Geo<PAIR>;
     constexpr int S = G::kStages;
+    // A rows gathered in the kernel (single-CTA gate/up) or loaded by TMA
+    constexpr bool GATHER = (MODE == kGateUp) && !PAIR;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -174,8 +194,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     // ---- setup: barriers, TMEM, tile bases --------------------------------
     if (tid == 0) {
+        // full[s]: the TMA producer's arrive (+ one per gatherer warp)
+        const uint32_t full_count = 1 + (GATHER ? kGatherWarps : 0);
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), full_count);
             ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -186,7 +208,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&tmA);
+        if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
         if (MODE == kGateUp) ptx::prefetch_tensormap(&tmB1);
     }
@@ -268,9 +290,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t full = ptx::smem_addr(&ctl->full[s]);
                 const uint32_t sA = smem_base + s * G::kStageBytes, sB = sA + kABytes;
                 const int ky = wrow + kb * BK;
+                // TMA bytes per CTA and stage: B always, A only when not gathered
+                constexpr uint32_t kTx = G::kStageBytes - (GATHER ? kABytes : 0);
                 if constexpr (PAIR) {
                     // both CTAs' loads complete on the even CTA's barrier
-                    if (leader) ptx::mbar_arrive_expect_tx(full, 2 * G::kStageBytes);
+                    if (leader) ptx::mbar_arrive_expect_tx(full, 2 * kTx);
                     const uint32_t fullc = ptx::mapa(full, 0);
                     ptx::tma_load_2d_pair(sA, &tmA, fullc, kb * BK, row0);
                     if (MODE == kGateUp) {
@@ -284,8 +308,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ptx::tma_load_2d_pair(sB + kBBox, &tmB0, fullc, x0 + 64, ky);
                     }
                 } else {
-                    ptx::mbar_arrive_expect_tx(full, G::kStageBytes);
-                    ptx::tma_load_2d(sA, &tmA, full, kb * BK, row0);
+                    ptx::mbar_arrive_expect_tx(full, kTx);
+                    if (!GATHER) ptx::tma_load_2d(sA, &tmA, full, kb * BK, row0);
                     if (MODE == kGateUp) {
                         ptx::tma_load_2d(sB + 0 * kBBox, &tmB0, full, nb * 128, ky);
                         ptx::tma_load_2d(sB + 1 * kBBox, &tmB0, full, nb * 128 + 64, ky);
@@ -351,6 +375,60 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         else
             ptx::tc_commit(ptx::smem_addr(&ctl->drain));
         bounded_wait<PAIR>(ptx::smem_addr(&ctl->drain), 0, args.err);
+    } else if (GATHER && (warp == 2 || warp == 3)) {
+        // ------------------------------------------------- A-row gatherers --
+        // Lane (rr, c) copies 16-byte chunk c of rows gw*4 + rr + 8i (i < 16) of
+        // the stage's 128-row A tile, placed at the 128-byte-swizzle position
+        // row*128 + ((c ^ (row & 7)) << 4) the MMA descriptor expects.
+        const int gw = warp - 2;
+        const int c = lane & 7, rr = lane >> 3;
+        const uint32_t full0 = ptx::smem_addr(&ctl->full[0]);
+        auto signal = [&](uint32_t j) {  // this warp's rows of stage j have landed
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(full0 + (j % S) * (uint32_t)sizeof(uint64_t));
+        };
+        uint32_t it = 0;
+        bool ok = true;
+        for (int u = first_unit; u < total_units && ok; u += unit_stride) {
+            int e, nb, row0, rows;
+            decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, per_tile, rank, e, nb, row0, rows);
+            int tok[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = gw * 4 + rr + 8 * i;
+                tok[i] = -1;
+                if (r < rows) {
+                    const int t = __ldg(args.perm_token + row0 + r);
+                    if (t >= 0 && t < args.T) tok[i] = t;
+                    else atomicOr(args.err, MOE_DEVERR_BAD_EXPERT);
+                }
+            }
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t s = it % S, ph = (it / S) & 1u;
+                if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, args.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sA = smem_base + s * G::kStageBytes;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = gw * 4 + rr + 8 * i;
+                    if (tok[i] >= 0)
+                        ptx::cp_async_16(sA + r * 128 + ((c ^ (r & 7)) << 4),
+                                         args.X + (int64_t)tok[i] * args.Kdim + kb * BK + c * 8);
+                }
+                ptx::cp_async_commit_group();
+                if (it >= (uint32_t)kGatherLag) {
+                    ptx::cp_async_wait_group<kGatherLag>();
+                    ptx::fence_proxy_async_smem();
+                    signal(it - kGatherLag);
+                }
+            }
+        }
+        // the last stages still in flight
+        ptx::cp_async_wait_group<0>();
+        ptx::fence_proxy_async_smem();
+        for (uint32_t j = it >= (uint32_t)kGatherLag ? it - kGatherLag : 0u; j < it; ++j) signal(j);
     } else if (warp >= 4) {
         // -------------------------------------------------------- epilogue --
         const int q = warp - 4;  // TMEM lanes 32q..32q+31 = tile rows
@@ -523,6 +601,7 @@ bool use_pair(int R, int E) {
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                         const GemmArgs &args, cudaStream_t s) {
+    // (gate/up chooses its variant itself: the A source differs)
     const int tiles = args.R / BM + args.E;  // upper bound of the 128-row tiles
     if (use_pair(args.R, args.E))
         return launch_variant<MODE, true>(a, b0, b1, args, (tiles / 2 + args.E) * args.NB, s);
@@ -531,14 +610,19 @@ cudaError_t launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUten
 
 }  // namespace
 
-cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *Xg, const __nv_bfloat16 *W1,
-                                const __nv_bfloat16 *W3, const int32_t *offsets, int R, int d,
-                                int E, int n, __nv_bfloat16 *H, uint32_t *err, cudaStream_t s) {
+cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_token, int T,
+                                const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                                const int32_t *offsets, int R, int d, int E, int n,
+                                __nv_bfloat16 *H, __nv_bfloat16 *xg, uint32_t *err,
+                                cudaStream_t s) {
     CUtensorMap ta, tb0, tb1;
-    if (!make_map(&ta, Xg, d, R, 64, BM) || !make_map(&tb0, W1, n, (uint64_t)E * d, 64, BK) ||
+    if (!make_map(&tb0, W1, n, (uint64_t)E * d, 64, BK) ||
         !make_map(&tb1, W3, n, (uint64_t)E * d, 64, BK))
         return cudaErrorInvalidValue;
     GemmArgs args{};
+    args.X = X;
+    args.perm_token = perm_token;
+    args.T = T;
     args.offsets = offsets;
     args.E = E;
     args.R = R;
@@ -547,7 +631,16 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *Xg, const __nv_bfloat16 *W1
     args.out = H;
     args.out_ld = n;
     args.err = err;
-    return launch_gemm<kGateUp>(ta, tb0, tb1, args, s);
+    const int tiles = R / BM + E;  // upper bound of the 128-row tiles
+    if (use_pair(R, E)) {
+        // CTA pairs load A by TMA from rows gathered into xg beforehand
+        cudaError_t e = launch_gather_rows(X, perm_token, T, R, d, xg, s);
+        if (e != cudaSuccess) return e;
+        if (!make_map(&ta, xg, d, R, 64, BM)) return cudaErrorInvalidValue;
+        return launch_variant<kGateUp, true>(ta, tb0, tb1, args, (tiles / 2 + E) * args.NB, s);
+    }
+    // single CTAs gather their A rows themselves; the A map argument is not read
+    return launch_variant<kGateUp, false>(tb0, tb0, tb1, args, tiles * args.NB, s);
 }
 
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,

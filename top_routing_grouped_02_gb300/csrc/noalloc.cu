@@ -63,7 +63,7 @@ extern "C" moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const int32
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((reinterpret_cast<uintptr_t>(tiles) & 15u) != 0) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, 0, E, K, 0);
-    if (L.xg > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;  // beyond the built-in scratch
+    if (L.grouping_end > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;  // beyond the built-in scratch
     moe_status_t s = current_device_is_sm103();
     if (s != MOE_OK) return s;
     void *scratch = nullptr;
