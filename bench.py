@@ -40,7 +40,7 @@ METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
 # the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
 # whenever the kernel changes, until it is captured again.
-GEMM1_TRAFFIC_BYTES = None
+GEMM1_TRAFFIC_BYTES = {"mixtral": 2.584302e9 + 0.231343e9}
 
 
 def workload_desc(name, c):
@@ -346,13 +346,73 @@ def run_gpu(args, c, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_router_only(args, world, rank, local):
+    """The router-only workload: given logits [T,8] fp32, softmax + top-2 +
+    counts (moe_route_logits), T in {256, 512, 1024, 2048}; microseconds per call."""
+    import torch
+    from top_routing_grouped_02_gb300 import moe, synth
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+    per_t = {}
+    import ctypes
+    lib = moe.lib()
+    for T in synth.ROUTER_T:
+        logits = synth.router_logits_input(T, device="cuda")
+        K, E = synth.ROUTER_K, synth.ROUTER_E
+        idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        ptrs = [ctypes.c_void_p(t.data_ptr()) for t in (logits, idx, w, counts)]
+
+        def call(st):
+            rc = lib.moe_route_logits(ptrs[0], T, E, K, 1, ptrs[1], ptrs[2], ptrs[3],
+                                      ctypes.c_void_p(st.cuda_stream))
+            if rc != 0:
+                raise moe.MoeError("moe_route_logits", rc)
+
+        for _ in range(args.warmup):
+            call(stream)
+        torch.cuda.synchronize()
+        # device time: the calls are captured once in a CUDA graph and replayed, so
+        # host launch overhead does not sit between them
+        side = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(args.steps):
+                    call(side)
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / args.steps
+        nbytes = T * synth.ROUTER_E * 4 + T * synth.ROUTER_K * 8 + synth.ROUTER_E * 4
+        per_t[T] = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 2)}
+    total_tokens = sum(synth.ROUTER_T)
+    total_us = sum(v["us"] for v in per_t.values())
+    if rank == 0:
+        print(json.dumps({
+            "metric": "router-only fused gating (softmax + top-2 + counts) time per call",
+            "value": round(total_tokens / (total_us * 1e-6), 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_us / 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "router-only logits [T,8] fp32, K=2, T in 256..2048"},
+            "gpu_launches": len(synth.ROUTER_T) * args.steps,
+            "extra": {"per_T": per_t}}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mixtral", choices=["tiny", "mixtral", "dsv3", "sonic"])
+    ap.add_argument("--workload", default="mixtral",
+                    choices=["tiny", "mixtral", "dsv3", "sonic", "router"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -360,8 +420,11 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from top_routing_grouped_02_gb300 import synth
-    c = dict(synth.WORKLOADS[args.workload])
     world, rank, local = dist_setup()
+    if args.workload == "router":
+        run_router_only(args, world, rank, local)
+        return
+    c = dict(synth.WORKLOADS[args.workload])
     if args.impl == "reference":
         run_reference(args, c, world, rank)
     else:

@@ -23,7 +23,9 @@
 //  2. select: one warp per token reads its E logits, merges (max, sum of exp)
 //     across lanes with the online recurrence, picks K by repeated warp argmax
 //     (ties -> lower index), writes indices and weights, and counts per expert in
-//     a block histogram flushed with one atomic per (block, expert).
+//     a block histogram flushed with one atomic per (block, expert). For small E
+//     and T a single block with one thread per token does the same and writes
+//     the counts directly, so no memset is needed.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -438,8 +440,86 @@ select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
         if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
 }
 
+// Small E: one thread per token and a single block, which zeroes and writes the
+// counts itself (no memset, one launch). Softmax statistics in the thread: the
+// maximum, then a compensated (Kahan) sum of exp(L - max) for the full
+// denominator; top-K by K passes (higher score wins, equal scores: lower index).
+constexpr int kSelSingleThreads = 1024;
+constexpr int kSelSingleMaxT = 16384;
+
+template <int EP>
+__global__ void __launch_bounds__(kSelSingleThreads)
+select_single_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
+                     int32_t *__restrict__ idx_out, float *__restrict__ w_out,
+                     int32_t *__restrict__ counts) {
+    __shared__ int hist[EP];
+    for (int e = threadIdx.x; e < EP; e += kSelSingleThreads) hist[e] = 0;
+    __syncthreads();
+    for (int64_t t = threadIdx.x; t < T; t += kSelSingleThreads) {
+        float v[EP];
+#pragma unroll
+        for (int e = 0; e < EP; ++e) v[e] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
+        float m = v[0];
+#pragma unroll
+        for (int e = 1; e < EP; ++e) m = fmaxf(m, v[e]);
+        uint32_t taken = 0;
+        int sel[kMaxK];
+        float kept = 0.f, ex[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k < K) {
+                int bi = -1;
+                float bv = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < EP; ++e)
+                    if (e < E && !(taken >> e & 1u) && (bi < 0 || v[e] > bv)) {
+                        bv = v[e];
+                        bi = e;
+                    }
+                taken |= 1u << bi;
+                sel[k] = bi;
+                ex[k] = expf(bv - m);
+                kept += ex[k];
+            }
+        }
+        float denom = kept;
+        if (!renorm) {
+            float sum = 0.f, comp = 0.f;
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                if (e < E) {
+                    const float y = expf(v[e] - m) - comp;
+                    const float tt = sum + y;
+                    comp = (tt - sum) - y;
+                    sum = tt;
+                }
+            }
+            denom = sum;
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k < K) {
+                idx_out[t * K + k] = sel[k];
+                w_out[t * K + k] = ex[k] / denom;
+                atomicAdd(&hist[sel[k]], 1);
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kSelSingleThreads) counts[e] = hist[e];
+}
+
 cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, int32_t *idx,
                           float *w, int32_t *counts, cudaStream_t s) {
+    if (E <= 16 && T <= kSelSingleMaxT) {
+        if (E <= 8)
+            select_single_kernel<8><<<1, kSelSingleThreads, 0, s>>>(logits, T, E, K, renorm, idx, w,
+                                                                    counts);
+        else
+            select_single_kernel<16><<<1, kSelSingleThreads, 0, s>>>(logits, T, E, K, renorm, idx,
+                                                                     w, counts);
+        return cudaGetLastError();
+    }
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((T + kSelThreads / 32 - 1) / (kSelThreads / 32));
