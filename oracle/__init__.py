@@ -67,6 +67,10 @@ def _load():
                 "oracle_combine_bf16": (None, [P, P, I64, I, I, P]),
                 "oracle_forward_tokens": (None, [P, P, P, P, P, P, I64, I, I, I, I, I, P, I64,
                                                  P, P, P]),
+                "oracle_token_rounding": (I64, [P, P, I64, I, I, I, I, I64, P, P, P, P, P]),
+                "oracle_combine_rows": (None, [P, P, I64, I, I, P]),
+                "oracle_combine_rows_bf16": (None, [P, P, I64, I, I, P]),
+                "oracle_forward_assigned": (None, [P, P, P, P, I64, I, I, I, P, P, P, I64, P]),
                 "oracle_num_threads": (I, []),
             }
             for name, (res, args) in sig.items():
@@ -249,3 +253,89 @@ def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
     """Exact float64 values of an array of bf16 bit patterns."""
     a = np.ascontiguousarray(a, np.uint16)
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ------------------------------------------------------------ token rounding
+
+def rounding_capacity(T: int, E: int, K: int, M: int) -> int:
+    """Most rows Token Rounding can produce: each expert moves by at most M//2
+    rows and keeps at most T."""
+    return min(T * E, T * K + E * (M // 2))
+
+
+def token_rounding(L: np.ndarray, idx: np.ndarray, M: int, renorm: bool = True) -> dict:
+    """Token Rounding of a top-K routing (see oracle_token_rounding in moe_oracle.h).
+    Returns counts [E], offsets [E+1], perm_token [R'], row_map [T,E], row_w [R']."""
+    L = _c(L, np.float32)
+    idx = _c(idx, np.int32)
+    T, E = L.shape
+    K = idx.shape[1]
+    assert idx.shape[0] == T and M >= 1
+    cap = rounding_capacity(T, E, K, M)
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    perm_token = np.empty(max(cap, 1), np.int32)
+    row_map = np.empty((T, E), np.int32)
+    row_w = np.empty(max(cap, 1), np.float32)
+    R = _load().oracle_token_rounding(_p(L), _p(idx), T, E, K, M, int(bool(renorm)), cap,
+                                      _p(counts), _p(offsets), _p(perm_token), _p(row_map),
+                                      _p(row_w))
+    if R < 0:
+        raise RuntimeError("token rounding produced more rows than its capacity bound")
+    return dict(counts=counts, offsets=offsets, perm_token=perm_token[:R].copy(),
+                row_map=row_map, row_w=row_w[:R].copy())
+
+
+def combine_rows(Z: np.ndarray, row_map: np.ndarray) -> np.ndarray:
+    """Y uint16 (bf16) [T,d] from double Z rows and row_map [T,E]."""
+    Z = _c(Z, np.float64)
+    row_map = _c(row_map, np.int32)
+    T, E = row_map.shape
+    d = Z.shape[1]
+    Y = np.empty((T, d), np.uint16)
+    _load().oracle_combine_rows(_p(Z), _p(row_map), T, E, d, _p(Y))
+    return Y
+
+
+def combine_rows_bf16(Z: np.ndarray, row_map: np.ndarray) -> np.ndarray:
+    Z = _c(Z, np.uint16)
+    row_map = _c(row_map, np.int32)
+    T, E = row_map.shape
+    d = Z.shape[1]
+    Y = np.empty((T, d), np.uint16)
+    _load().oracle_combine_rows_bf16(_p(Z), _p(row_map), T, E, d, _p(Y))
+    return Y
+
+
+def forward_rounded(X, Wr, bias, W1, W3, W2, K: int, renorm: bool = True, M: int = 128) -> dict:
+    """The layer under Token Rounding, through the grouped steps."""
+    L = router_logits(X, Wr, bias)
+    idx, w = topk_softmax(L, K, renorm)
+    tr = token_rounding(L, idx, M, renorm)
+    R = int(tr["offsets"][-1])
+    H = gate_up(X, W1, W3, tr["perm_token"], tr["offsets"])
+    # the weight of grouped row p is row_w[p]: an identity slot map
+    Z = down(H, W2, tr["row_w"], np.arange(R, dtype=np.int32), tr["offsets"])
+    Y = combine_rows(Z, tr["row_map"])
+    tiles = tile_schedule(tr["offsets"], 128)
+    return dict(logits=L, idx=idx, w=w, tiles=tiles, H=H, Z=Z, Y=Y, **tr)
+
+
+def forward_assigned(X, W1, W3, W2, row_map, row_w, tokens) -> np.ndarray:
+    """Y rows [n,d] (bf16 bits) for the listed tokens under a given assignment,
+    computed token by token."""
+    X = _c(X, np.uint16)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    W2 = _c(W2, np.uint16)
+    row_map = _c(row_map, np.int32)
+    row_w = _c(row_w, np.float32)
+    tokens = _c(np.asarray(tokens, np.int64), np.int64)
+    T, d = X.shape
+    E, _, n = W1.shape
+    assert row_map.shape == (T, E)
+    nt = tokens.shape[0]
+    Y = np.empty((nt, d), np.uint16)
+    _load().oracle_forward_assigned(_p(X), _p(W1), _p(W3), _p(W2), T, d, E, n, _p(row_map),
+                                    _p(row_w), _p(tokens), nt, _p(Y))
+    return Y

@@ -321,3 +321,152 @@ void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias
         free(y);
     }
 }
+
+/* ------------------------------------------------------ token rounding -- */
+
+typedef struct {
+    int member;  /* 1 when the token chose this expert in its top-K */
+    float v;     /* L[t,e] */
+    int64_t t;
+} candidate;
+
+/* chosen first; then higher score; then lower token index */
+static int by_member_score_token(const void *pa, const void *pb) {
+    const candidate *a = (const candidate *)pa, *b = (const candidate *)pb;
+    if (a->member != b->member) return a->member ? -1 : 1;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->t > b->t) - (a->t < b->t);
+}
+
+int64_t oracle_token_rounding(const float *L, const int32_t *idx, int64_t T, int E, int K,
+                              int M, int renorm, int64_t cap, int32_t *counts_out,
+                              int32_t *offsets, int32_t *perm_token, int32_t *row_map,
+                              float *row_w) {
+    /* 1. expert frequencies */
+    int32_t *f = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    oracle_expert_counts(idx, T, K, E, f);
+    /* 2. rounded targets */
+    for (int e = 0; e < E; ++e) {
+        int64_t c = (int64_t)M * ((f[e] + M / 2) / M);
+        if (c > T) c = (int64_t)M * (f[e] / M);
+        counts_out[e] = (int32_t)c;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts_out[e];
+    if (offsets[E] > cap) {
+        free(f);
+        return -1;
+    }
+    /* 3. the second sort, one expert at a time; keep[t*E+e] marks the kept pairs */
+    unsigned char *member = (unsigned char *)calloc((size_t)(T * E), 1);
+    unsigned char *keep = (unsigned char *)calloc((size_t)(T * E), 1);
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) member[t * E + idx[t * K + k]] = 1;
+    candidate *cand = (candidate *)malloc(sizeof(candidate) * (size_t)T);
+    for (int e = 0; e < E; ++e) {
+        for (int64_t t = 0; t < T; ++t) {
+            cand[t].member = member[t * E + e];
+            cand[t].v = L[t * E + e];
+            cand[t].t = t;
+        }
+        qsort(cand, (size_t)T, sizeof(candidate), by_member_score_token);
+        for (int32_t i = 0; i < counts_out[e]; ++i) keep[cand[i].t * E + e] = 1;
+    }
+    /* 4. rows grouped by expert, ascending t */
+    int32_t p = 0;
+    for (int e = 0; e < E; ++e)
+        for (int64_t t = 0; t < T; ++t) {
+            if (keep[t * E + e]) {
+                row_map[t * E + e] = p;
+                perm_token[p] = (int32_t)t;
+                ++p;
+            } else {
+                row_map[t * E + e] = -1;
+            }
+        }
+    /* 5. softmax weights of the kept pairs */
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = L + t * E;
+        double m = (double)l[0];
+        for (int e = 1; e < E; ++e)
+            if ((double)l[e] > m) m = (double)l[e];
+        double denom = 0.0;
+        for (int e = 0; e < E; ++e) denom += exp((double)l[e] - m);
+        double kept = 0.0;
+        for (int e = 0; e < E; ++e)
+            if (keep[t * E + e]) kept += exp((double)l[e] - m) / denom;
+        for (int e = 0; e < E; ++e)
+            if (keep[t * E + e]) {
+                double pe = exp((double)l[e] - m) / denom;
+                row_w[row_map[t * E + e]] = (float)(renorm ? pe / kept : pe);
+            }
+    }
+    free(cand);
+    free(keep);
+    free(member);
+    free(f);
+    return offsets[E];
+}
+
+void oracle_combine_rows(const double *Z, const int32_t *row_map, int64_t T, int E, int d,
+                         uint16_t *Y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int c = 0; c < d; ++c) {
+            double y = 0.0;
+            for (int e = 0; e < E; ++e) {
+                int32_t r = row_map[t * E + e];
+                if (r >= 0) y = y + Z[(int64_t)r * d + c];
+            }
+            Y[t * d + c] = oracle_bf16_from_double(y);
+        }
+}
+
+void oracle_combine_rows_bf16(const uint16_t *Z, const int32_t *row_map, int64_t T, int E,
+                              int d, uint16_t *Y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int c = 0; c < d; ++c) {
+            double y = 0.0;
+            for (int e = 0; e < E; ++e) {
+                int32_t r = row_map[t * E + e];
+                if (r >= 0) y = y + oracle_bf16_to_double(Z[(int64_t)r * d + c]);
+            }
+            Y[t * d + c] = oracle_bf16_from_double(y);
+        }
+}
+
+void oracle_forward_assigned(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                             const uint16_t *W2, int64_t T, int d, int E, int n,
+                             const int32_t *row_map, const float *row_w,
+                             const int64_t *tokens, int64_t n_tok, uint16_t *Y_rows) {
+    (void)T;
+#pragma omp parallel
+    {
+        double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
+        double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
+        uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n);
+        double *z = (double *)malloc(sizeof(double) * (size_t)d);
+        double *y = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_tok; ++i) {
+            int64_t t = tokens[i];
+            const uint16_t *x = X + t * d;
+            for (int c = 0; c < d; ++c) y[c] = 0.0;
+            for (int e = 0; e < E; ++e) {
+                int32_t r = row_map[t * E + e];
+                if (r < 0) continue;
+                gate_up_row(x, W1 + (int64_t)e * d * n, W3 + (int64_t)e * d * n, d, n, a1, a3, h);
+                down_row(h, W2 + (int64_t)e * n * d, (double)row_w[r], n, d, z);
+                for (int c = 0; c < d; ++c) y[c] = y[c] + z[c];
+            }
+            for (int c = 0; c < d; ++c) Y_rows[i * d + c] = oracle_bf16_from_double(y[c]);
+        }
+        free(a1);
+        free(a3);
+        free(h);
+        free(z);
+        free(y);
+    }
+}

@@ -103,6 +103,52 @@ void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias
                            const int64_t *tokens, int64_t n_tok,
                            uint16_t *Y_rows, int32_t *idx_rows, float *w_rows);
 
+/* ---- Token Rounding (SonicMoE page, §3 "令牌舍入路由"): a routing mode whose
+ * per-expert row counts are multiples of the tile size M, so no tile is padded.
+ *
+ * Inputs: the router logits L [T,E] and the plain top-K choice idx [T,K] made
+ * from them (oracle_topk_softmax). Steps:
+ *   1. f_e = the number of (t,k) with idx[t,k] == e (§3.1, expert frequency).
+ *   2. c_e = f_e rounded to the nearest multiple of M, halves up:
+ *      M * floor((f_e + floor(M/2)) / M) (§3.2's rounding kernel; §3.1 allows
+ *      either the rounded-up or the rounded-down multiple and this picks the
+ *      nearer). If that exceeds T (an expert can take each token at most once)
+ *      the rounded-down multiple is used.
+ *   3. The second sort (§3.1): for expert e, order all T tokens by (token chose
+ *      e in its top-K first, then L[t,e] descending, then t ascending) and keep
+ *      the first c_e. Rounding down drops the chosen tokens with the lowest
+ *      scores for e; rounding up adds the unchosen tokens with the highest.
+ *   4. Rows are grouped by expert, ascending t inside an expert:
+ *      offsets = exclusive prefix sum of c, perm_token[p] = t of row p,
+ *      row_map[t,e] = the row of (t,e), -1 when t is not kept by e.
+ *   5. Weights (§3.2, softmax renormalisation after rounding): p = softmax(L[t,:])
+ *      in double; row_w[row_map[t,e]] = p_e / (sum of p over the experts that
+ *      kept t) when renorm != 0, else p_e; rounded once to fp32.
+ * The score compared in step 3 is the logit, the same fp32 value that decided
+ * the top-K: for one token it orders experts exactly as p does.
+ * Returns the number of rows R' = offsets[E], or -1 (and writes no rows) when R'
+ * would exceed cap, the length of perm_token and row_w. counts_out is [E]. */
+int64_t oracle_token_rounding(const float *L, const int32_t *idx, int64_t T, int E, int K,
+                              int M, int renorm, int64_t cap, int32_t *counts_out,
+                              int32_t *offsets, int32_t *perm_token, int32_t *row_map,
+                              float *row_w);
+
+/* Y[t,:] = bf16( sum over e ascending with row_map[t,e] >= 0 of Z[row_map[t,e],:] ),
+ * double sum; a token no expert kept gets zeros. row_map is [T,E]. */
+void oracle_combine_rows(const double *Z, const int32_t *row_map, int64_t T, int E, int d,
+                         uint16_t *Y);
+/* Same with bf16 Z rows (used to check the combine step on its own). */
+void oracle_combine_rows_bf16(const uint16_t *Z, const int32_t *row_map, int64_t T, int E,
+                              int d, uint16_t *Y);
+
+/* The layer output for a list of tokens under a given expert assignment, token
+ * by token: Y[t] = bf16( sum over e ascending with row_map[t,e] >= 0 of
+ * row_w[row_map[t,e]] * SwiGLU-MLP_e(X[t]) ). */
+void oracle_forward_assigned(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                             const uint16_t *W2, int64_t T, int d, int E, int n,
+                             const int32_t *row_map, const float *row_w,
+                             const int64_t *tokens, int64_t n_tok, uint16_t *Y_rows);
+
 /* Threads the OpenMP loops use (1 when built without OpenMP). */
 int oracle_num_threads(void);
 

@@ -3,9 +3,11 @@
 Every mutation below is a plausible slip in the oracle's C source: a reordered or
 unfused logit chain, the wrong tie-break, a dropped renormalisation, a sign error
 in SiLU, swapped gate/up branches, a dropped routing weight, truncating instead
-of rounding, a transposed weight, an unstable grouping. The test copies the
-oracle into a temporary directory, applies one mutation, rebuilds it there and
-runs the pin suite against the copy; the suite has to fail.
+of rounding, a transposed weight, an unstable grouping, and in Token Rounding a
+wrong rounding rule, a wrong order in the second sort or a dropped
+renormalisation. The test copies the oracle into a temporary directory, applies
+one mutation, rebuilds it there and runs the pin suites against the copy; they
+have to fail.
 """
 import os
 import shutil
@@ -36,7 +38,22 @@ MUTATIONS = [
      "for (int64_t t = T - 1; t >= 0; --t)\n        for (int k = 0; k < K; ++k) {\n            int32_t slot"),
     ("gather_ignores_perm", "const uint16_t *x = X + (int64_t)perm_token[p] * d;",
      "const uint16_t *x = X + (int64_t)p * d;"),
+    # Token Rounding
+    ("tr_always_round_down", "(int64_t)M * ((f[e] + M / 2) / M);", "(int64_t)M * (f[e] / M);"),
+    ("tr_always_round_up", "(int64_t)M * ((f[e] + M / 2) / M);", "(int64_t)M * ((f[e] + M - 1) / M);"),
+    ("tr_halves_down", "(int64_t)M * ((f[e] + M / 2) / M);", "(int64_t)M * ((f[e] + (M - 1) / 2) / M);"),
+    ("tr_no_cap_at_T", "if (c > T) c = (int64_t)M * (f[e] / M);", ""),
+    ("tr_members_not_first", "return a->member ? -1 : 1;", "return a->member ? 1 : -1;"),
+    ("tr_low_scores_first", "if (a->v > b->v) return -1;\n    if (a->v < b->v) return 1;\n    return (a->t",
+     "if (a->v < b->v) return -1;\n    if (a->v > b->v) return 1;\n    return (a->t"),
+    ("tr_ties_to_high_token", "return (a->t > b->t) - (a->t < b->t);", "return (a->t < b->t) - (a->t > b->t);"),
+    ("tr_renorm_ignored", "renorm ? pe / kept : pe", "pe"),
+    ("tr_row_order_descending_t", "for (int e = 0; e < E; ++e)\n        for (int64_t t = 0; t < T; ++t) {\n            if (keep",
+     "for (int e = 0; e < E; ++e)\n        for (int64_t t = T - 1; t >= 0; --t) {\n            if (keep"),
+    ("combine_rows_skips_row0", "if (r >= 0) y = y + Z[", "if (r > 0) y = y + Z["),
 ]
+
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_rounding.py"]
 
 
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
@@ -49,6 +66,6 @@ def test_planted_mistake_fails_a_pin(tmp_path, name, old, new):
     (dst / "moe_oracle.c").write_text(src.replace(old, new))
     env = dict(os.environ, PYTHONPATH=f"{tmp_path}{os.pathsep}{ROOT}")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
                        env=env, capture_output=True, text=True, cwd=str(tmp_path), timeout=600)
     assert r.returncode != 0, f"mutation {name} passed every pin:\n{r.stdout[-2000:]}"
