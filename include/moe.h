@@ -163,7 +163,8 @@ moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_b
 
 /* Down-projection GEMM with the routing weight applied in its epilogue:
  *   Z[p,:] = bf16( topk_w[perm_slot[p]] * (H[p,:] W2[e]) ).
- * H [T*K,n] bf16 grouped rows; Z [T*K,d] bf16. */
+ * H [T*K,n] bf16 grouped rows; Z [T*K,d] bf16. perm_slot may be NULL: the
+ * weight of row p is then topk_w[p]. */
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
                            const int32_t *perm_slot, const int32_t *offsets,
                            int T, int d, int E, int K, int n, moe_bf16 *Z,
@@ -212,6 +213,74 @@ moe_status_t moe_forward_host(const moe_bf16 *X_host, moe_bf16 *Y_host,
                               const float *bias, const moe_bf16 *W1, const moe_bf16 *W3,
                               const moe_bf16 *W2, int T, int d, int E, int K, int n,
                               int renorm, void *ws, size_t ws_bytes, void *stream);
+
+/* ---- Token Rounding (SonicMoE page §3): a routing mode whose per-expert row
+ * counts are multiples of the tile size M, so grouped GEMM tiles carry no
+ * padding rows. Starting from the top-K choice (moe_route):
+ *   1. f_e = top-K count of expert e (§3.1);
+ *   2. c_e = f_e rounded to the nearest multiple of M, halves up (§3.2), or the
+ *      rounded-down multiple when that exceeds T;
+ *   3. the second sort (§3.1): expert e keeps the first c_e tokens in the order
+ *      (chose e in its top-K first, logit L[t,e] descending, t ascending), so a
+ *      rounded-down expert drops its lowest-scoring chosen tokens and a
+ *      rounded-up one gains the highest-scoring unchosen tokens;
+ *   4. rows grouped by expert, ascending t; row_map[t,e] = row of (t,e) or -1;
+ *   5. weights (§3.2): p = softmax(L[t,:]); row_w[row] = p_e / (sum of p over
+ *      the experts that kept t) with renorm, else p_e.
+ * A token may end with more or fewer than K experts, or none (its output is 0). */
+
+/* Most rows Token Rounding can produce: min(T*E, T*K + E*floor(M/2));
+ * -1 for invalid arguments. Size perm_token and row_w with it, and the tile
+ * list with capacity/128 + E entries. */
+int64_t moe_round_capacity(int T, int E, int K, int M);
+
+/* Workspace bytes of moe_round_routing: the error word, plus per-expert column
+ * scratch of 5*E*T bytes when T > 32768 (smaller T stage it on chip). */
+size_t moe_round_workspace_bytes(int T, int E);
+
+/* Token Rounding of a top-K routing. logits [T,E] fp32, topk_idx [T,K] and
+ * counts [E] exactly as moe_route / moe_route_logits wrote them; 1 <= M <= 65536.
+ * Outputs: counts_out [E] (c_e), offsets [E+1], perm_token [capacity]
+ * (offsets[E] entries written), row_map [T,E], row_w [capacity], tiles
+ * [capacity/128+E][4] int32 = {expert, first row, rows <= 128, 0} (16-byte
+ * aligned) and num_tiles [1]. ws: moe_round_workspace_bytes, zeroed once before
+ * first use (its first word is the device error word; counts that disagree
+ * with topk_idx set MOE_DEVERR_COUNT_MISMATCH and no row is written out of
+ * range). Two kernels; no host synchronisation. */
+moe_status_t moe_round_routing(const float *logits, const int32_t *topk_idx,
+                               const int32_t *counts, int T, int E, int K, int M, int renorm,
+                               int32_t *counts_out, int32_t *offsets, int32_t *perm_token,
+                               int32_t *row_map, float *row_w, int32_t *tiles,
+                               int32_t *num_tiles, void *ws, size_t ws_bytes, void *stream);
+
+/* Combine under a row map: Y[t,:] = bf16( sum over e = 0..E-1 ascending with
+ * 0 <= row_map[t,e] < rows of Z[row_map[t,e],:] ), fp32 accumulation, one
+ * rounding; a token with no row gets zeros. Z [rows,d] bf16, Y [T,d] bf16. */
+moe_status_t moe_combine_rows(const moe_bf16 *Z, const int32_t *row_map, int T, int E, int d,
+                              int64_t rows, moe_bf16 *Y, void *stream);
+
+/* Workspace bytes of moe_forward_rounded for this shape (0 if invalid). */
+size_t moe_workspace_bytes_rounded(int T, int d, int E, int K, int n);
+
+/* The whole layer under Token Rounding with M = 128 (the GEMM row tile):
+ * route -> round -> gate/up+SwiGLU -> down+row weight -> combine_rows.
+ * row_map_out [T,E] may be NULL (kept in the workspace then). The rounded
+ * counts, offsets, perm_token and row weights stay in the workspace.
+ * Enqueues 7 kernels (8 when the gate/up GEMM runs on CTA pairs) and at most
+ * one memset; no host synchronisation. */
+moe_status_t moe_forward_rounded(const moe_bf16 *X, const float *Wr, const float *bias,
+                                 const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
+                                 int T, int d, int E, int K, int n, int renorm, moe_bf16 *Y,
+                                 int32_t *row_map_out, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_forward_rounded recording 6 CUDA events like moe_forward_traced: before
+ * the router, then after route, rounding, gate/up GEMM, down GEMM, combine. */
+moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, const float *bias,
+                                        const moe_bf16 *W1, const moe_bf16 *W3,
+                                        const moe_bf16 *W2, int T, int d, int E, int K, int n,
+                                        int renorm, moe_bf16 *Y, int32_t *row_map_out,
+                                        void *ws, size_t ws_bytes, void *stream,
+                                        void *const *events, int n_events);
 
 /* Wait for `stream`, read and clear the workspace's device error word.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK (or

@@ -80,9 +80,16 @@ int sm_count() {
     return (di != nullptr && di->sms > 0) ? di->sms : 1;
 }
 
-WsLayout ws_layout(int T, int d, int E, int K, int n) {
+int64_t round_capacity(int T, int E, int K, int M) {
+    const int64_t a = (int64_t)T * E, b = (int64_t)T * K + (int64_t)E * (M / 2);
+    return a < b ? a : b;
+}
+
+namespace {
+
+WsLayout layout_impl(int T, int d, int E, int K, int n, size_t R, bool rounded) {
     WsLayout L{};
-    const size_t R = (size_t)T * K;
+    L.rows = R;
     L.nchunks = (T + kChunk - 1) / kChunk;
     L.max_tiles = (int)(R / kTileM) + E;
     size_t off = 0;
@@ -110,8 +117,24 @@ WsLayout ws_layout(int T, int d, int E, int K, int n) {
     L.h = take(2 * R * (size_t)n);
     L.z = take(2 * R * (size_t)d);
     L.logits = take(4 * (size_t)T * E);
+    if (rounded) {
+        L.counts_round = take(4 * (size_t)E);
+        L.row_map = take(4 * (size_t)T * E);
+        L.row_w = take(4 * R);
+        L.round_scratch = take(round_scratch_bytes(T, E));
+    }
     L.total = off;
     return L;
+}
+
+}  // namespace
+
+WsLayout ws_layout(int T, int d, int E, int K, int n) {
+    return layout_impl(T, d, E, K, n, (size_t)T * K, false);
+}
+
+WsLayout ws_layout_rounded(int T, int d, int E, int K, int n) {
+    return layout_impl(T, d, E, K, n, (size_t)round_capacity(T, E, K, kTileM), true);
 }
 
 }  // namespace moe
@@ -211,7 +234,7 @@ moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_b
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
                            const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
                            int K, int n, moe_bf16 *Z, void *ws, size_t ws_bytes, void *stream) {
-    if (!H || !W2 || !topk_w || !perm_slot || !offsets || !Z || !ws) return MOE_ERR_INVALID_ARG;
+    if (!H || !W2 || !topk_w || !offsets || !Z || !ws) return MOE_ERR_INVALID_ARG;
     moe_status_t s = check_mlp_shape(T, d, E, K, n);
     if (s != MOE_OK) return s;
     if (!aligned16(H) || !aligned16(W2) || !aligned16(Z)) return MOE_ERR_INVALID_ARG;
@@ -352,6 +375,137 @@ moe_status_t moe_sync_check(void *ws, void *stream, uint32_t *word_out) {
     if (word & MOE_DEVERR_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
     if (word != 0) return MOE_ERR_DEVICE_CHECK;
     return MOE_OK;
+}
+
+
+// ------------------------------------------------------------ Token Rounding
+
+int64_t moe_round_capacity(int T, int E, int K, int M) {
+    if (T < 1 || E < 1 || K < 1 || K > E || M < 1) return -1;
+    return round_capacity(T, E, K, M);
+}
+
+size_t moe_round_workspace_bytes(int T, int E) {
+    if (T < 1 || E < 1 || E > kMaxE) return 0;
+    return 256 + round_scratch_bytes(T, E);
+}
+
+moe_status_t moe_round_routing(const float *logits, const int32_t *topk_idx,
+                               const int32_t *counts, int T, int E, int K, int M, int renorm,
+                               int32_t *counts_out, int32_t *offsets, int32_t *perm_token,
+                               int32_t *row_map, float *row_w, int32_t *tiles,
+                               int32_t *num_tiles, void *ws, size_t ws_bytes, void *stream) {
+    if (!logits || !topk_idx || !counts || !counts_out || !offsets || !perm_token || !row_map ||
+        !row_w || !tiles || !num_tiles || !ws || (renorm != 0 && renorm != 1))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, 8, E, K);
+    if (s != MOE_OK) return s;
+    if (M < 1) return MOE_ERR_INVALID_ARG;
+    if (M > kMaxRoundM || (int64_t)T * E >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(tiles)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_round_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    void *scratch = round_scratch_bytes(T, E) ? static_cast<char *>(ws) + 256 : nullptr;
+    return from_cuda(launch_round(logits, topk_idx, counts, T, E, K, M, renorm, counts_out,
+                                  offsets, perm_token, row_map, row_w, tiles, num_tiles, scratch,
+                                  at<uint32_t>(ws, 0), as_stream(stream)));
+}
+
+moe_status_t moe_combine_rows(const moe_bf16 *Z, const int32_t *row_map, int T, int E, int d,
+                              int64_t rows, moe_bf16 *Y, void *stream) {
+    if (!Z || !row_map || !Y || rows < 0) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, d, E, 1);
+    if (s != MOE_OK) return s;
+    if (!aligned16(Z) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_combine_rows(reinterpret_cast<const __nv_bfloat16 *>(Z), row_map, T, E,
+                                         d, rows, reinterpret_cast<__nv_bfloat16 *>(Y),
+                                         as_stream(stream)));
+}
+
+size_t moe_workspace_bytes_rounded(int T, int d, int E, int K, int n) {
+    if (T < 1 || E < 1 || K < 1 || d < 0 || n < 0 || E > kMaxE || K > kMaxK || K > E) return 0;
+    return ws_layout_rounded(T, d, E, K, n).total;
+}
+
+moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, const float *bias,
+                                        const moe_bf16 *W1, const moe_bf16 *W3,
+                                        const moe_bf16 *W2, int T, int d, int E, int K, int n,
+                                        int renorm, moe_bf16 *Y, int32_t *row_map_out, void *ws,
+                                        size_t ws_bytes, void *stream, void *const *events,
+                                        int n_events) {
+    if (!X || !Wr || !W1 || !W3 || !W2 || !Y || !ws || (renorm != 0 && renorm != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (n_events < 0 || (n_events > 0 && events == nullptr)) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    const WsLayout L = ws_layout_rounded(T, d, E, K, n);
+    if ((int64_t)L.rows * (d > n ? d : n) >= (1ll << 31) || (int64_t)T * E >= (1ll << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(Y))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    int ev = 0;
+    auto mark = [&]() -> bool {
+        if (ev < n_events) {
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[ev]), st) != cudaSuccess)
+                return false;
+        }
+        ++ev;
+        return true;
+    };
+    const int R = (int)L.rows;
+    uint32_t *err = at<uint32_t>(ws, L.err);
+    float *logits = at<float>(ws, L.logits);
+    int32_t *idx = at<int32_t>(ws, L.topk_idx);
+    float *w = at<float>(ws, L.topk_w);
+    int32_t *counts = at<int32_t>(ws, L.counts);
+    int32_t *counts_r = at<int32_t>(ws, L.counts_round);
+    int32_t *offsets = at<int32_t>(ws, L.offsets);
+    int32_t *perm_token = at<int32_t>(ws, L.perm_token);
+    int32_t *row_map = row_map_out ? row_map_out : at<int32_t>(ws, L.row_map);
+    float *row_w = at<float>(ws, L.row_w);
+    __nv_bfloat16 *h = at<__nv_bfloat16>(ws, L.h);
+    __nv_bfloat16 *z = at<__nv_bfloat16>(ws, L.z);
+    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(X);
+    void *scratch = L.round_scratch != 0 && round_scratch_bytes(T, E) != 0
+                        ? static_cast<char *>(ws) + L.round_scratch
+                        : nullptr;
+
+    if (!mark()) return MOE_ERR_CUDA;
+    if (launch_route(x, Wr, bias, T, d, E, K, renorm, logits, idx, w, counts, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_round(logits, idx, counts, T, E, K, kTileM, renorm, counts_r, offsets, perm_token,
+                     row_map, row_w, at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.num_tiles),
+                     scratch, err, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                            reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n, h,
+                            at<__nv_bfloat16>(ws, L.xg), err, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    // the weight of grouped row p is row_w[p] (no slot indirection)
+    if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), row_w, nullptr, offsets,
+                         R, d, E, n, z, err, st) != cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    if (launch_combine_rows(z, row_map, T, E, d, R, reinterpret_cast<__nv_bfloat16 *>(Y), st) !=
+            cudaSuccess ||
+        !mark())
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_rounded(const moe_bf16 *X, const float *Wr, const float *bias,
+                                 const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2, int T,
+                                 int d, int E, int K, int n, int renorm, moe_bf16 *Y,
+                                 int32_t *row_map_out, void *ws, size_t ws_bytes, void *stream) {
+    return moe_forward_rounded_traced(X, Wr, bias, W1, W3, W2, T, d, E, K, n, renorm, Y,
+                                      row_map_out, ws, ws_bytes, stream, nullptr, 0);
 }
 
 }  // extern "C"

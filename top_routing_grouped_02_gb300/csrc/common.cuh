@@ -16,6 +16,8 @@ constexpr int kTileM = 128;
 // Largest supported expert count and top-K.
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
+// Largest Token Rounding tile size accepted.
+constexpr int kMaxRoundM = 1 << 16;
 // Tokens per grouping chunk (one warp, one bit per token).
 constexpr int kChunk = 32;
 
@@ -40,7 +42,12 @@ struct WsLayout {
     size_t h;           // bf16  [R, n]
     size_t z;           // bf16  [R, d]
     size_t logits;      // fp32  [T, E] router logits (moe_forward only)
+    size_t counts_round;// int32 [E]    Token Rounding counts (rounded layout only)
+    size_t row_map;     // int32 [T, E] Token Rounding rows (rounded layout only)
+    size_t row_w;       // fp32  [R]    Token Rounding row weights (rounded layout only)
+    size_t round_scratch; // Token Rounding column scratch (rounded layout, large T only)
     size_t total;
+    size_t rows;        // row capacity R of the grouped buffers
     int nchunks;
     int max_tiles;
 };
@@ -49,6 +56,13 @@ struct WsLayout {
 enum : int { kWordErr = 0, kWordDone = 1 };
 
 WsLayout ws_layout(int T, int d, int E, int K, int n);
+// Layout for the Token Rounding forward: grouped buffers sized for the largest
+// rounded row count, plus row_map, row_w and the rounding scratch.
+WsLayout ws_layout_rounded(int T, int d, int E, int K, int n);
+// Most rows Token Rounding with tile size M can produce.
+int64_t round_capacity(int T, int E, int K, int M);
+// Workspace bytes the rounding kernel needs besides its outputs.
+size_t round_scratch_bytes(int T, int E);
 
 // ---- launchers (each returns the CUDA error of its launch) -----------------
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
@@ -76,6 +90,16 @@ cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              __nv_bfloat16 *Z, uint32_t *err, cudaStream_t s);
 cudaError_t launch_combine(const __nv_bfloat16 *Z, const int32_t *row_of_slot, int T, int K,
                            int d, __nv_bfloat16 *Y, cudaStream_t s);
+
+// Token Rounding of a top-K routing (rounding.cu): rounded counts, grouped
+// offsets, perm_token, row_map [T,E], row weights and the 128-row tile list.
+cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *counts, int T, int E,
+                         int K, int M, int renorm, int32_t *counts_out, int32_t *offsets,
+                         int32_t *perm_token, int32_t *row_map, float *row_w, int32_t *tiles,
+                         int32_t *num_tiles, void *scratch, uint32_t *err, cudaStream_t s);
+// Y[t] = sum of Z[row_map[t,e]] over e ascending (rows >= rows_cap are skipped).
+cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map, int T, int E,
+                                int d, int64_t rows_cap, __nv_bfloat16 *Y, cudaStream_t s);
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();

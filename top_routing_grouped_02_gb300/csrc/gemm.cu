@@ -127,7 +127,7 @@ struct GemmArgs {
     __nv_bfloat16 *out;       // H [R, n] or Z [R, d]
     int out_ld;               // row length of out (elements)
     const float *topk_w;      // down only: routing weights [T*K]
-    const int32_t *perm_slot; // down only: slot of each grouped row
+    const int32_t *perm_slot; // down only: slot of each grouped row (NULL: the row itself)
     uint32_t *err;            // device error word
 };
 
@@ -472,7 +472,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else {
                 float w = 0.f;
                 if (valid) {
-                    const int slot = __ldg(args.perm_slot + p);
+                    const int slot = args.perm_slot != nullptr ? __ldg(args.perm_slot + p) : (int)p;
                     if (slot >= 0 && slot < args.R) w = __ldg(args.topk_w + slot);
                     else atomicOr(args.err, MOE_DEVERR_BAD_EXPERT);
                 }

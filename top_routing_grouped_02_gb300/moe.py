@@ -24,7 +24,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_CHECK"}
 # kernels each entry point launches (for launch accounting)
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
-            "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 8}
+            "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 8, "moe_round_routing": 2,
+            "moe_combine_rows": 1, "moe_forward_rounded": 7}
 TILE_M = 128
 
 
@@ -60,6 +61,16 @@ _SIGS = {
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
                               _P]),
     "moe_sync_check": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_round_capacity": (ctypes.c_int64, [_I, _I, _I, _I]),
+    "moe_round_workspace_bytes": (_SZ, [_I, _I]),
+    "moe_round_routing": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                               _P]),
+    "moe_combine_rows": (_I, [_P, _P, _I, _I, _I, ctypes.c_int64, _P, _P]),
+    "moe_workspace_bytes_rounded": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_rounded": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
+                                 _P]),
+    "moe_forward_rounded_traced": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P,
+                                        _SZ, _P, ctypes.POINTER(_P), _I]),
 }
 
 
@@ -295,3 +306,86 @@ def moe_sync_check(ws, stream=None):
     word = ctypes.c_uint32(0)
     st = lib().moe_sync_check(_ptr(ws), _stream(stream), ctypes.byref(word))
     return int(st), int(word.value)
+
+
+# ------------------------------------------------------------ Token Rounding
+
+def moe_round_capacity(T: int, E: int, K: int, M: int = TILE_M) -> int:
+    return int(lib().moe_round_capacity(T, E, K, M))
+
+
+def moe_round_routing(logits, topk_idx, counts, M: int = TILE_M, renorm: bool = True, ws=None,
+                      stream=None) -> dict:
+    """Token Rounding of a top-K routing (outputs of moe_route). Returns counts,
+    offsets, perm_token [capacity], row_map [T,E], row_w [capacity], tiles and
+    num_tiles; offsets[E] entries of perm_token/row_w are meaningful."""
+    T, E = logits.shape
+    K = topk_idx.shape[1]
+    dev = logits.device
+    cap = moe_round_capacity(T, E, K, M)
+    if cap < 0:
+        raise ValueError("invalid Token Rounding shape")
+    if ws is None:
+        ws = torch.zeros(int(lib().moe_round_workspace_bytes(T, E)), dtype=torch.uint8, device=dev)
+    out = dict(
+        counts=torch.empty(E, dtype=torch.int32, device=dev),
+        offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+        perm_token=torch.full((max(cap, 1),), -1, dtype=torch.int32, device=dev),
+        row_map=torch.empty((T, E), dtype=torch.int32, device=dev),
+        row_w=torch.zeros(max(cap, 1), dtype=torch.float32, device=dev),
+        tiles=torch.zeros((cap // TILE_M + E, 4), dtype=torch.int32, device=dev),
+        num_tiles=torch.empty(1, dtype=torch.int32, device=dev),
+    )
+    _check("moe_round_routing", lib().moe_round_routing(
+        _ptr(logits, torch.float32, "logits"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(counts, torch.int32, "counts"), T, E, K, M, int(bool(renorm)),
+        _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm_token"]), _ptr(out["row_map"]),
+        _ptr(out["row_w"]), _ptr(out["tiles"]), _ptr(out["num_tiles"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def moe_combine_rows(Z, row_map, stream=None):
+    R, d = Z.shape
+    T, E = row_map.shape
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device=Z.device)
+    _check("moe_combine_rows", lib().moe_combine_rows(
+        _ptr(Z, torch.bfloat16, "Z"), _ptr(row_map, torch.int32, "row_map"), T, E, d, R,
+        _ptr(Y), _stream(stream)))
+    return Y
+
+
+def workspace_rounded(T: int, d: int, E: int, K: int, n: int, device=None) -> torch.Tensor:
+    """A zeroed workspace tensor for moe_forward_rounded."""
+    nbytes = int(lib().moe_workspace_bytes_rounded(T, d, E, K, n))
+    if nbytes == 0:
+        raise ValueError("invalid layer shape")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_forward_rounded(X, Wr, W1, W3, W2, K: int, bias=None, renorm: bool = True, ws=None,
+                        Y=None, row_map=None, stream=None, events=None):
+    """Y [T,d] bf16 for the layer under Token Rounding (tile size 128). An optional
+    row_map [T,E] int32 receives each (token, expert) row or -1."""
+    T, d = X.shape
+    E, _, n = W1.shape
+    if ws is None:
+        ws = workspace_rounded(T, d, E, K, n, X.device)
+    if Y is None:
+        Y = torch.empty((T, d), dtype=torch.bfloat16, device=X.device)
+    args = (_ptr(X, torch.bfloat16, "X"), _ptr(Wr, torch.float32, "Wr"),
+            _ptr(bias, torch.float32, "bias"), _ptr(W1, torch.bfloat16, "W1"),
+            _ptr(W3, torch.bfloat16, "W3"), _ptr(W2, torch.bfloat16, "W2"), T, d, E, K, n,
+            int(bool(renorm)), _ptr(Y, torch.bfloat16, "Y"), _ptr(row_map, torch.int32, "row_map"),
+            _ptr(ws), ws.numel(), _stream(stream))
+    if events:
+        for e in events:
+            if e.cuda_event == 0:
+                e.record()
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check("moe_forward_rounded_traced", lib().moe_forward_rounded_traced(*args, arr,
+                                                                               len(events)))
+    else:
+        _check("moe_forward_rounded", lib().moe_forward_rounded(*args))
+    return Y
