@@ -15,6 +15,11 @@ Prints ONE JSON line on rank 0:
   clocks      nvidia-smi SM clocks / throttle reasons sampled during the timed region
   extra       tokens/s, per-kernel times, router and combine GB/s, % of peak
 
+--routing rounded runs the layer under Token Rounding (moe_forward_rounded: each
+expert's top-K count rounded to a multiple of the 128-row tile); its value
+counts the rows the rounded routing computes, and extra.topk_rows_equiv_tflops
+the top-K rows, T*K, over the same time.
+
 --impl reference times the CPU oracle (the only reference this layer has) on the
 same workload and metric. Under torchrun every rank runs its own replica (tokens
 are independent: weak scaling, no collective on the data path).
@@ -36,6 +41,9 @@ if ROOT not in sys.path:
 STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine"]
 KERNELS_PER_STAGE = {"route": 2, "permute": 3, "gemm_gate_up": 1, "gemm_down": 1, "combine": 1}
 KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
+# Token Rounding (--routing rounded): the grouping step is the rounding step
+STAGES_ROUNDED = ["route", "round", "gemm_gate_up", "gemm_down", "combine"]
+KERNELS_PER_STEP_ROUNDED = 2 + 3 + 1 + 1 + 1
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
 # the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
@@ -43,9 +51,10 @@ METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB
 GEMM1_TRAFFIC_BYTES = {"mixtral": 2.584302e9 + 0.231343e9}
 
 
-def workload_desc(name, c):
+def workload_desc(name, c, routing="topk"):
     return (f"{name}-shaped MoE layer forward T={c['T']} d={c['d']} E={c['E']} K={c['K']} "
-            f"n={c['n']}" + (" zipf-bias" if c.get("zipf") else ""))
+            f"n={c['n']}" + (" zipf-bias" if c.get("zipf") else "")
+            + (" token-rounding M=128" if routing == "rounded" else ""))
 
 
 def useful_flops(c, tokens=None):
@@ -234,22 +243,33 @@ def run_gpu(args, c, world, rank, local):
     dev = torch.device("cuda", local)
     T, d, E, K, n = c["T"], c["d"], c["E"], c["K"], c["n"]
     inp = synth.layer_inputs(device=dev, seed=args.seed + rank, **c)
-    ws = moe.workspace(T, d, E, K, n, dev)
+    rounded = args.routing == "rounded"
+    stages = STAGES_ROUNDED if rounded else STAGES
+    ws = (moe.workspace_rounded if rounded else moe.workspace)(T, d, E, K, n, dev)
     Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    row_map = torch.empty((T, E), dtype=torch.int32, device=dev) if rounded else None
     stream = torch.cuda.current_stream()
 
     def step(events=None):
-        moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"],
-                        ws=ws, Y=Y, stream=stream, events=events)
+        if rounded:
+            moe.moe_forward_rounded(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
+                                    inp["bias"], ws=ws, Y=Y, row_map=row_map, stream=stream,
+                                    events=events)
+        else:
+            moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"],
+                            ws=ws, Y=Y, stream=stream, events=events)
 
     for _ in range(args.warmup):
         step()
     st, word = moe.moe_sync_check(ws)
     if st != 0:
         raise RuntimeError(f"device error word {word:#x} during warm-up")
+    # rows the expert GEMMs compute: T*K for top-K routing; Token Rounding's
+    # rounded total (the same in every step: the inputs do not change)
+    R = int((row_map >= 0).sum().item()) if rounded else T * K
 
     # timed region: K steps, events between the stages of every step
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
            for _ in range(args.steps)]
     for row in evs:
         for e in row:
@@ -271,9 +291,9 @@ def run_gpu(args, c, world, rank, local):
     ms_total = start.elapsed_time(stop)
     ms_max = max_over_ranks(ms_total, world)
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
-                                  for i in range(args.steps)])) for j, s in enumerate(STAGES)}
+                                  for i in range(args.steps)])) for j, s in enumerate(stages)}
     ms_step = ms_max / args.steps
-    flops = useful_flops(c)
+    flops = 2.0 * R * 3 * d * n
     value = aggregate(flops * args.steps, ms_max / 1e3, world) / 1e12
 
     # end to end through the host-buffer entry point (pinned host memory)
@@ -282,20 +302,30 @@ def run_gpu(args, c, world, rank, local):
     Xd = torch.empty_like(inp["X"])
     Yd = torch.empty_like(inp["X"])
     e2e_steps = max(3, min(args.steps, 20))
+
+    def host_step():
+        if rounded:
+            # same sequence as moe_forward_host: copy in, layer, copy out, wait
+            Xd.copy_(Xh, non_blocking=True)
+            moe.moe_forward_rounded(Xd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
+                                    inp["bias"], ws=ws, Y=Yd, stream=stream)
+            Yh.copy_(Yd, non_blocking=True)
+            stream.synchronize()
+        else:
+            moe.moe_forward_host(Xh, Yh, Xd, Yd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
+                                 inp["bias"], ws=ws, stream=stream)
+
     for _ in range(2):
-        moe.moe_forward_host(Xh, Yh, Xd, Yd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
-                             inp["bias"], ws=ws, stream=stream)
+        host_step()
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        moe.moe_forward_host(Xh, Yh, Xd, Yd, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
-                             inp["bias"], ws=ws, stream=stream)
+        host_step()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
     e2e_value = aggregate(flops * e2e_steps, e2e_s, world) / 1e12
 
     peaks = load_peaks()
-    R = T * K
     g1_flops = 4.0 * R * d * n
     g1_tflops = g1_flops / (stage_ms["gemm_gate_up"] / 1e3) / 1e12
     g2_tflops = 2.0 * R * n * d / (stage_ms["gemm_down"] / 1e3) / 1e12
@@ -307,7 +337,8 @@ def run_gpu(args, c, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload_desc(args.workload, c), **{k: c[k] for k in "TdEKn"},
+        "config": {"workload": workload_desc(args.workload, c, args.routing),
+                   **{k: c[k] for k in "TdEKn"}, "routing": args.routing, "rows": R,
                    "seed": args.seed, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "inputs larger than L2: expert weights "
                          f"{3 * E * d * n * 2 / 1e9:.2f} GB per step, no flush"},
@@ -316,15 +347,16 @@ def run_gpu(args, c, world, rank, local):
         "roofline": {"kernel": "gemm_gate_up (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
                      "achieved": round(g1_tflops, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": round(g1_tflops / peaks["bf16"], 4),
-                     "traffic": (GEMM1_TRAFFIC_BYTES or {}).get(args.workload),
+                     "traffic": None if rounded else (GEMM1_TRAFFIC_BYTES or {}).get(args.workload),
                      "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
                      "algorithmic_flops_per_launch": g1_flops},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP_ROUNDED if rounded else KERNELS_PER_STEP) * args.steps,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "extra": {
             "tokens_per_s": round(T * world / (ms_step / 1e3), 1),
             "pct_bf16_peak_layer": round(value / world / peaks["bf16"] * 100, 2),
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "topk_rows_equiv_tflops": round(useful_flops(c) * world / (ms_step / 1e3) / 1e12, 3),
             "gemm_down_tflops": round(g2_tflops, 2),
             "router_GBps": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9, 1),
             "router_frac_hbm": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9 / peaks["hbm"], 4),
@@ -333,7 +365,7 @@ def run_gpu(args, c, world, rank, local):
             "power_w_max": clocks.get("power_w_max"),
         },
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not rounded:
         import oracle
         oracle.build()
         inp_np = host_inputs(inp)
@@ -413,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral",
                     choices=["tiny", "mixtral", "dsv3", "sonic", "router"])
+    ap.add_argument("--routing", choices=["topk", "rounded"], default="topk",
+                    help="rounded: Token Rounding of the top-K counts to multiples of 128")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

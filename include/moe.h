@@ -234,8 +234,8 @@ moe_status_t moe_forward_host(const moe_bf16 *X_host, moe_bf16 *Y_host,
  * list with capacity/128 + E entries. */
 int64_t moe_round_capacity(int T, int E, int K, int M);
 
-/* Workspace bytes of moe_round_routing: the error word, plus per-expert column
- * scratch of 5*E*T bytes when T > 32768 (smaller T stage it on chip). */
+/* Workspace bytes of moe_round_routing: the error word (256 bytes) plus the
+ * per-expert candidate keys, 4*E*ceil(T/32)*32 bytes. */
 size_t moe_round_workspace_bytes(int T, int E);
 
 /* Token Rounding of a top-K routing. logits [T,E] fp32, topk_idx [T,K] and
@@ -246,7 +246,7 @@ size_t moe_round_workspace_bytes(int T, int E);
  * aligned) and num_tiles [1]. ws: moe_round_workspace_bytes, zeroed once before
  * first use (its first word is the device error word; counts that disagree
  * with topk_idx set MOE_DEVERR_COUNT_MISMATCH and no row is written out of
- * range). Two kernels; no host synchronisation. */
+ * range). Three kernels; no host synchronisation. */
 moe_status_t moe_round_routing(const float *logits, const int32_t *topk_idx,
                                const int32_t *counts, int T, int E, int K, int M, int renorm,
                                int32_t *counts_out, int32_t *offsets, int32_t *perm_token,
@@ -266,7 +266,7 @@ size_t moe_workspace_bytes_rounded(int T, int d, int E, int K, int n);
  * route -> round -> gate/up+SwiGLU -> down+row weight -> combine_rows.
  * row_map_out [T,E] may be NULL (kept in the workspace then). The rounded
  * counts, offsets, perm_token and row weights stay in the workspace.
- * Enqueues 7 kernels (8 when the gate/up GEMM runs on CTA pairs) and at most
+ * Enqueues 8 kernels (9 when the gate/up GEMM runs on CTA pairs) and at most
  * one memset; no host synchronisation. */
 moe_status_t moe_forward_rounded(const moe_bf16 *X, const float *Wr, const float *bias,
                                  const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,

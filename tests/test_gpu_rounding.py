@@ -162,6 +162,30 @@ def test_forward_rounded_matches_oracle(cfg, pair, monkeypatch):
     check_y(bits(Y), ref["Y"], "Y")
 
 
+def _many_experts_inputs(device):
+    # router coordinate 0 adds 2*X[t,0] to every logit of token t; token 0 has
+    # X[0,0] = 8, so it outranks every other token for every expert, while its
+    # MLP input stays ordinary
+    cfg = dict(T=4096, d=256, E=64, K=2, n=256, zipf=False)
+    inp = synth.layer_inputs(device=device, **cfg)
+    inp["Wr"][0, :] = 2.0
+    inp["X"][0, 0] = 8.0
+    return cfg, inp
+
+
+def test_forward_rounded_token_with_many_experts():
+    # every expert that rounds up adds token 0: it ends with more rows than the
+    # compact per-token list holds, and the combine reads its row_map entries
+    cfg, inp = _many_experts_inputs("cuda")
+    Y, rm = _forward_rounded(inp, cfg["K"])
+    torch.cuda.synchronize()
+    X, Wr, bias, W1, W3, W2 = layer_np(inp)
+    ref = oracle.forward_rounded(X, Wr, bias, W1, W3, W2, cfg["K"])
+    assert (ref["row_map"][0] >= 0).sum() > 16
+    assert np.array_equal(rm.cpu().numpy(), ref["row_map"])
+    check_y(bits(Y), ref["Y"], "Y")
+
+
 def test_forward_rounded_sonic_shape_sampled():
     # the SonicMoE-shaped layer (T=16384 d=1536 E=128 K=4 n=256) at full size:
     # routing in full, Y on sampled tokens from the token-by-token definition

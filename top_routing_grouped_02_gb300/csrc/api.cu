@@ -122,6 +122,8 @@ WsLayout layout_impl(int T, int d, int E, int K, int n, size_t R, bool rounded) 
         L.row_map = take(4 * (size_t)T * E);
         L.row_w = take(4 * R);
         L.round_scratch = take(round_scratch_bytes(T, E));
+        L.tok_rows = take(4 * (size_t)T * kTokCap);
+        L.tok_n = take(4 * (size_t)T);
     }
     L.total = off;
     return L;
@@ -405,10 +407,10 @@ moe_status_t moe_round_routing(const float *logits, const int32_t *topk_idx,
     if (!aligned16(tiles)) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_round_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_arch()) != MOE_OK) return s;
-    void *scratch = round_scratch_bytes(T, E) ? static_cast<char *>(ws) + 256 : nullptr;
+    void *scratch = static_cast<char *>(ws) + 256;
     return from_cuda(launch_round(logits, topk_idx, counts, T, E, K, M, renorm, counts_out,
-                                  offsets, perm_token, row_map, row_w, tiles, num_tiles, scratch,
-                                  at<uint32_t>(ws, 0), as_stream(stream)));
+                                  offsets, perm_token, row_map, row_w, tiles, num_tiles, nullptr,
+                                  nullptr, scratch, at<uint32_t>(ws, 0), as_stream(stream)));
 }
 
 moe_status_t moe_combine_rows(const moe_bf16 *Z, const int32_t *row_map, int T, int E, int d,
@@ -418,9 +420,9 @@ moe_status_t moe_combine_rows(const moe_bf16 *Z, const int32_t *row_map, int T, 
     if (s != MOE_OK) return s;
     if (!aligned16(Z) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
     if ((s = check_arch()) != MOE_OK) return s;
-    return from_cuda(launch_combine_rows(reinterpret_cast<const __nv_bfloat16 *>(Z), row_map, T, E,
-                                         d, rows, reinterpret_cast<__nv_bfloat16 *>(Y),
-                                         as_stream(stream)));
+    return from_cuda(launch_combine_rows(reinterpret_cast<const __nv_bfloat16 *>(Z), row_map,
+                                         nullptr, nullptr, T, E, d, rows,
+                                         reinterpret_cast<__nv_bfloat16 *>(Y), as_stream(stream)));
 }
 
 size_t moe_workspace_bytes_rounded(int T, int d, int E, int K, int n) {
@@ -470,9 +472,7 @@ moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, cons
     __nv_bfloat16 *h = at<__nv_bfloat16>(ws, L.h);
     __nv_bfloat16 *z = at<__nv_bfloat16>(ws, L.z);
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(X);
-    void *scratch = L.round_scratch != 0 && round_scratch_bytes(T, E) != 0
-                        ? static_cast<char *>(ws) + L.round_scratch
-                        : nullptr;
+    void *scratch = static_cast<char *>(ws) + L.round_scratch;
 
     if (!mark()) return MOE_ERR_CUDA;
     if (launch_route(x, Wr, bias, T, d, E, K, renorm, logits, idx, w, counts, st) != cudaSuccess ||
@@ -480,7 +480,8 @@ moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, cons
         return MOE_ERR_CUDA;
     if (launch_round(logits, idx, counts, T, E, K, kTileM, renorm, counts_r, offsets, perm_token,
                      row_map, row_w, at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.num_tiles),
-                     scratch, err, st) != cudaSuccess ||
+                     at<int32_t>(ws, L.tok_rows), at<int32_t>(ws, L.tok_n), scratch, err,
+                     st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
     if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
@@ -493,8 +494,8 @@ moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, cons
                          R, d, E, n, z, err, st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
-    if (launch_combine_rows(z, row_map, T, E, d, R, reinterpret_cast<__nv_bfloat16 *>(Y), st) !=
-            cudaSuccess ||
+    if (launch_combine_rows(z, row_map, at<int32_t>(ws, L.tok_rows), at<int32_t>(ws, L.tok_n), T,
+                            E, d, R, reinterpret_cast<__nv_bfloat16 *>(Y), st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
     return MOE_OK;

@@ -16,6 +16,9 @@ constexpr int kTileM = 128;
 // Largest supported expert count and top-K.
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
+// Rows per token kept in the compact per-token row list of the Token Rounding
+// forward (a token with more falls back to its row_map entries).
+constexpr int kTokCap = 16;
 // Largest Token Rounding tile size accepted.
 constexpr int kMaxRoundM = 1 << 16;
 // Tokens per grouping chunk (one warp, one bit per token).
@@ -45,7 +48,9 @@ struct WsLayout {
     size_t counts_round;// int32 [E]    Token Rounding counts (rounded layout only)
     size_t row_map;     // int32 [T, E] Token Rounding rows (rounded layout only)
     size_t row_w;       // fp32  [R]    Token Rounding row weights (rounded layout only)
-    size_t round_scratch; // Token Rounding column scratch (rounded layout, large T only)
+    size_t round_scratch; // Token Rounding candidate keys (rounded layout only)
+    size_t tok_rows;    // int32 [T, kTokCap] compact per-token rows (rounded layout only)
+    size_t tok_n;       // int32 [T] (rounded layout only)
     size_t total;
     size_t rows;        // row capacity R of the grouped buffers
     int nchunks;
@@ -96,9 +101,12 @@ cudaError_t launch_combine(const __nv_bfloat16 *Z, const int32_t *row_of_slot, i
 cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *counts, int T, int E,
                          int K, int M, int renorm, int32_t *counts_out, int32_t *offsets,
                          int32_t *perm_token, int32_t *row_map, float *row_w, int32_t *tiles,
-                         int32_t *num_tiles, void *scratch, uint32_t *err, cudaStream_t s);
-// Y[t] = sum of Z[row_map[t,e]] over e ascending (rows >= rows_cap are skipped).
-cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map, int T, int E,
+                         int32_t *num_tiles, int32_t *tok_rows, int32_t *tok_n, void *scratch,
+                         uint32_t *err, cudaStream_t s);
+// Y[t] = sum of Z[row_map[t,e]] over e ascending (rows >= rows_cap are skipped);
+// tok_rows [T][kTokCap] / tok_n [T] (nullable) list each token's rows compactly.
+cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map,
+                                const int32_t *tok_rows, const int32_t *tok_n, int T, int E,
                                 int d, int64_t rows_cap, __nv_bfloat16 *Y, cudaStream_t s);
 
 // Streaming multiprocessors of the current device (cached per device).

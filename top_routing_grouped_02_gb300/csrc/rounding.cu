@@ -9,19 +9,24 @@
 // the kept scores are then renormalised by a softmax (§3.2).
 //
 // Kernels:
+//   round_prep_kernel     32 tokens per block: transposes the logit tile through
+//                         shared memory into per-expert candidate keys keyT[E][Tp]
+//                         (coalesced rows; 0 marks a token that is not a
+//                         candidate of that expert's selection) and fills the
+//                         tile's row_map with -1.
 //   round_select_kernel   one CTA per expert. Every CTA recomputes all rounded
 //                         counts and their prefix sums from counts[] (E <= 256,
-//                         one warp), so the grouped offsets need no second
+//                         one warp), so the grouped offsets need no extra
 //                         launch. The second sort is a selection, not a full
-//                         sort: an MSB-first radix select on order-preserving
-//                         32-bit keys of the expert's logit column finds the
-//                         threshold score, ties at the threshold go to the
-//                         lowest token indices, and one ordered pass over the
-//                         tokens writes perm_token and the expert's column of
-//                         row_map. The column (keys + chosen flags) is staged
-//                         in shared memory when it fits, else in workspace.
-//   round_weights_kernel  one warp per token: softmax of the logit row, the
-//                         weight of every kept (token, expert) pair, fp64 sums.
+//                         sort: an MSB-first radix select on the order-preserving
+//                         32-bit keys finds the threshold score, ties at the
+//                         threshold go to the lowest token indices. Each thread
+//                         owns a contiguous run of tokens, so one block-wide
+//                         prefix sum orders the kept tokens; they go to
+//                         perm_token and to the expert's entries of row_map.
+//   round_weights_kernel  one warp per token: softmax of the logit row and the
+//                         weight of every kept (token, expert) pair, with
+//                         compensated fp32 sums.
 //   combine_rows_kernel   one warp per token: sum of the token's kept rows in
 //                         ascending expert order (fp32, one bf16 rounding).
 #include <cuda_bf16.h>
@@ -31,63 +36,209 @@
 namespace moe {
 namespace {
 
-constexpr int kRThreads = 1024;
-constexpr int kRWarps = kRThreads / 32;
-static_assert(kRWarps == 32, "the block scan assumes 32 warps");
-
-// Largest token count whose logit column is staged in shared memory
-// (4-byte key + 1-byte flag per token: 160 KB).
-constexpr int kRoundSmemT = 32768;
+enum : int { kKeep = 0, kDown = 1, kUp = 2 };
 
 // Monotone map of an fp32 value to uint32 (larger value, larger key); -0 ranks
-// as +0 so that equal values have equal keys.
+// as +0 so that equal values have equal keys. Finite values never map to 0.
 __device__ __forceinline__ uint32_t order_key(float x) {
     uint32_t b = __float_as_uint(x);
     if (b == 0x80000000u) b = 0u;
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Exclusive prefix count of `flag` over the block in thread order. Every thread
-// of the block must call it; *total receives the block's count.
-__device__ __forceinline__ int block_excl_count(bool flag, int *ws, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) ws[warp] = __popc(bal);
-    __syncthreads();
-    if (warp == 0) {
-        const int v = ws[lane];
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
+// Rounded count of an expert chosen f times: nearest multiple of M (halves up),
+// the rounded-down multiple when that exceeds T.
+__device__ __forceinline__ int rounded_count(int f, int M, int T) {
+    const int c = M * ((f + M / 2) / M);
+    return c > T ? M * (f / M) : c;
+}
+
+// Token-axis stride of the key rows (a multiple of 32 tokens: 16-byte rows).
+__host__ __device__ __forceinline__ int key_stride(int T) { return (T + 31) / 32 * 32; }
+
+// ---------------------------------------------------------------- prep ----
+constexpr int kPT = 32;        // tokens per prep block
+constexpr int kPThreads = 256;
+
+__global__ void __launch_bounds__(kPThreads)
+round_prep_kernel(const float *__restrict__ L, const int32_t *__restrict__ idx,
+                  const int32_t *__restrict__ counts, int T, int E, int K, int M, bool vec,
+                  uint32_t *__restrict__ keyT, int32_t *__restrict__ row_map, uint32_t *err) {
+    __shared__ float s_L[kPT][kMaxE + 1];
+    __shared__ uint32_t s_mem[kPT][kMaxE / 32];
+    __shared__ int s_mode[kMaxE];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.x * kPT;
+    const int Tp = key_stride(T);
+    for (int e = tid; e < E; e += kPThreads) {
+        const int f = max(0, min(__ldg(counts + e), T));
+        const int c = rounded_count(f, M, T);
+        s_mode[e] = c == f ? kKeep : (c < f ? kDown : kUp);
+    }
+    for (int i = tid; i < kPT * (kMaxE / 32); i += kPThreads) (&s_mem[0][0])[i] = 0u;
+    // the tile's logits: rows t0..t0+31 are contiguous in L
+    const int rows = min(kPT, T - t0);
+    if (vec) {
+        const float4 *src = reinterpret_cast<const float4 *>(L + (size_t)t0 * E);
+        for (int q = tid; q < rows * E / 4; q += kPThreads) {
+            const float4 v = __ldg(src + q);
+            const int j = 4 * q / E, e = 4 * q - j * E;
+            s_L[j][e] = v.x;
+            s_L[j][e + 1] = v.y;
+            s_L[j][e + 2] = v.z;
+            s_L[j][e + 3] = v.w;
         }
-        ws[lane] = incl - v;
-        if (lane == 31) ws[32] = incl;
+    } else {
+        for (int q = tid; q < rows * E; q += kPThreads) {
+            const int j = q / E, e = q - j * E;
+            s_L[j][e] = __ldg(L + (size_t)t0 * E + q);
+        }
     }
     __syncthreads();
-    const int r = ws[warp] + in_warp;
+    for (int q = tid; q < kPT * K; q += kPThreads) {
+        const int j = q / K;
+        if (t0 + j >= T) continue;
+        const int ex = __ldg(idx + (size_t)t0 * K + q);
+        if (ex >= 0 && ex < E) atomicOr(&s_mem[j][ex >> 5], 1u << (ex & 31));
+        else atomicOr(err, MOE_DEVERR_BAD_EXPERT);
+    }
+    __syncthreads();
+    // candidate keys, one expert row per warp step: lane = token
+    {
+        const int t = t0 + lane;
+        for (int e = warp; e < E; e += kPThreads / 32) {
+            uint32_t key = 0;
+            if (t < T) {
+                const bool m = (s_mem[lane][e >> 5] >> (e & 31)) & 1u;
+                const int mode = s_mode[e];
+                // kept without a choice (kKeep): members, marked 1; rounded down:
+                // members compete; rounded up: non-members compete
+                if (mode == kKeep) key = m ? 1u : 0u;
+                else if (mode == kDown ? m : !m) key = order_key(s_L[lane][e]);
+            }
+            if (t < Tp) keyT[(size_t)e * Tp + t] = key;
+        }
+    }
+    if (vec) {
+        int4 *dst = reinterpret_cast<int4 *>(row_map + (size_t)t0 * E);
+        for (int q = tid; q < rows * E / 4; q += kPThreads) dst[q] = make_int4(-1, -1, -1, -1);
+    } else {
+        for (int q = tid; q < rows * E; q += kPThreads) row_map[(size_t)t0 * E + q] = -1;
+    }
+}
+
+// -------------------------------------------------------------- select ----
+constexpr int kRThreads = 1024;
+static_assert(kRThreads / 32 == 32, "the block scan assumes 32 warps");
+
+// Exclusive prefix sum of v over the block in thread order; every thread of the
+// block must call it; *total receives the block's sum.
+__device__ __forceinline__ int block_excl_sum(int v, int *ws, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int x = ws[lane];
+        int xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, xi, o);
+            if (lane >= o) xi += n;
+        }
+        ws[lane] = xi - x;
+        if (lane == 31) ws[32] = xi;
+    }
+    __syncthreads();
+    const int r = ws[warp] + incl - v;
     *total = ws[32];
     __syncthreads();  // ws is reused by the next call
     return r;
 }
 
-// Histogram update with one shared-memory atomic per distinct digit of a warp.
-// Every lane of the warp must call it.
-__device__ __forceinline__ void hist_add(int *hist, bool active, uint32_t digit) {
-    const unsigned act = __ballot_sync(0xffffffffu, active);
-    if (active) {
-        const unsigned peers = __match_any_sync(act, digit);
-        if ((int)(__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[digit], __popc(peers));
+// Radix histograms of 2^W bins (5 <= W <= 12) are split into 32 groups of
+// P = 2^(W-5) consecutive bins, each followed by 4 padding words: a group starts
+// 16-byte aligned and the 32 groups fall on different banks, so warp 0 reads a
+// group per lane with 16-byte loads and no bank conflicts.
+__device__ __forceinline__ int hpad(uint32_t bin, int W) { return (int)(bin + 4u * (bin >> (W - 5))); }
+constexpr int kHistWords = 4096 + 4 * 32;
+
+// The bin, scanning bins 2^W-1 down to 0, at which the running count reaches
+// `remaining`: sel = {bin, count in higher bins, count in the bin}, or
+// sel[0] = 0xFFFFFFFF when the histogram holds fewer than `remaining`. Lane l
+// of warp 0 takes group 31-l (the bins 2^W-1-l*P down to 2^W-(l+1)*P); every
+// thread of the block must call it.
+__device__ __forceinline__ void digit_select(const int *hist, int W, int remaining, uint32_t *sel) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int P = 1 << (W - 5), grp = 31 - lane;
+        const int4 *g4 = reinterpret_cast<const int4 *>(hist + grp * (P + 4));
+        int sum = 0;
+        for (int j = 0; j < P / 4; ++j) {
+            const int4 h = g4[j];
+            sum += h.x + h.y + h.z + h.w;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+        if (hit == 0) {
+            if (lane == 0) sel[0] = 0xFFFFFFFFu;
+        } else if (lane == __ffs(hit) - 1) {
+            // this group's bins from the highest down
+            int acc = incl - sum;
+            for (int j = P / 4 - 1; j >= 0; --j) {
+                const int4 h = g4[j];
+                const int hv[4] = {h.w, h.z, h.y, h.x};
+                int found = -1;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (found < 0 && acc + hv[u] >= remaining) found = u;
+                    else if (found < 0) acc += hv[u];
+                }
+                if (found >= 0) {
+                    sel[0] = (uint32_t)(grp * P + 4 * j + 3 - found);
+                    sel[1] = (uint32_t)acc;
+                    sel[2] = (uint32_t)hv[found];
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Candidate keys are copied on chip when there are at most this many (all of
+// an expert's candidates, or those sharing the threshold's first 12 bits).
+constexpr int kListCap = 6144;
+
+// Appends the keys with `in` set to list[*count...] (warp-aggregated); keys
+// past the list's capacity are counted but not stored. Every lane of the warp
+// must call it.
+__device__ __forceinline__ void list_append(uint32_t *list, int *count, bool in, uint32_t key) {
+    const int lane = threadIdx.x & 31;
+    const unsigned bal = __ballot_sync(0xffffffffu, in);
+    if (bal != 0) {
+        int at = 0;
+        if (lane == __ffs(bal) - 1) at = atomicAdd(count, __popc(bal));
+        at = __shfl_sync(0xffffffffu, at, __ffs(bal) - 1);
+        const int pos = at + __popc(bal & ((1u << lane) - 1u));
+        if (in && pos < kListCap) list[pos] = key;
     }
 }
 
 struct RoundArgs {
-    const float *L;         // [T,E] logits
-    const int32_t *idx;     // [T,K] top-K choice
+    const uint32_t *keyT;   // [E][Tp] candidate keys (round_prep_kernel)
     const int32_t *counts;  // [E]   top-K counts
-    int T, E, K, M;
+    int T, E, M;
     int64_t cap;            // length of perm_token (rows beyond it are never written)
     int max_tiles;          // length of the tile list
     int32_t *counts_out;    // [E]
@@ -96,23 +247,30 @@ struct RoundArgs {
     int32_t *row_map;       // [T,E]
     int32_t *tiles;         // [tiles][4]
     int32_t *num_tiles;     // [1]
-    uint32_t *keys_g;       // [E*T] column scratch when T > kRoundSmemT
-    uint8_t *flags_g;       // [E*T]
     uint32_t *err;
 };
 
-enum : int { kKeep = 0, kDown = 1, kUp = 2 };
+// Loop over the groups of 4 keys of this thread's run (unrolled when they are
+// held in registers).
+#define FOR_RUN(g)                                     \
+    _Pragma("unroll") for (int g = 0; g < kLoopG; ++g) \
+        if (g >= G) break;                             \
+        else
 
+// GM > 0: a thread's run has at most GM groups of 4 keys (T <= 4096*GM), which
+// stay in registers for all passes; GM == 0: every pass reads them again.
+template <int GM>
 __global__ void __launch_bounds__(kRThreads, 1) round_select_kernel(RoundArgs a) {
-    extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ int s_off[kMaxE + 1];  // exclusive prefix of the rounded counts
     __shared__ int s_tb[kMaxE + 1];   // exclusive prefix of the 128-row tile counts
-    __shared__ int s_hist[256];
+    __shared__ __align__(16) int s_hist[kHistWords];
+    __shared__ uint32_t s_list[kListCap];
     __shared__ int s_ws[33];
-    __shared__ int s_members;
-    __shared__ uint32_t s_sel[3];     // threshold prefix, still to take, equal-key count
+    __shared__ int s_members, s_nlist;
+    __shared__ uint32_t s_sel[3];     // see digit_select
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.T, E = a.E, K = a.K, M = a.M;
+    const int T = a.T, E = a.E, M = a.M;
+    const int Tp = key_stride(T);
 
     // rounded counts of all experts and their prefix sums: 8 experts per lane
     if (warp == 0) {
@@ -120,12 +278,7 @@ __global__ void __launch_bounds__(kRThreads, 1) round_select_kernel(RoundArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int ex = lane * 8 + i;
-            int c = 0;
-            if (ex < E) {
-                const int f = max(0, min(a.counts[ex], T));
-                c = M * ((f + M / 2) / M);
-                if (c > T) c = M * (f / M);
-            }
+            const int c = ex < E ? rounded_count(max(0, min(a.counts[ex], T)), M, T) : 0;
             c8[i] = c;
             t8[i] = (c + kTileM - 1) / kTileM;
             cs += c;
@@ -152,17 +305,63 @@ __global__ void __launch_bounds__(kRThreads, 1) round_select_kernel(RoundArgs a)
             cb += c8[i];
             tb += t8[i];
         }
-        if (lane == 31 && E == 256) {
+        if (lane == 31 && E == kMaxE) {
             s_off[E] = ci;
             s_tb[E] = ti;
         }
     }
-    if (tid == 0) s_members = 0;
-    if (tid < 256) s_hist[tid] = 0;
-    __syncthreads();
+    if (tid == 0) {
+        s_members = 0;
+        s_nlist = 0;
+    }
+    for (int i = tid; i < kHistWords / 4; i += kRThreads)
+                reinterpret_cast<int4 *>(s_hist)[i] = make_int4(0, 0, 0, 0);
 
-    const int base = s_off[e], ce = s_off[e + 1] - base;
+    // this expert's own rounded count, without waiting for the scan
     const int f = max(0, min(a.counts[e], T));
+    const int ce = rounded_count(f, M, T);
+    const int mode = ce == f ? kKeep : (ce < f ? kDown : kUp);
+    const int N = mode == kDown ? ce : (mode == kUp ? ce - f : 0);
+    const int ncand = mode == kDown ? f : (mode == kUp ? T - f : 0);
+    const bool need_sel = N > 0;
+
+    // this thread's run: G consecutive groups of 4 tokens
+    const uint4 *keys4 = reinterpret_cast<const uint4 *>(a.keyT + (size_t)e * Tp);
+    const int nq = Tp / 4;
+    const int G = (nq + kRThreads - 1) / kRThreads;
+    const int q0 = tid * G;
+    auto load4 = [&](int g) -> uint4 {
+        const int q = q0 + g;
+        return q < nq ? __ldg(keys4 + q) : make_uint4(0, 0, 0, 0);
+    };
+    constexpr int kLoopG = GM > 0 ? GM : 0x7fffffff;
+    uint4 kr[GM > 0 ? GM : 1];
+    if constexpr (GM > 0) {
+#pragma unroll
+        for (int g = 0; g < GM; ++g) kr[g] = g < G ? load4(g) : make_uint4(0, 0, 0, 0);
+    }
+    auto key4 = [&](int g) -> uint4 {
+        if constexpr (GM > 0) return kr[g];
+        else return load4(g);
+    };
+
+    // the expert's membership must agree with counts[] (checked at the end)
+    int members = 0;
+    FOR_RUN(g) {
+        const uint4 v = key4(g);
+        const uint32_t k4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 4 * (q0 + g) + i;
+            members += (t < T && ((k4[i] != 0) == (mode != kUp))) ? 1 : 0;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) members += __shfl_xor_sync(0xffffffffu, members, o);
+    __syncthreads();
+    if (lane == 0) atomicAdd(&s_members, members);
+
+    const int base = s_off[e];
     if (e == 0) {
         for (int i = tid; i <= E; i += kRThreads) a.offsets[i] = s_off[i];
         if (tid == 0) a.num_tiles[0] = s_tb[E];
@@ -174,176 +373,272 @@ __global__ void __launch_bounds__(kRThreads, 1) round_select_kernel(RoundArgs a)
             reinterpret_cast<int4 *>(a.tiles)[tb + i] =
                 make_int4(e, base + i * kTileM, min(kTileM, ce - i * kTileM), 0);
     }
-    const int mode = ce == f ? kKeep : (ce < f ? kDown : kUp);
-    const int N = mode == kDown ? ce : (mode == kUp ? ce - f : 0);
-    const bool need_sel = N > 0;
 
-    const bool in_smem = T <= kRoundSmemT;
-    uint32_t *keys = in_smem ? reinterpret_cast<uint32_t *>(dyn) : a.keys_g + (size_t)e * T;
-    uint8_t *flg = in_smem ? dyn + (size_t)4 * T : a.flags_g + (size_t)e * T;
-
-    // pass 0: membership from the top-K choice, keys of the logit column, and the
-    // histogram of the top key byte over the candidates
-    int members = 0;
-    for (int t0 = 0; t0 < T; t0 += kRThreads) {
-        const int t = t0 + tid;
-        const bool in = t < T;
-        bool m = false;
-        uint32_t key = 0;
-        if (in) {
-            const int32_t *ir = a.idx + (size_t)t * K;
-            for (int k = 0; k < K; ++k) m |= (__ldg(ir + k) == e);
-            key = order_key(__ldg(a.L + (size_t)t * E + e));
-            keys[t] = key;
-            flg[t] = m ? 1 : 0;
-        }
-        members += m ? 1 : 0;
-        const bool cand = in && need_sel && (mode == kDown ? m : !m);
-        hist_add(s_hist, cand, key >> 24);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) members += __shfl_xor_sync(0xffffffffu, members, o);
-    if (lane == 0) atomicAdd(&s_members, members);
-    __syncthreads();
-    if (tid == 0 && s_members != f) atomicOr(a.err, MOE_DEVERR_COUNT_MISMATCH);
-
-    // radix select of the N-th largest candidate key, one byte per pass
+    // radix select of the N-th largest candidate key, most significant digit
+    // first. Few candidates: all of them are copied on chip and take digits of
+    // 11, 11 and 10 bits there. Many: a 12-bit digit over every key first, then
+    // the keys of the threshold bin are copied on chip for two 10-bit digits.
+    // A digit whose bin is taken whole ends the search early.
     uint32_t prefix = 0;
+    int pbits = 0;  // leading bits of the threshold fixed so far
     int remaining = N, eq_count = 0;
+    bool bad = false, whole = false;
     if (need_sel) {
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            if (pass > 0) {
-                if (tid < 256) s_hist[tid] = 0;
-                __syncthreads();
-                const uint32_t hm = 0xFFFFFFFFu << (shift + 8);
-                for (int t0 = 0; t0 < T; t0 += kRThreads) {
-                    const int t = t0 + tid;
-                    bool cand = false;
-                    uint32_t key = 0;
-                    if (t < T) {
-                        key = keys[t];
-                        const bool m = flg[t] != 0;
-                        cand = (mode == kDown ? m : !m) && ((key & hm) == (prefix & hm));
-                    }
-                    hist_add(s_hist, cand, (key >> shift) & 255u);
-                }
-                __syncthreads();
+        bool on_chip = ncand <= kListCap;
+        if (on_chip) {
+            FOR_RUN(g) {
+                const uint4 q = key4(g);
+                const uint32_t k4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) list_append(s_list, &s_nlist, k4[i] != 0, k4[i]);
             }
-            if (warp == 0) {
-                // lane l holds digits 255-8l .. 248-8l (descending)
-                int h[8], sum = 0;
+        } else {
+            FOR_RUN(g) {
+                const uint4 q = key4(g);
+                const uint32_t k4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    h[i] = s_hist[255 - 8 * lane - i];
-                    sum += h[i];
-                }
-                int incl = sum;
+                for (int i = 0; i < 4; ++i)
+                    if (k4[i] != 0) atomicAdd(&s_hist[hpad(k4[i] >> 20, 12)], 1);
+            }
+            __syncthreads();
+            digit_select(s_hist, 12, remaining, s_sel);
+            if (s_sel[0] == 0xFFFFFFFFu) {
+                bad = true;
+            } else {
+                prefix = s_sel[0] << 20;
+                pbits = 12;
+                remaining -= (int)s_sel[1];
+                eq_count = (int)s_sel[2];
+                whole = eq_count == remaining;
+                on_chip = eq_count <= kListCap;
+                if (on_chip && !whole) {
+                    FOR_RUN(g) {
+                        const uint4 q = key4(g);
+                        const uint32_t k4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
-                }
-                const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
-                if (hit == 0) {
-                    // fewer candidates than the count asks for (counts[] does not
-                    // match idx): take none; the row count check flags it
-                    if (lane == 0) {
-                        s_sel[0] = 0xFFFFFFFFu;
-                        s_sel[1] = 0;
-                        s_sel[2] = 1;
+                        for (int i = 0; i < 4; ++i)
+                            list_append(s_list, &s_nlist, k4[i] != 0 && (k4[i] >> 20) == (prefix >> 20),
+                                        k4[i]);
                     }
-                } else if (lane == __ffs(hit) - 1) {
-                    int acc = incl - sum, dg = 0, cnt = 0;
+                }
+            }
+        }
+        __syncthreads();
+        const int nl = min(s_nlist, kListCap);
+        while (!bad && !whole && pbits < 32) {
+            const int W = pbits == 0 ? 11 : (pbits == 11 ? 11 : (32 - pbits > 10 ? 10 : 32 - pbits));
+            const int shift = 32 - pbits - W;
+            const uint32_t hm = pbits == 0 ? 0u : (0xFFFFFFFFu << (32 - pbits));
+            for (int i = tid; i < kHistWords / 4; i += kRThreads)
+                reinterpret_cast<int4 *>(s_hist)[i] = make_int4(0, 0, 0, 0);
+            __syncthreads();
+            if (on_chip) {
+                for (int j2 = tid; j2 < nl; j2 += kRThreads) {
+                    const uint32_t k = s_list[j2];
+                    if ((k & hm) == (prefix & hm))
+                        atomicAdd(&s_hist[hpad((k >> shift) & ((1u << W) - 1u), W)], 1);
+                }
+            } else {
+                FOR_RUN(g) {
+                    const uint4 q = key4(g);
+                    const uint32_t k4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (cnt == 0 && acc + h[i] >= remaining) {
-                            dg = 255 - 8 * lane - i;
-                            cnt = h[i];
-                        } else if (cnt == 0) {
-                            acc += h[i];
-                        }
-                    }
-                    s_sel[0] = prefix | ((uint32_t)dg << shift);
-                    s_sel[1] = (uint32_t)(remaining - acc);
-                    s_sel[2] = (uint32_t)cnt;
+                    for (int i = 0; i < 4; ++i)
+                        if (k4[i] != 0 && (k4[i] & hm) == (prefix & hm))
+                            atomicAdd(&s_hist[hpad((k4[i] >> shift) & ((1u << W) - 1u), W)], 1);
                 }
             }
             __syncthreads();
-            prefix = s_sel[0];
-            remaining = (int)s_sel[1];
+            digit_select(s_hist, W, remaining, s_sel);
+            if (s_sel[0] == 0xFFFFFFFFu) {
+                bad = true;
+                break;
+            }
+            prefix |= s_sel[0] << shift;
+            pbits += W;
+            remaining -= (int)s_sel[1];
             eq_count = (int)s_sel[2];
-            if (remaining == 0) break;  // (only after a mismatch) nothing more to take
+            whole = eq_count == remaining && pbits < 32;
+        }
+        if (bad) {
+            // fewer candidates than the count asks for (counts[] does not match
+            // idx): take none; the row count check flags it
+            prefix = 0xFFFFFFFFu;
+            remaining = 0;
+            eq_count = 0;
+        } else if (whole) {
+            // every key of the bin is taken: the threshold is the bin's lowest key
+            prefix = prefix == 0 ? 0u : prefix - 1u;
+            remaining = 0;
+            eq_count = 0;
         }
     }
     const uint32_t v = prefix;
     const bool all_eq = remaining >= eq_count;
 
-    // ordered pass: which tokens the expert keeps, their rows, its row_map column
-    int carry_eq = 0, carry_keep = 0;
-    for (int t0 = 0; t0 < T; t0 += kRThreads) {
-        const int t = t0 + tid;
-        const bool in = t < T;
-        uint32_t key = 0;
-        bool m = false;
-        if (in) {
-            key = keys[t];
-            m = flg[t] != 0;
+    // ordered pass: threshold ties go to the lowest tokens, then the kept tokens
+    // are numbered in token order
+    int eq_before = 0;
+    if (need_sel && !all_eq) {
+        int eq_local = 0;
+        FOR_RUN(g) {
+            const uint4 q = key4(g);
+            eq_local += (q.x != 0 && q.x == v) + (q.y != 0 && q.y == v) + (q.z != 0 && q.z == v) +
+                        (q.w != 0 && q.w == v);
         }
-        bool chosen = false;
-        if (need_sel) {
-            const bool cand = in && (mode == kDown ? m : !m);
-            const bool gt = cand && key > v, eq = cand && key == v && remaining > 0;
-            if (all_eq) {
-                chosen = gt || eq;
-            } else {
-                int tot;
-                const int r = block_excl_count(eq, s_ws, &tot);
-                chosen = gt || (eq && carry_eq + r < remaining);
-                carry_eq += tot;
-            }
-        }
-        const bool keep = in && (mode == kKeep ? m : (mode == kDown ? chosen : (m || chosen)));
         int tot;
-        const int r = block_excl_count(keep, s_ws, &tot);
-        if (in) {
-            int row = -1;
-            if (keep && carry_keep + r < ce && (int64_t)base + carry_keep + r < a.cap) {
-                row = base + carry_keep + r;
-                a.perm_token[row] = t;
+        eq_before = block_excl_sum(eq_local, s_ws, &tot);
+    }
+    auto kept = [&](uint32_t key, int t, int &eq_seen) -> bool {
+        if (t >= T) return false;
+        const bool cand = key != 0;
+        if (mode == kKeep) return cand;
+        bool chosen = false;
+        if (cand && need_sel) {
+            if (key > v) chosen = true;
+            else if (key == v && remaining > 0) chosen = all_eq || (eq_before + eq_seen++ < remaining);
+        }
+        return mode == kDown ? chosen : (!cand || chosen);
+    };
+    // keep flags of this thread's run, as a bit mask when the run has <= 32 tokens
+    const bool use_bits = G <= 8;
+    uint32_t kbits = 0;
+    int keep_local = 0;
+    {
+        int eq_seen = 0;
+        FOR_RUN(g) {
+            const uint4 q = key4(g);
+            const uint32_t k4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool k = kept(k4[i], 4 * (q0 + g) + i, eq_seen);
+                keep_local += k;
+                if (use_bits && k) kbits |= 1u << (4 * g + i);
             }
+        }
+    }
+    int total;
+    int row = base + block_excl_sum(keep_local, s_ws, &total);
+    auto emit = [&](int t) {
+        if (row < base + ce && (int64_t)row < a.cap) {
+            a.perm_token[row] = t;
             a.row_map[(size_t)t * E + e] = row;
         }
-        carry_keep += tot;
+        ++row;
+    };
+    if (use_bits) {
+        while (kbits != 0) {
+            const int j2 = __ffs(kbits) - 1;
+            kbits &= kbits - 1;
+            emit(4 * q0 + j2);
+        }
+    } else {
+        int eq_seen = 0;
+        FOR_RUN(g) {
+            const uint4 q = key4(g);
+            const uint32_t k4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * (q0 + g) + i;
+                if (kept(k4[i], t, eq_seen)) emit(t);
+            }
+        }
     }
-    if (tid == 0 && (carry_keep != ce || (int64_t)base + ce > a.cap))
+    if (tid == 0 && (total != ce || (int64_t)base + ce > a.cap || s_members != f))
         atomicOr(a.err, MOE_DEVERR_COUNT_MISMATCH);
 }
 
 constexpr int kWThreads = 256;
 constexpr int kWWarps = kWThreads / 32;
 constexpr int kPerLane = kMaxE / 32;
+static_assert(kPerLane == 8, "the 16-byte layout covers 256 experts in two halves");
+
+// s + c += x with the rounding error of the addition kept in c (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum_acc(float &s, float &c, float x) {
+    const float t = __fadd_rn(s, x);
+    const float bp = __fsub_rn(t, s);
+    const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(x, bp));
+    s = t;
+    c = __fadd_rn(c, err);
+}
 
 __global__ void __launch_bounds__(kWThreads)
 round_weights_kernel(const float *__restrict__ L, const int32_t *__restrict__ row_map, int T,
-                     int E, int renorm, float *__restrict__ row_w) {
+                     int E, int renorm, bool vec, float *__restrict__ row_w,
+                     int32_t *__restrict__ tok_rows, int32_t *__restrict__ tok_n) {
     const int64_t t = (int64_t)blockIdx.x * kWWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const int lane = threadIdx.x & 31;
+    // this lane's experts: e(i) = lane + 32 i, or with 16-byte loads
+    // e(i) = 128 (i / 4) + 4 lane + i % 4
     float l[kPerLane];
     int r[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        l[i] = -INFINITY;
+        r[i] = -1;
+    }
+    if (vec) {
+#pragma unroll
+        for (int h = 0; h < kPerLane / 4; ++h) {
+            const int e = 128 * h + 4 * lane;
+            if (e < E) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(L + t * E + e));
+                const int4 q = __ldg(reinterpret_cast<const int4 *>(row_map + t * E + e));
+                l[4 * h] = v.x, l[4 * h + 1] = v.y, l[4 * h + 2] = v.z, l[4 * h + 3] = v.w;
+                r[4 * h] = q.x, r[4 * h + 1] = q.y, r[4 * h + 2] = q.z, r[4 * h + 3] = q.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                l[i] = __ldg(L + t * E + e);
+                r[i] = __ldg(row_map + t * E + e);
+            }
+        }
+    }
+    if (tok_rows != nullptr) {
+        // the token's rows in ascending expert order (at most kTokCap stored)
+        int n = 0;
+        if (vec) {
+#pragma unroll
+            for (int h = 0; h < kPerLane / 4; ++h) {
+                int cnt = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cnt += r[4 * h + j] >= 0;
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                int pos = n + incl - cnt;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (r[4 * h + j] >= 0) {
+                        if (pos < kTokCap) tok_rows[t * kTokCap + pos] = r[4 * h + j];
+                        ++pos;
+                    }
+                n += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) {
+                const unsigned bal = __ballot_sync(0xffffffffu, r[i] >= 0);
+                const int pos = n + __popc(bal & ((1u << lane) - 1u));
+                if (r[i] >= 0 && pos < kTokCap) tok_rows[t * kTokCap + pos] = r[i];
+                n += __popc(bal);
+            }
+        }
+        if (lane == 0) tok_n[t] = n;
+    }
     float m_all = -INFINITY, m_kept = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        l[i] = -INFINITY;
-        r[i] = -1;
-        if (e < E) {
-            l[i] = __ldg(L + t * E + e);
-            r[i] = __ldg(row_map + t * E + e);
-            m_all = fmaxf(m_all, l[i]);
-            if (r[i] >= 0) m_kept = fmaxf(m_kept, l[i]);
-        }
+        m_all = fmaxf(m_all, l[i]);
+        if (r[i] >= 0) m_kept = fmaxf(m_kept, l[i]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -351,19 +646,28 @@ round_weights_kernel(const float *__restrict__ L, const int32_t *__restrict__ ro
         m_kept = fmaxf(m_kept, __shfl_xor_sync(0xffffffffu, m_kept, o));
     }
     if (m_kept == -INFINITY) return;  // no expert kept this token
-    // renormalised: exp(l - max over kept) / sum over kept; else the softmax over all
+    // renormalised: exp(l - max over kept) / sum over kept; else the softmax over
+    // all. The sum is compensated (each addition's rounding error is carried in
+    // c), so it is accurate to a few fp32 ulps for any E.
     const float mref = renorm ? m_kept : m_all;
-    double s = 0.0;
+    float ex[kPerLane];
+    float s = 0.f, c = 0.f;
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && (!renorm || r[i] >= 0)) s += (double)expf(l[i] - mref);
+        ex[i] = expf(l[i] - mref);  // 0 for the padding slots (l = -inf)
+        if (!renorm || r[i] >= 0) two_sum_acc(s, c, ex[i]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        two_sum_acc(s, c, s2);
+        c = __fadd_rn(c, c2);
+    }
+    const float denom = __fadd_rn(s, c);
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i)
-        if (r[i] >= 0) row_w[r[i]] = (float)((double)expf(l[i] - mref) / s);
+        if (r[i] >= 0) row_w[r[i]] = __fdiv_rn(ex[i], denom);
 }
 
 constexpr int kCThreads = 256;
@@ -379,41 +683,26 @@ __device__ __forceinline__ void add_bf16x8(float *acc, const uint4 &v) {
     }
 }
 
-__global__ void __launch_bounds__(kCThreads)
-combine_rows_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restrict__ row_map,
-                    int T, int E, int d, int64_t rows_cap, __nv_bfloat16 *__restrict__ Y) {
-    __shared__ int s_rows[kCWarps][kMaxE];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kCWarps + warp;
-    if (t >= T) return;
-    int *rows = s_rows[warp];
-    int n = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        int r = e < E ? __ldg(row_map + t * E + e) : -1;
-        if (r >= rows_cap) r = -1;  // out of range: treated as not kept
-        const unsigned bal = __ballot_sync(0xffffffffu, r >= 0);
-        if (r >= 0) rows[n + __popc(bal & ((1u << lane) - 1u))] = r;
-        n += __popc(bal);
-    }
-    __syncwarp();
+// Y row = bf16( sum of the n rows of Z listed in rows[], in that order ), fp32.
+__device__ __forceinline__ void sum_rows(const __nv_bfloat16 *__restrict__ Z, const int *rows, int n,
+                                         int d, int lane, __nv_bfloat16 *__restrict__ y) {
     const int nv = d / 8;
-    uint4 *dst = reinterpret_cast<uint4 *>(Y + t * d);
+    uint4 *dst = reinterpret_cast<uint4 *>(y);
     for (int c = lane; c < nv; c += 32) {
         float acc[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-        int i = 0;
-        for (; i + 4 <= n; i += 4) {
-            uint4 v[4];
+        // batches of 8 rows, every load of a batch issued before the first add
+        for (int i = 0; i < n; i += 8) {
+            uint4 v[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v[j] = __ldg(reinterpret_cast<const uint4 *>(Z + (int64_t)rows[i + j] * d) + c);
+            for (int j = 0; j < 8; ++j)
+                if (i + j < n)
+                    v[j] = __ldg(reinterpret_cast<const uint4 *>(Z + (int64_t)rows[i + j] * d) + c);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) add_bf16x8(acc, v[j]);
+            for (int j = 0; j < 8; ++j)
+                if (i + j < n) add_bf16x8(acc, v[j]);
         }
-        for (; i < n; ++i)
-            add_bf16x8(acc, __ldg(reinterpret_cast<const uint4 *>(Z + (int64_t)rows[i] * d) + c));
         uint4 out;
         __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&out);
 #pragma unroll
@@ -422,24 +711,66 @@ combine_rows_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restri
     }
 }
 
+__global__ void __launch_bounds__(kCThreads)
+combine_rows_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restrict__ row_map,
+                    const int32_t *__restrict__ tok_rows, const int32_t *__restrict__ tok_n,
+                    int T, int E, int d, int64_t rows_cap, __nv_bfloat16 *__restrict__ Y) {
+    __shared__ int s_rows[kCWarps][kMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kCWarps + warp;
+    if (t >= T) return;
+    int *rows = s_rows[warp];
+    const int nl = tok_rows != nullptr ? __ldg(tok_n + t) : kTokCap + 1;
+    if (nl <= kTokCap) {
+        // the compact list (already in ascending expert order)
+        int r = lane < nl ? __ldg(tok_rows + t * kTokCap + lane) : -1;
+        if (r >= rows_cap) r = -1;
+        const unsigned bal = __ballot_sync(0xffffffffu, r >= 0);
+        if (r >= 0) rows[__popc(bal & ((1u << lane) - 1u))] = r;
+        __syncwarp();
+        sum_rows(Z, rows, __popc(bal), d, lane, Y + t * d);
+        return;
+    }
+    int rr[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+        const int e = lane + 32 * i;
+        rr[i] = e < E ? __ldg(row_map + t * E + e) : -1;
+    }
+    int n = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+        const int r = rr[i] < rows_cap ? rr[i] : -1;  // out of range: treated as not kept
+        const unsigned bal = __ballot_sync(0xffffffffu, r >= 0);
+        if (r >= 0) rows[n + __popc(bal & ((1u << lane) - 1u))] = r;
+        n += __popc(bal);
+    }
+    __syncwarp();
+    sum_rows(Z, rows, n, d, lane, Y + t * d);
+}
+
 }  // namespace
 
-size_t round_scratch_bytes(int T, int E) {
-    if (T <= kRoundSmemT) return 0;
-    return (size_t)5 * E * T;
-}
+size_t round_scratch_bytes(int T, int E) { return (size_t)4 * E * key_stride(T); }
 
 cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *counts, int T, int E,
                          int K, int M, int renorm, int32_t *counts_out, int32_t *offsets,
                          int32_t *perm_token, int32_t *row_map, float *row_w, int32_t *tiles,
-                         int32_t *num_tiles, void *scratch, uint32_t *err, cudaStream_t s) {
+                         int32_t *num_tiles, int32_t *tok_rows, int32_t *tok_n, void *scratch,
+                         uint32_t *err, cudaStream_t s) {
+    uint32_t *keyT = static_cast<uint32_t *>(scratch);
+    // 16-byte accesses when every row of L and row_map starts 16-byte aligned
+    const bool vec = (E % 4) == 0 && ((reinterpret_cast<uintptr_t>(L) |
+                                       reinterpret_cast<uintptr_t>(row_map)) & 15u) == 0;
+    round_prep_kernel<<<(unsigned)(key_stride(T) / kPT), kPThreads, 0, s>>>(
+        L, idx, counts, T, E, K, M, vec, keyT, row_map, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     RoundArgs a{};
-    a.L = L;
-    a.idx = idx;
+    a.keyT = keyT;
     a.counts = counts;
     a.T = T;
     a.E = E;
-    a.K = K;
     a.M = M;
     a.cap = round_capacity(T, E, K, M);
     a.max_tiles = (int)(a.cap / kTileM) + E;
@@ -449,32 +780,22 @@ cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *coun
     a.row_map = row_map;
     a.tiles = tiles;
     a.num_tiles = num_tiles;
-    a.keys_g = static_cast<uint32_t *>(scratch);
-    a.flags_g = scratch ? static_cast<uint8_t *>(scratch) + (size_t)4 * E * T : nullptr;
     a.err = err;
-    const size_t smem = T <= kRoundSmemT ? (size_t)5 * T : 0;
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(round_select_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             5 * kRoundSmemT);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    round_select_kernel<<<E, kRThreads, smem, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (key_stride(T) <= 4 * 4 * kRThreads)
+        round_select_kernel<4><<<E, kRThreads, 0, s>>>(a);
+    else
+        round_select_kernel<0><<<E, kRThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     round_weights_kernel<<<(unsigned)((T + kWWarps - 1) / kWWarps), kWThreads, 0, s>>>(
-        L, row_map, T, E, renorm, row_w);
+        L, row_map, T, E, renorm, vec, row_w, tok_rows, tok_n);
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map, int T, int E,
+cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map,
+                                const int32_t *tok_rows, const int32_t *tok_n, int T, int E,
                                 int d, int64_t rows_cap, __nv_bfloat16 *Y, cudaStream_t s) {
     combine_rows_kernel<<<(unsigned)((T + kCWarps - 1) / kCWarps), kCThreads, 0, s>>>(
-        Z, row_map, T, E, d, rows_cap, Y);
+        Z, row_map, tok_rows, tok_n, T, E, d, rows_cap, Y);
     return cudaGetLastError();
 }
 
