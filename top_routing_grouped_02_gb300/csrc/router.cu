@@ -199,36 +199,41 @@ logits_small_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
 }
 
 // ---- E > 32: register-tiled product ------------------------------------------
-// One warp per block; block tile 32 tokens x 64 experts, so a launch has
-// ceil(T/32) * ceil(E/64) small blocks and the SMs stay evenly loaded. Lane
-// (ty, tx) = (lane / 8, lane % 8) owns tokens {4ty..4ty+3, 16+4ty..16+4ty+3} and
-// experts {4tx..4tx+3, 32+4tx..32+4tx+3}: per reduction step it reads two
-// float4 of x and two float4 of weights, each conflict-free (a half-warp touches
-// 2 distinct x addresses and 128 contiguous bytes of weights), then does 64 FMAs.
+// Block tile 32 tokens x 64 experts, two warps of 16 tokens each, so a launch
+// has ceil(T/32) * ceil(E/64) blocks and about 13 warps per SM at the workload
+// sizes (the FP32 pipe needs several warps per scheduler to hide latency). In
+// warp w, lane (ty, tx) = (lane / 8, lane % 8) owns tokens 16w + 4ty .. +3 and
+// experts {4tx..4tx+3, 32+4tx..32+4tx+3}: per reduction step it reads one
+// float4 of x and two float4 of weights, all conflict-free, and issues 16
+// packed FMAs over expert pairs (each component rounds exactly like
+// __fmaf_rn, so every output is still one sequential fma chain over j).
 // 32-step stages are double-buffered: weights by cp.async, x through registers
 // (converted to fp32 and transposed on the way into shared memory).
 constexpr int kWT = 32;  // tokens per block tile
 constexpr int kWE = 64;  // experts per block tile
 constexpr int kWK = 32;  // reduction steps per stage
+constexpr int kWThreads = 64;
 
 template <bool VEC>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kWThreads)
 logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
                     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
     __shared__ __align__(16) float xs[2][kWK][kWT];
     __shared__ __align__(16) float ws[2][kWK][kWE];
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ty = lane >> 3, tx = lane & 7;
     const int64_t t0 = (int64_t)blockIdx.x * kWT;
     const int e0 = blockIdx.y * kWE;
     const int nchunk = (d + kWK - 1) / kWK;
 
-    uint4 xr[4];  // token t0+lane, 32 consecutive j
+    // x: thread tid loads token t0 + (tid & 31), 16 consecutive j from 16*(tid >> 5)
+    uint4 xr[2];
+    const int xt = tid & 31, xj = 16 * (tid >> 5);
     auto load_x = [&](int c) {
-        const int j0 = c * kWK;
-        const int64_t t = t0 + lane;
+        const int j0 = c * kWK + xj;
+        const int64_t t = t0 + xt;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             if (t < T && j0 + 8 * i < d)
                 xr[i] = __ldg(reinterpret_cast<const uint4 *>(X + t * d + j0 + 8 * i));
             else
@@ -237,22 +242,22 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
     };
     auto store_x = [&](int buf) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&xr[i]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float2 f = __bfloat1622float2(h2[u]);
-                xs[buf][8 * i + 2 * u][lane] = f.x;
-                xs[buf][8 * i + 2 * u + 1][lane] = f.y;
+                xs[buf][xj + 8 * i + 2 * u][xt] = f.x;
+                xs[buf][xj + 8 * i + 2 * u + 1][xt] = f.y;
             }
         }
     };
-    // weights: 32 rows j x 64 experts = 512 x 16 B, 16 per lane
+    // weights: 32 rows j x 64 experts = 512 x 16 B, 8 per thread
     auto issue_w = [&](int c, int buf) {
         const int j0 = c * kWK;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int q = lane + 32 * i;
+        for (int i = 0; i < 8; ++i) {
+            const int q = tid + kWThreads * i;
             const int jj = q >> 4, e4 = (q & 15) * 4;
             const int j = j0 + jj, e = e0 + e4;
             if (j >= d) continue;
@@ -271,13 +276,15 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         cp_async_commit();
     };
 
-    // accumulators paired along experts: acc[a][p] = (expert 2p, expert 2p+1)
-    float2 acc[8][4];
+    // accumulators paired along experts: acc[a][p] = (expert 2p, expert 2p+1) of
+    // the lane's 8 experts, for its token a
+    float2 acc[4][4];
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int p = 0; p < 4; ++p) acc[a][p] = make_float2(0.f, 0.f);
 
+    const int xo = 16 * warp + 4 * ty;  // the lane's first token within the tile
     issue_w(0, 0);
     load_x(0);
     store_x(0);
@@ -291,23 +298,22 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         }
         const int jn = min(kWK, d - c * kWK);
         auto step = [&](int jj) {
-            const float4 x0 = *reinterpret_cast<const float4 *>(&xs[buf][jj][4 * ty]);
-            const float4 x1 = *reinterpret_cast<const float4 *>(&xs[buf][jj][16 + 4 * ty]);
+            const float4 x0 = *reinterpret_cast<const float4 *>(&xs[buf][jj][xo]);
             const float4 w0 = *reinterpret_cast<const float4 *>(&ws[buf][jj][4 * tx]);
             const float4 w1 = *reinterpret_cast<const float4 *>(&ws[buf][jj][32 + 4 * tx]);
-            const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float xa[4] = {x0.x, x0.y, x0.z, x0.w};
             const float2 wp[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
                                   make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
             // packed fp32 FMA: each component rounds exactly like __fmaf_rn
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
+            for (int a = 0; a < 4; ++a) {
                 const float2 xx = make_float2(xa[a], xa[a]);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) acc[a][p] = __ffma2_rn(xx, wp[p], acc[a][p]);
             }
         };
         if (jn == kWK) {
-#pragma unroll 4
+#pragma unroll 8
             for (int jj = 0; jj < kWK; ++jj) step(jj);
         } else {
             for (int jj = 0; jj < jn; ++jj) step(jj);
@@ -319,8 +325,8 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         __syncthreads();
     }
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int64_t t = t0 + (a < 4 ? 4 * ty + a : 16 + 4 * ty + a - 4);
+    for (int a = 0; a < 4; ++a) {
+        const int64_t t = t0 + xo + a;
         if (t >= T) continue;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
@@ -575,9 +581,9 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
     } else {
         const dim3 grid((unsigned)((T + kWT - 1) / kWT), (unsigned)((E + kWE - 1) / kWE));
         if (E % 4 == 0 && wr16)
-            logits_tiled_kernel<true><<<grid, 32, 0, s>>>(X, Wr, bias, T, d, E, L);
+            logits_tiled_kernel<true><<<grid, kWThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
         else
-            logits_tiled_kernel<false><<<grid, 32, 0, s>>>(X, Wr, bias, T, d, E, L);
+            logits_tiled_kernel<false><<<grid, kWThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
     }
     return cudaGetLastError();
 }
