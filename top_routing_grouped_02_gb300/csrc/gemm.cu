@@ -41,7 +41,11 @@
 //               accumulator to the epilogue.
 //   warp 2      allocates / frees 512 TMEM columns (2 accumulators x 256).
 //   warps 4-7   epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
-//               activation or scaling in fp32, bf16 stores.
+//               activation or scaling in fp32, bf16 packing; each 32 x 32
+//               chunk goes through a swizzled shared-memory buffer and one TMA
+//               store (whole 64-byte row segments instead of 32 half-sector
+//               writes per store instruction); a warp whose 32 rows cross the
+//               end of the expert's rows stores its valid rows directly.
 // Every wait is bounded (about one second); a wait that gives up sets
 // MOE_DEVERR_TIMEOUT in the error word and that role stops. Before the TMEM is
 // released, in-flight MMAs and TMA loads of a stopped role are drained.
@@ -110,9 +114,14 @@ struct Ctl {
     int32_t scan[kThreads / 32 + 1];
 };
 
+// Epilogue staging: per epilogue warp two 32-row x 32-column bf16 buffers
+// (64-byte rows, 64-byte swizzle) that a TMA store writes out.
+constexpr uint32_t kEpiBuf = 32 * 32 * 2;
+constexpr uint32_t kEpiBytes = 4 * 2 * kEpiBuf;
+
 template <bool PAIR>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes + sizeof(Ctl);
+    return 1024 + (size_t)Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes + kEpiBytes + sizeof(Ctl);
 }
 
 struct GemmArgs {
@@ -175,7 +184,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
+                    const GemmArgs args) {
     using G = Geo<PAIR>;
     constexpr int S = G::kStages;
     // A rows gathered in the kernel (single-CTA gate/up) or loaded by TMA
@@ -183,7 +193,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)S * G::kStageBytes);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)S * G::kStageBytes + kEpiBytes);
     const uint32_t smem_base = ptx::smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = args.E;
@@ -211,6 +221,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
         if (MODE == kGateUp) ptx::prefetch_tensormap(&tmB1);
+        ptx::prefetch_tensormap(&tmOut);
     }
     if (warp == 2) {
         if constexpr (PAIR) {
@@ -435,6 +446,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int r = q * 32 + lane;
         const uint32_t tempty0 = PAIR ? ptx::mapa(ptx::smem_addr(&ctl->tempty[0]), 0)
                                       : ptx::smem_addr(&ctl->tempty[0]);
+        // this warp's two output staging buffers
+        const uint32_t epi_base = smem_base + (uint32_t)S * G::kStageBytes + (uint32_t)q * 2 * kEpiBuf;
+        uint32_t epi_groups = 0;  // TMA store groups this warp has committed
         uint32_t uc = 0;
         for (int u = first_unit; u < total_units; u += unit_stride, ++uc) {
             int e, nb, row0, rows;
@@ -445,6 +459,37 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const bool valid = r < rows;
             const int64_t p = (int64_t)row0 + r;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
+            // A warp whose 32 rows all belong to the tile writes each 32-column
+            // chunk through shared memory and a TMA store (whole 64-byte row
+            // segments); otherwise each valid row is stored directly.
+            const bool whole = q * 32 + 31 < rows;
+            auto emit = [&](const uint32_t (&packed)[16], __nv_bfloat16 *dst, int col) {
+                if (whole) {
+                    // buffers alternate with the store groups, so the group that
+                    // last read this buffer is the one before the most recent
+                    const uint32_t buf = epi_base + (epi_groups & 1u) * kEpiBuf;
+                    if (lane == 0 && epi_groups >= 2) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        ptx::st_shared_v4(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4),
+                                          packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                          packed[4 * i + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tmOut, buf, col, row0 + q * 32);
+                        ptx::bulk_commit_group();
+                    }
+                    ++epi_groups;
+                } else if (valid) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                           packed[4 * i + 3]);
+                }
+            };
             if (MODE == kGateUp) {
                 __nv_bfloat16 *dst = args.out + p * args.out_ld + nb * 128;
 #pragma unroll 1
@@ -461,13 +506,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
                         packed[i] = pack_bf16x2(h0, h1);
                     }
-                    if (valid) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                               packed[4 * i + 3]);
-                    }
+                    emit(packed, dst + c * 32, nb * 128 + c * 32);
                 }
             } else {
                 float w = 0.f;
@@ -486,13 +525,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int i = 0; i < 16; ++i)
                         packed[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]),
                                                 w * __uint_as_float(v[2 * i + 1]));
-                    if (valid) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                               packed[4 * i + 3]);
-                    }
+                    emit(packed, dst + c * 32, nb * BN + c * 32);
                 }
             }
             ptx::tc_fence_before();
@@ -504,6 +537,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 else ptx::mbar_arrive(bar);
             }
         }
+        // this warp's TMA stores have completed before the CTA exits
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
     }
 
     // ---- teardown -----------------------------------------------------------
@@ -538,9 +574,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box box_cols x box_rows,
-// 128-byte swizzle, zero fill outside the tensor.
+// 128-byte swizzle unless given, zero fill outside the tensor.
 bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows) {
+              uint32_t box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -548,13 +585,14 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, 
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int MODE, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                           const GemmArgs &args, int max_units, cudaStream_t s) {
+                           const CUtensorMap &out, const GemmArgs &args, int max_units,
+                           cudaStream_t s) {
     constexpr size_t kSmem = smem_bytes<PAIR>();
     static bool configured[64] = {};
     int dev = 0;
@@ -567,7 +605,7 @@ cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CU
     }
     if (!PAIR) {
         const int grid = max(1, min(sm_count(), max_units));
-        grouped_gemm_kernel<MODE, false><<<grid, kThreads, kSmem, s>>>(a, b0, b1, args);
+        grouped_gemm_kernel<MODE, false><<<grid, kThreads, kSmem, s>>>(a, b0, b1, out, args);
         return cudaGetLastError();
     }
     // one cluster of 2 CTAs (an SM pair) per unit slot
@@ -584,7 +622,7 @@ cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, true>, a, b0, b1, args);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, true>, a, b0, b1, out, args);
 }
 
 // CTA pairs halve the B bytes each SM receives per MMA and so allow a deeper
@@ -600,12 +638,12 @@ bool use_pair(int R, int E) {
 
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                        const GemmArgs &args, cudaStream_t s) {
+                        const CUtensorMap &out, const GemmArgs &args, cudaStream_t s) {
     // (gate/up chooses its variant itself: the A source differs)
     const int tiles = args.R / BM + args.E;  // upper bound of the 128-row tiles
     if (use_pair(args.R, args.E))
-        return launch_variant<MODE, true>(a, b0, b1, args, (tiles / 2 + args.E) * args.NB, s);
-    return launch_variant<MODE, false>(a, b0, b1, args, tiles * args.NB, s);
+        return launch_variant<MODE, true>(a, b0, b1, out, args, (tiles / 2 + args.E) * args.NB, s);
+    return launch_variant<MODE, false>(a, b0, b1, out, args, tiles * args.NB, s);
 }
 
 }  // namespace
@@ -615,9 +653,10 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_toke
                                 const int32_t *offsets, int R, int d, int E, int n,
                                 __nv_bfloat16 *H, __nv_bfloat16 *xg, uint32_t *err,
                                 cudaStream_t s) {
-    CUtensorMap ta, tb0, tb1;
+    CUtensorMap ta, tb0, tb1, th;
     if (!make_map(&tb0, W1, n, (uint64_t)E * d, 64, BK) ||
-        !make_map(&tb1, W3, n, (uint64_t)E * d, 64, BK))
+        !make_map(&tb1, W3, n, (uint64_t)E * d, 64, BK) ||
+        !make_map(&th, H, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     GemmArgs args{};
     args.X = X;
@@ -637,18 +676,19 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_toke
         cudaError_t e = launch_gather_rows(X, perm_token, T, R, d, xg, s);
         if (e != cudaSuccess) return e;
         if (!make_map(&ta, xg, d, R, 64, BM)) return cudaErrorInvalidValue;
-        return launch_variant<kGateUp, true>(ta, tb0, tb1, args, (tiles / 2 + E) * args.NB, s);
+        return launch_variant<kGateUp, true>(ta, tb0, tb1, th, args, (tiles / 2 + E) * args.NB, s);
     }
     // single CTAs gather their A rows themselves; the A map argument is not read
-    return launch_variant<kGateUp, false>(tb0, tb0, tb1, args, tiles * args.NB, s);
+    return launch_variant<kGateUp, false>(tb0, tb0, tb1, th, args, tiles * args.NB, s);
 }
 
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,
                              __nv_bfloat16 *Z, uint32_t *err, cudaStream_t s) {
-    CUtensorMap ta, tb0;
-    if (!make_map(&ta, H, n, R, 64, BM) || !make_map(&tb0, W2, d, (uint64_t)E * n, 64, BK))
+    CUtensorMap ta, tb0, tz;
+    if (!make_map(&ta, H, n, R, 64, BM) || !make_map(&tb0, W2, d, (uint64_t)E * n, 64, BK) ||
+        !make_map(&tz, Z, d, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     GemmArgs args{};
     args.offsets = offsets;
@@ -661,7 +701,7 @@ cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
     args.topk_w = topk_w;
     args.perm_slot = perm_slot;
     args.err = err;
-    return launch_gemm<kDown>(ta, tb0, tb0, args, s);
+    return launch_gemm<kDown>(ta, tb0, tb0, tz, args, s);
 }
 
 }  // namespace moe
