@@ -15,7 +15,7 @@
 //     bit-identical to a sequential evaluation. The chain cannot be split over
 //     threads or tensor-core instructions without changing the rounding, so every
 //     chain stays in one thread and parallelism comes from tokens x experts:
-//       - E <= 32: one thread per (token, expert) chain fed from a cp.async
+//       - E <= 32: two (token, expert) chains per thread fed from a cp.async
 //         shared-memory pipeline; bound by the latency of d dependent FMAs.
 //       - E > 32: one-warp blocks on 32-token x 64-expert tiles, 8x8 register
 //         micro-tiles fed by conflict-free float4 shared-memory reads; bound by
@@ -44,51 +44,54 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ---- E <= 32: one thread per (token, expert) chain --------------------------
-// Block: 128 threads = NT tokens x EP experts. Stages of JC reduction steps:
-// the block's NT rows of X (bf16) and JC rows of Wr (fp32) are copied to shared
-// memory with cp.async, 4 stages deep. Each stage is then widened once into fp32
-// x [NT][JC+4] and transposed weights w [EP][JC+4], so the chain's inner loop is
-// two conflict-free float4 reads per 4 fused multiply-adds.
+// ---- E <= 32: two (token, expert) chains per thread -------------------------
+// Block: 8 tokens x EP experts, one thread per (token, expert pair), so 4*EP
+// threads (EP/8 warps). Stages of kChainJC reduction steps: the block's 8 rows
+// of X (bf16) and kChainJC rows of Wr (fp32) are copied to shared memory with
+// cp.async, 4 stages deep; the X rows are widened once per stage to fp32. Per
+// 4 steps a thread reads one float4 of x (shared by the threads of its token)
+// and four float2 of weights for 8 fused multiply-adds on two independent
+// chains, so shared-memory traffic is a quarter of one-chain-per-thread's and
+// the kernel approaches the latency of the d-long chain itself.
 // Requires d % 8 == 0, E % 4 == 0 and a 16-byte-aligned Wr.
-constexpr int kChainThreads = 128;
+constexpr int kChainTok = 8;
 constexpr int kChainStages = 4;
+constexpr int kChainJC = 128;
 
 template <int EP>
 struct ChainCfg {
-    static constexpr int NT = kChainThreads / EP;        // tokens per block
-    static constexpr int JC = EP >= 32 ? 128 : 256;      // reduction steps per stage
-    static constexpr int RXBYTES = NT * JC * 2;          // raw X rows (bf16)
-    static constexpr int RWBYTES = JC * EP * 4;          // raw Wr rows (EP floats each)
+    static constexpr int THREADS = kChainTok * EP / 2;
+    static constexpr int RXBYTES = kChainTok * kChainJC * 2;  // raw X rows (bf16)
+    static constexpr int RWBYTES = kChainJC * EP * 4;         // raw Wr rows (EP floats each)
     static constexpr int RSTAGE = RXBYTES + RWBYTES;
-    static constexpr int LD = JC + 4;                    // widened row length (floats)
-    static constexpr int SMEM = kChainStages * RSTAGE + (NT + EP) * LD * 4;
+    static constexpr int LD = kChainJC + 4;                   // widened x row (floats)
+    static constexpr int SMEM = kChainStages * RSTAGE + kChainTok * LD * 4;
 };
 
 template <int EP>
-__global__ void __launch_bounds__(kChainThreads)
+__global__ void __launch_bounds__(ChainCfg<EP>::THREADS)
 logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
                     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
     using C = ChainCfg<EP>;
+    constexpr int NTH = C::THREADS;
     extern __shared__ __align__(16) unsigned char sm[];
-    float *xf = reinterpret_cast<float *>(sm + kChainStages * C::RSTAGE);  // [NT][LD]
-    float *wt = xf + C::NT * C::LD;                                          // [EP][LD]
+    float *xf = reinterpret_cast<float *>(sm + kChainStages * C::RSTAGE);  // [8][LD]
     const int tid = threadIdx.x;
-    const int e = tid % EP, tl = tid / EP;
-    const int64_t t0 = (int64_t)blockIdx.x * C::NT;
-    const int nst = (d + C::JC - 1) / C::JC;
+    const int h = tid % (EP / 2), tl = tid / (EP / 2);  // experts 2h, 2h+1 of token tl
+    const int64_t t0 = (int64_t)blockIdx.x * kChainTok;
+    const int nst = (d + kChainJC - 1) / kChainJC;
 
     auto issue = [&](int st) {
         unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
         unsigned char *ws = xs + C::RXBYTES;
-        const int j0 = st * C::JC;
-        for (int q = tid; q < C::NT * (C::JC / 8); q += kChainThreads) {
-            const int r = q / (C::JC / 8), c = q % (C::JC / 8);
+        const int j0 = st * kChainJC;
+        for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
+            const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
             const int64_t t = t0 + r;
             const int j = j0 + c * 8;
-            if (t < T && j < d) cp_async16(xs + r * (C::JC * 2) + c * 16, X + t * d + j);
+            if (t < T && j < d) cp_async16(xs + r * (kChainJC * 2) + c * 16, X + t * d + j);
         }
-        for (int q = tid; q < C::JC * (EP / 4); q += kChainThreads) {
+        for (int q = tid; q < kChainJC * (EP / 4); q += NTH) {
             const int jj = q / (EP / 4), c4 = (q % (EP / 4)) * 4;
             const int j = j0 + jj;
             if (j < d && c4 < E) cp_async16(ws + (jj * EP + c4) * 4, Wr + (int64_t)j * E + c4);
@@ -99,65 +102,59 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         if (st < nst) issue(st);
         cp_async_commit();
     }
-    const int ec = e < E ? e : 0;
     const float4 *xrow = reinterpret_cast<const float4 *>(xf + tl * C::LD);
-    const float4 *wrow = reinterpret_cast<const float4 *>(wt + ec * C::LD);
-    float acc = 0.f;
+    float acc0 = 0.f, acc1 = 0.f;
     for (int st = 0; st < nst; ++st) {
         cp_async_wait<kChainStages - 2>();
         __syncthreads();  // raw stage st landed; the previous stage's compute is done
         if (st + kChainStages - 1 < nst) issue(st + kChainStages - 1);
         cp_async_commit();
-        {
-            const unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
-            const float *ws = reinterpret_cast<const float *>(xs + C::RXBYTES);
-            for (int q = tid; q < C::NT * (C::JC / 8); q += kChainThreads) {
-                const int r = q / (C::JC / 8), c = q % (C::JC / 8);
-                const uint4 raw = *reinterpret_cast<const uint4 *>(xs + r * (C::JC * 2) + c * 16);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-                float4 *dst = reinterpret_cast<float4 *>(xf + r * C::LD + c * 8);
-                const float2 a = __bfloat1622float2(h2[0]), b = __bfloat1622float2(h2[1]);
-                const float2 c2 = __bfloat1622float2(h2[2]), d2 = __bfloat1622float2(h2[3]);
-                dst[0] = make_float4(a.x, a.y, b.x, b.y);
-                dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
-            }
-            for (int jj = tid; jj < C::JC; jj += kChainThreads) {
-#pragma unroll
-                for (int c4 = 0; c4 < EP; c4 += 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(ws + jj * EP + c4);
-                    wt[(c4 + 0) * C::LD + jj] = v.x;
-                    wt[(c4 + 1) * C::LD + jj] = v.y;
-                    wt[(c4 + 2) * C::LD + jj] = v.z;
-                    wt[(c4 + 3) * C::LD + jj] = v.w;
-                }
-            }
+        const unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
+        const float2 *w2 = reinterpret_cast<const float2 *>(xs + C::RXBYTES) + h;  // row stride EP/2
+        for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
+            const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
+            const uint4 raw = *reinterpret_cast<const uint4 *>(xs + r * (kChainJC * 2) + c * 16);
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+            float4 *dst = reinterpret_cast<float4 *>(xf + r * C::LD + c * 8);
+            const float2 a = __bfloat1622float2(h2[0]), b = __bfloat1622float2(h2[1]);
+            const float2 c2 = __bfloat1622float2(h2[2]), d2 = __bfloat1622float2(h2[3]);
+            dst[0] = make_float4(a.x, a.y, b.x, b.y);
+            dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
         }
         __syncthreads();
-        const int jn = min(C::JC, d - st * C::JC);  // a multiple of 8
-        if (jn == C::JC) {
+        const int jn = min(kChainJC, d - st * kChainJC);  // a multiple of 8
+        auto step4 = [&](int v) {
+            const float4 xv = xrow[v];
+            const float2 wa = w2[(4 * v + 0) * (EP / 2)], wb = w2[(4 * v + 1) * (EP / 2)];
+            const float2 wc = w2[(4 * v + 2) * (EP / 2)], wd = w2[(4 * v + 3) * (EP / 2)];
+            acc0 = __fmaf_rn(xv.x, wa.x, acc0);
+            acc1 = __fmaf_rn(xv.x, wa.y, acc1);
+            acc0 = __fmaf_rn(xv.y, wb.x, acc0);
+            acc1 = __fmaf_rn(xv.y, wb.y, acc1);
+            acc0 = __fmaf_rn(xv.z, wc.x, acc0);
+            acc1 = __fmaf_rn(xv.z, wc.y, acc1);
+            acc0 = __fmaf_rn(xv.w, wd.x, acc0);
+            acc1 = __fmaf_rn(xv.w, wd.y, acc1);
+        };
+        if (jn == kChainJC) {
 #pragma unroll 8
-            for (int v = 0; v < C::JC / 4; ++v) {
-                const float4 xv = xrow[v], wv = wrow[v];
-                acc = __fmaf_rn(xv.x, wv.x, acc);
-                acc = __fmaf_rn(xv.y, wv.y, acc);
-                acc = __fmaf_rn(xv.z, wv.z, acc);
-                acc = __fmaf_rn(xv.w, wv.w, acc);
-            }
+            for (int v = 0; v < kChainJC / 4; ++v) step4(v);
         } else {
-            for (int v = 0; v < jn / 4; ++v) {
-                const float4 xv = xrow[v], wv = wrow[v];
-                acc = __fmaf_rn(xv.x, wv.x, acc);
-                acc = __fmaf_rn(xv.y, wv.y, acc);
-                acc = __fmaf_rn(xv.z, wv.z, acc);
-                acc = __fmaf_rn(xv.w, wv.w, acc);
-            }
+            for (int v = 0; v < jn / 4; ++v) step4(v);
         }
     }
     cp_async_wait<0>();
     const int64_t t = t0 + tl;
-    if (t < T && e < E) {
-        if (bias != nullptr) acc = __fadd_rn(acc, __ldg(bias + e));
-        L[t * E + e] = acc;
+    if (t < T) {
+        const int e0 = 2 * h;
+        if (e0 < E) {
+            if (bias != nullptr) acc0 = __fadd_rn(acc0, __ldg(bias + e0));
+            L[t * E + e0] = acc0;
+        }
+        if (e0 + 1 < E) {
+            if (bias != nullptr) acc1 = __fadd_rn(acc1, __ldg(bias + e0 + 1));
+            L[t * E + e0 + 1] = acc1;
+        }
     }
 }
 
@@ -553,8 +550,8 @@ cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *b
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const unsigned grid = (unsigned)((T + C::NT - 1) / C::NT);
-    logits_chain_kernel<EP><<<grid, kChainThreads, C::SMEM, s>>>(X, Wr, bias, T, d, E, L);
+    const unsigned grid = (unsigned)((T + kChainTok - 1) / kChainTok);
+    logits_chain_kernel<EP><<<grid, C::THREADS, C::SMEM, s>>>(X, Wr, bias, T, d, E, L);
     return cudaGetLastError();
 }
 
