@@ -66,7 +66,7 @@ typedef enum {
 /* Human-readable name of a status code (static string). */
 const char *moe_status_string(int status);
 
-/* Version of this ABI (major*100 + minor). */
+/* Version of this ABI (major*100 + minor). 101 added the Token Rounding calls. */
 int moe_abi_version(void);
 
 /* Bytes of workspace the calls below need for this layer shape; 0 for an

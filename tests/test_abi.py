@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 100
+    assert lib.moe_abi_version() == 101
     for code, name in moe.STATUS.items():
         assert lib.moe_status_string(code).decode() == name
     assert lib.moe_status_string(99).decode() == "MOE_ERR_UNKNOWN"

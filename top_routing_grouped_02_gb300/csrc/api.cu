@@ -159,7 +159,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n) {
     if (T < 1 || E < 1 || K < 1 || d < 0 || n < 0 || E > kMaxE || K > kMaxK || K > E) return 0;
