@@ -23,7 +23,7 @@
  *     and row-major. Integer outputs are int32.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work on it and return; none waits for the GPU (except
- *     moe_sync_check and moe_forward_host, which say so).
+ *     moe_sync_check, moe_forward_host and moe_forward_host_stream, which say so).
  *   - Argument and shape errors are reported synchronously, before anything is
  *     enqueued. A failed launch returns MOE_ERR_CUDA. Problems the kernels
  *     detect on the device (an expert index out of range, a stalled pipeline
@@ -281,6 +281,21 @@ moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, cons
                                         int renorm, moe_bf16 *Y, int32_t *row_map_out,
                                         void *ws, size_t ws_bytes, void *stream,
                                         void *const *events, int n_events);
+
+/* A sequence of n_batches layer forwards straight from host memory, with the
+ * copies overlapped with the layer: X_host / Y_host are [n_batches, T, d] bf16
+ * (host, pinned for the copies to overlap); X_dev2 / Y_dev2 are caller-owned
+ * device buffers [2, T, d] (double buffered). Batch i is uploaded on
+ * h2d_stream while the layer runs batch i-1 on `stream`, and its output is
+ * downloaded on d2h_stream while the layer runs batch i+1; events order the
+ * reuse of each device buffer. The three streams must be distinct. Returns
+ * after every output has reached Y_host (it waits for all three streams). */
+moe_status_t moe_forward_host_stream(const moe_bf16 *X_host, moe_bf16 *Y_host, int n_batches,
+                                     moe_bf16 *X_dev2, moe_bf16 *Y_dev2, const float *Wr,
+                                     const float *bias, const moe_bf16 *W1, const moe_bf16 *W3,
+                                     const moe_bf16 *W2, int T, int d, int E, int K, int n,
+                                     int renorm, void *ws, size_t ws_bytes, void *stream,
+                                     void *h2d_stream, void *d2h_stream);
 
 /* Wait for `stream`, read and clear the workspace's device error word.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK (or

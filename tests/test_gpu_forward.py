@@ -124,6 +124,40 @@ def test_forward_host_roundtrip_matches_device_call():
     assert torch.equal(Yh.view(torch.int16), Y_dev_ref.cpu().view(torch.int16))
 
 
+def test_forward_host_stream_matches_device_calls():
+    # three different batches through the overlapped host path, each against a
+    # plain device call on the same batch
+    cfg = dict(synth.WORKLOADS["tiny"])
+    T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    Xs = torch.stack([synth.normal("X", (T, d), 1.0, torch.bfloat16, "cpu", seed=s)
+                      for s in (1, 2, 3)]).pin_memory()
+    Ys = torch.empty_like(Xs).pin_memory()
+    Xd2 = torch.empty((2, T, d), dtype=torch.bfloat16, device="cuda")
+    Yd2 = torch.empty_like(Xd2)
+    stream = torch.cuda.Stream()
+    moe.moe_forward_host_stream(Xs, Ys, Xd2, Yd2, inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K,
+                                inp["bias"], stream=stream)
+    for i in range(3):
+        one = dict(inp, X=Xs[i].cuda())
+        Y_ref, _, _ = _forward(one, K)
+        assert torch.equal(Ys[i].view(torch.int16), Y_ref.cpu().view(torch.int16))
+
+
+def test_forward_host_stream_rejects_shared_streams():
+    cfg = dict(synth.WORKLOADS["tiny"])
+    T, d, K = cfg["T"], cfg["d"], cfg["K"]
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    Xs = torch.zeros((1, T, d), dtype=torch.bfloat16).pin_memory()
+    Ys = torch.empty_like(Xs).pin_memory()
+    Xd2 = torch.empty((2, T, d), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward_host_stream(Xs, Ys, Xd2, torch.empty_like(Xd2), inp["Wr"], inp["W1"],
+                                    inp["W3"], inp["W2"], K, stream=s, h2d_stream=s)
+    assert e.value.status == 1
+
+
 def test_forward_traced_records_stage_events():
     cfg = dict(synth.WORKLOADS["tiny"])
     inp = synth.layer_inputs(device="cuda", **cfg)

@@ -365,6 +365,78 @@ moe_status_t moe_forward_host(const moe_bf16 *X_host, moe_bf16 *Y_host, moe_bf16
     return from_cuda(cudaStreamSynchronize(st));
 }
 
+moe_status_t moe_forward_host_stream(const moe_bf16 *X_host, moe_bf16 *Y_host, int n_batches,
+                                     moe_bf16 *X_dev2, moe_bf16 *Y_dev2, const float *Wr,
+                                     const float *bias, const moe_bf16 *W1, const moe_bf16 *W3,
+                                     const moe_bf16 *W2, int T, int d, int E, int K, int n,
+                                     int renorm, void *ws, size_t ws_bytes, void *stream,
+                                     void *h2d_stream, void *d2h_stream) {
+    if (!X_host || !Y_host || !X_dev2 || !Y_dev2 || n_batches < 0) return MOE_ERR_INVALID_ARG;
+    if (stream == h2d_stream || stream == d2h_stream || h2d_stream == d2h_stream)
+        return MOE_ERR_INVALID_ARG;  // the overlap needs three distinct streams
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (n_batches == 0) return MOE_OK;
+    cudaStream_t sc = as_stream(stream), sin = as_stream(h2d_stream), sout = as_stream(d2h_stream);
+    const size_t elems = (size_t)T * d, bytes = elems * sizeof(moe_bf16);
+    // per device buffer b: X landed / X free again (layer done) / Y written / Y copied out
+    cudaEvent_t x_in[2], x_free[2], y_done[2], y_out[2];
+    int created = 0;
+    cudaError_t ce = cudaSuccess;
+    for (int b = 0; b < 2 && ce == cudaSuccess; ++b) {
+        cudaEvent_t *evs[4] = {&x_in[b], &x_free[b], &y_done[b], &y_out[b]};
+        for (int k = 0; k < 4 && ce == cudaSuccess; ++k) {
+            ce = cudaEventCreateWithFlags(evs[k], cudaEventDisableTiming);
+            if (ce == cudaSuccess) ++created;
+        }
+    }
+    auto destroy = [&]() {
+        int left = created;
+        for (int b = 0; b < 2; ++b) {
+            cudaEvent_t evs[4] = {x_in[b], x_free[b], y_done[b], y_out[b]};
+            for (int k = 0; k < 4 && left > 0; ++k, --left) cudaEventDestroy(evs[k]);
+        }
+    };
+    if (ce != cudaSuccess) {
+        destroy();
+        return MOE_ERR_CUDA;
+    }
+    s = MOE_OK;
+    for (int i = 0; i < n_batches && s == MOE_OK; ++i) {
+        const int b = i & 1;
+        moe_bf16 *xd = X_dev2 + b * elems, *yd = Y_dev2 + b * elems;
+        // upload batch i once the layer of batch i-2 no longer reads this buffer
+        if ((i >= 2 && cudaStreamWaitEvent(sin, x_free[b], 0) != cudaSuccess) ||
+            cudaMemcpyAsync(xd, X_host + (size_t)i * elems, bytes, cudaMemcpyHostToDevice, sin) !=
+                cudaSuccess ||
+            cudaEventRecord(x_in[b], sin) != cudaSuccess) {
+            s = MOE_ERR_CUDA;
+            break;
+        }
+        // the layer, after the upload and after batch i-2's output has left yd
+        if (cudaStreamWaitEvent(sc, x_in[b], 0) != cudaSuccess ||
+            (i >= 2 && cudaStreamWaitEvent(sc, y_out[b], 0) != cudaSuccess)) {
+            s = MOE_ERR_CUDA;
+            break;
+        }
+        s = moe_forward(xd, Wr, bias, W1, W3, W2, T, d, E, K, n, renorm, yd, nullptr, nullptr, ws,
+                        ws_bytes, stream);
+        if (s != MOE_OK) break;
+        if (cudaEventRecord(x_free[b], sc) != cudaSuccess ||
+            cudaEventRecord(y_done[b], sc) != cudaSuccess ||
+            cudaStreamWaitEvent(sout, y_done[b], 0) != cudaSuccess ||
+            cudaMemcpyAsync(Y_host + (size_t)i * elems, yd, bytes, cudaMemcpyDeviceToHost, sout) !=
+                cudaSuccess ||
+            cudaEventRecord(y_out[b], sout) != cudaSuccess)
+            s = MOE_ERR_CUDA;
+    }
+    const cudaError_t e1 = cudaStreamSynchronize(sin), e2 = cudaStreamSynchronize(sc),
+                      e3 = cudaStreamSynchronize(sout);
+    destroy();
+    if (s != MOE_OK) return s;
+    return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess) ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status_t moe_sync_check(void *ws, void *stream, uint32_t *word_out) {
     if (ws == nullptr) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);

@@ -61,6 +61,8 @@ _SIGS = {
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
                               _P]),
     "moe_sync_check": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_forward_host_stream": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                     _I, _P, _SZ, _P, _P, _P]),
     "moe_round_capacity": (ctypes.c_int64, [_I, _I, _I, _I]),
     "moe_round_workspace_bytes": (_SZ, [_I, _I]),
     "moe_round_routing": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -298,6 +300,34 @@ def moe_forward_host(X_host, Y_host, X_dev, Y_dev, Wr, W1, W3, W2, K: int, bias=
         _ptr(bias, torch.float32), _ptr(W1, torch.bfloat16), _ptr(W3, torch.bfloat16),
         _ptr(W2, torch.bfloat16), T, d, E, K, n, int(bool(renorm)), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return Y_host
+
+
+def moe_forward_host_stream(X_host, Y_host, X_dev2, Y_dev2, Wr, W1, W3, W2, K: int, bias=None,
+                            renorm: bool = True, ws=None, stream=None, h2d_stream=None,
+                            d2h_stream=None):
+    """n batches from host memory with copies overlapped: X_host / Y_host are CPU
+    bf16 [n, T, d] (pinned), X_dev2 / Y_dev2 CUDA bf16 [2, T, d]. Returns after
+    Y_host holds every output."""
+    nb, T, d = X_host.shape
+    E, _, n = W1.shape
+    for name, t in (("X_host", X_host), ("Y_host", Y_host)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a contiguous CPU bf16 tensor")
+    if tuple(X_dev2.shape) != (2, T, d) or tuple(Y_dev2.shape) != (2, T, d):
+        raise ValueError("X_dev2 / Y_dev2 must be [2, T, d]")
+    if ws is None:
+        ws = workspace(T, d, E, K, n, X_dev2.device)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    h2d_stream = h2d_stream or torch.cuda.Stream(device=X_dev2.device)
+    d2h_stream = d2h_stream or torch.cuda.Stream(device=X_dev2.device)
+    _check("moe_forward_host_stream", lib().moe_forward_host_stream(
+        ctypes.c_void_p(X_host.data_ptr()), ctypes.c_void_p(Y_host.data_ptr()), nb,
+        _ptr(X_dev2, torch.bfloat16), _ptr(Y_dev2, torch.bfloat16), _ptr(Wr, torch.float32),
+        _ptr(bias, torch.float32), _ptr(W1, torch.bfloat16), _ptr(W3, torch.bfloat16),
+        _ptr(W2, torch.bfloat16), T, d, E, K, n, int(bool(renorm)), _ptr(ws), ws.numel(),
+        _stream(stream), _stream(h2d_stream), _stream(d2h_stream)))
     return Y_host
 
 
