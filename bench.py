@@ -249,7 +249,7 @@ def run_gpu(args, c, world, rank, local):
     ws = (moe.workspace_rounded if rounded else moe.workspace)(T, d, E, K, n, dev)
     Y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     row_map = torch.empty((T, E), dtype=torch.int32, device=dev) if rounded else None
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)  # a capturable (non-legacy) stream
 
     def step(events=None):
         if rounded:
@@ -276,13 +276,32 @@ def run_gpu(args, c, world, rank, local):
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
+    # Direct calls by default. --graph captures the K steps (their stage events
+    # included, as external event nodes) once as a CUDA graph and replays it; the
+    # event nodes between stages cost about what the graph saves in launch gaps.
+    graph, launch = None, "direct calls"
+    if args.graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(args.steps):
+                    step(evs[i])
+            torch.cuda.synchronize()
+            launch = "one CUDA graph of the K steps"
+        except RuntimeError as exc:  # capture unsupported here: time direct calls
+            graph, launch = None, f"direct calls (graph capture failed: {exc})"[:200]
+            torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
         start.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                graph.replay()
+        else:
+            for i in range(args.steps):
+                step(evs[i])
         stop.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -357,7 +376,8 @@ def run_gpu(args, c, world, rank, local):
         "data": "synthetic",
         "config": {"workload": workload_desc(args.workload, c, args.routing),
                    **{k: c[k] for k in "TdEKn"}, "routing": args.routing, "rows": R,
-                   "seed": args.seed, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "seed": args.seed, "launch": launch,
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "inputs larger than L2: expert weights "
                          f"{3 * E * d * n * 2 / 1e9:.2f} GB per step, no flush"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
@@ -468,6 +488,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time one CUDA graph of the K steps instead of direct calls")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

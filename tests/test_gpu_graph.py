@@ -36,3 +36,30 @@ def test_forward_captured_in_cuda_graph_matches_direct_call(name, pair, monkeypa
         assert torch.equal(Y.view(torch.int16), Y_direct.view(torch.int16))
     status, word = moe.moe_sync_check(ws)
     assert status == 0, word
+
+
+def test_traced_forward_events_time_inside_a_captured_graph():
+    # the stage events of moe_forward_traced become external event nodes when
+    # the stream is capturing, so each replay records them and they can be timed
+    cfg = synth.WORKLOADS["tiny"]
+    T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    ws = moe.workspace(T, d, E, K, n)
+    Y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record(side)
+    with torch.cuda.stream(side):
+        moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"],
+                        ws=ws, Y=Y, stream=side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        moe.moe_forward(inp["X"], inp["Wr"], inp["W1"], inp["W3"], inp["W2"], K, inp["bias"],
+                        ws=ws, Y=Y, stream=side, events=ev)
+    with torch.cuda.stream(side):
+        graph.replay()
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t > 0 for t in times), times

@@ -68,6 +68,15 @@ moe_status_t check_mlp_shape(int T, int d, int E, int K, int n) {
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
+// Records a caller's timing event on st. Inside a stream capture the record
+// becomes an external event node, so each replay of the graph records it.
+bool record_event(void *event, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return false;
+    const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u;
+    return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event), st, flags) == cudaSuccess;
+}
+
 template <typename T>
 T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
@@ -291,10 +300,7 @@ moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float 
     cudaStream_t st = as_stream(stream);
     int ev = 0;
     auto mark = [&]() -> bool {
-        if (ev < n_events) {
-            if (cudaEventRecord(static_cast<cudaEvent_t>(events[ev]), st) != cudaSuccess)
-                return false;
-        }
+        if (ev < n_events && !record_event(events[ev], st)) return false;
         ++ev;
         return true;
     };
@@ -523,10 +529,7 @@ moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, cons
     cudaStream_t st = as_stream(stream);
     int ev = 0;
     auto mark = [&]() -> bool {
-        if (ev < n_events) {
-            if (cudaEventRecord(static_cast<cudaEvent_t>(events[ev]), st) != cudaSuccess)
-                return false;
-        }
+        if (ev < n_events && !record_event(events[ev], st)) return false;
         ++ev;
         return true;
     };
