@@ -297,6 +297,13 @@ moe_status_t moe_forward_host_stream(const moe_bf16 *X_host, moe_bf16 *Y_host, i
                                      int renorm, void *ws, size_t ws_bytes, void *stream,
                                      void *h2d_stream, void *d2h_stream);
 
+/* Failure-detection self-test: enqueues one CTA that waits, through the same
+ * bounded wait as the GEMM pipelines, on a barrier nothing arrives at. After
+ * the wait limit (about 1 s) it sets MOE_DEVERR_TIMEOUT in the workspace's
+ * error word and exits; moe_sync_check then returns MOE_ERR_DEVICE_TIMEOUT and
+ * the context stays usable. ws: any workspace of >= 64 bytes. */
+moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream);
+
 /* Wait for `stream`, read and clear the workspace's device error word.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_CHECK (or
  * MOE_ERR_CUDA); *word_out (may be NULL) receives the raw bits. */

@@ -443,6 +443,13 @@ moe_status_t moe_forward_host_stream(const moe_bf16 *X_host, moe_bf16 *Y_host, i
     return (e1 == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess) ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, void *stream) {
+    if (ws == nullptr || ws_bytes < 64) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_arch();
+    if (s != MOE_OK) return s;
+    return from_cuda(launch_wait_timeout_selftest(at<uint32_t>(ws, 0), as_stream(stream)));
+}
+
 moe_status_t moe_sync_check(void *ws, void *stream, uint32_t *word_out) {
     if (ws == nullptr) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);

@@ -24,15 +24,17 @@ constexpr int kWarps = kThreads / 32;
 
 __global__ void __launch_bounds__(kThreads)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ X, const int32_t *__restrict__ perm_token,
-                   int T, int R, int d, __nv_bfloat16 *__restrict__ Xg) {
+                   int T, int R, const int32_t *__restrict__ rows_used, int d,
+                   __nv_bfloat16 *__restrict__ Xg, uint32_t *err) {
     const int64_t p = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (p >= R) return;
+    if (p >= R || (rows_used != nullptr && p >= __ldg(rows_used))) return;
     const int lane = threadIdx.x & 31;
     const int64_t t = perm_token[p];
     uint4 *dst = reinterpret_cast<uint4 *>(Xg + p * d);
     const int nv = d / 8;
-    if (t < 0 || t >= T) {  // a row no slot maps to: zeros
+    if (t < 0 || t >= T) {  // a token index out of range: zeros, flagged
         for (int c = lane; c < nv; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        if (lane == 0 && err != nullptr) atomicOr(err, MOE_DEVERR_BAD_EXPERT);
         return;
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(X + t * d);
@@ -85,8 +87,10 @@ combine_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restrict__ 
 }  // namespace
 
 cudaError_t launch_gather_rows(const __nv_bfloat16 *X, const int32_t *perm_token, int T, int R,
-                               int d, __nv_bfloat16 *Xg, cudaStream_t s) {
-    gather_rows_kernel<<<(R + kWarps - 1) / kWarps, kThreads, 0, s>>>(X, perm_token, T, R, d, Xg);
+                               const int32_t *rows_used, int d, __nv_bfloat16 *Xg, uint32_t *err,
+                               cudaStream_t s) {
+    gather_rows_kernel<<<(R + kWarps - 1) / kWarps, kThreads, 0, s>>>(X, perm_token, T, R,
+                                                                       rows_used, d, Xg, err);
     return cudaGetLastError();
 }
 

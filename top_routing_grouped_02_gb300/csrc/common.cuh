@@ -81,8 +81,11 @@ cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, 
                            int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
                            int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
                            const WsLayout &L, char *ws, cudaStream_t s);
+// Rows p < min(R, *rows_used) (rows_used: device, nullable); a token index out of
+// range gives a zero row and sets MOE_DEVERR_BAD_EXPERT in *err.
 cudaError_t launch_gather_rows(const __nv_bfloat16 *X, const int32_t *perm_token, int T, int R,
-                               int d, __nv_bfloat16 *Xg, cudaStream_t s);
+                               const int32_t *rows_used, int d, __nv_bfloat16 *Xg, uint32_t *err,
+                               cudaStream_t s);
 // xg: scratch [R, d] for the gathered rows (used when the CTA-pair kernel runs)
 cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_token, int T,
                                 const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
@@ -108,6 +111,10 @@ cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *coun
 cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map,
                                 const int32_t *tok_rows, const int32_t *tok_n, int T, int E,
                                 int d, int64_t rows_cap, __nv_bfloat16 *Y, cudaStream_t s);
+
+// One CTA whose pipeline wait on a barrier nothing arrives at runs out after the
+// wait limit (about 1 s) and sets MOE_DEVERR_TIMEOUT in *err.
+cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s);
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();

@@ -553,6 +553,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
 }
 
+// Failure-detection self-test: one thread waits, through the pipeline's own
+// bounded wait, on a shared-memory barrier that nothing arrives at. After the
+// time limit the wait gives up, sets MOE_DEVERR_TIMEOUT and the kernel returns.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint32_t *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = ptx::smem_addr(&bar);
+    ptx::mbar_init(b, 1);
+    ptx::fence_barrier_init();
+    bounded_wait<false>(b, 0, err);  // phase 0 never completes
+}
+
 // ------------------------------------------------------------ host side --
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -673,13 +685,19 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_toke
     const int tiles = R / BM + E;  // upper bound of the 128-row tiles
     if (use_pair(R, E)) {
         // CTA pairs load A by TMA from rows gathered into xg beforehand
-        cudaError_t e = launch_gather_rows(X, perm_token, T, R, d, xg, s);
+        // the grouped rows in use end at offsets[E]
+        cudaError_t e = launch_gather_rows(X, perm_token, T, R, offsets + E, d, xg, err, s);
         if (e != cudaSuccess) return e;
         if (!make_map(&ta, xg, d, R, 64, BM)) return cudaErrorInvalidValue;
         return launch_variant<kGateUp, true>(ta, tb0, tb1, th, args, (tiles / 2 + E) * args.NB, s);
     }
     // single CTAs gather their A rows themselves; the A map argument is not read
     return launch_variant<kGateUp, false>(tb0, tb0, tb1, th, args, tiles * args.NB, s);
+}
+
+cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
                               _P]),
     "moe_sync_check": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_selftest_wait_timeout": (_I, [_P, _SZ, _P]),
     "moe_forward_host_stream": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                      _I, _P, _SZ, _P, _P, _P]),
     "moe_round_capacity": (ctypes.c_int64, [_I, _I, _I, _I]),
@@ -329,6 +330,12 @@ def moe_forward_host_stream(X_host, Y_host, X_dev2, Y_dev2, Wr, W1, W3, W2, K: i
         _ptr(W2, torch.bfloat16), T, d, E, K, n, int(bool(renorm)), _ptr(ws), ws.numel(),
         _stream(stream), _stream(h2d_stream), _stream(d2h_stream)))
     return Y_host
+
+
+def moe_selftest_wait_timeout(ws, stream=None):
+    """Enqueue the bounded-wait self-test (sets MOE_DEVERR_TIMEOUT after ~1 s)."""
+    _check("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(
+        _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_sync_check(ws, stream=None):
