@@ -14,7 +14,8 @@ Prints ONE JSON line on rank 0:
   roofline    the dominant kernel (gate/up GEMM) against the measured bf16 peak
   cpu_baseline  the CPU oracle on a bounded token sample (rank 0, N=1 only)
   clocks      nvidia-smi SM clocks / throttle reasons sampled during the timed region
-  extra       tokens/s, per-kernel times, router and combine GB/s, % of peak
+  extra       tokens/s, per-kernel times, router and combine GB/s, % of peak, routing
+              statistics (tile padding, rows per expert)
 
 --routing rounded runs the layer under Token Rounding (moe_forward_rounded: each
 expert's top-K count rounded to a multiple of the 128-row tile); its value
@@ -362,6 +363,20 @@ def run_gpu(args, c, world, rank, local):
     barrier(world)
     e2e_value = aggregate(flops * e2e_steps, e2e_s, world) / 1e12
 
+    # routing statistics (outside the timed region): tile padding and expert load
+    if rounded:
+        cnt = (row_map >= 0).sum(dim=0).cpu().numpy()
+    else:
+        _, _, cnt_t = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"])
+        cnt = cnt_t.cpu().numpy()
+    tiles_used = int(np.sum((cnt + 127) // 128))
+    routing_stats = {
+        "active_experts": int((cnt > 0).sum()), "rows_per_expert_max": int(cnt.max()),
+        "rows_per_expert_min": int(cnt.min()), "rows_per_expert_var": round(float(cnt.var()), 1),
+        "tiles_128": tiles_used,
+        "padded_rows_pct": round(100.0 * (tiles_used * 128 - int(cnt.sum())) / max(1, tiles_used * 128), 2),
+    }
+
     peaks = load_peaks()
     g1_flops = 4.0 * R * d * n
     g1_tflops = g1_flops / (stage_ms["gemm_gate_up"] / 1e3) / 1e12
@@ -395,6 +410,7 @@ def run_gpu(args, c, world, rank, local):
             "pct_bf16_peak_layer": round(value / world / peaks["bf16"] * 100, 2),
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
             "topk_rows_equiv_tflops": round(useful_flops(c) * world / (ms_step / 1e3) / 1e12, 3),
+            "routing": routing_stats,
             "gemm_down_tflops": round(g2_tflops, 2),
             "router_GBps": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9, 1),
             "router_frac_hbm": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9 / peaks["hbm"], 4),
