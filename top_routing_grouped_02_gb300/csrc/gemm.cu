@@ -27,7 +27,7 @@
 // complete on the even CTA's barrier, MMA completion is multicast to both, and
 // both CTAs' epilogues release the accumulator to the even CTA.
 //
-// Warp roles (256 threads):
+// Warp roles (128 + 32 * EW threads):
 //   warp 0      TMA producer: B tile 64x256 (MN-major, four 64-column boxes;
 //               two per CTA of a pair) per stage, 128-byte swizzle, and the A
 //               tile 128x64 (K-major) unless the A rows are gathered.
@@ -40,7 +40,9 @@
 //               back to the producer and, after the last stage, the
 //               accumulator to the epilogue.
 //   warp 2      allocates / frees 512 TMEM columns (2 accumulators x 256).
-//   warps 4-7   epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
+//   warps 4..    epilogue, EW = 4 or 8 warps: warp w reads TMEM lanes
+//               32(w%4)..+31 (= tile rows); with 8 the two warps of each lane
+//               quadrant take half of the columns: tcgen05.ld of the lanes,
 //               activation or scaling in fp32, bf16 packing; each 32 x 32
 //               chunk goes through a swizzled shared-memory buffer and one TMA
 //               store (whole 64-byte row segments instead of 32 half-sector
@@ -59,7 +61,11 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+// Epilogue warps: 4, or 8 when a tile's main loop is short (see choose_ew).
+// A launch has 128 + 32 * EW threads.
+constexpr int kMaxThreads = 128 + 32 * 8;
+template <int EW>
+constexpr int threads_of() { return 128 + 32 * EW; }
 constexpr int BM = kTileM;  // 128 rows per CTA
 constexpr int BK = 64;      // reduction depth per stage (128 bytes of bf16)
 constexpr int BN = 256;     // accumulator columns per unit
@@ -86,7 +92,7 @@ struct Geo {
     static constexpr uint32_t kStageBytes = kABytes + kBBoxes * kBBox;
     static constexpr uint32_t kIdesc =
         ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
-    static constexpr uint32_t kTemptyCount = PAIR ? 8 : 4;  // epilogue warps signalling
+
 };
 
 enum Mode : int { kGateUp = 0, kDown = 1 };
@@ -111,13 +117,14 @@ struct Ctl {
     uint32_t tmem_base;
     int32_t tile_base[kMaxE + 1];
     int32_t offsets[kMaxE + 1];
-    int32_t scan[kThreads / 32 + 1];
+    int32_t scan[kMaxThreads / 32 + 1];
 };
 
-// Epilogue staging: per epilogue warp two 32-row x 32-column bf16 buffers
-// (64-byte rows, 64-byte swizzle) that a TMA store writes out.
+// Epilogue staging: 32-row x 32-column bf16 buffers (64-byte rows, 64-byte
+// swizzle) that TMA stores write out; 8 of them, two per warp with 4 epilogue
+// warps and one per warp with 8.
 constexpr uint32_t kEpiBuf = 32 * 32 * 2;
-constexpr uint32_t kEpiBytes = 4 * 2 * kEpiBuf;
+constexpr uint32_t kEpiBytes = 8 * kEpiBuf;
 
 template <bool PAIR>
 constexpr size_t smem_bytes() {
@@ -181,13 +188,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int MODE, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, bool PAIR, int EW>
+__global__ void __launch_bounds__(threads_of<EW>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
                     const GemmArgs args) {
     using G = Geo<PAIR>;
     constexpr int S = G::kStages;
+    constexpr int kThreads = threads_of<EW>();
+    // epilogue warps signalling an accumulator release (both CTAs of a pair)
+    constexpr uint32_t kTemptyCount = PAIR ? 2 * EW : EW;
+    constexpr int kNBuf = 8 / EW;  // staging buffers per epilogue warp
     // A rows gathered in the kernel (single-CTA gate/up) or loaded by TMA
     constexpr bool GATHER = (MODE == kGateUp) && !PAIR;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -212,7 +223,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&ctl->tfull[a]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), G::kTemptyCount);
+            ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), kTemptyCount);
         }
         ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
         ptx::fence_barrier_init();
@@ -442,12 +453,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (uint32_t j = it >= (uint32_t)kGatherLag ? it - kGatherLag : 0u; j < it; ++j) signal(j);
     } else if (warp >= 4) {
         // -------------------------------------------------------- epilogue --
-        const int q = warp - 4;  // TMEM lanes 32q..32q+31 = tile rows
+        // TMEM lanes 32q..32q+31 (= tile rows) belong to warps with warp % 4 == q;
+        // with 8 epilogue warps the two warps of a quadrant split the tile's
+        // 32-column chunks
+        const int q = warp & 3, half = (warp - 4) >> 2, nhalf = EW / 4;
         const int r = q * 32 + lane;
         const uint32_t tempty0 = PAIR ? ptx::mapa(ptx::smem_addr(&ctl->tempty[0]), 0)
                                       : ptx::smem_addr(&ctl->tempty[0]);
-        // this warp's two output staging buffers
-        const uint32_t epi_base = smem_base + (uint32_t)S * G::kStageBytes + (uint32_t)q * 2 * kEpiBuf;
+        // this warp's output staging buffers
+        const uint32_t epi_base =
+            smem_base + (uint32_t)S * G::kStageBytes + (uint32_t)(warp - 4) * kNBuf * kEpiBuf;
         uint32_t epi_groups = 0;  // TMA store groups this warp has committed
         uint32_t uc = 0;
         for (int u = first_unit; u < total_units; u += unit_stride, ++uc) {
@@ -465,10 +480,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const bool whole = q * 32 + 31 < rows;
             auto emit = [&](const uint32_t (&packed)[16], __nv_bfloat16 *dst, int col) {
                 if (whole) {
-                    // buffers alternate with the store groups, so the group that
-                    // last read this buffer is the one before the most recent
-                    const uint32_t buf = epi_base + (epi_groups & 1u) * kEpiBuf;
-                    if (lane == 0 && epi_groups >= 2) ptx::bulk_wait_group_read<1>();
+                    // buffers rotate with the store groups, so the group that last
+                    // read this buffer is the kNBuf-th most recent one
+                    const uint32_t buf = epi_base + (epi_groups % kNBuf) * kEpiBuf;
+                    if (lane == 0 && epi_groups >= (uint32_t)kNBuf)
+                        ptx::bulk_wait_group_read<kNBuf - 1>();
                     __syncwarp();
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -493,7 +509,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (MODE == kGateUp) {
                 __nv_bfloat16 *dst = args.out + p * args.out_ld + nb * 128;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = half * (4 / nhalf); c < (half + 1) * (4 / nhalf); ++c) {
                     uint32_t g[32], v[32];
                     ptx::tmem_ld32(taddr + c * 32, g);
                     ptx::tmem_ld32(taddr + 128 + c * 32, v);
@@ -517,7 +533,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 __nv_bfloat16 *dst = args.out + p * args.out_ld + nb * BN;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld32(taddr + c * 32, v);
                     uint32_t packed[16];
@@ -601,23 +617,24 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool PAIR>
-cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                           const CUtensorMap &out, const GemmArgs &args, int max_units,
-                           cudaStream_t s) {
+template <int MODE, bool PAIR, int EW>
+cudaError_t launch_ew(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                      const CUtensorMap &out, const GemmArgs &args, int max_units,
+                      cudaStream_t s) {
     constexpr size_t kSmem = smem_bytes<PAIR>();
+    constexpr int kThreads = threads_of<EW>();
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, PAIR>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, PAIR, EW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     if (!PAIR) {
         const int grid = max(1, min(sm_count(), max_units));
-        grouped_gemm_kernel<MODE, false><<<grid, kThreads, kSmem, s>>>(a, b0, b1, out, args);
+        grouped_gemm_kernel<MODE, false, EW><<<grid, kThreads, kSmem, s>>>(a, b0, b1, out, args);
         return cudaGetLastError();
     }
     // one cluster of 2 CTAs (an SM pair) per unit slot
@@ -634,7 +651,19 @@ cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, true>, a, b0, b1, out, args);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, true, EW>, a, b0, b1, out, args);
+}
+
+// Eight epilogue warps when a tile's main loop is at most 8 k-blocks (the
+// epilogue then dominates: measured on the SonicMoE-shaped down GEMM, n = 256,
+// 0.082 -> 0.072 ms); four otherwise (with longer main loops the extra warps
+// cost slightly: DeepSeek-V3-shaped GEMMs about 1% slower).
+template <int MODE, bool PAIR>
+cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                           const CUtensorMap &out, const GemmArgs &args, int max_units,
+                           cudaStream_t s) {
+    if (args.Kdim / BK <= 8) return launch_ew<MODE, PAIR, 8>(a, b0, b1, out, args, max_units, s);
+    return launch_ew<MODE, PAIR, 4>(a, b0, b1, out, args, max_units, s);
 }
 
 // CTA pairs halve the B bytes each SM receives per MMA and so allow a deeper
