@@ -1,6 +1,7 @@
 // C ABI of libmoe.so: argument checking, workspace layout and the sequence of
 // kernel launches for each entry point declared in include/moe.h.
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 
@@ -83,6 +84,14 @@ T *at(void *ws, size_t off) {
 }
 
 }  // namespace
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("MOE_PDL");
+        return !(v != nullptr && v[0] == '0');
+    }();
+    return on;
+}
 
 int sm_count() {
     const DeviceInfo *di = device_info();

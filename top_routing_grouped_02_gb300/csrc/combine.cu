@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kThreads)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ X, const int32_t *__restrict__ perm_token,
                    int T, int R, const int32_t *__restrict__ rows_used, int d,
                    __nv_bfloat16 *__restrict__ Xg, uint32_t *err) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t p = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (p >= R || (rows_used != nullptr && p >= __ldg(rows_used))) return;
     const int lane = threadIdx.x & 31;
@@ -45,6 +47,8 @@ template <int KU>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restrict__ row_of_slot,
                int T, int K, int d, __nv_bfloat16 *__restrict__ Y) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const int lane = threadIdx.x & 31;
@@ -89,21 +93,16 @@ combine_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restrict__ 
 cudaError_t launch_gather_rows(const __nv_bfloat16 *X, const int32_t *perm_token, int T, int R,
                                const int32_t *rows_used, int d, __nv_bfloat16 *Xg, uint32_t *err,
                                cudaStream_t s) {
-    gather_rows_kernel<<<(R + kWarps - 1) / kWarps, kThreads, 0, s>>>(X, perm_token, T, R,
-                                                                       rows_used, d, Xg, err);
-    return cudaGetLastError();
+    return launch_k(gather_rows_kernel, dim3((R + kWarps - 1) / kWarps), dim3(kThreads), 0, s, X,
+                    perm_token, T, R, rows_used, d, Xg, err);
 }
 
 cudaError_t launch_combine(const __nv_bfloat16 *Z, const int32_t *row_of_slot, int T, int K,
                            int d, __nv_bfloat16 *Y, cudaStream_t s) {
     const unsigned blocks = (unsigned)((T + kWarps - 1) / kWarps);
-    if (K <= 2)
-        combine_kernel<2><<<blocks, kThreads, 0, s>>>(Z, row_of_slot, T, K, d, Y);
-    else if (K <= 4)
-        combine_kernel<4><<<blocks, kThreads, 0, s>>>(Z, row_of_slot, T, K, d, Y);
-    else
-        combine_kernel<8><<<blocks, kThreads, 0, s>>>(Z, row_of_slot, T, K, d, Y);
-    return cudaGetLastError();
+    if (K <= 2) return launch_k(combine_kernel<2>, dim3(blocks), dim3(kThreads), 0, s, Z, row_of_slot, T, K, d, Y);
+    if (K <= 4) return launch_k(combine_kernel<4>, dim3(blocks), dim3(kThreads), 0, s, Z, row_of_slot, T, K, d, Y);
+    return launch_k(combine_kernel<8>, dim3(blocks), dim3(kThreads), 0, s, Z, row_of_slot, T, K, d, Y);
 }
 
 }  // namespace moe

@@ -116,6 +116,37 @@ cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map,
 // wait limit (about 1 s) and sets MOE_DEVERR_TIMEOUT in *err.
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s);
 
+// ---- programmatic dependent launch ------------------------------------------
+// Kernels of the path are launched so that each may start (and run the setup
+// that touches no global memory) while its predecessor on the stream finishes.
+// Every such kernel calls pdl_wait() before its first global-memory access, which
+// returns once the predecessor grid has completed and its writes are visible
+// (at once for a launch without the attribute), then pdl_trigger(), which lets
+// its own dependent be scheduled. A dependent launches only after every CTA of
+// its predecessor is resident, so waiting CTAs never block their predecessor.
+// MOE_PDL=0 in the environment launches them in plain stream order.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 

@@ -243,6 +243,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ptx::tmem_relinquish();
         }
     }
+    // barriers, TMEM and tensor maps are set up; from here on global memory
+    // written by the previous kernel is read
+    pdl_wait();
+    pdl_trigger();
     {
         // work-tile bases: exclusive scan over experts of ceil(rows_e / 128)
         // tiles (single CTA) or of ceil(tiles_e / 2) tile pairs (CTA pair)
@@ -634,8 +638,8 @@ cudaError_t launch_ew(const CUtensorMap &a, const CUtensorMap &b0, const CUtenso
     }
     if (!PAIR) {
         const int grid = max(1, min(sm_count(), max_units));
-        grouped_gemm_kernel<MODE, false, EW><<<grid, kThreads, kSmem, s>>>(a, b0, b1, out, args);
-        return cudaGetLastError();
+        return launch_k(grouped_gemm_kernel<MODE, false, EW>, dim3(grid), dim3(kThreads), kSmem, s,
+                        a, b0, b1, out, args);
     }
     // one cluster of 2 CTAs (an SM pair) per unit slot
     const int pairs = max(1, min(sm_count() / 2, max_units));
@@ -644,13 +648,15 @@ cudaError_t launch_ew(const CUtensorMap &a, const CUtensorMap &b0, const CUtenso
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, true, EW>, a, b0, b1, out, args);
 }
 

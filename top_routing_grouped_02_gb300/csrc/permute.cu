@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kThreads)
 rank_kernel(const int32_t *__restrict__ idx, int T, int E, int K, int nchunks,
             int32_t *__restrict__ rank, int32_t *__restrict__ chunk_cnt,
             uint32_t *__restrict__ ctrl) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ uint32_t masks[kThreads / 32][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[kWordDone] = 0;  // ticket for the scan
@@ -96,6 +98,8 @@ scan_kernel(int32_t *__restrict__ chunk_cnt, int nchunks, int E, const int32_t *
             int32_t *__restrict__ totals, int32_t *__restrict__ offsets,
             int32_t *__restrict__ tile_base, int32_t *__restrict__ tiles,
             int32_t *__restrict__ num_tiles, uint32_t *__restrict__ ctrl) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int warp_sums[kThreads / 32 + 1];
     __shared__ bool is_last;
     const int e = blockIdx.x;
@@ -153,6 +157,8 @@ scatter_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ rank
                int T, int E, int K, int nchunks, int32_t *__restrict__ perm_token,
                int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of_slot,
                uint32_t *__restrict__ ctrl) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t slot = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t R = (int64_t)T * K;
     if (slot >= R) return;
@@ -187,17 +193,16 @@ cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, 
     int32_t *tile_base = reinterpret_cast<int32_t *>(ws + L.tile_base);
     const int nchunks = L.nchunks;
     const int64_t R = (int64_t)T * K;
-    rank_kernel<<<(nchunks + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, s>>>(
-        idx, T, E, K, nchunks, rank, chunk, ctrl);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_k(rank_kernel, dim3((nchunks + kThreads / 32 - 1) / (kThreads / 32)),
+                               dim3(kThreads), 0, s, idx, T, E, K, nchunks, rank, chunk, ctrl);
     if (err != cudaSuccess) return err;
-    scan_kernel<<<E, kThreads, 0, s>>>(chunk, nchunks, E, counts_in, totals, offsets, tile_base,
-                                       tiles, num_tiles, ctrl);
-    err = cudaGetLastError();
+    err = launch_k(scan_kernel, dim3(E), dim3(kThreads), 0, s, chunk, nchunks, E, counts_in, totals,
+                   offsets, tile_base, tiles, num_tiles, ctrl);
     if (err != cudaSuccess) return err;
-    scatter_kernel<<<(unsigned)((R + kThreads - 1) / kThreads), kThreads, 0, s>>>(
-        idx, rank, chunk, offsets, T, E, K, nchunks, perm_token, perm_slot, row_of_slot, ctrl);
-    return cudaGetLastError();
+    return launch_k(scatter_kernel, dim3((unsigned)((R + kThreads - 1) / kThreads)), dim3(kThreads),
+                    0, s, idx, static_cast<const int32_t *>(rank), static_cast<const int32_t *>(chunk),
+                    static_cast<const int32_t *>(offsets), T, E, K, nchunks, perm_token, perm_slot,
+                    row_of_slot, ctrl);
 }
 
 }  // namespace moe

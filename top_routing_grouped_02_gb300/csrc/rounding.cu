@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(kPThreads)
 round_prep_kernel(const float *__restrict__ L, const int32_t *__restrict__ idx,
                   const int32_t *__restrict__ counts, int T, int E, int K, int M, bool vec,
                   uint32_t *__restrict__ keyT, int32_t *__restrict__ row_map, uint32_t *err) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_L[kPT][kMaxE + 1];
     __shared__ uint32_t s_mem[kPT][kMaxE / 32];
     __shared__ int s_mode[kMaxE];
@@ -261,6 +263,8 @@ struct RoundArgs {
 // stay in registers for all passes; GM == 0: every pass reads them again.
 template <int GM>
 __global__ void __launch_bounds__(kRThreads, 1) round_select_kernel(RoundArgs a) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_off[kMaxE + 1];  // exclusive prefix of the rounded counts
     __shared__ int s_tb[kMaxE + 1];   // exclusive prefix of the 128-row tile counts
     __shared__ __align__(16) int s_hist[kHistWords];
@@ -566,6 +570,8 @@ __global__ void __launch_bounds__(kWThreads)
 round_weights_kernel(const float *__restrict__ L, const int32_t *__restrict__ row_map, int T,
                      int E, int renorm, bool vec, float *__restrict__ row_w,
                      int32_t *__restrict__ tok_rows, int32_t *__restrict__ tok_n) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t t = (int64_t)blockIdx.x * kWWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const int lane = threadIdx.x & 31;
@@ -715,6 +721,8 @@ __global__ void __launch_bounds__(kCThreads)
 combine_rows_kernel(const __nv_bfloat16 *__restrict__ Z, const int32_t *__restrict__ row_map,
                     const int32_t *__restrict__ tok_rows, const int32_t *__restrict__ tok_n,
                     int T, int E, int d, int64_t rows_cap, __nv_bfloat16 *__restrict__ Y) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_rows[kCWarps][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kCWarps + warp;
@@ -762,9 +770,9 @@ cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *coun
     // 16-byte accesses when every row of L and row_map starts 16-byte aligned
     const bool vec = (E % 4) == 0 && ((reinterpret_cast<uintptr_t>(L) |
                                        reinterpret_cast<uintptr_t>(row_map)) & 15u) == 0;
-    round_prep_kernel<<<(unsigned)(key_stride(T) / kPT), kPThreads, 0, s>>>(
-        L, idx, counts, T, E, K, M, vec, keyT, row_map, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_k(round_prep_kernel, dim3((unsigned)(key_stride(T) / kPT)),
+                             dim3(kPThreads), 0, s, L, idx, counts, T, E, K, M, vec, keyT, row_map,
+                             err);
     if (e != cudaSuccess) return e;
     RoundArgs a{};
     a.keyT = keyT;
@@ -781,22 +789,18 @@ cudaError_t launch_round(const float *L, const int32_t *idx, const int32_t *coun
     a.tiles = tiles;
     a.num_tiles = num_tiles;
     a.err = err;
-    if (key_stride(T) <= 4 * 4 * kRThreads)
-        round_select_kernel<4><<<E, kRThreads, 0, s>>>(a);
-    else
-        round_select_kernel<0><<<E, kRThreads, 0, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    round_weights_kernel<<<(unsigned)((T + kWWarps - 1) / kWWarps), kWThreads, 0, s>>>(
-        L, row_map, T, E, renorm, vec, row_w, tok_rows, tok_n);
-    return cudaGetLastError();
+    auto sel = key_stride(T) <= 4 * 4 * kRThreads ? round_select_kernel<4> : round_select_kernel<0>;
+    if ((e = launch_k(sel, dim3(E), dim3(kRThreads), 0, s, a)) != cudaSuccess) return e;
+    return launch_k(round_weights_kernel, dim3((unsigned)((T + kWWarps - 1) / kWWarps)),
+                    dim3(kWThreads), 0, s, L, static_cast<const int32_t *>(row_map), T, E, renorm,
+                    vec, row_w, tok_rows, tok_n);
 }
 
 cudaError_t launch_combine_rows(const __nv_bfloat16 *Z, const int32_t *row_map,
                                 const int32_t *tok_rows, const int32_t *tok_n, int T, int E,
                                 int d, int64_t rows_cap, __nv_bfloat16 *Y, cudaStream_t s) {
-    combine_rows_kernel<<<(unsigned)((T + kCWarps - 1) / kCWarps), kCThreads, 0, s>>>(
-        Z, row_map, tok_rows, tok_n, T, E, d, rows_cap, Y);
-    return cudaGetLastError();
+    return launch_k(combine_rows_kernel, dim3((unsigned)((T + kCWarps - 1) / kCWarps)),
+                    dim3(kCThreads), 0, s, Z, row_map, tok_rows, tok_n, T, E, d, rows_cap, Y);
 }
 
 }  // namespace moe

@@ -72,6 +72,8 @@ template <int EP>
 __global__ void __launch_bounds__(ChainCfg<EP>::THREADS)
 logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
                     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    pdl_wait();
+    pdl_trigger();
     using C = ChainCfg<EP>;
     constexpr int NTH = C::THREADS;
     extern __shared__ __align__(16) unsigned char sm[];
@@ -166,6 +168,8 @@ template <int EP>
 __global__ void __launch_bounds__(kSmallThreads)
 logits_small_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
                     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int kTok = kSmallThreads / EP;
     const int e = threadIdx.x % EP;
     const int64_t t = (int64_t)blockIdx.x * kTok + threadIdx.x / EP;
@@ -215,6 +219,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(kWThreads)
 logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
                     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ __align__(16) float xs[2][kWK][kWT];
     __shared__ __align__(16) float ws[2][kWK][kWE];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -352,6 +358,8 @@ __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
               int32_t *__restrict__ idx_out, float *__restrict__ w_out,
               int32_t *__restrict__ counts) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int hist[kMaxE];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int e = tid; e < kMaxE; e += kSelThreads) hist[e] = 0;
@@ -455,6 +463,8 @@ __global__ void __launch_bounds__(kSelSingleThreads)
 select_single_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
                      int32_t *__restrict__ idx_out, float *__restrict__ w_out,
                      int32_t *__restrict__ counts) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int hist[EP];
     for (int e = threadIdx.x; e < EP; e += kSelSingleThreads) hist[e] = 0;
     __syncthreads();
@@ -515,26 +525,19 @@ select_single_kernel(const float *__restrict__ logits, int T, int E, int K, int 
 cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, int32_t *idx,
                           float *w, int32_t *counts, cudaStream_t s) {
     if (E <= 16 && T <= kSelSingleMaxT) {
-        if (E <= 8)
-            select_single_kernel<8><<<1, kSelSingleThreads, 0, s>>>(logits, T, E, K, renorm, idx, w,
-                                                                    counts);
-        else
-            select_single_kernel<16><<<1, kSelSingleThreads, 0, s>>>(logits, T, E, K, renorm, idx,
-                                                                     w, counts);
-        return cudaGetLastError();
+        auto kern = E <= 8 ? select_single_kernel<8> : select_single_kernel<16>;
+        return launch_k(kern, dim3(1), dim3(kSelSingleThreads), 0, s, logits, T, E, K, renorm, idx,
+                        w, counts);
     }
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((T + kSelThreads / 32 - 1) / (kSelThreads / 32));
-    if (E <= 32)
-        select_kernel<1><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    else if (E <= 64)
-        select_kernel<2><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    else if (E <= 128)
-        select_kernel<4><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    else
-        select_kernel<8><<<blocks, kSelThreads, 0, s>>>(logits, T, E, K, renorm, idx, w, counts);
-    return cudaGetLastError();
+    auto kern = E <= 32    ? select_kernel<1>
+                : E <= 64  ? select_kernel<2>
+                : E <= 128 ? select_kernel<4>
+                           : select_kernel<8>;
+    return launch_k(kern, dim3(blocks), dim3(kSelThreads), 0, s, logits, T, E, K, renorm, idx, w,
+                    counts);
 }
 
 template <int EP>
@@ -551,8 +554,8 @@ cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *b
         configured[dev] = true;
     }
     const unsigned grid = (unsigned)((T + kChainTok - 1) / kChainTok);
-    logits_chain_kernel<EP><<<grid, C::THREADS, C::SMEM, s>>>(X, Wr, bias, T, d, E, L);
-    return cudaGetLastError();
+    return launch_k(logits_chain_kernel<EP>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM, s, X,
+                    Wr, bias, T, d, E, L);
 }
 
 }  // namespace
@@ -566,23 +569,15 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
         return launch_chain<32>(X, Wr, bias, T, d, E, L, s);
     }
     if (E <= 32) {
-        auto grid = [&](int ep) {
-            return (unsigned)(((int64_t)T * ep + kSmallThreads - 1) / kSmallThreads);
-        };
-        if (E <= 8)
-            logits_small_kernel<8><<<grid(8), kSmallThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
-        else if (E <= 16)
-            logits_small_kernel<16><<<grid(16), kSmallThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
-        else
-            logits_small_kernel<32><<<grid(32), kSmallThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
-    } else {
-        const dim3 grid((unsigned)((T + kWT - 1) / kWT), (unsigned)((E + kWE - 1) / kWE));
-        if (E % 4 == 0 && wr16)
-            logits_tiled_kernel<true><<<grid, kWThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
-        else
-            logits_tiled_kernel<false><<<grid, kWThreads, 0, s>>>(X, Wr, bias, T, d, E, L);
+        const int ep = E <= 8 ? 8 : (E <= 16 ? 16 : 32);
+        auto kern = E <= 8 ? logits_small_kernel<8>
+                           : (E <= 16 ? logits_small_kernel<16> : logits_small_kernel<32>);
+        const unsigned grid = (unsigned)(((int64_t)T * ep + kSmallThreads - 1) / kSmallThreads);
+        return launch_k(kern, dim3(grid), dim3(kSmallThreads), 0, s, X, Wr, bias, T, d, E, L);
     }
-    return cudaGetLastError();
+    const dim3 grid((unsigned)((T + kWT - 1) / kWT), (unsigned)((E + kWE - 1) / kWE));
+    auto kern = (E % 4 == 0 && wr16) ? logits_tiled_kernel<true> : logits_tiled_kernel<false>;
+    return launch_k(kern, grid, dim3(kWThreads), 0, s, X, Wr, bias, T, d, E, L);
 }
 
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
