@@ -93,6 +93,28 @@ def test_route_from_activations(T, d, E, K, zipf):
     _check_routing(idx, w, counts, idx_r, w_r, E)
 
 
+@pytest.mark.parametrize("pairs", ["4", "5", "6", "7", "8", None])
+@pytest.mark.parametrize("T,d,E,K,zipf", [
+    (9000, 200, 132, 4, True),   # second expert block holds 4 experts; d ends mid-stage
+    (700, 72, 256, 8, False),    # two full expert blocks, partial token block
+    (300, 96, 64, 6, False),     # fewer experts than a block
+])
+def test_router_logits_one_block_per_sm_kernel(T, d, E, K, zipf, pairs, monkeypatch):
+    # the 2P-token x 8-expert register tile, for every P (None: the host's choice)
+    if pairs is not None:
+        monkeypatch.setenv("MOE_ROUTER_PAIRS", pairs)
+    X = synth.normal("X", (T, d), 1.0, torch.bfloat16, "cuda")
+    Wr = synth.normal("Wr", (d, E), 1.0 / math.sqrt(d), torch.float32, "cuda")
+    bias = synth.zipf_bias(E).cuda() if zipf else None
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx, w, counts = moe.moe_route(X, Wr, K, bias, logits=logits)
+    torch.cuda.synchronize()
+    L = oracle.router_logits(bits(X), Wr.cpu().numpy(), None if bias is None else bias.cpu().numpy())
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), L.view(np.uint32))
+    idx_r, w_r = oracle.topk_softmax(L, K, True)
+    _check_routing(idx, w, counts, idx_r, w_r, E)
+
+
 def test_route_zero_activations_and_exact_ties():
     T, d, E, K = 100, 64, 8, 3
     X = torch.zeros(T, d, dtype=torch.bfloat16, device="cuda")

@@ -17,9 +17,10 @@
 //     chain stays in one thread and parallelism comes from tokens x experts:
 //       - E <= 32: two (token, expert) chains per thread fed from a cp.async
 //         shared-memory pipeline; bound by the latency of d dependent FMAs.
-//       - E > 32: one-warp blocks on 32-token x 64-expert tiles, 8x8 register
-//         micro-tiles fed by conflict-free float4 shared-memory reads; bound by
-//         the FP32 FMA pipe.
+//       - E > 32: two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
+//         micro-tiles fed by conflict-free float4 shared-memory reads.
+//       - E >= 128 with many tokens: one block per SM, each lane 2P tokens x 8
+//         experts, x read as bf16 pairs, so the FP32 FMA pipe is the limit.
 //  2. select: one warp per token reads its E logits, merges (max, sum of exp)
 //     across lanes with the online recurrence, picks K by repeated warp argmax
 //     (ties -> lower index), writes indices and weights, and counts per expert in
@@ -28,6 +29,7 @@
 //     the counts directly, so no memset is needed.
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 
@@ -343,6 +345,198 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
     }
 }
 
+// ---- E >= 128 with many tokens: one block per SM, two warps per scheduler -----
+// Block: 8 warps on 16(PA+PB) tokens x 128 experts. Lane (ty, tx) = (lane / 16,
+// lane % 16) of warp w owns the tokens of group g = 2w + ty (2PA of them for
+// w < 4, 2PB for w >= 4) and experts {4tx..4tx+3, 64+4tx..64+4tx+3}; its
+// accumulators are float2 pairs over neighbouring tokens. Warps w and w + 4 share
+// a scheduler, so each scheduler carries PA + PB token pairs in two warps: one
+// warp's issue slots fill the other's gaps after packed FMAs. Per reduction step
+// a lane reads its tokens' x as bf16 pairs (one 128-bit load, converted with byte
+// permutes) and its 8 weights (two 128-bit loads, conflict-free), and issues 8PA
+// or 8PB packed FMAs; each component rounds like __fmaf_rn, so every output is
+// still one sequential fma chain over j. 64-step stages, 3 deep, arrive by
+// cp.async (zero-filled beyond T, d and E): the weights as [j][e] rows, X as its
+// own [t][j] rows with the 16-byte chunks of a row pair XOR-swizzled, which one
+// pass per stage turns into the transposed, token-paired layout the steps read.
+// PA + PB (4..8) is chosen on the host so that the block count fills the SMs.
+constexpr int kBK = 64;        // reduction steps per stage
+constexpr int kBE = 128;       // experts per block
+constexpr int kBWords = 64;    // words in a transposed x row: 16 groups x 4 token pairs
+constexpr int kBStages = 3;
+constexpr int kBThreads = 256;
+constexpr int kBWBytes = kBK * kBE * 4;        // weight stage: 32 KB
+constexpr int kBXBytes = 2 * kBWords * kBK * 2;  // raw X stage (up to 128 rows): 16 KB
+constexpr int kBStage = kBWBytes + kBXBytes;
+constexpr int kBXsBytes = kBK * kBWords * 4;   // transposed x: 16 KB
+constexpr int kBSmem = kBStages * kBStage + 2 * kBXsBytes;
+
+__device__ __forceinline__ void cp_async16_zfill(void *smem_dst, const void *gmem_src, bool ok) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src),
+                 "r"(ok ? 16 : 0)
+                 : "memory");
+}
+
+// jn reduction steps of one stage for a lane with N token pairs (acc[0..N-1])
+template <int N, int PMAX, bool FULL>
+__device__ __forceinline__ void big_steps(float2 (&acc)[PMAX][8], const uint32_t *xs,
+                                          const float *w, int jn) {
+    auto step = [&](int jj) {
+        const uint4 xa = *reinterpret_cast<const uint4 *>(xs + jj * kBWords);
+        const float4 w0 = *reinterpret_cast<const float4 *>(w + jj * kBE);
+        const float4 w1 = *reinterpret_cast<const float4 *>(w + jj * kBE + 64);
+        const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float2 xp[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            xp[i] = make_float2(__uint_as_float(__byte_perm(xw[i], 0u, 0x1044)),
+                                __uint_as_float(__byte_perm(xw[i], 0u, 0x3244)));
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const float2 ww = make_float2(wv[b], wv[b]);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i][b] = __ffma2_rn(xp[i], ww, acc[i][b]);
+        }
+    };
+    if (FULL) {
+#pragma unroll 4
+        for (int jj = 0; jj < kBK; ++jj) step(jj);
+    } else {
+        for (int jj = 0; jj < jn; ++jj) step(jj);
+    }
+}
+
+template <int PA, int PB>
+__global__ void __launch_bounds__(kBThreads, 1)
+logits_big_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
+                  const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+    static_assert(PA >= PB && PA <= 4 && PB >= 1, "token pairs per lane");
+    pdl_wait();
+    pdl_trigger();
+    constexpr int kTok = 16 * (PA + PB);  // tokens per block
+    extern __shared__ __align__(16) uint8_t big_smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ty = lane >> 4, tx = lane & 15;
+    const int64_t t0 = (int64_t)blockIdx.x * kTok;
+    const int e0 = blockIdx.y * kBE;
+    const int nchunk = (d + kBK - 1) / kBK;
+
+    auto stage_w = [&](int c) {
+        return reinterpret_cast<float *>(big_smem + (c % kBStages) * kBStage);
+    };
+    auto stage_x = [&](int c) { return big_smem + (c % kBStages) * kBStage + kBWBytes; };
+    auto xs_of = [&](int c) {
+        return reinterpret_cast<uint32_t *>(big_smem + kBStages * kBStage + (c & 1) * kBXsBytes);
+    };
+
+    auto issue = [&](int c) {
+        if (c < nchunk) {
+            const int j0 = c * kBK;
+            float *w = stage_w(c);
+#pragma unroll
+            for (int i = 0; i < kBK * 32 / kBThreads; ++i) {
+                const int q = tid + kBThreads * i;
+                const int jj = q >> 5, ch = q & 31;
+                const int j = j0 + jj, e = e0 + 4 * ch;
+                const bool ok = j < d && e < E;
+                cp_async16_zfill(w + jj * kBE + 4 * ch, ok ? Wr + (int64_t)j * E + e : Wr, ok);
+            }
+            uint8_t *x = stage_x(c);
+            for (int q = tid; q < kTok * 8; q += kBThreads) {
+                const int r = q >> 3, ch = q & 7;
+                const int64_t t = t0 + r;
+                const int j = j0 + 8 * ch;
+                const bool ok = t < T && j < d;
+                cp_async16_zfill(x + r * 128 + ((ch ^ ((r >> 1) & 7)) << 4),
+                                 ok ? X + t * d + j : X, ok);
+            }
+        }
+        cp_async_commit();
+    };
+    // raw rows 2p, 2p+1 -> transposed words xs[j][4g + i] = (x[2p][j], x[2p+1][j])
+    // as a bf16 pair, where pair p is pair i of token group g
+    auto transpose = [&](int c) {
+        const uint8_t *x = stage_x(c);
+        uint32_t *xs = xs_of(c);
+        for (int q = tid; q < 8 * (PA + PB) * 8; q += kBThreads) {
+            const int p = q % (8 * (PA + PB)), ch = q / (8 * (PA + PB));
+            const int pos = (ch ^ (p & 7)) << 4;
+            const uint4 a = *reinterpret_cast<const uint4 *>(x + (2 * p) * 128 + pos);
+            const uint4 b = *reinterpret_cast<const uint4 *>(x + (2 * p + 1) * 128 + pos);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            const int word = p < 8 * PA ? 4 * (p / PA) + p % PA
+                                        : 4 * (8 + (p - 8 * PA) / PB) + (p - 8 * PA) % PB;
+            uint32_t *dst = xs + (8 * ch) * kBWords + word;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                dst[(2 * m) * kBWords] = __byte_perm(aw[m], bw[m], 0x5410);
+                dst[(2 * m + 1) * kBWords] = __byte_perm(aw[m], bw[m], 0x7632);
+            }
+        }
+    };
+
+    float2 acc[PA][8];
+#pragma unroll
+    for (int i = 0; i < PA; ++i)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[i][b] = make_float2(0.f, 0.f);
+
+    const int g = 2 * warp + ty;  // the lane's token group
+    const bool wa = warp < 4;     // PA token pairs (else PB)
+
+    issue(0);
+    issue(1);
+    cp_async_wait<1>();
+    __syncthreads();
+    transpose(0);
+    for (int c = 0; c < nchunk; ++c) {
+        cp_async_wait<0>();  // stage c + 1 (issued one stage earlier) has landed
+        __syncthreads();     // and every thread is past stage c - 1 and transpose(c)
+        issue(c + 2);        // into the slot stage c - 1 used
+        if (c + 1 < nchunk) transpose(c + 1);
+        const uint32_t *xs = xs_of(c) + 4 * g;
+        const float *w = stage_w(c) + 4 * tx;
+        const int jn = min(kBK, d - c * kBK);
+        if (jn == kBK) {
+            if (wa) big_steps<PA, PA, true>(acc, xs, w, jn);
+            else big_steps<PB, PA, true>(acc, xs, w, jn);
+        } else {
+            if (wa) big_steps<PA, PA, false>(acc, xs, w, jn);
+            else big_steps<PB, PA, false>(acc, xs, w, jn);
+        }
+    }
+    cp_async_wait<0>();
+
+    // lane's token 2i (.x) and 2i+1 (.y) of its group; experts 4tx+b (b < 4),
+    // 64+4tx+b-4
+    const int np = wa ? PA : PB;
+    const int64_t tg = t0 + (g < 8 ? 2 * PA * g : 16 * PA + 2 * PB * (g - 8));
+#pragma unroll
+    for (int i = 0; i < PA; ++i) {
+        if (i >= np) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t t = tg + 2 * i + h;
+            if (t >= T) continue;
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+                const int e = e0 + 64 * gg + 4 * tx;
+                if (e >= E) continue;
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 a = acc[i][4 * gg + u];
+                    v[u] = h ? a.y : a.x;
+                    if (bias != nullptr) v[u] = __fadd_rn(v[u], __ldg(bias + e + u));
+                }
+                *reinterpret_cast<float4 *>(L + t * E + e) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- select --
 
 constexpr int kSelThreads = 256;
@@ -558,11 +752,72 @@ cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *b
                     Wr, bias, T, d, E, L);
 }
 
+template <int PA, int PB>
+cudaError_t launch_big(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T, int d,
+                       int E, float *L, cudaStream_t s) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(logits_big_kernel<PA, PB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    constexpr int kTok = 16 * (PA + PB);
+    const dim3 grid((unsigned)((T + kTok - 1) / kTok), (unsigned)((E + kBE - 1) / kBE));
+    return launch_k(logits_big_kernel<PA, PB>, grid, dim3(kBThreads), (size_t)kBSmem, s, X, Wr,
+                    bias, T, d, E, L);
+}
+
+int sm_count() {
+    static int count[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (count[dev] == 0 &&
+        cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        count[dev] = 148;
+    return count[dev];
+}
+
+// Token pairs per scheduler (P = PA + PB) of the one-block-per-SM kernel (0: use
+// the 4 x 8 tile). Every block runs the same d steps of 8P packed FMAs per
+// scheduler lane, so the time is about (waves of blocks) x P; the smallest such cost wins, the larger P on a
+// tie. MOE_ROUTER_PAIRS=4..8 forces P and MOE_ROUTER_PAIRS=0 the 4 x 8 tile
+// (tests and measurements use it to run each variant).
+int big_tile_pairs(int T, int E) {
+    if (const char *env = getenv("MOE_ROUTER_PAIRS"); env != nullptr && *env != 0) {
+        const int p = atoi(env);
+        if (p == 0 || (p >= 4 && p <= 8)) return p;
+    }
+    if (E < kBE || (int64_t)T * E < (int64_t)1 << 20) return 0;
+    const int64_t sms = sm_count(), eb = (E + kBE - 1) / kBE;
+    int best = 0;
+    int64_t best_cost = 0;
+    for (int P = 8; P >= 4; --P) {
+        const int64_t blocks = (T + 16 * P - 1) / (16 * P) * eb;
+        const int64_t cost = (blocks + sms - 1) / sms * P;
+        if (best == 0 || cost < best_cost) best = P, best_cost = cost;
+    }
+    return best;
+}
+
 }  // namespace
 
 cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const float *bias,
                                  int T, int d, int E, float *L, cudaStream_t s) {
     const bool wr16 = (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
+    if (E > 32 && E % 4 == 0 && wr16) {
+        switch (big_tile_pairs(T, E)) {
+            case 4: return launch_big<2, 2>(X, Wr, bias, T, d, E, L, s);
+            case 5: return launch_big<3, 2>(X, Wr, bias, T, d, E, L, s);
+            case 6: return launch_big<3, 3>(X, Wr, bias, T, d, E, L, s);
+            case 7: return launch_big<4, 3>(X, Wr, bias, T, d, E, L, s);
+            case 8: return launch_big<4, 4>(X, Wr, bias, T, d, E, L, s);
+            default: break;
+        }
+    }
     if (E <= 32 && E % 4 == 0 && wr16) {
         if (E <= 8) return launch_chain<8>(X, Wr, bias, T, d, E, L, s);
         if (E <= 16) return launch_chain<16>(X, Wr, bias, T, d, E, L, s);
