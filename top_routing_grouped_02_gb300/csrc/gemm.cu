@@ -33,8 +33,10 @@
 //               tile 128x64 (K-major) unless the A rows are gathered.
 //   warps 2-3   single-CTA gate/up only: gather the A tile's 128 token rows
 //               straight from X (cp.async into the same 128-byte-swizzled K-major
-//               layout), so no gathered copy of X goes through HBM. (CTA pairs
-//               load A by TMA from rows gathered beforehand: measured faster.)
+//               layout), so no gathered copy of X goes through HBM. The token
+//               indices of the next unit are loaded while the current unit is
+//               copied, so no unit boundary waits on them. (CTA pairs load A by
+//               TMA from rows gathered beforehand: measured faster.)
 //   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma (M128 N256 K16)
 //               per stage into the current TMEM accumulator, commits the stage
 //               back to the producer and, after the last stage, the
@@ -415,20 +417,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         };
         uint32_t it = 0;
         bool ok = true;
-        for (int u = first_unit; u < total_units && ok; u += unit_stride) {
+        // token indices of a unit's rows, loaded one unit ahead so that their
+        // latency hides behind the current unit's copies (-2: past the rows)
+        auto load_tok = [&](int uu, int (&raw)[16]) {
             int e, nb, row0, rows;
-            decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, per_tile, rank, e, nb, row0, rows);
-            int tok[16];
+            decode_unit(uu, NB, E, ctl->tile_base, ctl->offsets, per_tile, rank, e, nb, row0, rows);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = gw * 4 + rr + 8 * i;
+                raw[i] = r < rows ? __ldg(args.perm_token + row0 + r) : -2;
+            }
+        };
+        int nxt[16];
+        if (first_unit < total_units) load_tok(first_unit, nxt);
+        for (int u = first_unit; u < total_units && ok; u += unit_stride) {
+            int tok[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = nxt[i];
                 tok[i] = -1;
-                if (r < rows) {
-                    const int t = __ldg(args.perm_token + row0 + r);
+                if (t != -2) {
                     if (t >= 0 && t < args.T) tok[i] = t;
                     else atomicOr(args.err, MOE_DEVERR_BAD_EXPERT);
                 }
             }
+            if (u + unit_stride < total_units) load_tok(u + unit_stride, nxt);
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, args.err)) {
