@@ -5,8 +5,9 @@
 // §4.1 (subtract the maximum first), §4.2 (per-expert counts with atomics,
 // bucketed per block); "混合专家模型(MoE)架构优化与SonicMoE实践" §1 (E scores per
 // token, keep the best K), §3.2 (renormalise the kept scores); "Triton GPU 内核编程
-// 实战：用 Python 写高性能 AI 推理算子" §5.2 (online softmax recurrence
-// m_new = max(m_old, s), l_new = e^(m_old - m_new) l_old + e^(s - m_new)).
+// 实战：用 Python 写高性能 AI 推理算子" §5.2 (softmax statistics: the maximum
+// and the sum of exp(s - max); here the maximum is the top-1 score, so one pass
+// over the scores suffices).
 //
 // Two kernels:
 //  1. logits: L[t,e] = fp32 fused multiply-add chain over j = 0..d-1 in ascending
@@ -21,12 +22,14 @@
 //         micro-tiles fed by conflict-free float4 shared-memory reads.
 //       - E >= 128 with many tokens: one block per SM, each lane 2P tokens x 8
 //         experts, x read as bf16 pairs, so the FP32 FMA pipe is the limit.
-//  2. select: one warp per token reads its E logits, merges (max, sum of exp)
-//     across lanes with the online recurrence, picks K by repeated warp argmax
-//     (ties -> lower index), writes indices and weights, and counts per expert in
-//     a block histogram flushed with one atomic per (block, expert). For small E
-//     and T a single block with one thread per token does the same and writes
-//     the counts directly, so no memset is needed.
+//  2. select: one warp per token reads its E logits, picks K by repeated warp
+//     argmax over order-preserving keys (ties -> lower index), writes indices
+//     and weights, and counts per expert in a block histogram flushed with one
+//     atomic per (block, expert). The softmax needs no separate maximum pass: the
+//     maximum is the first kept score, so the renormalised weights come from the
+//     K kept scores alone and the full denominator from one sum of exp(L - max).
+//     For small E and T a single block with one thread per token does the same
+//     and writes the counts directly, so no memset is needed.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdlib.h>
@@ -541,12 +544,24 @@ logits_big_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__
 
 constexpr int kSelThreads = 256;
 
-__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
-    // higher score wins; equal scores: lower expert index wins
-    return v1 > v2 || (v1 == v2 && i1 < i2);
+// Scores as unsigned keys in the same order as the floats: larger score, larger
+// key. -0.0 is first made +0.0 (adding +0.0 does that and changes nothing else),
+// so the two zeros stay equal scores. Finite scores map above 0, which marks an
+// expert that is taken or does not exist.
+__device__ __forceinline__ uint32_t score_key(float v) {
+    const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// One warp per token: lane l holds experts l, l+32, ... (NPL per lane).
+// One warp per token: lane l holds experts l, l+32, ... (NPL per lane). Each of
+// the K rounds takes the warp maximum of the lanes' best untaken keys and then
+// the lowest expert index among the lanes that hold it (two warp reductions),
+// so ties go to the lower index. The weights need only the kept scores and
+// the maximum, which is the first kept score: exp(L_k - L_max) over their sum
+// (renormalised) or over the sum of exp(L_e - L_max) over every expert.
 template <int NPL>
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
@@ -561,66 +576,38 @@ select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
     const int64_t t = (int64_t)blockIdx.x * (kSelThreads / 32) + warp;
     if (t < T) {
         float v[NPL];
+        uint32_t key[NPL];
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             const int e = lane + 32 * i;
-            v[i] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
+            v[i] = (e < E) ? __ldg(logits + t * E + e) : 0.f;
+            key[i] = (e < E) ? score_key(v[i]) : 0u;
         }
-        // online softmax statistics (max, sum of exp) per lane, merged over the warp
-        float m = -INFINITY, s = 0.f;
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-            if (lane + 32 * i < E) {
-                const float mn = fmaxf(m, v[i]);
-                s = s * expf(m - mn) + expf(v[i] - mn);
-                m = mn;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-            const float so = __shfl_xor_sync(0xffffffffu, s, off);
-            const float mn = fmaxf(m, mo);
-            const float a = (m == -INFINITY) ? 0.f : s * expf(m - mn);
-            const float b = (mo == -INFINITY) ? 0.f : so * expf(mo - mn);
-            s = a + b;
-            m = mn;
-        }
-        bool taken[NPL];
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) taken[i] = (lane + 32 * i) >= E;
         int sel_idx[kMaxK];
         float sel_val[kMaxK];
 #pragma unroll
         for (int k = 0; k < kMaxK; ++k) {
             if (k < K) {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
-#pragma unroll
-                for (int i = 0; i < NPL; ++i) {
-                    const int e = lane + 32 * i;
-                    if (!taken[i] && better(v[i], e, bv, bi)) {
-                        bv = v[i];
-                        bi = e;
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    if (better(ov, oi, bv, bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
+                // lane's best untaken key; within a lane the indices ascend, so
+                // the strict comparison keeps the lower index on equal keys
+                uint32_t bk = 0u;
+                int bi = -1;
 #pragma unroll
                 for (int i = 0; i < NPL; ++i)
-                    if (lane + 32 * i == bi) taken[i] = true;
-                sel_idx[k] = bi;
-                sel_val[k] = bv;
+                    if (key[i] > bk) {
+                        bk = key[i];
+                        bi = lane + 32 * i;
+                    }
+                const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+                const uint32_t win = __reduce_min_sync(
+                    0xffffffffu, (bk == kmax && bi >= 0) ? (uint32_t)bi : 0xffffffffu);
+#pragma unroll
+                for (int i = 0; i < NPL; ++i)
+                    if ((uint32_t)(lane + 32 * i) == win) key[i] = 0u;
+                sel_idx[k] = (int)win;
+                sel_val[k] = key_score(kmax);
             }
         }
-        // weights: exp(L_k - max) over the kept sum (renormalised) or the full sum
         const float mtop = sel_val[0];
         float kept = 0.f, ex[kMaxK];
 #pragma unroll
@@ -630,7 +617,16 @@ select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
                 kept += ex[k];
             }
         }
-        const float denom = renorm ? kept : s * expf(m - mtop);
+        float denom = kept;
+        if (!renorm) {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (lane + 32 * i < E) s += expf(v[i] - mtop);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            denom = s;
+        }
 #pragma unroll
         for (int k = 0; k < kMaxK; ++k) {
             if (k < K && lane == k) {
@@ -716,15 +712,23 @@ select_single_kernel(const float *__restrict__ logits, int T, int E, int K, int 
     for (int e = threadIdx.x; e < E; e += kSelSingleThreads) counts[e] = hist[e];
 }
 
+// The single-block select writes the counts itself; the multi-block one adds
+// into counts that must be zero first.
+bool select_needs_zero_counts(int T, int E) { return !(E <= 16 && T <= kSelSingleMaxT); }
+
+// counts_zeroed: the caller has already set counts to zero on this stream (so
+// that no memset sits between the logits and select kernels).
 cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, int32_t *idx,
-                          float *w, int32_t *counts, cudaStream_t s) {
-    if (E <= 16 && T <= kSelSingleMaxT) {
+                          float *w, int32_t *counts, bool counts_zeroed, cudaStream_t s) {
+    if (!select_needs_zero_counts(T, E)) {
         auto kern = E <= 8 ? select_single_kernel<8> : select_single_kernel<16>;
         return launch_k(kern, dim3(1), dim3(kSelSingleThreads), 0, s, logits, T, E, K, renorm, idx,
                         w, counts);
     }
-    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
-    if (e != cudaSuccess) return e;
+    if (!counts_zeroed) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+        if (e != cudaSuccess) return e;
+    }
     const unsigned blocks = (unsigned)((T + kSelThreads / 32 - 1) / (kSelThreads / 32));
     auto kern = E <= 32    ? select_kernel<1>
                 : E <= 64  ? select_kernel<2>
@@ -838,14 +842,19 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
                          int d, int E, int K, int renorm, float *logits, int32_t *idx, float *w,
                          int32_t *counts, cudaStream_t s) {
+    const bool zero = select_needs_zero_counts(T, E);
+    if (zero) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+        if (e != cudaSuccess) return e;
+    }
     cudaError_t e = launch_router_logits(X, Wr, bias, T, d, E, logits, s);
     if (e != cudaSuccess) return e;
-    return launch_select(logits, T, E, K, renorm, idx, w, counts, s);
+    return launch_select(logits, T, E, K, renorm, idx, w, counts, zero, s);
 }
 
 cudaError_t launch_route_logits(const float *logits, int T, int E, int K, int renorm,
                                 int32_t *idx, float *w, int32_t *counts, cudaStream_t s) {
-    return launch_select(logits, T, E, K, renorm, idx, w, counts, s);
+    return launch_select(logits, T, E, K, renorm, idx, w, counts, false, s);
 }
 
 }  // namespace moe
