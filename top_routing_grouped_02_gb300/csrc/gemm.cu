@@ -19,6 +19,10 @@
 // Units are ordered expert-major, then column block, then row tile, and CTA b
 // takes units b, b + gridDim.x, ...: CTAs running at the same time share one
 // expert's weight block through L2 while its few activation tiles stay hot.
+// Experts with at most two tiles (one pair) read a weight block per one or two
+// units, faster than HBM delivers at tensor-core pace; their units are spread
+// evenly through the sequence of the others, so each wave of CTAs mixes
+// weight-streaming units with compute-bound ones.
 //
 // Two variants share the code. Single CTA: M=128 tiles, B tile 64x256 per stage
 // (48 KB stages, 4 deep). CTA pair (a cluster of 2 CTAs on one SM pair,
@@ -117,9 +121,9 @@ struct Ctl {
     uint64_t tempty[2];
     uint64_t drain;
     uint32_t tmem_base;
-    int32_t tile_base[kMaxE + 1];
+    int32_t tile_base[2][kMaxE + 1];  // work-tile bases: [0] heavy experts, [1] light
     int32_t offsets[kMaxE + 1];
-    int32_t scan[kMaxThreads / 32 + 1];
+    uint64_t scan[kMaxThreads / 32 + 1];
 };
 
 // Epilogue staging: 32-row x 32-column bf16 buffers (64-byte rows, 64-byte
@@ -164,13 +168,44 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint
     }
 }
 
-// Unit u -> (expert, column block, first row, rows). tile_base[e] counts the
-// work tiles of experts before e (128-row tiles, or pairs of them for a CTA
-// pair, whose CTA `rank` takes the pair's tile 2*pt + rank); empty experts own
-// no units. `rows` can be <= 0 for the second tile of an odd pair.
-__device__ __forceinline__ void decode_unit(int u, int NB, int E, const int32_t *tb,
+// Experts with few work tiles share each weight block among few units, so their
+// units need more weight bytes per FLOP than HBM delivers at tensor-core pace;
+// experts with many tiles are compute-bound. Position p of the unit sequence
+// therefore interleaves two streams: the light experts' units sit at evenly
+// spread positions (a Bresenham split of the N positions, L of them light) and
+// the heavy experts' units fill the rest, so every wave of CTAs mixes both.
+// With no light expert the sequence is the heavy stream itself.
+// An expert is light when it has at most light_tiles<PAIR>() work tiles (two
+// 128-row tiles, or one tile pair).
+template <bool PAIR>
+constexpr int light_tiles() { return PAIR ? 1 : 2; }
+
+// Position p -> (expert, column block, first row, rows). Within a stream,
+// tile_base[st][e] counts the work tiles of that stream's experts before e
+// (128-row tiles, or pairs of them for a CTA pair, whose CTA `rank` takes the
+// pair's tile 2*pt + rank); units run expert-major, then column block, then row
+// tile, and experts outside the stream own no units in it. `rows` can be <= 0
+// for the second tile of an odd pair.
+__device__ __forceinline__ void decode_unit(int p, int NB, int E, const int32_t (*tbs)[kMaxE + 1],
                                             const int32_t *off, int per_tile, int rank, int &e,
                                             int &nb, int &row0, int &rows) {
+    const uint64_t L = (uint64_t)tbs[1][E] * NB;
+    int st = 0, u = p;
+    if (L != 0) {
+        const uint64_t N = (uint64_t)tbs[0][E] * NB + L;
+        const uint64_t pl = (uint64_t)p * L;
+        uint64_t a, a1;  // light positions before p and before p + 1
+        if (N * L <= 0xffffffffull) {
+            a = (uint32_t)pl / (uint32_t)N;
+            a1 = (uint32_t)(pl + L) / (uint32_t)N;
+        } else {
+            a = pl / N;
+            a1 = (pl + L) / N;
+        }
+        st = a1 != a ? 1 : 0;
+        u = st ? (int)a : p - (int)a;
+    }
+    const int32_t *tb = tbs[st];
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -268,28 +303,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (tid == 0) atomicOr(args.err, MOE_DEVERR_BAD_EXPERT);
             c = 0;
         }
-        int incl = c;
+        // both streams in one scan: heavy tiles in the low 32 bits, light in the
+        // high 32 (the sums stay below 2^31, so the halves never carry)
+        const bool light = c <= light_tiles<PAIR>();
+        const uint64_t cs = light ? (uint64_t)c << 32 : (uint64_t)c;
+        uint64_t incl = cs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            const uint64_t v = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += v;
         }
         if (lane == 31) ctl->scan[warp] = incl;
         __syncthreads();
         if (warp == 0) {
-            const int ws = lane < kThreads / 32 ? ctl->scan[lane] : 0;
-            int wi = ws;
+            const uint64_t ws = lane < kThreads / 32 ? ctl->scan[lane] : 0ull;
+            uint64_t wi = ws;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, wi, o);
+                const uint64_t v = __shfl_up_sync(0xffffffffu, wi, o);
                 if (lane >= o) wi += v;
             }
             if (lane < kThreads / 32) ctl->scan[lane] = wi - ws;
             if (lane == kThreads / 32 - 1) ctl->scan[kThreads / 32] = wi;
         }
         __syncthreads();
-        if (e < E) ctl->tile_base[e] = ctl->scan[warp] + incl - c;
-        if (e == 0) ctl->tile_base[E] = ctl->scan[kThreads / 32];
+        if (e < E) {
+            const uint64_t ex = ctl->scan[warp] + incl - cs;
+            ctl->tile_base[0][e] = (int32_t)(uint32_t)ex;
+            ctl->tile_base[1][e] = (int32_t)(ex >> 32);
+        }
+        if (e == 0) {
+            const uint64_t tot = ctl->scan[kThreads / 32];
+            ctl->tile_base[0][E] = (int32_t)(uint32_t)tot;
+            ctl->tile_base[1][E] = (int32_t)(tot >> 32);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -297,7 +344,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const int NB = args.NB;
-    const int total_units = ctl->tile_base[E] * NB;
+    const int total_units = (ctl->tile_base[0][E] + ctl->tile_base[1][E]) * NB;
     const int KB = args.Kdim / BK;
     const int per_tile = PAIR ? 2 : 1;
 
