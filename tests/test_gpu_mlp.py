@@ -28,6 +28,10 @@ MLP_CASES = [
     (1, 256, 4, 1, 128, False),     # one token
     (700, 256, 1, 1, 256, False),   # K = E = 1: one dense SwiGLU MLP
     (1024, 768, 8, 2, 256, False),  # rows per expert around exact tile multiples
+    # Zipf-skewed loads: experts with at most two tiles (one pair) and experts with
+    # more, so the GEMM's unit order interleaves both streams
+    (2000, 256, 8, 1, 256, True),   # 6 light and 2 heavy experts
+    (3000, 256, 32, 4, 128, True),  # 22 light and 10 heavy experts
 ]
 
 
