@@ -7,15 +7,19 @@ Mixtral-shaped layer (T=4096, d=4096, E=8, K=2, n=14336, bf16, fp32 accumulate).
 
 Prints ONE JSON line on rank 0:
   value       useful TFLOP/s (2*T*K*3*d*n per step) of all ranks together, device
-              timed with CUDA events, inputs resident in HBM
+              timed with CUDA events around K forwards exactly as a user calls them
+              (no events inside a step), inputs resident in HBM
   e2e         same metric from pinned host memory, host<->device copies of every
               step inside the timed region (moe_forward_host_stream: the copies of
               neighbouring batches overlap the layer)
-  roofline    the dominant kernel (gate/up GEMM) against the measured bf16 peak
+  roofline    the dominant kernel (gate/up GEMM) against the measured bf16 peak; its
+              duration comes from a second region of K forwards right after the
+              timed one, with an event between every two stages
+  gpu_launches  kernels per step (8, or 9 with the CTA-pair row gather) x K
   cpu_baseline  the CPU oracle on a bounded token sample (rank 0, N=1 only)
   clocks      nvidia-smi SM clocks / throttle reasons sampled during the timed region
-  extra       tokens/s, per-kernel times, router and combine GB/s, % of peak, routing
-              statistics (tile padding, rows per expert)
+  extra       tokens/s, per-stage times (from the second region), router and combine
+              GB/s, % of peak, routing statistics (tile padding, rows per expert)
 
 --routing rounded runs the layer under Token Rounding (moe_forward_rounded: each
 expert's top-K count rounded to a multiple of the 128-row tile); its value
@@ -46,6 +50,16 @@ KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
 # Token Rounding (--routing rounded): the grouping step is the rounding step
 STAGES_ROUNDED = ["route", "round", "gemm_gate_up", "gemm_down", "combine"]
 KERNELS_PER_STEP_ROUNDED = 2 + 3 + 1 + 1 + 1
+
+
+def kernels_per_step(rounded, R, E):
+    """Kernels one forward launches: the fixed ones, plus the row gather that the
+    gate/up GEMM runs first on CTA pairs (the library picks pairs when the
+    experts average at least 8 row tiles, R >= 8*128*E, unless MOE_GEMM_CTA_PAIR
+    forces a variant)."""
+    env = os.environ.get("MOE_GEMM_CTA_PAIR", "")
+    pair = env == "1" if env in ("0", "1") else R >= 8 * 128 * E
+    return (KERNELS_PER_STEP_ROUNDED if rounded else KERNELS_PER_STEP) + (1 if pair else 0)
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
 # the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
@@ -270,23 +284,16 @@ def run_gpu(args, c, world, rank, local):
     # rounded total (the same in every step: the inputs do not change)
     R = int((row_map >= 0).sum().item()) if rounded else T * K
 
-    # timed region: K steps, events between the stages of every step
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
-           for _ in range(args.steps)]
-    for row in evs:
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    # Direct calls by default. --graph captures the K steps (their stage events
-    # included, as external event nodes) once as a CUDA graph and replays it; the
-    # event nodes between stages cost about what the graph saves in launch gaps.
+    # Timed region: K forwards as a user runs them (no events inside a step, so
+    # every kernel boundary keeps its programmatic dependent launch). Direct calls
+    # by default; --graph captures the K steps once as a CUDA graph and replays it.
     graph, launch = None, "direct calls"
     if args.graph:
         try:
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 for i in range(args.steps):
-                    step(evs[i])
+                    step()
             torch.cuda.synchronize()
             launch = "one CUDA graph of the K steps"
         except RuntimeError as exc:  # capture unsupported here: time direct calls
@@ -302,7 +309,7 @@ def run_gpu(args, c, world, rank, local):
                 graph.replay()
         else:
             for i in range(args.steps):
-                step(evs[i])
+                step()
         stop.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -311,6 +318,19 @@ def run_gpu(args, c, world, rank, local):
         raise RuntimeError(f"device error word {word:#x} in the timed region")
     ms_total = start.elapsed_time(stop)
     ms_max = max_over_ranks(ms_total, world)
+
+    # Stage region right after it: the same K forwards with an event between
+    # every two stages (the traced forward records them on the launch stream),
+    # for the per-kernel times and the roofline of the dominant kernel.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    st, word = moe.moe_sync_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} in the stage region")
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
                                   for i in range(args.steps)])) for j, s in enumerate(stages)}
     ms_step = ms_max / args.steps
@@ -403,7 +423,7 @@ def run_gpu(args, c, world, rank, local):
                      "traffic": None if rounded else (GEMM1_TRAFFIC_BYTES or {}).get(args.workload),
                      "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
                      "algorithmic_flops_per_launch": g1_flops},
-        "gpu_launches": (KERNELS_PER_STEP_ROUNDED if rounded else KERNELS_PER_STEP) * args.steps,
+        "gpu_launches": kernels_per_step(rounded, R, E) * args.steps,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "extra": {
             "tokens_per_s": round(T * world / (ms_step / 1e3), 1),
