@@ -71,25 +71,41 @@ uint16_t oracle_bf16_from_double(double v) {
 
 /* ------------------------------------------------------------- router -- */
 
-/* Logits of one token row: for each expert e, acc = +0.0f, then for
- * j = 0..d-1 in order acc = fmaf(x_j, Wr[j,e], acc); then acc + bias[e]. */
+/* Logits of one token row. The sum over j runs in blocks of LOGIT_BLOCK
+ * reduction steps: for block b and expert e, s = +0.0f, then for j in the block
+ * in ascending order s = fmaf(x_j, Wr[j,e], s). The block sums are then added in
+ * ascending block order (acc = s_0, then acc = acc + s_b for b = 1, 2, ...),
+ * and finally acc + bias[e]. With d <= LOGIT_BLOCK this is the single fused
+ * multiply-add chain over j = 0..d-1. */
+#define LOGIT_BLOCK 1024
 static void logits_row(const uint16_t *x, const float *Wr, const float *bias,
-                       int d, int E, float *acc) {
-    for (int e = 0; e < E; ++e) acc[e] = 0.0f;
-    for (int j = 0; j < d; ++j) {
-        float xj = bf16_to_float(x[j]);
-        const float *w = Wr + (int64_t)j * E;
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(xj, w[e], acc[e]);
+                       int d, int E, float *acc, float *blk) {
+    for (int j0 = 0; j0 < d; j0 += LOGIT_BLOCK) {
+        const int j1 = j0 + LOGIT_BLOCK < d ? j0 + LOGIT_BLOCK : d;
+        for (int e = 0; e < E; ++e) blk[e] = 0.0f;
+        for (int j = j0; j < j1; ++j) {
+            float xj = bf16_to_float(x[j]);
+            const float *w = Wr + (int64_t)j * E;
+            for (int e = 0; e < E; ++e) blk[e] = fmaf(xj, w[e], blk[e]);
+        }
+        for (int e = 0; e < E; ++e) acc[e] = j0 == 0 ? blk[e] : acc[e] + blk[e];
     }
+    if (d == 0)
+        for (int e = 0; e < E; ++e) acc[e] = 0.0f;
     if (bias)
         for (int e = 0; e < E; ++e) acc[e] = acc[e] + bias[e];
 }
 
 void oracle_router_logits(const uint16_t *X, const float *Wr, const float *bias,
                           int64_t T, int d, int E, float *L) {
-#pragma omp parallel for schedule(static)
-    for (int64_t t = 0; t < T; ++t)
-        logits_row(X + t * d, Wr, bias, d, E, L + t * E);
+#pragma omp parallel
+    {
+        float *blk = (float *)malloc(sizeof(float) * (size_t)(E > 0 ? E : 1));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t)
+            logits_row(X + t * d, Wr, bias, d, E, L + t * E, blk);
+        free(blk);
+    }
 }
 
 typedef struct {
@@ -291,6 +307,7 @@ void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias
 #pragma omp parallel
     {
         float *L = (float *)malloc(sizeof(float) * (size_t)E);
+        float *blk = (float *)malloc(sizeof(float) * (size_t)E);
         double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
         double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
         uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n);
@@ -302,7 +319,7 @@ void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias
             const uint16_t *x = X + t * d;
             int32_t *idx = idx_rows + i * K;
             float *w = w_rows + i * K;
-            logits_row(x, Wr, bias, d, E, L);
+            logits_row(x, Wr, bias, d, E, L, blk);
             route_row(L, E, K, renorm, idx, w);
             for (int c = 0; c < d; ++c) y[c] = 0.0;
             for (int k = 0; k < K; ++k) {
@@ -314,6 +331,7 @@ void oracle_forward_tokens(const uint16_t *X, const float *Wr, const float *bias
             for (int c = 0; c < d; ++c) Y_rows[i * d + c] = oracle_bf16_from_double(y[c]);
         }
         free(L);
+        free(blk);
         free(a1);
         free(a3);
         free(h);

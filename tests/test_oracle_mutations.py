@@ -1,7 +1,7 @@
 """Planted mistakes in a copy of the oracle must each fail a pin (CPU only).
 
-Every mutation below is a plausible slip in the oracle's C source: a reordered or
-unfused logit chain, the wrong tie-break, a dropped renormalisation, a sign error
+Every mutation below is a plausible slip in the oracle's C source: a reordered,
+unfused or unblocked logit chain, the wrong tie-break, a dropped renormalisation, a sign error
 in SiLU, swapped gate/up branches, a dropped routing weight, truncating instead
 of rounding, a transposed weight, an unstable grouping, and in Token Rounding a
 wrong rounding rule, a wrong order in the second sort or a dropped
@@ -19,9 +19,11 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTATIONS = [
-    ("unfused_logits", "acc[e] = fmaf(xj, w[e], acc[e]);", "acc[e] = acc[e] + xj * w[e];"),
-    ("descending_j", "for (int j = 0; j < d; ++j) {\n        float xj",
-     "for (int j = d - 1; j >= 0; --j) {\n        float xj"),
+    ("unfused_logits", "blk[e] = fmaf(xj, w[e], blk[e]);", "blk[e] = blk[e] + xj * w[e];"),
+    ("descending_j", "for (int j = j0; j < j1; ++j) {\n            float xj",
+     "for (int j = j1 - 1; j >= j0; --j) {\n            float xj"),
+    ("logits_unblocked", "#define LOGIT_BLOCK 1024", "#define LOGIT_BLOCK (1 << 30)"),
+    ("logit_blocks_not_restarted", "for (int e = 0; e < E; ++e) blk[e] = 0.0f;", ""),
     ("ties_to_high_index", "return (a->e > b->e) - (a->e < b->e);",
      "return (a->e < b->e) - (a->e > b->e);"),
     ("no_renorm", "renorm ? p / kept : p", "p"),

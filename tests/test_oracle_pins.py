@@ -86,9 +86,18 @@ def _read_logit_cases():
         if not line or line.startswith("#"):
             continue
         xs, ws, b, exp = [p.strip() for p in line.split("|")]
-        cases.append(([float.fromhex(v) for v in xs.split()], [float.fromhex(v) for v in ws.split()],
-                      None if b == "-" else float.fromhex(b), float.fromhex(exp)))
+        cases.append((_hex_list(xs), _hex_list(ws), None if b == "-" else float.fromhex(b),
+                       float.fromhex(exp)))
     return cases
+
+
+def _hex_list(text):
+    # hex floats; "a*n" stands for n copies of a
+    out = []
+    for tok in text.split():
+        v, _, n = tok.partition("*")
+        out.extend([float.fromhex(v)] * (int(n) if n else 1))
+    return out
 
 
 @pytest.mark.parametrize("case", _read_logit_cases())
