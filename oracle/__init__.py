@@ -105,9 +105,9 @@ def bf16_to_double(b: int) -> float:
 
 
 def router_logits(X: np.ndarray, Wr: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
-    """L[T,E] fp32: an fma chain over each 1024-step block of j (ascending, from
-    +0.0f), the block sums added in ascending block order, + bias. X uint16 (bf16)
-    [T,d]."""
+    """L[T,E] fp32: an fma chain over j ascending from +0.0f (with E <= 32, one
+    chain per 1024-step block of j, the block sums added in ascending block
+    order), + bias. X uint16 (bf16) [T,d]."""
     X = _c(X, np.uint16)
     Wr = _c(Wr, np.float32)
     T, d = X.shape

@@ -71,17 +71,20 @@ uint16_t oracle_bf16_from_double(double v) {
 
 /* ------------------------------------------------------------- router -- */
 
-/* Logits of one token row. The sum over j runs in blocks of LOGIT_BLOCK
- * reduction steps: for block b and expert e, s = +0.0f, then for j in the block
- * in ascending order s = fmaf(x_j, Wr[j,e], s). The block sums are then added in
+/* Logits of one token row. With E <= LOGIT_FEW_EXPERTS the sum over j runs in
+ * blocks of LOGIT_BLOCK reduction steps; with more experts the whole of j is
+ * one block. For block b and expert e, s = +0.0f, then for j in the block in
+ * ascending order s = fmaf(x_j, Wr[j,e], s). The block sums are then added in
  * ascending block order (acc = s_0, then acc = acc + s_b for b = 1, 2, ...),
- * and finally acc + bias[e]. With d <= LOGIT_BLOCK this is the single fused
+ * and finally acc + bias[e]. With one block this is the single fused
  * multiply-add chain over j = 0..d-1. */
 #define LOGIT_BLOCK 1024
+#define LOGIT_FEW_EXPERTS 32
 static void logits_row(const uint16_t *x, const float *Wr, const float *bias,
                        int d, int E, float *acc, float *blk) {
-    for (int j0 = 0; j0 < d; j0 += LOGIT_BLOCK) {
-        const int j1 = j0 + LOGIT_BLOCK < d ? j0 + LOGIT_BLOCK : d;
+    const int len = E <= LOGIT_FEW_EXPERTS ? LOGIT_BLOCK : d;
+    for (int j0 = 0; j0 < d; j0 += len) {
+        const int j1 = j0 + len < d ? j0 + len : d;
         for (int e = 0; e < E; ++e) blk[e] = 0.0f;
         for (int j = j0; j < j1; ++j) {
             float xj = bf16_to_float(x[j]);

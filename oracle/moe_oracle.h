@@ -27,9 +27,9 @@
  *
  * Readings where the pages are silent (each is stated where it is used):
  *   - router logits are fp32: per (token, expert), one fused multiply-add chain
- *     over each block of 1024 consecutive j (ascending, from +0.0f), the block
- *     sums added in ascending block order, then + bias[e] as a single fp32 add
- *     (with d <= 1024, one chain over j = 0..d-1);
+ *     over j = 0..d-1 ascending from +0.0f when E > 32; with E <= 32 one such
+ *     chain over each block of 1024 consecutive j, the block sums added in
+ *     ascending block order; then + bias[e] as a single fp32 add;
  *   - top-K is chosen on the logits (softmax is strictly increasing, so the same
  *     set), ties go to the lower expert index, output in descending order;
  *   - probabilities and weights are computed in double, rounded once to fp32;
@@ -53,8 +53,9 @@ uint16_t oracle_bf16_from_double(double v);
 /* Exact value of a bf16 bit pattern. */
 double oracle_bf16_to_double(uint16_t b);
 
-/* L[t,e] = fp32 fma chains over 1024-step blocks of j ascending of
- * X[t,j]*Wr[j,e], block sums added in ascending order, + bias[e]. */
+/* L[t,e] = fp32 fma chain over j ascending of X[t,j]*Wr[j,e] (with E <= 32,
+ * one chain per 1024-step block of j, block sums added in ascending order),
+ * + bias[e]. */
 void oracle_router_logits(const uint16_t *X, const float *Wr, const float *bias,
                           int64_t T, int d, int E, float *L);
 

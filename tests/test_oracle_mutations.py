@@ -23,6 +23,7 @@ MUTATIONS = [
     ("descending_j", "for (int j = j0; j < j1; ++j) {\n            float xj",
      "for (int j = j1 - 1; j >= j0; --j) {\n            float xj"),
     ("logits_unblocked", "#define LOGIT_BLOCK 1024", "#define LOGIT_BLOCK (1 << 30)"),
+    ("logits_blocked_for_every_E", "#define LOGIT_FEW_EXPERTS 32", "#define LOGIT_FEW_EXPERTS (1 << 30)"),
     ("logit_blocks_not_restarted", "for (int e = 0; e < E; ++e) blk[e] = 0.0f;", ""),
     ("ties_to_high_index", "return (a->e > b->e) - (a->e < b->e);",
      "return (a->e < b->e) - (a->e > b->e);"),

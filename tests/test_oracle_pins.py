@@ -111,6 +111,19 @@ def test_logits_golden_order_and_fusion(oracle_lib, case):
     assert L[0, 0] == np.float32(exp), (L[0, 0].hex() if hasattr(L[0, 0], "hex") else L[0, 0])
 
 
+def test_logits_blocks_only_with_few_experts(oracle_lib):
+    # the block case of the golden file (a 2^24 weight in block 0, two 1-weights
+    # in block 1, x = 1): blocks give 2^24 + 2, one chain over all j gives 2^24.
+    # With E <= 32 every column is blocked, with E = 33 none is.
+    d = 2048
+    w = np.zeros(d, np.float32)
+    w[0], w[1024], w[1025] = 2.0 ** 24, 1.0, 1.0
+    X = torch_bf16_bits_from_f32(np.ones((1, d), np.float32))
+    for E, expect in ((32, 2.0 ** 24 + 2), (33, 2.0 ** 24)):
+        L = oracle.router_logits(X, np.ascontiguousarray(np.repeat(w[:, None], E, axis=1)))
+        assert np.all(L == np.float32(expect)), (E, L[0, :3])
+
+
 def test_logits_exact_integer_dot(oracle_lib):
     # small integers: every partial sum is exact in fp32, so L equals the exact dot
     rng = np.random.default_rng(2)
