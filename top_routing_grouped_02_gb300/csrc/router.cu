@@ -10,14 +10,18 @@
 // over the scores suffices).
 //
 // Two kernels:
-//  1. logits: L[t,e] = fp32 fused multiply-add chain over j = 0..d-1 in ascending
-//     order from +0.0f, then one fp32 add of bias[e]. That order is the definition
-//     the results are pinned to, so L (and hence the top-K indices) is
-//     bit-identical to a sequential evaluation. The chain cannot be split over
-//     threads or tensor-core instructions without changing the rounding, so every
-//     chain stays in one thread and parallelism comes from tokens x experts:
-//       - E <= 32: two (token, expert) chains per thread fed from a cp.async
-//         shared-memory pipeline; bound by the latency of d dependent FMAs.
+//  1. logits: L[t,e] in fp32, then one fp32 add of bias[e]. With E > 32 the sum
+//     is one fused multiply-add chain over j = 0..d-1 in ascending order from
+//     +0.0f; with E <= 32 it runs in blocks of 1024 steps, one such chain per
+//     block, the block sums added in ascending block order (a few-expert router
+//     has too few (token, expert) chains to hide a d-long dependency). That
+//     order is the definition the results are pinned to, so L (and hence the
+//     top-K indices) is bit-identical to a sequential evaluation of it. A chain
+//     cannot be split over threads or tensor-core instructions without changing
+//     the rounding, so every chain stays in one thread:
+//       - E <= 32: two (token, expert) chains per thread, one thread group per
+//         block of the reduction, fed from cp.async shared-memory pipelines; the
+//         groups' block sums are added in order at the end.
 //       - E > 32: two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
 //         micro-tiles fed by conflict-free float4 shared-memory reads.
 //       - E >= 128 with many tokens: one block per SM, each lane 2P tokens x 8
@@ -49,32 +53,42 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ---- E <= 32: two (token, expert) chains per thread -------------------------
-// Block: 8 tokens x EP experts, one thread per (token, expert pair), so 4*EP
-// threads (EP/8 warps). Stages of kChainJC reduction steps: the block's 8 rows
-// of X (bf16) and kChainJC rows of Wr (fp32) are copied to shared memory with
-// cp.async, 4 stages deep; the X rows are widened once per stage to fp32. Per
-// 4 steps a thread reads one float4 of x (shared by the threads of its token)
-// and four float2 of weights for 8 fused multiply-adds on two independent
-// chains, so shared-memory traffic is a quarter of one-chain-per-thread's and
-// the kernel approaches the latency of the d-long chain itself.
-// Requires d % 8 == 0, E % 4 == 0 and a 16-byte-aligned Wr.
+// With E <= 32 the logits' reduction runs in blocks of kLogitBlock steps: one
+// fma chain per block, the block sums added in ascending block order (with
+// d <= kLogitBlock the single chain over j). The E <= 32 kernels' stage lengths
+// divide kLogitBlock.
+constexpr int kLogitBlock = 1024;
+
+// ---- E <= 32: two (token, expert) chains per thread, one group per block ----
+// A thread group covers 8 tokens x EP experts, one thread per (token, expert
+// pair), so 4*EP threads; a CTA holds NG groups, and group g runs the chains of
+// blocks g, g + NG, ... of the reduction, so the blocks of one logit run side by
+// side. Each group streams its block through its own ring of 64-step stages
+// (3 deep, cp.async): the 8 rows of X (bf16, widened once per stage to fp32)
+// and the rows of Wr. Per 4 steps a thread reads one float4 of x and four
+// float2 of weights for 8 fused multiply-adds on its two chains. At the end each
+// group's block sums go to shared memory and the first group adds them in
+// ascending block order. Requires d % 8 == 0, E % 4 == 0, a 16-byte-aligned Wr
+// and at most kChainMaxBlocks blocks.
 constexpr int kChainTok = 8;
-constexpr int kChainStages = 4;
-constexpr int kChainJC = 128;
+constexpr int kChainStages = 3;
+constexpr int kChainJC = 64;
+constexpr int kChainMaxBlocks = 16;
 
 template <int EP>
 struct ChainCfg {
-    static constexpr int THREADS = kChainTok * EP / 2;
+    static constexpr int THREADS = kChainTok * EP / 2;        // one group
     static constexpr int RXBYTES = kChainTok * kChainJC * 2;  // raw X rows (bf16)
     static constexpr int RWBYTES = kChainJC * EP * 4;         // raw Wr rows (EP floats each)
     static constexpr int RSTAGE = RXBYTES + RWBYTES;
     static constexpr int LD = kChainJC + 4;                   // widened x row (floats)
-    static constexpr int SMEM = kChainStages * RSTAGE + kChainTok * LD * 4;
+    static constexpr int GROUP_SMEM = kChainStages * RSTAGE + kChainTok * LD * 4;
+    static constexpr int MAXG = EP == 8 ? 8 : (EP == 16 ? 4 : 2);  // groups per CTA
+    static constexpr int MAX_SMEM = MAXG * GROUP_SMEM + kChainMaxBlocks * THREADS * 8;
 };
 
 template <int EP>
-__global__ void __launch_bounds__(ChainCfg<EP>::THREADS)
+__global__ void __launch_bounds__(ChainCfg<EP>::THREADS * ChainCfg<EP>::MAXG)
 logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
                     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
     pdl_wait();
@@ -82,85 +96,106 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
     using C = ChainCfg<EP>;
     constexpr int NTH = C::THREADS;
     extern __shared__ __align__(16) unsigned char sm[];
-    float *xf = reinterpret_cast<float *>(sm + kChainStages * C::RSTAGE);  // [8][LD]
-    const int tid = threadIdx.x;
+    const int NG = blockDim.x / NTH;
+    const int g = threadIdx.x / NTH, tid = threadIdx.x % NTH;
+    unsigned char *gsm = sm + g * C::GROUP_SMEM;
+    float *xf = reinterpret_cast<float *>(gsm + kChainStages * C::RSTAGE);  // [8][LD]
+    float2 *part = reinterpret_cast<float2 *>(sm + NG * C::GROUP_SMEM);     // [nb][NTH]
     const int h = tid % (EP / 2), tl = tid / (EP / 2);  // experts 2h, 2h+1 of token tl
     const int64_t t0 = (int64_t)blockIdx.x * kChainTok;
-    const int nst = (d + kChainJC - 1) / kChainJC;
-
-    auto issue = [&](int st) {
-        unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
-        unsigned char *ws = xs + C::RXBYTES;
-        const int j0 = st * kChainJC;
-        for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
-            const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
-            const int64_t t = t0 + r;
-            const int j = j0 + c * 8;
-            if (t < T && j < d) cp_async16(xs + r * (kChainJC * 2) + c * 16, X + t * d + j);
-        }
-        for (int q = tid; q < kChainJC * (EP / 4); q += NTH) {
-            const int jj = q / (EP / 4), c4 = (q % (EP / 4)) * 4;
-            const int j = j0 + jj;
-            if (j < d && c4 < E) cp_async16(ws + (jj * EP + c4) * 4, Wr + (int64_t)j * E + c4);
-        }
+    const int nb = (d + kLogitBlock - 1) / kLogitBlock;
+    auto group_sync = [&]() {
+        if constexpr (NTH == 32) __syncwarp();
+        else asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "r"(NTH) : "memory");
     };
-
-    for (int st = 0; st < kChainStages - 1; ++st) {
-        if (st < nst) issue(st);
-        cp_async_commit();
-    }
     const float4 *xrow = reinterpret_cast<const float4 *>(xf + tl * C::LD);
-    float acc0 = 0.f, acc1 = 0.f;
-    for (int st = 0; st < nst; ++st) {
-        cp_async_wait<kChainStages - 2>();
-        __syncthreads();  // raw stage st landed; the previous stage's compute is done
-        if (st + kChainStages - 1 < nst) issue(st + kChainStages - 1);
-        cp_async_commit();
-        const unsigned char *xs = sm + (st % kChainStages) * C::RSTAGE;
-        const float2 *w2 = reinterpret_cast<const float2 *>(xs + C::RXBYTES) + h;  // row stride EP/2
-        for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
-            const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
-            const uint4 raw = *reinterpret_cast<const uint4 *>(xs + r * (kChainJC * 2) + c * 16);
-            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-            float4 *dst = reinterpret_cast<float4 *>(xf + r * C::LD + c * 8);
-            const float2 a = __bfloat1622float2(h2[0]), b = __bfloat1622float2(h2[1]);
-            const float2 c2 = __bfloat1622float2(h2[2]), d2 = __bfloat1622float2(h2[3]);
-            dst[0] = make_float4(a.x, a.y, b.x, b.y);
-            dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
-        }
-        __syncthreads();
-        const int jn = min(kChainJC, d - st * kChainJC);  // a multiple of 8
-        auto step4 = [&](int v) {
-            const float4 xv = xrow[v];
-            const float2 wa = w2[(4 * v + 0) * (EP / 2)], wb = w2[(4 * v + 1) * (EP / 2)];
-            const float2 wc = w2[(4 * v + 2) * (EP / 2)], wd = w2[(4 * v + 3) * (EP / 2)];
-            acc0 = __fmaf_rn(xv.x, wa.x, acc0);
-            acc1 = __fmaf_rn(xv.x, wa.y, acc1);
-            acc0 = __fmaf_rn(xv.y, wb.x, acc0);
-            acc1 = __fmaf_rn(xv.y, wb.y, acc1);
-            acc0 = __fmaf_rn(xv.z, wc.x, acc0);
-            acc1 = __fmaf_rn(xv.z, wc.y, acc1);
-            acc0 = __fmaf_rn(xv.w, wd.x, acc0);
-            acc1 = __fmaf_rn(xv.w, wd.y, acc1);
+
+    for (int b = g; b < nb; b += NG) {
+        const int jb = b * kLogitBlock;
+        const int len = min(kLogitBlock, d - jb);
+        const int nst = (len + kChainJC - 1) / kChainJC;
+        auto issue = [&](int st) {
+            unsigned char *xs = gsm + (st % kChainStages) * C::RSTAGE;
+            unsigned char *ws = xs + C::RXBYTES;
+            const int j0 = jb + st * kChainJC;
+            for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
+                const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
+                const int64_t t = t0 + r;
+                const int j = j0 + c * 8;
+                if (t < T && j < jb + len) cp_async16(xs + r * (kChainJC * 2) + c * 16, X + t * d + j);
+            }
+            for (int q = tid; q < kChainJC * (EP / 4); q += NTH) {
+                const int jj = q / (EP / 4), c4 = (q % (EP / 4)) * 4;
+                const int j = j0 + jj;
+                if (j < jb + len && c4 < E) cp_async16(ws + (jj * EP + c4) * 4, Wr + (int64_t)j * E + c4);
+            }
         };
-        if (jn == kChainJC) {
-#pragma unroll 8
-            for (int v = 0; v < kChainJC / 4; ++v) step4(v);
-        } else {
-            for (int v = 0; v < jn / 4; ++v) step4(v);
+        for (int st = 0; st < kChainStages - 1; ++st) {
+            if (st < nst) issue(st);
+            cp_async_commit();
         }
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int st = 0; st < nst; ++st) {
+            cp_async_wait<kChainStages - 2>();
+            group_sync();  // raw stage st landed; the group is past the previous stage
+            if (st + kChainStages - 1 < nst) issue(st + kChainStages - 1);
+            cp_async_commit();
+            const unsigned char *xs = gsm + (st % kChainStages) * C::RSTAGE;
+            const float2 *w2 = reinterpret_cast<const float2 *>(xs + C::RXBYTES) + h;  // row stride EP/2
+            for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
+                const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
+                const uint4 raw = *reinterpret_cast<const uint4 *>(xs + r * (kChainJC * 2) + c * 16);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                float4 *dst = reinterpret_cast<float4 *>(xf + r * C::LD + c * 8);
+                const float2 a = __bfloat1622float2(h2[0]), b2 = __bfloat1622float2(h2[1]);
+                const float2 c2 = __bfloat1622float2(h2[2]), d2 = __bfloat1622float2(h2[3]);
+                dst[0] = make_float4(a.x, a.y, b2.x, b2.y);
+                dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
+            }
+            group_sync();
+            const int jn = min(kChainJC, len - st * kChainJC);  // a multiple of 8
+            auto step4 = [&](int v) {
+                const float4 xv = xrow[v];
+                const float2 wa = w2[(4 * v + 0) * (EP / 2)], wb = w2[(4 * v + 1) * (EP / 2)];
+                const float2 wc = w2[(4 * v + 2) * (EP / 2)], wd = w2[(4 * v + 3) * (EP / 2)];
+                acc0 = __fmaf_rn(xv.x, wa.x, acc0);
+                acc1 = __fmaf_rn(xv.x, wa.y, acc1);
+                acc0 = __fmaf_rn(xv.y, wb.x, acc0);
+                acc1 = __fmaf_rn(xv.y, wb.y, acc1);
+                acc0 = __fmaf_rn(xv.z, wc.x, acc0);
+                acc1 = __fmaf_rn(xv.z, wc.y, acc1);
+                acc0 = __fmaf_rn(xv.w, wd.x, acc0);
+                acc1 = __fmaf_rn(xv.w, wd.y, acc1);
+            };
+            if (jn == kChainJC) {
+#pragma unroll 8
+                for (int v = 0; v < kChainJC / 4; ++v) step4(v);
+            } else {
+                for (int v = 0; v < jn / 4; ++v) step4(v);
+            }
+        }
+        cp_async_wait<0>();
+        group_sync();  // the ring and xf are free for the group's next block
+        part[b * NTH + tid] = make_float2(acc0, acc1);
     }
-    cp_async_wait<0>();
+    __syncthreads();
+    if (g != 0) return;
+    float2 s = part[tid];
+    for (int b = 1; b < nb; ++b) {
+        const float2 p = part[b * NTH + tid];
+        s.x = __fadd_rn(s.x, p.x);
+        s.y = __fadd_rn(s.y, p.y);
+    }
     const int64_t t = t0 + tl;
     if (t < T) {
         const int e0 = 2 * h;
         if (e0 < E) {
-            if (bias != nullptr) acc0 = __fadd_rn(acc0, __ldg(bias + e0));
-            L[t * E + e0] = acc0;
+            if (bias != nullptr) s.x = __fadd_rn(s.x, __ldg(bias + e0));
+            L[t * E + e0] = s.x;
         }
         if (e0 + 1 < E) {
-            if (bias != nullptr) acc1 = __fadd_rn(acc1, __ldg(bias + e0 + 1));
-            L[t * E + e0 + 1] = acc1;
+            if (bias != nullptr) s.y = __fadd_rn(s.y, __ldg(bias + e0 + 1));
+            L[t * E + e0 + 1] = s.y;
         }
     }
 }
@@ -182,7 +217,7 @@ logits_small_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
     const int ec = e < E ? e : E - 1;  // padding lanes compute a copy and store nothing
     const uint4 *xr = reinterpret_cast<const uint4 *>(X + t * d);
     const float *wc = Wr + ec;
-    float acc = 0.f;
+    float tot = 0.f, acc = 0.f;  // block sums folded so far; the current block's chain
     const int nv = d / 8;
 #pragma unroll 4
     for (int v = 0; v < nv; ++v) {
@@ -197,10 +232,14 @@ logits_small_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
             acc = __fmaf_rn(f.x, w[2 * u], acc);
             acc = __fmaf_rn(f.y, w[2 * u + 1], acc);
         }
+        if ((8 * (v + 1)) % kLogitBlock == 0 || v + 1 == nv) {  // a block ends here
+            tot = 8 * v < kLogitBlock ? acc : __fadd_rn(tot, acc);
+            acc = 0.f;
+        }
     }
     if (e < E) {
-        if (bias != nullptr) acc = __fadd_rn(acc, __ldg(bias + e));
-        L[t * E + e] = acc;
+        if (bias != nullptr) tot = __fadd_rn(tot, __ldg(bias + e));
+        L[t * E + e] = tot;
     }
 }
 
@@ -747,13 +786,16 @@ cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *b
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(logits_chain_kernel<EP>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::MAX_SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
+    const int nb = (d + kLogitBlock - 1) / kLogitBlock;
+    const int ng = nb < C::MAXG ? nb : C::MAXG;
+    const size_t smem = (size_t)ng * C::GROUP_SMEM + (size_t)nb * C::THREADS * 8;
     const unsigned grid = (unsigned)((T + kChainTok - 1) / kChainTok);
-    return launch_k(logits_chain_kernel<EP>, dim3(grid), dim3(C::THREADS), (size_t)C::SMEM, s, X,
-                    Wr, bias, T, d, E, L);
+    return launch_k(logits_chain_kernel<EP>, dim3(grid), dim3(ng * C::THREADS), smem, s, X, Wr,
+                    bias, T, d, E, L);
 }
 
 template <int PA, int PB>
@@ -822,7 +864,7 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
             default: break;
         }
     }
-    if (E <= 32 && E % 4 == 0 && wr16) {
+    if (E <= 32 && E % 4 == 0 && wr16 && d <= kChainMaxBlocks * kLogitBlock) {
         if (E <= 8) return launch_chain<8>(X, Wr, bias, T, d, E, L, s);
         if (E <= 16) return launch_chain<16>(X, Wr, bias, T, d, E, L, s);
         return launch_chain<32>(X, Wr, bias, T, d, E, L, s);
