@@ -92,8 +92,10 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  *          topk_idx [T,K] int32 (descending score; ties -> lower index),
  *          topk_w [T,K] fp32, counts [E] int32 (tokens routed to each expert;
  *          the call zeroes it first).
- * Logits are fp32 fused multiply-add chains over j = 0..d-1 ascending from +0,
- * then + bias[e]: bit-identical to that sequential definition. */
+ * Logits are fp32 fused multiply-add chains over j ascending from +0, then
+ * + bias[e]: with E > 32 one chain over j = 0..d-1; with E <= 32 one chain per
+ * block of 1024 consecutive j, the block sums added in ascending block order.
+ * Bit-identical to that sequential definition. */
 moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias,
                        int T, int d, int E, int K, int renorm, float *logits,
                        int32_t *topk_idx, float *topk_w, int32_t *counts, void *stream);
