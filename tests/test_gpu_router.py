@@ -73,6 +73,11 @@ ROUTE_CASES = [
     (40, 1024, 33, 2, False),     # smallest tiled E, scalar weight loads
     (1000, 512, 32, 4, False),    # largest per-thread-chain E
     (3000, 1000, 12, 3, False),   # chain kernel, d not a multiple of its stage
+    # E <= 32 sums in 1024-step blocks, one thread group per block
+    (600, 3000, 32, 4, True),     # 3 blocks, 2 groups: group 0 also runs block 2; partial last block
+    (200, 9216, 8, 2, False),     # 9 blocks, 8 groups
+    (64, 16392, 8, 2, False),     # 17 blocks: beyond the chain kernel, the small kernel folds them
+    (130, 2056, 20, 3, True),     # E padded to 32, a last block of 8 steps
 ]
 
 
