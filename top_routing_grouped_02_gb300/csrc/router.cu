@@ -19,7 +19,7 @@
 //     top-K indices) is bit-identical to a sequential evaluation of it. A chain
 //     cannot be split over threads or tensor-core instructions without changing
 //     the rounding, so every chain stays in one thread:
-//       - E <= 32: two (token, expert) chains per thread, one thread group per
+//       - E <= 32: four (token, expert) chains per thread, one thread group per
 //         block of the reduction, fed from cp.async shared-memory pipelines; the
 //         groups' block sums are added in order at the end.
 //       - E > 32: two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
@@ -59,32 +59,34 @@ __device__ __forceinline__ void cp_async_wait() {
 // divide kLogitBlock.
 constexpr int kLogitBlock = 1024;
 
-// ---- E <= 32: two (token, expert) chains per thread, one group per block ----
-// A thread group covers 8 tokens x EP experts, one thread per (token, expert
-// pair), so 4*EP threads; a CTA holds NG groups, and group g runs the chains of
-// blocks g, g + NG, ... of the reduction, so the blocks of one logit run side by
-// side. Each group streams its block through its own ring of 64-step stages
-// (3 deep, cp.async): the 8 rows of X (bf16, widened once per stage to fp32)
-// and the rows of Wr. Per 4 steps a thread reads one float4 of x and four
-// float2 of weights for 8 fused multiply-adds on its two chains. At the end each
-// group's block sums go to shared memory and the first group adds them in
-// ascending block order. Requires d % 8 == 0, E % 4 == 0, a 16-byte-aligned Wr
-// and at most kChainMaxBlocks blocks.
-constexpr int kChainTok = 8;
+// ---- E <= 32: four (token, expert) chains per thread, one group per block ----
+// A thread group covers 16 tokens x EP experts, one thread per (token slot,
+// expert pair) with the tokens of slots tl and tl + 8, so 4*EP threads; a CTA
+// holds NG groups, and group g runs the chains of blocks g, g + NG, ... of the
+// reduction, so the blocks of one logit run side by side. Each group streams
+// its block through its own ring of 64-step stages (3 deep, cp.async): the 16
+// rows of X (bf16, widened once per stage to fp32) and the rows of Wr. Per 4
+// steps a thread reads two float4 of x and four float2 of weights for 16 fused
+// multiply-adds on its four chains. At the end each group's block sums go to
+// shared memory and the first group adds them in ascending block order.
+// Requires d % 8 == 0, E % 4 == 0, a 16-byte-aligned Wr and at most
+// kChainMaxBlocks blocks.
+constexpr int kChainSlots = 8;   // token slots of a group; a thread takes slots tl and tl + 8
+constexpr int kChainTok = 16;    // tokens of a group
 constexpr int kChainStages = 3;
 constexpr int kChainJC = 64;
 constexpr int kChainMaxBlocks = 16;
 
 template <int EP>
 struct ChainCfg {
-    static constexpr int THREADS = kChainTok * EP / 2;        // one group
+    static constexpr int THREADS = kChainSlots * EP / 2;      // one group
     static constexpr int RXBYTES = kChainTok * kChainJC * 2;  // raw X rows (bf16)
     static constexpr int RWBYTES = kChainJC * EP * 4;         // raw Wr rows (EP floats each)
     static constexpr int RSTAGE = RXBYTES + RWBYTES;
     static constexpr int LD = kChainJC + 4;                   // widened x row (floats)
     static constexpr int GROUP_SMEM = kChainStages * RSTAGE + kChainTok * LD * 4;
     static constexpr int MAXG = EP == 8 ? 8 : (EP == 16 ? 4 : 2);  // groups per CTA
-    static constexpr int MAX_SMEM = MAXG * GROUP_SMEM + kChainMaxBlocks * THREADS * 8;
+    static constexpr int MAX_SMEM = MAXG * GROUP_SMEM + kChainMaxBlocks * THREADS * 16;
 };
 
 template <int EP>
@@ -100,8 +102,8 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
     const int g = threadIdx.x / NTH, tid = threadIdx.x % NTH;
     unsigned char *gsm = sm + g * C::GROUP_SMEM;
     float *xf = reinterpret_cast<float *>(gsm + kChainStages * C::RSTAGE);  // [8][LD]
-    float2 *part = reinterpret_cast<float2 *>(sm + NG * C::GROUP_SMEM);     // [nb][NTH]
-    const int h = tid % (EP / 2), tl = tid / (EP / 2);  // experts 2h, 2h+1 of token tl
+    float4 *part = reinterpret_cast<float4 *>(sm + NG * C::GROUP_SMEM);     // [nb][NTH]
+    const int h = tid % (EP / 2), tl = tid / (EP / 2);  // experts 2h, 2h+1 of tokens tl, tl + 8
     const int64_t t0 = (int64_t)blockIdx.x * kChainTok;
     const int nb = (d + kLogitBlock - 1) / kLogitBlock;
     auto group_sync = [&]() {
@@ -109,6 +111,7 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         else asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "r"(NTH) : "memory");
     };
     const float4 *xrow = reinterpret_cast<const float4 *>(xf + tl * C::LD);
+    const float4 *xrow2 = reinterpret_cast<const float4 *>(xf + (tl + kChainSlots) * C::LD);
 
     for (int b = g; b < nb; b += NG) {
         const int jb = b * kLogitBlock;
@@ -134,7 +137,7 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
             if (st < nst) issue(st);
             cp_async_commit();
         }
-        float acc0 = 0.f, acc1 = 0.f;
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // (tl, 2h), (tl, 2h+1), (tl+8, ...)
         for (int st = 0; st < nst; ++st) {
             cp_async_wait<kChainStages - 2>();
             group_sync();  // raw stage st landed; the group is past the previous stage
@@ -155,17 +158,25 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
             group_sync();
             const int jn = min(kChainJC, len - st * kChainJC);  // a multiple of 8
             auto step4 = [&](int v) {
-                const float4 xv = xrow[v];
+                const float4 xv = xrow[v], xu = xrow2[v];
                 const float2 wa = w2[(4 * v + 0) * (EP / 2)], wb = w2[(4 * v + 1) * (EP / 2)];
                 const float2 wc = w2[(4 * v + 2) * (EP / 2)], wd = w2[(4 * v + 3) * (EP / 2)];
                 acc0 = __fmaf_rn(xv.x, wa.x, acc0);
                 acc1 = __fmaf_rn(xv.x, wa.y, acc1);
+                acc2 = __fmaf_rn(xu.x, wa.x, acc2);
+                acc3 = __fmaf_rn(xu.x, wa.y, acc3);
                 acc0 = __fmaf_rn(xv.y, wb.x, acc0);
                 acc1 = __fmaf_rn(xv.y, wb.y, acc1);
+                acc2 = __fmaf_rn(xu.y, wb.x, acc2);
+                acc3 = __fmaf_rn(xu.y, wb.y, acc3);
                 acc0 = __fmaf_rn(xv.z, wc.x, acc0);
                 acc1 = __fmaf_rn(xv.z, wc.y, acc1);
+                acc2 = __fmaf_rn(xu.z, wc.x, acc2);
+                acc3 = __fmaf_rn(xu.z, wc.y, acc3);
                 acc0 = __fmaf_rn(xv.w, wd.x, acc0);
                 acc1 = __fmaf_rn(xv.w, wd.y, acc1);
+                acc2 = __fmaf_rn(xu.w, wd.x, acc2);
+                acc3 = __fmaf_rn(xu.w, wd.y, acc3);
             };
             if (jn == kChainJC) {
 #pragma unroll 8
@@ -176,26 +187,32 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         }
         cp_async_wait<0>();
         group_sync();  // the ring and xf are free for the group's next block
-        part[b * NTH + tid] = make_float2(acc0, acc1);
+        part[b * NTH + tid] = make_float4(acc0, acc1, acc2, acc3);
     }
     __syncthreads();
     if (g != 0) return;
-    float2 s = part[tid];
+    float4 s = part[tid];
     for (int b = 1; b < nb; ++b) {
-        const float2 p = part[b * NTH + tid];
+        const float4 p = part[b * NTH + tid];
         s.x = __fadd_rn(s.x, p.x);
         s.y = __fadd_rn(s.y, p.y);
+        s.z = __fadd_rn(s.z, p.z);
+        s.w = __fadd_rn(s.w, p.w);
     }
-    const int64_t t = t0 + tl;
-    if (t < T) {
-        const int e0 = 2 * h;
-        if (e0 < E) {
-            if (bias != nullptr) s.x = __fadd_rn(s.x, __ldg(bias + e0));
-            L[t * E + e0] = s.x;
-        }
-        if (e0 + 1 < E) {
-            if (bias != nullptr) s.y = __fadd_rn(s.y, __ldg(bias + e0 + 1));
-            L[t * E + e0 + 1] = s.y;
+    const int e0 = 2 * h;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int64_t t = t0 + tl + k * kChainSlots;
+        float v0 = k ? s.z : s.x, v1 = k ? s.w : s.y;
+        if (t < T) {
+            if (e0 < E) {
+                if (bias != nullptr) v0 = __fadd_rn(v0, __ldg(bias + e0));
+                L[t * E + e0] = v0;
+            }
+            if (e0 + 1 < E) {
+                if (bias != nullptr) v1 = __fadd_rn(v1, __ldg(bias + e0 + 1));
+                L[t * E + e0 + 1] = v1;
+            }
         }
     }
 }
@@ -792,7 +809,7 @@ cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *b
     }
     const int nb = (d + kLogitBlock - 1) / kLogitBlock;
     const int ng = nb < C::MAXG ? nb : C::MAXG;
-    const size_t smem = (size_t)ng * C::GROUP_SMEM + (size_t)nb * C::THREADS * 8;
+    const size_t smem = (size_t)ng * C::GROUP_SMEM + (size_t)nb * C::THREADS * 16;
     const unsigned grid = (unsigned)((T + kChainTok - 1) / kChainTok);
     return launch_k(logits_chain_kernel<EP>, dim3(grid), dim3(ng * C::THREADS), smem, s, X, Wr,
                     bias, T, d, E, L);
