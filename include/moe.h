@@ -34,6 +34,17 @@
  *     router and combine alone); T*K*max(d,n) < 2^31. Anything else returns
  *     MOE_ERR_UNSUPPORTED_SHAPE.
  *   - The kernels are built for sm_103a only; any other device returns MOE_ERR_ARCH.
+ *   - Every kernel is launched with programmatic dependent launch: it may start
+ *     while the previous kernel on the stream finishes, and waits for that
+ *     kernel's results before reading global memory. Results do not depend on it.
+ *   - Environment variables that choose between kernels computing the same
+ *     results (for tests and measurements; unset is the default choice):
+ *       MOE_PDL=0             launch without programmatic dependent launch (read
+ *                             once per process);
+ *       MOE_GEMM_CTA_PAIR=0/1 expert GEMMs on single CTAs / on CTA pairs;
+ *       MOE_ROUTER_PAIRS=4..8 router logits (E > 32) on the one-block-per-SM
+ *                             kernel with that many token pairs per scheduler;
+ *                             0: on the 4 x 8 register-tile kernel.
  */
 #ifndef MOE_H
 #define MOE_H
