@@ -37,8 +37,9 @@
  *   - Every kernel is launched with programmatic dependent launch: it may start
  *     while the previous kernel on the stream finishes, and waits for that
  *     kernel's results before reading global memory. Results do not depend on it.
- *   - Environment variables that choose between kernels computing the same
- *     results (for tests and measurements; unset is the default choice):
+ *   - Environment variables that choose between kernels for the same step (for
+ *     tests and measurements; unset is the default choice). Routing results are
+ *     bit-identical either way; GEMM outputs may differ within rounding:
  *       MOE_PDL=0             launch without programmatic dependent launch (read
  *                             once per process);
  *       MOE_GEMM_CTA_PAIR=0/1 expert GEMMs on single CTAs / on CTA pairs;
