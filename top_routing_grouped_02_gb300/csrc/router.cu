@@ -697,12 +697,13 @@ select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
         if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
 }
 
-// Small E: one thread per token and a single block, which zeroes and writes the
-// counts itself (no memset, one launch). Softmax statistics in the thread: the
+// Small E and T <= 2048: one thread per token and a single block, which zeroes
+// and writes the counts itself (no memset, one launch; above 2048 tokens the
+// warp-per-token kernel is faster, its counts zeroed before the logits kernel). Softmax statistics in the thread: the
 // maximum, then a compensated (Kahan) sum of exp(L - max) for the full
 // denominator; top-K by K passes (higher score wins, equal scores: lower index).
 constexpr int kSelSingleThreads = 1024;
-constexpr int kSelSingleMaxT = 16384;
+constexpr int kSelSingleMaxT = 2048;
 
 template <int EP>
 __global__ void __launch_bounds__(kSelSingleThreads)
