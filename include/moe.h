@@ -201,7 +201,9 @@ moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, i
 
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
- * Enqueues 8 kernels and one memset; no host synchronisation. */
+ * Enqueues 8 kernels (9 when the gate/up GEMM runs on CTA pairs, which gather
+ * their rows first) and, unless E <= 16 and T <= 2048, one memset of the
+ * counts; no host synchronisation. */
 moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
                          const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                          int T, int d, int E, int K, int n, int renorm,
