@@ -65,9 +65,10 @@ constexpr int kLogitBlock = 1024;
 // holds NG groups, and group g runs the chains of blocks g, g + NG, ... of the
 // reduction, so the blocks of one logit run side by side. Each group streams
 // its block through its own ring of 64-step stages (3 deep, cp.async): the 16
-// rows of X (bf16, widened once per stage to fp32) and the rows of Wr. Per 4
-// steps a thread reads two float4 of x and four float2 of weights for 16 fused
-// multiply-adds on its four chains. At the end each group's block sums go to
+// rows of X (bf16, 16-byte chunks XOR-swizzled by row) and the rows of Wr. Per
+// 4 steps a thread reads 8 bytes of bf16 x for each of its two tokens (widened
+// in registers) and four float2 of weights for 16 fused multiply-adds on its
+// four chains. At the end each group's block sums go to
 // shared memory and the first group adds them in ascending block order.
 // Requires d % 8 == 0, E % 4 == 0, a 16-byte-aligned Wr and at most
 // kChainMaxBlocks blocks.
@@ -83,8 +84,7 @@ struct ChainCfg {
     static constexpr int RXBYTES = kChainTok * kChainJC * 2;  // raw X rows (bf16)
     static constexpr int RWBYTES = kChainJC * EP * 4;         // raw Wr rows (EP floats each)
     static constexpr int RSTAGE = RXBYTES + RWBYTES;
-    static constexpr int LD = kChainJC + 4;                   // widened x row (floats)
-    static constexpr int GROUP_SMEM = kChainStages * RSTAGE + kChainTok * LD * 4;
+    static constexpr int GROUP_SMEM = kChainStages * RSTAGE;
     static constexpr int MAXG = EP == 8 ? 8 : (EP == 16 ? 4 : 2);  // groups per CTA
     static constexpr int MAX_SMEM = MAXG * GROUP_SMEM + kChainMaxBlocks * THREADS * 16;
 };
@@ -101,7 +101,6 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
     const int NG = blockDim.x / NTH;
     const int g = threadIdx.x / NTH, tid = threadIdx.x % NTH;
     unsigned char *gsm = sm + g * C::GROUP_SMEM;
-    float *xf = reinterpret_cast<float *>(gsm + kChainStages * C::RSTAGE);  // [8][LD]
     float4 *part = reinterpret_cast<float4 *>(sm + NG * C::GROUP_SMEM);     // [nb][NTH]
     const int h = tid % (EP / 2), tl = tid / (EP / 2);  // experts 2h, 2h+1 of tokens tl, tl + 8
     const int64_t t0 = (int64_t)blockIdx.x * kChainTok;
@@ -110,8 +109,6 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
         if constexpr (NTH == 32) __syncwarp();
         else asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "r"(NTH) : "memory");
     };
-    const float4 *xrow = reinterpret_cast<const float4 *>(xf + tl * C::LD);
-    const float4 *xrow2 = reinterpret_cast<const float4 *>(xf + (tl + kChainSlots) * C::LD);
 
     for (int b = g; b < nb; b += NG) {
         const int jb = b * kLogitBlock;
@@ -125,7 +122,8 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
                 const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
                 const int64_t t = t0 + r;
                 const int j = j0 + c * 8;
-                if (t < T && j < jb + len) cp_async16(xs + r * (kChainJC * 2) + c * 16, X + t * d + j);
+                if (t < T && j < jb + len)
+                    cp_async16(xs + r * (kChainJC * 2) + ((c ^ (r & 7)) << 4), X + t * d + j);
             }
             for (int q = tid; q < kChainJC * (EP / 4); q += NTH) {
                 const int jj = q / (EP / 4), c4 = (q % (EP / 4)) * 4;
@@ -145,20 +143,19 @@ logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
             cp_async_commit();
             const unsigned char *xs = gsm + (st % kChainStages) * C::RSTAGE;
             const float2 *w2 = reinterpret_cast<const float2 *>(xs + C::RXBYTES) + h;  // row stride EP/2
-            for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
-                const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
-                const uint4 raw = *reinterpret_cast<const uint4 *>(xs + r * (kChainJC * 2) + c * 16);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-                float4 *dst = reinterpret_cast<float4 *>(xf + r * C::LD + c * 8);
-                const float2 a = __bfloat1622float2(h2[0]), b2 = __bfloat1622float2(h2[1]);
-                const float2 c2 = __bfloat1622float2(h2[2]), d2 = __bfloat1622float2(h2[3]);
-                dst[0] = make_float4(a.x, a.y, b2.x, b2.y);
-                dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
-            }
-            group_sync();
             const int jn = min(kChainJC, len - st * kChainJC);  // a multiple of 8
+            // the thread's two token rows in the stage: 8 bytes (4 steps) per read,
+            // 16-byte chunks XOR-swizzled by row so the reads are conflict-free
+            const unsigned char *xa = xs + tl * (kChainJC * 2);
+            const unsigned char *xb = xs + (tl + kChainSlots) * (kChainJC * 2);
             auto step4 = [&](int v) {
-                const float4 xv = xrow[v], xu = xrow2[v];
+                const int off = (((v >> 1) ^ (tl & 7)) << 4) + (v & 1) * 8;
+                const uint2 ra = *reinterpret_cast<const uint2 *>(xa + off);
+                const uint2 rb = *reinterpret_cast<const uint2 *>(xb + off);
+                const float4 xv = make_float4(__uint_as_float(ra.x << 16), __uint_as_float(ra.x & 0xffff0000u),
+                                              __uint_as_float(ra.y << 16), __uint_as_float(ra.y & 0xffff0000u));
+                const float4 xu = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
+                                              __uint_as_float(rb.y << 16), __uint_as_float(rb.y & 0xffff0000u));
                 const float2 wa = w2[(4 * v + 0) * (EP / 2)], wb = w2[(4 * v + 1) * (EP / 2)];
                 const float2 wc = w2[(4 * v + 2) * (EP / 2)], wd = w2[(4 * v + 3) * (EP / 2)];
                 acc0 = __fmaf_rn(xv.x, wa.x, acc0);
