@@ -72,6 +72,9 @@ def _load():
                 "oracle_combine_rows_bf16": (None, [P, P, I64, I, I, P]),
                 "oracle_forward_assigned": (None, [P, P, P, P, I64, I, I, I, P, P, P, I64, P]),
                 "oracle_num_threads": (I, []),
+                "oracle_forward_fixed": (None, [P, P, P, P, P, P, P, I64, I, I, I, I, I, P]),
+                "oracle_backward": (None, [P, P, P, P, P, P, P, P, I64, I, I, I, I, I,
+                                           P, P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -341,3 +344,43 @@ def forward_assigned(X, W1, W3, W2, row_map, row_w, tokens) -> np.ndarray:
     _load().oracle_forward_assigned(_p(X), _p(W1), _p(W3), _p(W2), T, d, E, n, _p(row_map),
                                     _p(row_w), _p(tokens), nt, _p(Y))
     return Y
+
+
+def _f64_input(a):
+    # bf16 tensors arrive as uint16 bit patterns and widen exactly; others as floats
+    a = np.asarray(a)
+    return bf16_bits_to_f64(a) if a.dtype == np.uint16 else _c(a, np.float64)
+
+
+def forward_fixed(X, Wr, bias, W1, W3, W2, idx, renorm: bool = True) -> np.ndarray:
+    """Y [T,d] float64 of the layer with the top-K choice idx [T,K] held fixed,
+    in double and without the bf16 roundings of H and Y (the function the
+    backward differentiates). X, W1, W3, W2 as bf16 bits (uint16) or floats."""
+    X, Wr, W1, W3, W2 = (_f64_input(a) for a in (X, Wr, W1, W3, W2))
+    bias = None if bias is None else _f64_input(bias)
+    idx = _c(idx, np.int32)
+    T, d = X.shape
+    E, _, n = W1.shape
+    K = idx.shape[1]
+    Y = np.empty((T, d), np.float64)
+    _load().oracle_forward_fixed(_p(X), _p(Wr), _p(bias), _p(W1), _p(W3), _p(W2), _p(idx),
+                                 T, d, E, K, n, int(renorm), _p(Y))
+    return Y
+
+
+def backward(X, Wr, bias, W1, W3, W2, idx, dY, renorm: bool = True) -> dict:
+    """Gradient of sum(Y * dY) for Y = forward_fixed(...): dX [T,d], dWr [d,E],
+    dbias [E], dW1, dW3 [E,d,n], dW2 [E,n,d], all float64."""
+    X, Wr, W1, W3, W2 = (_f64_input(a) for a in (X, Wr, W1, W3, W2))
+    bias = None if bias is None else _f64_input(bias)
+    idx = _c(idx, np.int32)
+    dY = _c(dY, np.float64)
+    T, d = X.shape
+    E, _, n = W1.shape
+    K = idx.shape[1]
+    out = {"dX": np.empty((T, d)), "dWr": np.empty((d, E)), "dbias": np.empty(E),
+           "dW1": np.empty((E, d, n)), "dW3": np.empty((E, d, n)), "dW2": np.empty((E, n, d))}
+    _load().oracle_backward(_p(X), _p(Wr), _p(bias), _p(W1), _p(W3), _p(W2), _p(idx), _p(dY),
+                            T, d, E, K, n, int(renorm), _p(out["dX"]), _p(out["dWr"]),
+                            _p(out["dbias"]), _p(out["dW1"]), _p(out["dW3"]), _p(out["dW2"]))
+    return out

@@ -491,3 +491,169 @@ void oracle_forward_assigned(const uint16_t *X, const uint16_t *W1, const uint16
         free(y);
     }
 }
+
+/* ------------------------------------------------------------ backward -- */
+
+/* The layer in double with the top-K choice held fixed (idx [T,K]): the
+ * function whose gradient oracle_backward returns. Every input is double (bf16
+ * and fp32 tensors widen exactly). For token t:
+ *   L[e] = sum_j x_j Wr[j,e] (+ bias[e]); p = softmax(L) over all E;
+ *   w_k = p[idx_k] / sum_k' p[idx_k'] (renorm) or p[idx_k];
+ *   a1 = x W1[e], a3 = x W3[e], h = silu(a1) * a3, o = h W2[e] for e = idx_k;
+ *   Y[t] = sum_k w_k o_k.
+ * No bf16 rounding of h or Y and no fp32 logits: the forward pass's roundings
+ * pass gradients through unchanged, so this is the function they differentiate. */
+static void fixed_token(const double *x, const double *Wr, const double *bias,
+                        const int32_t *idx, int d, int E, int K, int renorm, double *p,
+                        double *w) {
+    double m = -INFINITY;
+    for (int e = 0; e < E; ++e) {
+        double l = 0.0;
+        for (int j = 0; j < d; ++j) l += x[j] * Wr[(int64_t)j * E + e];
+        if (bias) l += bias[e];
+        p[e] = l;
+        if (l > m) m = l;
+    }
+    double s = 0.0;
+    for (int e = 0; e < E; ++e) {
+        p[e] = exp(p[e] - m);
+        s += p[e];
+    }
+    for (int e = 0; e < E; ++e) p[e] /= s;
+    double kept = 0.0;
+    for (int k = 0; k < K; ++k) kept += p[idx[k]];
+    for (int k = 0; k < K; ++k) w[k] = renorm ? p[idx[k]] / kept : p[idx[k]];
+}
+
+static void expert_acts(const double *x, const double *W1e, const double *W3e, int d, int n,
+                        double *a1, double *a3) {
+    for (int i = 0; i < n; ++i) a1[i] = a3[i] = 0.0;
+    for (int j = 0; j < d; ++j) {
+        const double *w1 = W1e + (int64_t)j * n, *w3 = W3e + (int64_t)j * n;
+        for (int i = 0; i < n; ++i) {
+            a1[i] += x[j] * w1[i];
+            a3[i] += x[j] * w3[i];
+        }
+    }
+}
+
+void oracle_forward_fixed(const double *X, const double *Wr, const double *bias,
+                          const double *W1, const double *W3, const double *W2,
+                          const int32_t *idx, int64_t T, int d, int E, int K, int n, int renorm,
+                          double *Y) {
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    double *w = (double *)malloc(sizeof(double) * (size_t)K);
+    double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int64_t t = 0; t < T; ++t) {
+        const double *x = X + t * d;
+        const int32_t *it = idx + t * K;
+        fixed_token(x, Wr, bias, it, d, E, K, renorm, p, w);
+        double *y = Y + t * d;
+        for (int c = 0; c < d; ++c) y[c] = 0.0;
+        for (int k = 0; k < K; ++k) {
+            const int e = it[k];
+            expert_acts(x, W1 + (int64_t)e * d * n, W3 + (int64_t)e * d * n, d, n, a1, a3);
+            const double *W2e = W2 + (int64_t)e * n * d;
+            for (int i = 0; i < n; ++i) {
+                const double h = silu(a1[i]) * a3[i];
+                for (int c = 0; c < d; ++c) y[c] += w[k] * h * W2e[(int64_t)i * d + c];
+            }
+        }
+    }
+    free(p);
+    free(w);
+    free(a1);
+    free(a3);
+}
+
+/* Gradient of sum(Y * dY) for Y = oracle_forward_fixed(...), by the chain rule
+ * written out per token and routed pair (single-threaded: the weight gradients
+ * accumulate over tokens). With s = sigmoid(a1), silu(a1) = a1 s and
+ * silu'(a1) = s (1 + a1 (1 - s)):
+ *   o = h W2[e];  dw_k = dY[t] . o;  dh = w_k (dY[t] W2[e]^T);
+ *   dW2[e] += h^T (w_k dY[t]);  da1 = dh * a3 * silu'(a1);  da3 = dh * silu(a1);
+ *   dX[t] += da1 W1[e]^T + da3 W3[e]^T;  dW1[e] += x^T da1;  dW3[e] += x^T da3.
+ * Router: dp[idx_k] = (dw_k - sum_k' w_k' dw_k') / kept (renorm) or dw_k, 0 for
+ * the other experts; dL = p * (dp - sum_e p_e dp_e) (softmax); dbias += dL;
+ * dWr += x^T dL;  dX[t] += dL Wr^T.
+ * Outputs are overwritten; bias and dbias may be NULL. */
+void oracle_backward(const double *X, const double *Wr, const double *bias,
+                     const double *W1, const double *W3, const double *W2,
+                     const int32_t *idx, const double *dY, int64_t T, int d, int E, int K, int n,
+                     int renorm, double *dX, double *dWr, double *dbias, double *dW1,
+                     double *dW3, double *dW2) {
+    memset(dX, 0, sizeof(double) * (size_t)(T * d));
+    memset(dWr, 0, sizeof(double) * (size_t)d * E);
+    if (dbias) memset(dbias, 0, sizeof(double) * (size_t)E);
+    memset(dW1, 0, sizeof(double) * (size_t)E * d * n);
+    memset(dW3, 0, sizeof(double) * (size_t)E * d * n);
+    memset(dW2, 0, sizeof(double) * (size_t)E * n * d);
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)E);
+    double *w = (double *)malloc(sizeof(double) * (size_t)K);
+    double *dw = (double *)malloc(sizeof(double) * (size_t)K);
+    double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
+    double *dh = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int64_t t = 0; t < T; ++t) {
+        const double *x = X + t * d;
+        const int32_t *it = idx + t * K;
+        const double *g = dY + t * d;
+        double *dx = dX + t * d;
+        fixed_token(x, Wr, bias, it, d, E, K, renorm, p, w);
+        for (int k = 0; k < K; ++k) {
+            const int e = it[k];
+            const double *W1e = W1 + (int64_t)e * d * n, *W3e = W3 + (int64_t)e * d * n;
+            const double *W2e = W2 + (int64_t)e * n * d;
+            expert_acts(x, W1e, W3e, d, n, a1, a3);
+            dw[k] = 0.0;
+            for (int i = 0; i < n; ++i) {
+                const double h = silu(a1[i]) * a3[i];
+                const double *w2 = W2e + (int64_t)i * d;
+                double gw = 0.0;  /* dY[t] . W2[e][i,:] */
+                for (int c = 0; c < d; ++c) {
+                    gw += g[c] * w2[c];
+                    dW2[((int64_t)e * n + i) * d + c] += h * w[k] * g[c];
+                }
+                dw[k] += h * gw;  /* dY[t] . o = sum_i h_i (dY[t] . W2[e][i,:]) */
+                dh[i] = w[k] * gw;
+            }
+            for (int i = 0; i < n; ++i) {
+                const double s = 1.0 / (1.0 + exp(-a1[i]));
+                const double da1 = dh[i] * a3[i] * s * (1.0 + a1[i] * (1.0 - s));
+                const double da3 = dh[i] * a1[i] * s;
+                for (int j = 0; j < d; ++j) {
+                    dx[j] += da1 * W1e[(int64_t)j * n + i] + da3 * W3e[(int64_t)j * n + i];
+                    dW1[((int64_t)e * d + j) * n + i] += x[j] * da1;
+                    dW3[((int64_t)e * d + j) * n + i] += x[j] * da3;
+                }
+            }
+        }
+        /* router */
+        double kept = 0.0, wdw = 0.0;
+        for (int k = 0; k < K; ++k) {
+            kept += p[it[k]];
+            wdw += w[k] * dw[k];
+        }
+        for (int e = 0; e < E; ++e) dp[e] = 0.0;
+        for (int k = 0; k < K; ++k) dp[it[k]] += renorm ? (dw[k] - wdw) / kept : dw[k];
+        double pdp = 0.0;
+        for (int e = 0; e < E; ++e) pdp += p[e] * dp[e];
+        for (int e = 0; e < E; ++e) {
+            const double dl = p[e] * (dp[e] - pdp);
+            if (dbias) dbias[e] += dl;
+            for (int j = 0; j < d; ++j) {
+                dWr[(int64_t)j * E + e] += x[j] * dl;
+                dx[j] += dl * Wr[(int64_t)j * E + e];
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    free(w);
+    free(dw);
+    free(a1);
+    free(a3);
+    free(dh);
+}

@@ -155,6 +155,24 @@ void oracle_forward_assigned(const uint16_t *X, const uint16_t *W1, const uint16
 /* Threads the OpenMP loops use (1 when built without OpenMP). */
 int oracle_num_threads(void);
 
+/* Backward of the layer with the top-K choice idx [T,K] held fixed (routing
+ * is not differentiable; the weights are). oracle_forward_fixed computes, in
+ * double, Y [T,d] of the layer with that choice and without the bf16 roundings
+ * of H and Y (the roundings pass gradients through unchanged); oracle_backward
+ * returns the gradient of sum(Y * dY) with respect to X (dX [T,d]), Wr (dWr
+ * [d,E]), bias (dbias [E], may be NULL), W1 and W3 (dW1, dW3 [E,d,n]) and W2
+ * (dW2 [E,n,d]). All inputs and outputs are double (bf16 and fp32 tensors
+ * widen exactly). Single-threaded: sized for tests. */
+void oracle_forward_fixed(const double *X, const double *Wr, const double *bias,
+                          const double *W1, const double *W3, const double *W2,
+                          const int32_t *idx, int64_t T, int d, int E, int K, int n, int renorm,
+                          double *Y);
+void oracle_backward(const double *X, const double *Wr, const double *bias,
+                     const double *W1, const double *W3, const double *W2,
+                     const int32_t *idx, const double *dY, int64_t T, int d, int E, int K, int n,
+                     int renorm, double *dX, double *dWr, double *dbias, double *dW1,
+                     double *dW3, double *dW2);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,13 +1,16 @@
 """Planted mistakes in a copy of the oracle must each fail a pin (CPU only).
 
-Every mutation below is a plausible slip in the oracle's C source: a reordered,
-unfused or unblocked logit chain, the wrong tie-break, a dropped renormalisation, a sign error
-in SiLU, swapped gate/up branches, a dropped routing weight, truncating instead
-of rounding, a transposed weight, an unstable grouping, and in Token Rounding a
-wrong rounding rule, a wrong order in the second sort or a dropped
-renormalisation. The test copies the oracle into a temporary directory, applies
-one mutation, rebuilds it there and runs the pin suites against the copy; they
-have to fail.
+Every mutation below is a plausible slip in the oracle's C source:
+- in the forward pass: a reordered, unfused or unblocked logit chain, the wrong
+  tie-break, a dropped renormalisation, a sign error in SiLU, swapped gate/up
+  branches, a dropped routing weight, truncating instead of rounding, a
+  transposed weight, an unstable grouping;
+- in Token Rounding: a wrong rounding rule, a wrong order in the second sort or
+  a dropped renormalisation;
+- in the backward pass: a wrong SiLU derivative, a dropped routing weight or
+  renormalisation term, or the wrong weight in dX.
+The test copies the oracle into a temporary directory, applies one mutation,
+rebuilds it there and runs the pin suites against the copy; they have to fail.
 """
 import os
 import shutil
@@ -54,9 +57,15 @@ MUTATIONS = [
     ("tr_row_order_descending_t", "for (int e = 0; e < E; ++e)\n        for (int64_t t = 0; t < T; ++t) {\n            if (keep",
      "for (int e = 0; e < E; ++e)\n        for (int64_t t = T - 1; t >= 0; --t) {\n            if (keep"),
     ("combine_rows_skips_row0", "if (r >= 0) y = y + Z[", "if (r > 0) y = y + Z["),
+    # backward
+    ("bwd_silu_derivative", "s * (1.0 + a1[i] * (1.0 - s))", "s * (1.0 + a1[i] * s)"),
+    ("bwd_dh_unweighted", "dh[i] = w[k] * gw;", "dh[i] = gw;"),
+    ("bwd_dw2_unweighted", "+= h * w[k] * g[c];", "+= h * g[c];"),
+    ("bwd_router_renorm_term_dropped", "(dw[k] - wdw) / kept", "dw[k] / kept"),
+    ("bwd_dx_through_w1_twice", "da3 * W3e[(int64_t)j * n + i]", "da3 * W1e[(int64_t)j * n + i]"),
 ]
 
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_rounding.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_rounding.py", "test_oracle_backward.py"]
 
 
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
