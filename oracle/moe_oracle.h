@@ -1,5 +1,6 @@
 /*
- * CPU oracle for the forward pass of one Mixture-of-Experts layer.
+ * CPU oracle for the forward pass of one Mixture-of-Experts layer, and for its
+ * backward pass with the top-K choice held fixed.
  *
  * TEST INFRASTRUCTURE ONLY. This is the slow, plain reference the CUDA library
  * is checked against. Only the test suite, the smoke check and the benchmark's
@@ -14,7 +15,10 @@
  *       §1    X in R^{T x d}; the router scores E experts per token and keeps the
  *             best K; then Gather, a two-layer expert MLP (GEMM), and Scatter back
  *             to the tokens' positions; H = SiLU(W1 X) held at 2 bytes/element.
- *       §2.2  SwiGLU fused into the GEMM epilogue; intermediates grouped by expert.
+ *       §2.2  SwiGLU fused into the GEMM epilogue; intermediates grouped by expert;
+ *             the backward pass (dH, and the routing-score gradient dS fused
+ *             into it) exists, its formulas are not printed: the backward here is
+ *             the chain rule of the forward definition.
  *       §3.1  expert_frequency_estimation: per-expert counts as a loop over t, k.
  *       §3.2  the kept routing scores are renormalised (softmax renormalisation).
  *   "Triton优化MoE模型：topk_gating算子融合实战" (top-k gating page)
