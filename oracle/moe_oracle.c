@@ -1,11 +1,13 @@
 /*
- * CPU oracle for the forward pass of one Mixture-of-Experts layer.
+ * CPU oracle for the forward pass of one Mixture-of-Experts layer, and for its
+ * backward pass with the top-K choice held fixed.
  *
  * TEST INFRASTRUCTURE ONLY: loaded by the test suite, the smoke check and the
  * benchmark's CPU-baseline leg, never by the CUDA library. It is deliberately
  * slow and plain: each function is the definition written out, in the order the
- * pages state it, with no blocking, fusion or reordering. The sources and the
- * readings taken where the pages are silent are listed in moe_oracle.h.
+ * pages state it, with no blocking, fusion or reordering beyond what the
+ * definition itself fixes (the router logits' 1024-step blocks). The sources and
+ * the readings taken where the pages are silent are listed in moe_oracle.h.
  *
  * Build: plain C11, -ffp-contract=off (no implicit fused multiply-adds; the one
  * fma that belongs to the definition is written as fmaf), no fast-math. OpenMP
