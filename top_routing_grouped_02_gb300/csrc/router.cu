@@ -24,8 +24,9 @@
 //         groups' block sums are added in order at the end.
 //       - E > 32: two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
 //         micro-tiles fed by conflict-free float4 shared-memory reads.
-//       - E >= 128 with many tokens: one block per SM, each lane 2P tokens x 8
-//         experts, x read as bf16 pairs, so the FP32 FMA pipe is the limit.
+//       - E >= 128 with many tokens: one 8-warp block per SM, two warps per
+//         scheduler, each lane 2*PA or 2*PB tokens x 8 experts with x read as
+//         bf16 pairs, so the FP32 FMA pipe is the limit.
 //  2. select: one warp per token reads its E logits, picks K by repeated warp
 //     argmax over order-preserving keys (ties -> lower index), writes indices
 //     and weights, and counts per expert in a block histogram flushed with one
