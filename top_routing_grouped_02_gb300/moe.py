@@ -23,6 +23,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
           6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_CHECK"}
 # kernels each entry point launches (for launch accounting)
+# Kernels each call enqueues; the gate/up GEMM, and so each forward, launches one
+# more (a row gather) when it runs on CTA pairs.
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
             "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 8, "moe_round_routing": 3,
             "moe_combine_rows": 1, "moe_forward_rounded": 8}
