@@ -45,21 +45,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine"]
-KERNELS_PER_STAGE = {"route": 2, "permute": 3, "gemm_gate_up": 1, "gemm_down": 1, "combine": 1}
-KERNELS_PER_STEP = sum(KERNELS_PER_STAGE.values())
 # Token Rounding (--routing rounded): the grouping step is the rounding step
 STAGES_ROUNDED = ["route", "round", "gemm_gate_up", "gemm_down", "combine"]
-KERNELS_PER_STEP_ROUNDED = 2 + 3 + 1 + 1 + 1
-
-
-def kernels_per_step(rounded, R, E):
-    """Kernels one forward launches: the fixed ones, plus the row gather that the
-    gate/up GEMM runs first on CTA pairs (the library picks pairs when the
-    experts average at least 8 row tiles, R >= 8*128*E, unless MOE_GEMM_CTA_PAIR
-    forces a variant)."""
-    env = os.environ.get("MOE_GEMM_CTA_PAIR", "")
-    pair = env == "1" if env in ("0", "1") else R >= 8 * 128 * E
-    return (KERNELS_PER_STEP_ROUNDED if rounded else KERNELS_PER_STEP) + (1 if pair else 0)
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
 # the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
@@ -333,6 +320,14 @@ def run_gpu(args, c, world, rank, local):
         raise RuntimeError(f"device error word {word:#x} in the stage region")
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
                                   for i in range(args.steps)])) for j, s in enumerate(stages)}
+    # kernels per forward: 6 outside the expert GEMMs, which take 1 launch when
+    # fused, 2 apart, 3 on CTA pairs (the row gather)
+    launches = moe.forward_launches(T, d, E, K, n, rounded)
+    fused = launches - 6 == 1
+    if fused:  # one launch holds both GEMMs: the gate/up interval (down is empty)
+        stage_ms = {("expert_mlp_fused" if k == "gemm_gate_up" else k):
+                    (v + stage_ms["gemm_down"] if k == "gemm_gate_up" else v)
+                    for k, v in stage_ms.items() if k != "gemm_down"}
     ms_step = ms_max / args.steps
     flops = 2.0 * R * 3 * d * n
     value = aggregate(flops * args.steps, ms_max / 1e3, world) / 1e12
@@ -398,9 +393,15 @@ def run_gpu(args, c, world, rank, local):
     }
 
     peaks = load_peaks()
-    g1_flops = 4.0 * R * d * n
-    g1_tflops = g1_flops / (stage_ms["gemm_gate_up"] / 1e3) / 1e12
-    g2_tflops = 2.0 * R * n * d / (stage_ms["gemm_down"] / 1e3) / 1e12
+    # the roofline object: the gate/up GEMM, or the fused launch of both GEMMs
+    if fused:
+        g1_name, g1_flops = "expert_mlp_fused (tcgen05 gate/up + SwiGLU and down, one launch)", flops
+        g1_tflops = g1_flops / (stage_ms["expert_mlp_fused"] / 1e3) / 1e12
+        g2_tflops = None
+    else:
+        g1_name, g1_flops = "gemm_gate_up (tcgen05 grouped GEMM + SwiGLU)", 4.0 * R * d * n
+        g1_tflops = g1_flops / (stage_ms["gemm_gate_up"] / 1e3) / 1e12
+        g2_tflops = 2.0 * R * n * d / (stage_ms["gemm_down"] / 1e3) / 1e12
     router_bytes = T * d * 2 + d * E * 4 + R * 8 + E * 4
     combine_bytes = (R + T) * d * 2
     clocks = clk.summary()
@@ -417,13 +418,14 @@ def run_gpu(args, c, world, rank, local):
                          f"{3 * E * d * n * 2 / 1e9:.2f} GB per step, no flush"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
-        "roofline": {"kernel": "gemm_gate_up (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
+        "roofline": {"kernel": g1_name, "bound": "tensor",
                      "achieved": round(g1_tflops, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": round(g1_tflops / peaks["bf16"], 4),
-                     "traffic": None if rounded else (GEMM1_TRAFFIC_BYTES or {}).get(args.workload),
+                     "traffic": None if rounded or fused
+                     else (GEMM1_TRAFFIC_BYTES or {}).get(args.workload),
                      "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
                      "algorithmic_flops_per_launch": g1_flops},
-        "gpu_launches": kernels_per_step(rounded, R, E) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "extra": {
             "tokens_per_s": round(T * world / (ms_step / 1e3), 1),
@@ -431,7 +433,7 @@ def run_gpu(args, c, world, rank, local):
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
             "topk_rows_equiv_tflops": round(useful_flops(c) * world / (ms_step / 1e3) / 1e12, 3),
             "routing": routing_stats,
-            "gemm_down_tflops": round(g2_tflops, 2),
+            "gemm_down_tflops": None if g2_tflops is None else round(g2_tflops, 2),
             "router_GBps": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9, 1),
             "router_frac_hbm": round(router_bytes / (stage_ms["route"] / 1e3) / 1e9 / peaks["hbm"], 4),
             "combine_GBps": round(combine_bytes / (stage_ms["combine"] / 1e3) / 1e9, 1),

@@ -43,6 +43,11 @@
  *       MOE_PDL=0             launch without programmatic dependent launch (read
  *                             once per process);
  *       MOE_GEMM_CTA_PAIR=0/1 expert GEMMs on single CTAs / on CTA pairs;
+ *       MOE_GEMM_FUSED=1      both expert GEMMs in one launch where n <= 2048
+ *                             (default: two launches; see moe_expert_mlp);
+ *       MOE_FUSED_GAP_ROUNDS=g rounds the fused launch keeps between a
+ *                             gate/up round and the down rounds reading it
+ *                             (default 2);
  *       MOE_ROUTER_PAIRS=4..8 router logits (E > 32) on the one-block-per-SM
  *                             kernel with that many token pairs per scheduler;
  *                             0: on the 4 x 8 register-tile kernel.
@@ -184,7 +189,17 @@ moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *t
                            int T, int d, int E, int K, int n, moe_bf16 *Z,
                            void *ws, size_t ws_bytes, void *stream);
 
-/* Both expert GEMMs: moe_gemm_gate_up then moe_gemm_down. */
+/* Both expert GEMMs: H as moe_gemm_gate_up writes it, then Z as moe_gemm_down
+ * writes it, bit for bit. Two launches (three on CTA pairs); with
+ * MOE_GEMM_FUSED=1 and n <= 2048, ONE persistent launch (the SonicMoE page's
+ * fine-grained experts keep H small): its CTAs run rounds of gate/up units
+ * (128 rows x 128 H columns) and of down units (128 rows x 256 Z columns), and a
+ * down unit starts once the gate/up units of its row tile have stored H,
+ * signalled through per-tile counter words in the workspace (bounded waits; a
+ * wait that runs out sets MOE_DEVERR_TIMEOUT). On the SonicMoE-shaped layer the
+ * fused launch measured slower than the two (0.183-0.191 against 0.170 ms).
+ * ws: workspace of this shape, zeroed once before first use and not shared by
+ * calls that overlap on the GPU. */
 moe_status_t moe_expert_mlp(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
                             const moe_bf16 *W2, const float *topk_w,
                             const int32_t *perm_token, const int32_t *perm_slot,
@@ -199,11 +214,18 @@ moe_status_t moe_expert_mlp(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf1
 moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, int K, int d,
                          moe_bf16 *Y, void *stream);
 
+/* Kernels moe_forward (rounded = 0) or moe_forward_rounded (rounded = 1)
+ * enqueues for this shape on the current device (its SM count bounds a fused
+ * launch's rounds) under the current environment variables; -1 for an invalid
+ * shape or flag. Host only: nothing is enqueued. */
+int moe_forward_launches(int T, int d, int E, int K, int n, int rounded);
+
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
- * Enqueues 8 kernels (9 when the gate/up GEMM runs on CTA pairs, which gather
- * their rows first) and, unless E <= 16 and T <= 2048, one memset of the
- * counts; no host synchronisation. */
+ * Enqueues moe_forward_launches(T, d, E, K, n, 0) kernels: 8, or 9 on CTA
+ * pairs, which gather their rows first, or 7 when both expert GEMMs run in one
+ * launch (see moe_expert_mlp); and, unless E <= 16 and T <= 2048, one memset
+ * of the counts; no host synchronisation. */
 moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
                          const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                          int T, int d, int E, int K, int n, int renorm,
@@ -213,7 +235,8 @@ moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
 /* moe_forward that also records CUDA events (cudaEvent_t as void*) on `stream`
  * between its stages, for per-kernel timing: events[0] before the router,
  * then after route, permute, gate/up GEMM, down GEMM, combine (6 events).
- * n_events < 6 records the first n_events of them. */
+ * When both GEMMs run in one launch, the gate/up interval holds it and the
+ * down interval is empty. n_events < 6 records the first n_events of them. */
 moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float *bias,
                                 const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                                 int T, int d, int E, int K, int n, int renorm,
@@ -282,8 +305,8 @@ size_t moe_workspace_bytes_rounded(int T, int d, int E, int K, int n);
  * route -> round -> gate/up+SwiGLU -> down+row weight -> combine_rows.
  * row_map_out [T,E] may be NULL (kept in the workspace then). The rounded
  * counts, offsets, perm_token and row weights stay in the workspace.
- * Enqueues 8 kernels (9 when the gate/up GEMM runs on CTA pairs) and at most
- * one memset; no host synchronisation. */
+ * Enqueues moe_forward_launches(T, d, E, K, n, 1) kernels (7, 8 or 9 as for
+ * moe_forward) and at most one memset; no host synchronisation. */
 moe_status_t moe_forward_rounded(const moe_bf16 *X, const float *Wr, const float *bias,
                                  const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                                  int T, int d, int E, int K, int n, int renorm, moe_bf16 *Y,

@@ -48,6 +48,30 @@ def test_workspace_bytes(lib):
     assert moe.moe_workspace_bytes(2 * T, d, E, K, n) > b
 
 
+def test_forward_launch_counts(lib, monkeypatch):
+    # kernels per forward: router 2, grouping (or rounding) 3, combine 1, and the
+    # expert GEMMs: two launches, a row gather more on CTA pairs (experts of at
+    # least 8 row tiles on average), or one fused launch on request
+    for var in ("MOE_GEMM_FUSED", "MOE_GEMM_CTA_PAIR"):
+        monkeypatch.delenv(var, raising=False)
+    assert moe.forward_launches(512, 256, 8, 2, 512) == 8            # tiny
+    assert moe.forward_launches(16384, 1536, 128, 4, 256) == 8       # SonicMoE
+    assert moe.forward_launches(16384, 1536, 128, 4, 256, True) == 8
+    assert moe.forward_launches(8192, 7168, 256, 8, 2048) == 8       # DeepSeek-V3
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 9        # Mixtral: CTA pairs
+    # (whether a fused launch's units fit its rounds depends on the device's SM
+    # count, unknown here; these cases do not depend on it)
+    monkeypatch.setenv("MOE_GEMM_FUSED", "1")
+    assert moe.forward_launches(512, 256, 8, 2, 512) == 7            # 80 units at most
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 9        # too wide to fuse
+    assert moe.forward_launches(64, 256, 4, 1, 2176) == 8            # n > 2048
+    monkeypatch.setenv("MOE_GEMM_FUSED", "0")
+    assert moe.forward_launches(16384, 1536, 128, 4, 256) == 8
+    with pytest.raises(ValueError):
+        moe.forward_launches(512, 200, 8, 2, 512)
+    assert lib.moe_forward_launches(512, 256, 8, 2, 512, 2) == -1
+
+
 FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation
 
 

@@ -131,6 +131,7 @@ WsLayout layout_impl(int T, int d, int E, int K, int n, size_t R, bool rounded) 
     L.tiles = take(16 * (size_t)L.max_tiles);
     L.num_tiles = take(4);
     L.grouping_end = off;
+    L.dep = take(4 * (size_t)L.max_tiles);
     L.xg = take(2 * R * (size_t)d);
     L.h = take(2 * R * (size_t)n);
     L.z = take(2 * R * (size_t)d);
@@ -178,6 +179,14 @@ const char *moe_status_string(int status) {
 }
 
 int moe_abi_version(void) { return 101; }
+
+int moe_forward_launches(int T, int d, int E, int K, int n, int rounded) {
+    if ((rounded != 0 && rounded != 1) || check_mlp_shape(T, d, E, K, n) != MOE_OK) return -1;
+    const int R = rounded ? (int)ws_layout_rounded(T, d, E, K, n).rows : T * K;
+    // router 2, grouping or rounding 3, combine 1, and the expert GEMMs
+    const int gemms = use_fused_mlp(R, d, E, n) ? 1 : (gemm_uses_pair(R, E) ? 3 : 2);
+    return 2 + 3 + gemms + 1;
+}
 
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n) {
     if (T < 1 || E < 1 || K < 1 || d < 0 || n < 0 || E > kMaxE || K > kMaxK || K > E) return 0;
@@ -273,10 +282,23 @@ moe_status_t moe_expert_mlp(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf1
                             const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
                             int K, int n, moe_bf16 *H, moe_bf16 *Z, void *ws, size_t ws_bytes,
                             void *stream) {
-    moe_status_t s = moe_gemm_gate_up(X, W1, W3, perm_token, offsets, T, d, E, K, n, H, ws,
-                                      ws_bytes, stream);
+    if (!X || !W1 || !W3 || !W2 || !topk_w || !perm_token || !offsets || !H || !Z || !ws)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
     if (s != MOE_OK) return s;
-    return moe_gemm_down(H, W2, topk_w, perm_slot, offsets, T, d, E, K, n, Z, ws, ws_bytes, stream);
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(H) ||
+        !aligned16(Z))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, K, n);
+    if (ws_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_expert_mlp(
+        reinterpret_cast<const __nv_bfloat16 *>(X), perm_token, T,
+        reinterpret_cast<const __nv_bfloat16 *>(W1), reinterpret_cast<const __nv_bfloat16 *>(W3),
+        reinterpret_cast<const __nv_bfloat16 *>(W2), topk_w, perm_slot, offsets, T * K, d, E, n,
+        reinterpret_cast<__nv_bfloat16 *>(H), reinterpret_cast<__nv_bfloat16 *>(Z),
+        at<__nv_bfloat16>(ws, L.xg), at<uint32_t>(ws, L.dep), at<uint32_t>(ws, L.err),
+        as_stream(stream)));
 }
 
 moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, int K, int d,
@@ -336,15 +358,27 @@ moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float 
                        static_cast<char *>(ws), st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
-    if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
-                            reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n, h,
-                            at<__nv_bfloat16>(ws, L.xg), err, st) != cudaSuccess ||
-        !mark())
-        return MOE_ERR_CUDA;
-    if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), w, perm_slot, offsets, R,
-                         d, E, n, z, err, st) != cudaSuccess ||
-        !mark())
-        return MOE_ERR_CUDA;
+    if (use_fused_mlp(R, d, E, n)) {
+        // one launch for both GEMMs: its time is the gate/up stage, the down
+        // stage's events are adjacent
+        if (launch_expert_mlp(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                              reinterpret_cast<const __nv_bfloat16 *>(W3),
+                              reinterpret_cast<const __nv_bfloat16 *>(W2), w, perm_slot, offsets,
+                              R, d, E, n, h, z, at<__nv_bfloat16>(ws, L.xg),
+                              at<uint32_t>(ws, L.dep), err, st) != cudaSuccess ||
+            !mark() || !mark())
+            return MOE_ERR_CUDA;
+    } else {
+        if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                                reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n,
+                                h, at<__nv_bfloat16>(ws, L.xg), err, st) != cudaSuccess ||
+            !mark())
+            return MOE_ERR_CUDA;
+        if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), w, perm_slot,
+                             offsets, R, d, E, n, z, err, st) != cudaSuccess ||
+            !mark())
+            return MOE_ERR_CUDA;
+    }
     if (launch_combine(z, row_of_slot, T, K, d, reinterpret_cast<__nv_bfloat16 *>(Y), st) !=
             cudaSuccess ||
         !mark())
@@ -575,16 +609,26 @@ moe_status_t moe_forward_rounded_traced(const moe_bf16 *X, const float *Wr, cons
                      st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
-    if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
-                            reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n, h,
-                            at<__nv_bfloat16>(ws, L.xg), err, st) != cudaSuccess ||
-        !mark())
-        return MOE_ERR_CUDA;
     // the weight of grouped row p is row_w[p] (no slot indirection)
-    if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), row_w, nullptr, offsets,
-                         R, d, E, n, z, err, st) != cudaSuccess ||
-        !mark())
-        return MOE_ERR_CUDA;
+    if (use_fused_mlp(R, d, E, n)) {
+        if (launch_expert_mlp(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                              reinterpret_cast<const __nv_bfloat16 *>(W3),
+                              reinterpret_cast<const __nv_bfloat16 *>(W2), row_w, nullptr,
+                              offsets, R, d, E, n, h, z, at<__nv_bfloat16>(ws, L.xg),
+                              at<uint32_t>(ws, L.dep), err, st) != cudaSuccess ||
+            !mark() || !mark())
+            return MOE_ERR_CUDA;
+    } else {
+        if (launch_gemm_gate_up(x, perm_token, T, reinterpret_cast<const __nv_bfloat16 *>(W1),
+                                reinterpret_cast<const __nv_bfloat16 *>(W3), offsets, R, d, E, n,
+                                h, at<__nv_bfloat16>(ws, L.xg), err, st) != cudaSuccess ||
+            !mark())
+            return MOE_ERR_CUDA;
+        if (launch_gemm_down(h, reinterpret_cast<const __nv_bfloat16 *>(W2), row_w, nullptr,
+                             offsets, R, d, E, n, z, err, st) != cudaSuccess ||
+            !mark())
+            return MOE_ERR_CUDA;
+    }
     if (launch_combine_rows(z, row_map, at<int32_t>(ws, L.tok_rows), at<int32_t>(ws, L.tok_n), T,
                             E, d, R, reinterpret_cast<__nv_bfloat16 *>(Y), st) != cudaSuccess ||
         !mark())

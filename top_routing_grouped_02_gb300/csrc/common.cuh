@@ -41,6 +41,7 @@ struct WsLayout {
     size_t tiles;       // int32 [max_tiles][4]
     size_t num_tiles;   // int32 [1]
     size_t grouping_end;// end of the grouping regions (what moe_permute needs)
+    size_t dep;         // uint32 [max_tiles] row-tile counters of the fused expert MLP
     size_t xg;          // bf16  [R, d]  gathered rows (CTA-pair gate/up GEMM)
     size_t h;           // bf16  [R, n]
     size_t z;           // bf16  [R, d]
@@ -57,8 +58,10 @@ struct WsLayout {
     int max_tiles;
 };
 
-// Control words at the start of the workspace (uint32 each).
-enum : int { kWordErr = 0, kWordDone = 1 };
+// Control words at the start of the workspace (uint32 each): the error word,
+// the grouping scan's ticket, and the fused expert MLP's launch epoch and
+// ticket (its row-tile counters carry the epoch, so they need no clearing).
+enum : int { kWordErr = 0, kWordDone = 1, kWordEpoch = 2, kWordTicket = 3 };
 
 WsLayout ws_layout(int T, int d, int E, int K, int n);
 // Layout for the Token Rounding forward: grouped buffers sized for the largest
@@ -96,6 +99,20 @@ cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,
                              __nv_bfloat16 *Z, uint32_t *err, cudaStream_t s);
+// Both expert GEMMs, H then Z. With small n (and the single-CTA variant) one
+// persistent kernel runs the units of both (see gemm.cu), which needs the
+// workspace's control words (err points at them) and dep [max_tiles];
+// otherwise launch_gemm_gate_up then launch_gemm_down.
+cudaError_t launch_expert_mlp(const __nv_bfloat16 *X, const int32_t *perm_token, int T,
+                              const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                              const __nv_bfloat16 *W2, const float *topk_w,
+                              const int32_t *perm_slot, const int32_t *offsets, int R, int d,
+                              int E, int n, __nv_bfloat16 *H, __nv_bfloat16 *Z,
+                              __nv_bfloat16 *xg, uint32_t *dep, uint32_t *err, cudaStream_t s);
+// Whether launch_expert_mlp runs the fused kernel for this shape, and whether
+// the gate/up GEMM runs on CTA pairs (after a separate row gather).
+bool use_fused_mlp(int R, int d, int E, int n);
+bool gemm_uses_pair(int R, int E);
 cudaError_t launch_combine(const __nv_bfloat16 *Z, const int32_t *row_of_slot, int T, int K,
                            int d, __nv_bfloat16 *Y, cudaStream_t s);
 

@@ -22,12 +22,11 @@ MOE_OK = 0
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
           6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_CHECK"}
-# kernels each entry point launches (for launch accounting)
-# Kernels each call enqueues; the gate/up GEMM, and so each forward, launches one
-# more (a row gather) when it runs on CTA pairs.
+# Kernels each call enqueues; the gate/up GEMM launches one more (a row gather)
+# when it runs on CTA pairs, and the whole-layer calls depend on the shape
+# (forward_launches).
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
-            "moe_gemm_down": 1, "moe_combine": 1, "moe_forward": 8, "moe_round_routing": 3,
-            "moe_combine_rows": 1, "moe_forward_rounded": 8}
+            "moe_gemm_down": 1, "moe_combine": 1, "moe_round_routing": 3, "moe_combine_rows": 1}
 TILE_M = 128
 
 
@@ -46,6 +45,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_abi_version": (_I, []),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_route_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -122,6 +122,15 @@ def _check(fn: str, status: int):
 
 def moe_workspace_bytes(T: int, d: int, E: int, K: int, n: int) -> int:
     return int(lib().moe_workspace_bytes(T, d, E, K, n))
+
+
+def forward_launches(T: int, d: int, E: int, K: int, n: int, rounded: bool = False) -> int:
+    """Kernels moe_forward (or moe_forward_rounded) enqueues for this shape under
+    the current environment (host only)."""
+    v = int(lib().moe_forward_launches(T, d, E, K, n, int(rounded)))
+    if v < 0:
+        raise ValueError("invalid layer shape")
+    return v
 
 
 def workspace(T: int, d: int, E: int, K: int, n: int, device=None) -> torch.Tensor:
