@@ -320,10 +320,10 @@ def run_gpu(args, c, world, rank, local):
         raise RuntimeError(f"device error word {word:#x} in the stage region")
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
                                   for i in range(args.steps)])) for j, s in enumerate(stages)}
-    # kernels per forward: 6 outside the expert GEMMs, which take 1 launch when
-    # fused, 2 apart, 3 on CTA pairs (the row gather)
+    # kernels per forward, as the library reports them; the expert GEMMs take 1
+    # launch when fused, 2 apart, 3 on CTA pairs (the row gather)
     launches = moe.forward_launches(T, d, E, K, n, rounded)
-    fused = launches - 6 == 1
+    fused = moe.forward_launches(T, d, E, K, n, rounded, part="expert_mlp") == 1
     if fused:  # one launch holds both GEMMs: the gate/up interval (down is empty)
         stage_ms = {("expert_mlp_fused" if k == "gemm_gate_up" else k):
                     (v + stage_ms["gemm_down"] if k == "gemm_gate_up" else v)

@@ -112,7 +112,8 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * Logits are fp32 fused multiply-add chains over j ascending from +0, then
  * + bias[e]: with E > 32 one chain over j = 0..d-1; with E <= 32 one chain per
  * block of 1024 consecutive j, the block sums added in ascending block order.
- * Bit-identical to that sequential definition. */
+ * Bit-identical to that sequential definition. Two kernels (logits, then
+ * softmax and top-K) and, unless E <= 16 and T <= 2048, a memset of counts. */
 moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias,
                        int T, int d, int E, int K, int renorm, float *logits,
                        int32_t *topk_idx, float *topk_w, int32_t *counts, void *stream);
@@ -219,6 +220,10 @@ moe_status_t moe_combine(const moe_bf16 *Z, const int32_t *row_of_slot, int T, i
  * launch's rounds) under the current environment variables; -1 for an invalid
  * shape or flag. Host only: nothing is enqueued. */
 int moe_forward_launches(int T, int d, int E, int K, int n, int rounded);
+
+/* The part of moe_forward_launches that the expert GEMMs take: 1 fused, 2, or
+ * 3 on CTA pairs; -1 for an invalid shape or flag. */
+int moe_expert_mlp_launches(int T, int d, int E, int K, int n, int rounded);
 
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).

@@ -61,8 +61,11 @@ def test_forward_launch_counts(lib, monkeypatch):
     assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 9        # Mixtral: CTA pairs
     # (whether a fused launch's units fit its rounds depends on the device's SM
     # count, unknown here; these cases do not depend on it)
+    assert moe.forward_launches(16384, 1536, 128, 4, 256, part="expert_mlp") == 2
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336, part="expert_mlp") == 3
     monkeypatch.setenv("MOE_GEMM_FUSED", "1")
     assert moe.forward_launches(512, 256, 8, 2, 512) == 7            # 80 units at most
+    assert moe.forward_launches(512, 256, 8, 2, 512, part="expert_mlp") == 1
     assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 9        # too wide to fuse
     assert moe.forward_launches(64, 256, 4, 1, 2176) == 8            # n > 2048
     monkeypatch.setenv("MOE_GEMM_FUSED", "0")

@@ -60,13 +60,13 @@ def test_fused_matches_oracle_and_separate_launches(T, d, E, K, n, zipf, single_
     inp, (X, W1, W3, W2), (w, off, pt, ps), dev = _setup(T, d, E, K, n, zipf)
     ws = moe.workspace(T, d, E, K, n)
     single_cta.setenv("MOE_GEMM_FUSED", "1")
-    assert moe.forward_launches(T, d, E, K, n) == 7
+    assert moe.forward_launches(T, d, E, K, n, part="expert_mlp") == 1
     H, Z = _mlp(inp, dev, K, ws)
     H_ref = oracle.gate_up(X, W1, W3, pt, off)
     check_hz(bits(H), H_ref, "H")
     check_hz(bits(Z), oracle.down(H_ref, W2, w, ps, off), "Z")
     single_cta.setenv("MOE_GEMM_FUSED", "0")
-    assert moe.forward_launches(T, d, E, K, n) == 8
+    assert moe.forward_launches(T, d, E, K, n, part="expert_mlp") == 2
     H2, Z2 = _mlp(inp, dev, K, ws)
     assert _same(H, H2) and _same(Z, Z2)
 

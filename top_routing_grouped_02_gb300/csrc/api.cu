@@ -180,11 +180,16 @@ const char *moe_status_string(int status) {
 
 int moe_abi_version(void) { return 101; }
 
-int moe_forward_launches(int T, int d, int E, int K, int n, int rounded) {
+int moe_expert_mlp_launches(int T, int d, int E, int K, int n, int rounded) {
     if ((rounded != 0 && rounded != 1) || check_mlp_shape(T, d, E, K, n) != MOE_OK) return -1;
     const int R = rounded ? (int)ws_layout_rounded(T, d, E, K, n).rows : T * K;
+    return use_fused_mlp(R, d, E, n) ? 1 : (gemm_uses_pair(R, E) ? 3 : 2);
+}
+
+int moe_forward_launches(int T, int d, int E, int K, int n, int rounded) {
+    const int gemms = moe_expert_mlp_launches(T, d, E, K, n, rounded);
+    if (gemms < 0) return -1;
     // router 2, grouping or rounding 3, combine 1, and the expert GEMMs
-    const int gemms = use_fused_mlp(R, d, E, n) ? 1 : (gemm_uses_pair(R, E) ? 3 : 2);
     return 2 + 3 + gemms + 1;
 }
 

@@ -46,6 +46,7 @@ _SIGS = {
     "moe_abi_version": (_I, []),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I, _I]),
+    "moe_expert_mlp_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_route_logits": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -124,10 +125,13 @@ def moe_workspace_bytes(T: int, d: int, E: int, K: int, n: int) -> int:
     return int(lib().moe_workspace_bytes(T, d, E, K, n))
 
 
-def forward_launches(T: int, d: int, E: int, K: int, n: int, rounded: bool = False) -> int:
-    """Kernels moe_forward (or moe_forward_rounded) enqueues for this shape under
-    the current environment (host only)."""
-    v = int(lib().moe_forward_launches(T, d, E, K, n, int(rounded)))
+def forward_launches(T: int, d: int, E: int, K: int, n: int, rounded: bool = False,
+                     part: str = "forward") -> int:
+    """Kernels moe_forward (or moe_forward_rounded) enqueues for this shape on the
+    current device under the current environment (host only); part="expert_mlp":
+    the expert GEMMs' share (1 when fused)."""
+    fn = lib().moe_forward_launches if part == "forward" else lib().moe_expert_mlp_launches
+    v = int(fn(T, d, E, K, n, int(rounded)))
     if v < 0:
         raise ValueError("invalid layer shape")
     return v
