@@ -25,8 +25,8 @@
 //       - E > 32: two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
 //         micro-tiles fed by conflict-free float4 shared-memory reads.
 //       - E >= 128 with many tokens: one 8-warp block per SM, two warps per
-//         scheduler, each lane 2*PA or 2*PB tokens x 8 experts with x read as
-//         bf16 pairs, so the FP32 FMA pipe is the limit.
+//         scheduler, each lane 2*PA or 2*PB tokens x 8 experts with x widened to
+//         fp32 pairs once per stage, so the FP32 FMA pipe is the limit.
 //  2. select: one warp per token reads its E logits, picks K by repeated warp
 //     argmax over order-preserving keys (ties -> lower index), writes indices
 //     and weights, and counts per expert in a block histogram flushed with one
@@ -409,23 +409,24 @@ logits_tiled_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict
 // accumulators are float2 pairs over neighbouring tokens. Warps w and w + 4 share
 // a scheduler, so each scheduler carries PA + PB token pairs in two warps: one
 // warp's issue slots fill the other's gaps after packed FMAs. Per reduction step
-// a lane reads its tokens' x as bf16 pairs (one 128-bit load, converted with byte
-// permutes) and its 8 weights (two 128-bit loads, conflict-free), and issues 8PA
-// or 8PB packed FMAs; each component rounds like __fmaf_rn, so every output is
-// still one sequential fma chain over j. 64-step stages, 3 deep, arrive by
-// cp.async (zero-filled beyond T, d and E): the weights as [j][e] rows, X as its
-// own [t][j] rows with the 16-byte chunks of a row pair XOR-swizzled, which one
-// pass per stage turns into the transposed, token-paired layout the steps read.
+// a lane reads its tokens' x as fp32 pairs (one or two 128-bit loads) and its 8
+// weights (two 128-bit loads, conflict-free), and issues 8PA or 8PB packed FMAs;
+// each component rounds like __fmaf_rn, so every output is still one sequential
+// fma chain over j. 64-step stages, 3 deep, arrive by cp.async (zero-filled
+// beyond T, d and E): the weights as [j][e] rows, X as its own [t][j] rows with
+// the 16-byte chunks of a row pair XOR-swizzled, which one pass per stage turns
+// into the transposed, token-paired fp32 layout the steps read (widening each
+// bf16 there once, instead of in every step that reads it).
 // PA + PB (4..8) is chosen on the host so that the block count fills the SMs.
 constexpr int kBK = 64;        // reduction steps per stage
 constexpr int kBE = 128;       // experts per block
-constexpr int kBWords = 64;    // words in a transposed x row: 16 groups x 4 token pairs
+constexpr int kBWords = 64;    // pairs in a transposed x row: 16 groups x 4 token pairs
 constexpr int kBStages = 3;
 constexpr int kBThreads = 256;
 constexpr int kBWBytes = kBK * kBE * 4;        // weight stage: 32 KB
 constexpr int kBXBytes = 2 * kBWords * kBK * 2;  // raw X stage (up to 128 rows): 16 KB
 constexpr int kBStage = kBWBytes + kBXBytes;
-constexpr int kBXsBytes = kBK * kBWords * 4;   // transposed x: 16 KB
+constexpr int kBXsBytes = kBK * kBWords * 8;   // transposed x, fp32 pairs: 32 KB
 constexpr int kBSmem = kBStages * kBStage + 2 * kBXsBytes;
 
 __device__ __forceinline__ void cp_async16_zfill(void *smem_dst, const void *gmem_src, bool ok) {
@@ -437,19 +438,20 @@ __device__ __forceinline__ void cp_async16_zfill(void *smem_dst, const void *gme
 
 // jn reduction steps of one stage for a lane with N token pairs (acc[0..N-1])
 template <int N, int PMAX, bool FULL>
-__device__ __forceinline__ void big_steps(float2 (&acc)[PMAX][8], const uint32_t *xs,
+__device__ __forceinline__ void big_steps(float2 (&acc)[PMAX][8], const float2 *xs,
                                           const float *w, int jn) {
     auto step = [&](int jj) {
-        const uint4 xa = *reinterpret_cast<const uint4 *>(xs + jj * kBWords);
+        const float4 xa = *reinterpret_cast<const float4 *>(xs + jj * kBWords);
+        float4 xb = xa;
+        if (N > 2) xb = *reinterpret_cast<const float4 *>(xs + jj * kBWords + 2);
         const float4 w0 = *reinterpret_cast<const float4 *>(w + jj * kBE);
         const float4 w1 = *reinterpret_cast<const float4 *>(w + jj * kBE + 64);
-        const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
         const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const float2 xq[4] = {make_float2(xa.x, xa.y), make_float2(xa.z, xa.w),
+                              make_float2(xb.x, xb.y), make_float2(xb.z, xb.w)};
         float2 xp[N];
 #pragma unroll
-        for (int i = 0; i < N; ++i)
-            xp[i] = make_float2(__uint_as_float(__byte_perm(xw[i], 0u, 0x1044)),
-                                __uint_as_float(__byte_perm(xw[i], 0u, 0x3244)));
+        for (int i = 0; i < N; ++i) xp[i] = xq[i];
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             const float2 ww = make_float2(wv[b], wv[b]);
@@ -485,7 +487,7 @@ logits_big_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__
     };
     auto stage_x = [&](int c) { return big_smem + (c % kBStages) * kBStage + kBWBytes; };
     auto xs_of = [&](int c) {
-        return reinterpret_cast<uint32_t *>(big_smem + kBStages * kBStage + (c & 1) * kBXsBytes);
+        return reinterpret_cast<float2 *>(big_smem + kBStages * kBStage + (c & 1) * kBXsBytes);
     };
 
     auto issue = [&](int c) {
@@ -512,11 +514,11 @@ logits_big_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__
         }
         cp_async_commit();
     };
-    // raw rows 2p, 2p+1 -> transposed words xs[j][4g + i] = (x[2p][j], x[2p+1][j])
-    // as a bf16 pair, where pair p is pair i of token group g
+    // raw rows 2p, 2p+1 -> transposed pairs xs[j][4g + i] = (x[2p][j], x[2p+1][j])
+    // widened to fp32, where pair p is pair i of token group g
     auto transpose = [&](int c) {
         const uint8_t *x = stage_x(c);
-        uint32_t *xs = xs_of(c);
+        float2 *xs = xs_of(c);
         for (int q = tid; q < 8 * (PA + PB) * 8; q += kBThreads) {
             const int p = q % (8 * (PA + PB)), ch = q / (8 * (PA + PB));
             const int pos = (ch ^ (p & 7)) << 4;
@@ -525,11 +527,14 @@ logits_big_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__
             const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
             const int word = p < 8 * PA ? 4 * (p / PA) + p % PA
                                         : 4 * (8 + (p - 8 * PA) / PB) + (p - 8 * PA) % PB;
-            uint32_t *dst = xs + (8 * ch) * kBWords + word;
+            float2 *dst = xs + (8 * ch) * kBWords + word;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                dst[(2 * m) * kBWords] = __byte_perm(aw[m], bw[m], 0x5410);
-                dst[(2 * m + 1) * kBWords] = __byte_perm(aw[m], bw[m], 0x7632);
+                // word m holds steps 8ch + 2m (low half) and 8ch + 2m + 1 (high half)
+                dst[(2 * m) * kBWords] = make_float2(__uint_as_float(aw[m] << 16),
+                                                     __uint_as_float(bw[m] << 16));
+                dst[(2 * m + 1) * kBWords] = make_float2(__uint_as_float(aw[m] & 0xffff0000u),
+                                                         __uint_as_float(bw[m] & 0xffff0000u));
             }
         }
     };
@@ -553,7 +558,7 @@ logits_big_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__
         __syncthreads();     // and every thread is past stage c - 1 and transpose(c)
         issue(c + 2);        // into the slot stage c - 1 used
         if (c + 1 < nchunk) transpose(c + 1);
-        const uint32_t *xs = xs_of(c) + 4 * g;
+        const float2 *xs = xs_of(c) + 4 * g;
         const float *w = stage_w(c) + 4 * tx;
         const int jn = min(kBK, d - c * kBK);
         if (jn == kBK) {
