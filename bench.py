@@ -49,9 +49,9 @@ STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine"]
 STAGES_ROUNDED = ["route", "round", "gemm_gate_up", "gemm_down", "combine"]
 METRIC = "MoE layer fwd useful TFLOPS and % of GB300 BF16 tensor peak; router GB/s"
 # ncu: dram__bytes_read.sum + dram__bytes_write.sum of one gate/up GEMM launch on
-# the Mixtral-shaped workload (profiles/gemm_grouped_mixtral.md). Set back to None
+# the Mixtral-shaped workload (profiles/traffic_gemm_mixtral.md). Set back to None
 # whenever the kernel changes, until it is captured again.
-GEMM1_TRAFFIC_BYTES = {"mixtral": 2.940549e9 + 0.231746e9}
+GEMM1_TRAFFIC_BYTES = {"mixtral": 2.861423e9 + 0.231877e9}
 
 
 def workload_desc(name, c, routing="topk"):
