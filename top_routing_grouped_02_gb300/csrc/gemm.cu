@@ -10,7 +10,7 @@
 // persistent CTAs, one per SM, take tiles from a schedule; expert-grouped tile
 // order for L2 reuse of expert weights; TMA loads of expert weights).
 //
-// One kernel template serves both GEMMs of the expert MLP:
+// One kernel template serves both GEMMs of the expert MLP (and, fused, both at once):
 //   gate/up:  acc[128 x 256] = X[perm_token[rows], d] . [W1[e][:, 128 cols] | W3[e][:, 128 cols]]
 //             H[rows, 128 cols] = bf16( SiLU(gate) * up )
 //   down:     acc[128 x 256] = H[rows, n] . W2[e][:, 256 cols]
@@ -54,11 +54,13 @@
 //               store (whole 64-byte row segments instead of 32 half-sector
 //               writes per store instruction); a warp whose 32 rows cross the
 //               end of the expert's rows stores its valid rows directly.
-// Fused expert MLP (small n, single CTA): one persistent launch runs the units
-// of both GEMMs, so that on every SM the down units' short main loops and long
-// epilogues (Z writes) overlap the gate/up units' long main loops through the
-// two TMEM accumulators, instead of the down GEMM running epilogue-bound on its
-// own. The unit sequence is a list of rounds, one unit per CTA in each, every
+//
+// Fused expert MLP (MODE kFused, single CTA, on request only): one persistent
+// launch runs the units of both GEMMs, so that on every SM the down units'
+// short main loops and long epilogues (Z writes) can overlap the gate/up units'
+// long main loops through the two TMEM accumulators. On the SonicMoE-shaped
+// layer it measured slower than the two launches: both unit kinds wait on the
+// same operand latency, which interleaving does not hide. The unit sequence is a list of rounds, one unit per CTA in each, every
 // round drawn from one GEMM, so that all CTAs run the same kind of unit at the
 // same time. A down unit reads the H tile that the n/128 gate/up units of its
 // row tile wrote; each of their epilogue warps, once its TMA stores of that tile
