@@ -75,6 +75,8 @@ def _load():
                 "oracle_forward_fixed": (None, [P, P, P, P, P, P, P, I64, I, I, I, I, I, P]),
                 "oracle_backward": (None, [P, P, P, P, P, P, P, P, I64, I, I, I, I, I,
                                            P, P, P, P, P, P]),
+                "oracle_backward_rows": (None, [P, P, P, P, P, P, P, P, P, I64, I, I, I, I, I,
+                                                P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -366,6 +368,28 @@ def forward_fixed(X, Wr, bias, W1, W3, W2, idx, renorm: bool = True) -> np.ndarr
     _load().oracle_forward_fixed(_p(X), _p(Wr), _p(bias), _p(W1), _p(W3), _p(W2), _p(idx),
                                  T, d, E, K, n, int(renorm), _p(Y))
     return Y
+
+
+def backward_rows(X, Wr, bias, W1, W3, W2, idx, perm_slot, dY, renorm: bool = True) -> dict:
+    """The backward's per-row quantities in grouped row order (perm_slot as
+    permute() gives it): dS [T*K], dA1, dA3 [T*K,n], dXg [T*K,d] and per token
+    dL [T,E], all float64 (see oracle_backward_rows in moe_oracle.c)."""
+    X, Wr, W1, W3, W2 = (_f64_input(a) for a in (X, Wr, W1, W3, W2))
+    bias = None if bias is None else _f64_input(bias)
+    idx = _c(idx, np.int32)
+    perm_slot = _c(perm_slot, np.int32)
+    dY = _c(dY, np.float64)
+    T, d = X.shape
+    E, _, n = W1.shape
+    K = idx.shape[1]
+    R = T * K
+    out = {"dS": np.empty(R), "dA1": np.empty((R, n)), "dA3": np.empty((R, n)),
+           "dXg": np.empty((R, d)), "dL": np.empty((T, E))}
+    _load().oracle_backward_rows(_p(X), _p(Wr), _p(bias), _p(W1), _p(W3), _p(W2), _p(idx),
+                                 _p(perm_slot), _p(dY), T, d, E, K, n, int(renorm),
+                                 _p(out["dS"]), _p(out["dA1"]), _p(out["dA3"]), _p(out["dXg"]),
+                                 _p(out["dL"]))
+    return out
 
 
 def backward(X, Wr, bias, W1, W3, W2, idx, dY, renorm: bool = True) -> dict:

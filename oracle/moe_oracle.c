@@ -659,3 +659,103 @@ void oracle_backward(const double *X, const double *Wr, const double *bias,
     free(a3);
     free(dh);
 }
+
+/* The backward's per-row quantities in grouped row order, for checking a
+ * backward that runs expert by expert. Row p holds slot perm_slot[p] = t*K + k
+ * (expert e = idx[t,k]); with a1 = x W1[e], a3 = x W3[e], h = silu(a1) a3 and
+ * g = dY[t] W2[e]^T (the gradient of h W2[e] taken through W2):
+ *   dS[p]    = h . g, the gradient of the routing weight w_k (dY[t] . h W2[e]);
+ *   dA1[p,:] = w_k g a3 silu'(a1) and dA3[p,:] = w_k g silu(a1);
+ *   dXg[p,:] = dA1 W1[e]^T + dA3 W3[e]^T, row p's share of dX[t];
+ * and per token dL[t,:], the gradient of the logits (the routing weights'
+ * softmax and renormalisation taken backwards from the K values dS).
+ * Then dX[t] = sum over t's rows of dXg + dL[t] Wr^T, dW1[e] = sum over e's
+ * rows of x^T dA1 (dW3 likewise) and dWr = sum_t x^T dL[t]: the outputs of
+ * oracle_backward, computed there token by token. */
+void oracle_backward_rows(const double *X, const double *Wr, const double *bias,
+                          const double *W1, const double *W3, const double *W2,
+                          const int32_t *idx, const int32_t *perm_slot, const double *dY,
+                          int64_t T, int d, int E, int K, int n, int renorm, double *dS,
+                          double *dA1, double *dA3, double *dXg, double *dL) {
+    const int64_t R = T * K;
+    double *P = (double *)malloc(sizeof(double) * (size_t)(T * E));  /* softmax per token */
+    double *g = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a1 = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a3 = (double *)malloc(sizeof(double) * (size_t)n);
+    int64_t *row_of = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+    /* routing probabilities of every token */
+    for (int64_t t = 0; t < T; ++t) {
+        double *pt = P + t * E, mx = -INFINITY, z = 0.0;
+        for (int e = 0; e < E; ++e) {
+            double l = bias ? bias[e] : 0.0;
+            for (int j = 0; j < d; ++j) l += X[t * d + j] * Wr[(int64_t)j * E + e];
+            pt[e] = l;
+            mx = l > mx ? l : mx;
+        }
+        for (int e = 0; e < E; ++e) z += (pt[e] = exp(pt[e] - mx));
+        for (int e = 0; e < E; ++e) pt[e] /= z;
+    }
+    for (int64_t p = 0; p < R; ++p) {
+        const int64_t slot = perm_slot[p], t = slot / K;
+        const int e = idx[slot];
+        row_of[slot] = p;
+        const double *x = X + t * d, *gy = dY + t * d, *pt = P + t * E;
+        double kept = 0.0;
+        for (int k = 0; k < K; ++k) kept += pt[idx[t * K + k]];
+        const double wk = renorm ? pt[e] / kept : pt[e];
+        const double *W1e = W1 + (int64_t)e * d * n, *W3e = W3 + (int64_t)e * d * n;
+        const double *W2e = W2 + (int64_t)e * n * d;
+        double ds = 0.0;
+        for (int i = 0; i < n; ++i) {
+            double u = 0.0, v = 0.0, q = 0.0;
+            for (int j = 0; j < d; ++j) {
+                u += x[j] * W1e[(int64_t)j * n + i];
+                v += x[j] * W3e[(int64_t)j * n + i];
+            }
+            for (int c = 0; c < d; ++c) q += gy[c] * W2e[(int64_t)i * d + c];
+            a1[i] = u;
+            a3[i] = v;
+            g[i] = q;
+            ds += silu(u) * v * q;
+        }
+        dS[p] = ds;
+        double *r1 = dA1 + p * n, *r3 = dA3 + p * n, *rx = dXg + p * d;
+        for (int i = 0; i < n; ++i) {
+            const double sg = 1.0 / (1.0 + exp(-a1[i]));
+            r1[i] = wk * g[i] * a3[i] * (sg + a1[i] * sg * (1.0 - sg));
+            r3[i] = wk * g[i] * a1[i] * sg;
+        }
+        for (int j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < n; ++i)
+                acc += r1[i] * W1e[(int64_t)j * n + i] + r3[i] * W3e[(int64_t)j * n + i];
+            rx[j] = acc;
+        }
+    }
+    /* logits: w_k = p_k / kept (renorm) or p_k; p = softmax(L) */
+    for (int64_t t = 0; t < T; ++t) {
+        const double *pt = P + t * E;
+        double *dl = dL + t * E;
+        double kept = 0.0, sw = 0.0;
+        for (int k = 0; k < K; ++k) kept += pt[idx[t * K + k]];
+        for (int e = 0; e < E; ++e) dl[e] = 0.0;  /* first dp, then dL in place */
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[t * K + k];
+            const double wk = renorm ? pt[e] / kept : pt[e];
+            sw += wk * dS[row_of[t * K + k]];
+        }
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[t * K + k];
+            const double s = dS[row_of[t * K + k]];
+            dl[e] += renorm ? (s - sw) / kept : s;
+        }
+        double mean = 0.0;
+        for (int e = 0; e < E; ++e) mean += pt[e] * dl[e];
+        for (int e = 0; e < E; ++e) dl[e] = pt[e] * (dl[e] - mean);
+    }
+    free(P);
+    free(g);
+    free(a1);
+    free(a3);
+    free(row_of);
+}

@@ -176,6 +176,17 @@ void oracle_backward(const double *X, const double *Wr, const double *bias,
                      const int32_t *idx, const double *dY, int64_t T, int d, int E, int K, int n,
                      int renorm, double *dX, double *dWr, double *dbias, double *dW1,
                      double *dW3, double *dW2);
+/* The same gradient's per-row quantities in grouped row order (perm_slot [T*K]
+ * as oracle_permute writes it): dS [T*K] (the routing weights' gradients),
+ * dA1, dA3 [T*K,n] (the gradients of x W1[e] and x W3[e]), dXg [T*K,d] (each
+ * row's share of dX) and dL [T,E] (the logits' gradient). Summed as the
+ * comment at its definition says, they give oracle_backward's dX, dW1, dW3,
+ * dWr and dbias. */
+void oracle_backward_rows(const double *X, const double *Wr, const double *bias,
+                          const double *W1, const double *W3, const double *W2,
+                          const int32_t *idx, const int32_t *perm_slot, const double *dY,
+                          int64_t T, int d, int E, int K, int n, int renorm, double *dS,
+                          double *dA1, double *dA3, double *dXg, double *dL);
 
 #ifdef __cplusplus
 }

@@ -100,3 +100,53 @@ def test_identical_experts_give_the_router_no_gradient(oracle_lib):
                         dY, True)
     assert np.max(np.abs(g["dWr"])) <= 1e-12 and np.max(np.abs(g["dbias"])) <= 1e-12
     assert np.max(np.abs(g["dX"])) > 1e-3
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_backward_rows_sum_to_the_backward(oracle_lib, renorm):
+    # the per-row quantities, summed per token and per expert as their definition
+    # says, give the token-by-token backward (itself pinned by finite differences)
+    inp, idx, dY = _tiny(T=7, d=6, E=4, K=3, n=5, seed=3)
+    T, d = inp["X"].shape
+    E, _, n = inp["W1"].shape
+    K = idx.shape[1]
+    off, pt, ps, ros = oracle.permute(idx, E)
+    r = oracle.backward_rows(inp["X"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"],
+                             idx, ps, dY, renorm)
+    g = oracle.backward(inp["X"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], idx,
+                        dY, renorm)
+    dX = r["dL"] @ inp["Wr"].T
+    dW1 = np.zeros_like(g["dW1"])
+    dW3 = np.zeros_like(g["dW3"])
+    for p in range(T * K):
+        t, e = pt[p], idx.ravel()[ps[p]]
+        assert ps[p] // K == t
+        dX[t] += r["dXg"][p]
+        dW1[e] += np.outer(inp["X"][t], r["dA1"][p])
+        dW3[e] += np.outer(inp["X"][t], r["dA3"][p])
+    # rows of one expert are contiguous in the grouped order
+    for e in range(E):
+        assert np.all(idx.ravel()[ps[off[e]:off[e + 1]]] == e)
+    for name, got in (("dX", dX), ("dW1", dW1), ("dW3", dW3), ("dWr", inp["X"].T @ r["dL"]),
+                      ("dbias", r["dL"].sum(axis=0))):
+        want = g[name]
+        assert np.max(np.abs(got - want)) <= 1e-12 * max(1.0, np.max(np.abs(want))), name
+
+
+def test_backward_rows_weight_gradient_is_output_dot_dy(oracle_lib):
+    # dS of row (t, k) is dY[t] . o with o = (silu(x W1) * (x W3)) W2 of expert
+    # idx[t, k], the routed output before its weight
+    inp, idx, dY = _tiny(T=5, d=6, E=4, K=2, n=5, seed=7)
+    T, _ = inp["X"].shape
+    E = inp["W1"].shape[0]
+    K = idx.shape[1]
+    _, pt, ps, _ = oracle.permute(idx, E)
+    r = oracle.backward_rows(inp["X"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"],
+                             idx, ps, dY, True)
+    x_t = torch.tensor(inp["X"], dtype=torch.float64)
+    for p in range(T * K):
+        t, e = int(pt[p]), int(idx.ravel()[ps[p]])
+        a1 = x_t[t] @ torch.tensor(inp["W1"][e])
+        a3 = x_t[t] @ torch.tensor(inp["W3"][e])
+        o = (torch.nn.functional.silu(a1) * a3) @ torch.tensor(inp["W2"][e])
+        assert abs(float(o @ torch.tensor(dY[t])) - r["dS"][p]) <= 1e-12 * max(1.0, abs(r["dS"][p]))

@@ -60,6 +60,12 @@ MUTATIONS = [
     # backward
     ("bwd_silu_derivative", "s * (1.0 + a1[i] * (1.0 - s))", "s * (1.0 + a1[i] * s)"),
     ("bwd_dh_unweighted", "dh[i] = w[k] * gw;", "dh[i] = gw;"),
+    # backward, per row
+    ("bwd_rows_ds_drops_a3", "ds += silu(u) * v * q;", "ds += silu(u) * q;"),
+    ("bwd_rows_dxg_w3_for_w1", "acc += r1[i] * W1e[(int64_t)j * n + i] + r3[i] * W3e",
+     "acc += r1[i] * W3e[(int64_t)j * n + i] + r3[i] * W3e"),
+    ("bwd_rows_renorm_mean_dropped", "dl[e] += renorm ? (s - sw) / kept : s;",
+     "dl[e] += renorm ? s / kept : s;"),
     ("bwd_dw2_unweighted", "+= h * w[k] * g[c];", "+= h * g[c];"),
     ("bwd_router_renorm_term_dropped", "(dw[k] - wdw) / kept", "dw[k] / kept"),
     ("bwd_dx_through_w1_twice", "da3 * W3e[(int64_t)j * n + i]", "da3 * W1e[(int64_t)j * n + i]"),
