@@ -499,6 +499,41 @@ def run_router_only(args, world, rank, local):
         us = a.elapsed_time(b) * 1e3 / args.steps
         nbytes = T * synth.ROUTER_E * 4 + T * synth.ROUTER_K * 8 + synth.ROUTER_E * 4
         per_t[T] = {"us": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 2)}
+    # Supplementary sweep (not the metric): the same call at 2^20 .. 2^23 tokens,
+    # where the traffic is large enough to compare with HBM bandwidth. Logits of
+    # 2^22 tokens and more exceed L2; the smaller ones may partly stay in it.
+    peaks = load_peaks()
+    sweep = {}
+    for T in (1 << 20, 1 << 21, 1 << 22, 1 << 23):
+        K, E = synth.ROUTER_K, synth.ROUTER_E
+        logits = synth.router_logits_input(T, device="cuda")
+        idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        ptrs = [ctypes.c_void_p(t.data_ptr()) for t in (logits, idx, w, counts)]
+
+        def call_big(st, T=T, ptrs=ptrs):
+            rc = lib.moe_route_logits(ptrs[0], T, E, K, 1, ptrs[1], ptrs[2], ptrs[3],
+                                      ctypes.c_void_p(st.cuda_stream))
+            if rc != 0:
+                raise moe.MoeError("moe_route_logits", rc)
+
+        reps = 20
+        for _ in range(3):
+            call_big(stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            call_big(stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        nbytes = T * E * 4 + T * K * 8 + E * 4
+        sweep[T] = {"us": round(us, 2), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                    "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm"], 3),
+                    "bytes": nbytes}
+        del logits, idx, w, counts
     total_tokens = sum(synth.ROUTER_T)
     total_us = sum(v["us"] for v in per_t.values())
     if rank == 0:
@@ -510,7 +545,12 @@ def run_router_only(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "router-only logits [T,8] fp32, K=2, T in 256..2048"},
             "gpu_launches": len(synth.ROUTER_T) * args.steps,
-            "extra": {"per_T": per_t}}), flush=True)
+            "extra": {"per_T": per_t,
+                      "supplementary_sweep": {"note": "same call at large T, direct calls "
+                                              "(memset + one kernel each); logits exceed L2 "
+                                              "from T = 2^22; HBM peak " + peaks["source"],
+                                              "hbm_peak_GBps": peaks["hbm"], "per_T": sweep}}}),
+              flush=True)
 
 
 def main(argv=None):

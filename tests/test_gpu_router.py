@@ -40,6 +40,22 @@ def test_route_logits_router_only_workload(T, renorm):
     _check_routing(idx, w, counts, idx_r, w_r, synth.ROUTER_E)
 
 
+@pytest.mark.parametrize("T,E,K", [(2049, 8, 2), (70000, 8, 2), (5000, 16, 4), (3001, 5, 3),
+                                   (1 << 20, 8, 2)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_logits_many_blocks_thread_per_token(T, E, K, renorm):
+    # E <= 16 above 2048 tokens: one thread per token over many blocks, with ties
+    # and signed zeros mixed in
+    logits = synth.router_logits_input(T, E=E, seed=T)
+    logits[::5] = torch.round(logits[::5])   # exact ties
+    logits[1::97] = 0.0
+    logits[2::97] = -0.0
+    idx_r, w_r = oracle.topk_softmax(logits.numpy(), K, renorm)
+    idx, w, counts = moe.moe_route_logits(logits.cuda(), K, renorm)
+    torch.cuda.synchronize()
+    _check_routing(idx, w, counts, idx_r, w_r, E)
+
+
 @pytest.mark.parametrize("E,K", [(8, 1), (8, 8), (5, 2), (64, 6), (128, 4), (256, 8), (200, 3)])
 def test_route_logits_ties_and_extremes(E, K):
     g = torch.Generator().manual_seed(E * 31 + K)

@@ -700,25 +700,29 @@ select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
         if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
 }
 
-// Small E and T <= 2048: one thread per token and a single block, which zeroes
-// and writes the counts itself (no memset, one launch; above 2048 tokens the
-// warp-per-token kernel is faster, its counts zeroed before the logits kernel). Softmax statistics in the thread: the
-// maximum, then a compensated (Kahan) sum of exp(L - max) for the full
-// denominator; top-K by K passes (higher score wins, equal scores: lower index).
+// E <= 16: one thread per token. With T <= 2048 a single block zeroes and
+// writes the counts itself (no memset, one launch); above that, blocks of 256
+// threads add their histograms into counts zeroed before the logits kernel.
+// Softmax statistics in the thread: the maximum, then a compensated (Kahan) sum
+// of exp(L - max) for the full denominator; top-K by K passes (higher score
+// wins, equal scores: lower index).
 constexpr int kSelSingleThreads = 1024;
 constexpr int kSelSingleMaxT = 2048;
+constexpr int kSelThreadBlock = 256;
 
-template <int EP>
-__global__ void __launch_bounds__(kSelSingleThreads)
-select_single_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
+template <int EP, bool SINGLE>
+__global__ void __launch_bounds__(SINGLE ? kSelSingleThreads : kSelThreadBlock)
+select_thread_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
                      int32_t *__restrict__ idx_out, float *__restrict__ w_out,
                      int32_t *__restrict__ counts) {
     pdl_wait();
     pdl_trigger();
     __shared__ int hist[EP];
-    for (int e = threadIdx.x; e < EP; e += kSelSingleThreads) hist[e] = 0;
+    for (int e = threadIdx.x; e < EP; e += blockDim.x) hist[e] = 0;
     __syncthreads();
-    for (int64_t t = threadIdx.x; t < T; t += kSelSingleThreads) {
+    const int64_t t0 = SINGLE ? threadIdx.x : (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t tstep = SINGLE ? blockDim.x : T;  // multi-block: one token per thread
+    for (int64_t t = t0; t < T; t += tstep) {
         float v[EP];
 #pragma unroll
         for (int e = 0; e < EP; ++e) v[e] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
@@ -769,7 +773,10 @@ select_single_kernel(const float *__restrict__ logits, int T, int E, int K, int 
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kSelSingleThreads) counts[e] = hist[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (SINGLE) counts[e] = hist[e];
+        else if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
+    }
 }
 
 // The single-block select writes the counts itself; the multi-block one adds
@@ -781,13 +788,19 @@ bool select_needs_zero_counts(int T, int E) { return !(E <= 16 && T <= kSelSingl
 cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, int32_t *idx,
                           float *w, int32_t *counts, bool counts_zeroed, cudaStream_t s) {
     if (!select_needs_zero_counts(T, E)) {
-        auto kern = E <= 8 ? select_single_kernel<8> : select_single_kernel<16>;
+        auto kern = E <= 8 ? select_thread_kernel<8, true> : select_thread_kernel<16, true>;
         return launch_k(kern, dim3(1), dim3(kSelSingleThreads), 0, s, logits, T, E, K, renorm, idx,
                         w, counts);
     }
     if (!counts_zeroed) {
         cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
         if (e != cudaSuccess) return e;
+    }
+    if (E <= 16) {
+        auto kern = E <= 8 ? select_thread_kernel<8, false> : select_thread_kernel<16, false>;
+        const unsigned blocks = (unsigned)((T + kSelThreadBlock - 1) / kSelThreadBlock);
+        return launch_k(kern, dim3(blocks), dim3(kSelThreadBlock), 0, s, logits, T, E, K, renorm,
+                        idx, w, counts);
     }
     const unsigned blocks = (unsigned)((T + kSelThreads / 32 - 1) / (kSelThreads / 32));
     auto kern = E <= 32    ? select_kernel<1>
