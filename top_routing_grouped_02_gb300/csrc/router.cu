@@ -705,12 +705,13 @@ select_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
 // threads add their histograms into counts zeroed before the logits kernel.
 // Softmax statistics in the thread: the maximum, then a compensated (Kahan) sum
 // of exp(L - max) for the full denominator; top-K by K passes (higher score
-// wins, equal scores: lower index).
+// wins, equal scores: lower index). VEC (E == EP, logits 16-byte aligned): a
+// token's logits arrive as EP/4 128-bit loads.
 constexpr int kSelSingleThreads = 1024;
 constexpr int kSelSingleMaxT = 2048;
 constexpr int kSelThreadBlock = 256;
 
-template <int EP, bool SINGLE>
+template <int EP, bool SINGLE, bool VEC>
 __global__ void __launch_bounds__(SINGLE ? kSelSingleThreads : kSelThreadBlock)
 select_thread_kernel(const float *__restrict__ logits, int T, int E, int K, int renorm,
                      int32_t *__restrict__ idx_out, float *__restrict__ w_out,
@@ -724,8 +725,20 @@ select_thread_kernel(const float *__restrict__ logits, int T, int E, int K, int 
     const int64_t tstep = SINGLE ? blockDim.x : T;  // multi-block: one token per thread
     for (int64_t t = t0; t < T; t += tstep) {
         float v[EP];
+        if constexpr (VEC) {
+            const float4 *src = reinterpret_cast<const float4 *>(logits + t * EP);
 #pragma unroll
-        for (int e = 0; e < EP; ++e) v[e] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
+            for (int q = 0; q < EP / 4; ++q) {
+                const float4 f = __ldg(src + q);
+                v[4 * q] = f.x;
+                v[4 * q + 1] = f.y;
+                v[4 * q + 2] = f.z;
+                v[4 * q + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EP; ++e) v[e] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
+        }
         float m = v[0];
 #pragma unroll
         for (int e = 1; e < EP; ++e) m = fmaxf(m, v[e]);
@@ -787,8 +800,12 @@ bool select_needs_zero_counts(int T, int E) { return !(E <= 16 && T <= kSelSingl
 // that no memset sits between the logits and select kernels).
 cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, int32_t *idx,
                           float *w, int32_t *counts, bool counts_zeroed, cudaStream_t s) {
+    const bool vec = (E == 8 || E == 16) && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
     if (!select_needs_zero_counts(T, E)) {
-        auto kern = E <= 8 ? select_thread_kernel<8, true> : select_thread_kernel<16, true>;
+        auto kern = E <= 8 ? (vec ? select_thread_kernel<8, true, true>
+                                  : select_thread_kernel<8, true, false>)
+                           : (vec ? select_thread_kernel<16, true, true>
+                                  : select_thread_kernel<16, true, false>);
         return launch_k(kern, dim3(1), dim3(kSelSingleThreads), 0, s, logits, T, E, K, renorm, idx,
                         w, counts);
     }
@@ -797,7 +814,10 @@ cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, 
         if (e != cudaSuccess) return e;
     }
     if (E <= 16) {
-        auto kern = E <= 8 ? select_thread_kernel<8, false> : select_thread_kernel<16, false>;
+        auto kern = E <= 8 ? (vec ? select_thread_kernel<8, false, true>
+                                  : select_thread_kernel<8, false, false>)
+                           : (vec ? select_thread_kernel<16, false, true>
+                                  : select_thread_kernel<16, false, false>);
         const unsigned blocks = (unsigned)((T + kSelThreadBlock - 1) / kSelThreadBlock);
         return launch_k(kern, dim3(blocks), dim3(kSelThreadBlock), 0, s, logits, T, E, K, renorm,
                         idx, w, counts);
