@@ -105,6 +105,23 @@ FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails va
                              None, FAKE, 1 << 30, None), 1),
     (lambda L: L.moe_workspace_init(None, 64, None), 1),
     (lambda L: L.moe_sync_check(None, None, None), 1),
+    # both expert GEMMs (two launches or one fused): null W2, unsupported d,
+    # unaligned Z, workspace too small for the counter words
+    (lambda L: L.moe_expert_mlp(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 16, 256, 8, 2, 128,
+                                FAKE, FAKE, FAKE, 1 << 30, None), 1),
+    (lambda L: L.moe_expert_mlp(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 200, 8, 2, 128,
+                                FAKE, FAKE, FAKE, 1 << 30, None), 2),
+    (lambda L: L.moe_expert_mlp(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 256, 8, 2, 128,
+                                FAKE, ctypes.c_void_p((1 << 20) + 8), FAKE, 1 << 30, None), 1),
+    (lambda L: L.moe_expert_mlp(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 256, 8, 2, 128,
+                                FAKE, FAKE, FAKE, 4096, None), 3),
+    # Token Rounding entry points
+    (lambda L: L.moe_forward_rounded(FAKE, FAKE, None, FAKE, FAKE, FAKE, 16, 256, 8, 2, 128, 2,
+                                     FAKE, None, FAKE, 1 << 30, None), 1),
+    (lambda L: L.moe_forward_rounded(FAKE, FAKE, None, FAKE, FAKE, FAKE, 16, 256, 8, 2, 128, 1,
+                                     FAKE, None, FAKE, 1024, None), 3),
+    (lambda L: L.moe_combine_rows(None, FAKE, 16, 8, 64, 32, FAKE, None), 1),
+    (lambda L: L.moe_combine_rows(FAKE, FAKE, 16, 8, 64, -1, FAKE, None), 1),
 ])
 def test_bad_arguments_are_rejected_on_the_host(lib, call, expect):
     assert call(lib) == expect
