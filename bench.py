@@ -19,7 +19,9 @@ Prints ONE JSON line on rank 0:
   cpu_baseline  the CPU oracle on a bounded token sample (rank 0, N=1 only)
   clocks      nvidia-smi SM clocks / throttle reasons sampled during the timed region
   extra       tokens/s, per-stage times (from the second region), router and combine
-              GB/s, % of peak, routing statistics (tile padding, rows per expert)
+              GB/s, % of peak, routing statistics (tile padding, rows per expert), and
+              `sustained`: back-to-back forwards over about 2 s against the sustained
+              bf16 peak (the K-step `value` is a burst figure)
 
 --routing rounded runs the layer under Token Rounding (moe_forward_rounded: each
 expert's top-K count rounded to a multiple of the 128-row tile); its value
@@ -332,6 +334,37 @@ def run_gpu(args, c, world, rank, local):
     flops = 2.0 * R * 3 * d * n
     value = aggregate(flops * args.steps, ms_max / 1e3, world) / 1e12
 
+    # Sustained region: back-to-back forwards for about --sustained-seconds, long
+    # enough for the power cap to settle, against the sustained bf16 peak (the
+    # K-step `value` above is a burst figure for the short window it times).
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = max(args.steps, int(math.ceil(args.sustained_seconds * 1e3 / ms_step)))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk_sus:
+            barrier(world)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(n_sus):
+                step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            barrier(world)
+        st, word = moe.moe_sync_check(ws)
+        if st != 0:
+            raise RuntimeError(f"device error word {word:#x} in the sustained region")
+        ms_sus = max_over_ranks(a.elapsed_time(b), world)
+        sus_value = aggregate(flops * n_sus, ms_sus / 1e3, world) / 1e12
+        sus_peak = load_peaks()["bf16_sustained"]
+        csum = clk_sus.summary()
+        sustained = {"steps": n_sus, "seconds": round(ms_sus / 1e3, 3),
+                     "ms_per_step": round(ms_sus / n_sus, 4), "value": round(sus_value, 3),
+                     "unit": "TFLOP/s", "peak_sustained": sus_peak,
+                     "frac_of_sustained_peak": None if not sus_peak
+                     else round(sus_value / world / sus_peak, 4),
+                     "clocks": {k: csum.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons",
+                                                         "power_w_max")}}
+
     # end to end from pinned host memory: every step copies its batch in and its
     # output out. Top-K routing goes through moe_forward_host_stream, which
     # overlaps the copies of neighbouring batches with the layer.
@@ -439,6 +472,7 @@ def run_gpu(args, c, world, rank, local):
             "combine_GBps": round(combine_bytes / (stage_ms["combine"] / 1e3) / 1e9, 1),
             "hbm_peak_GBps": peaks["hbm"], "clock_samples": clocks.get("samples"),
             "power_w_max": clocks.get("power_w_max"),
+            "sustained": sustained,
         },
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not rounded:
@@ -566,6 +600,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of the sustained region reported in extra.sustained (0: skip)")
     ap.add_argument("--graph", action="store_true",
                     help="time one CUDA graph of the K steps instead of direct calls")
     args = ap.parse_args(argv)

@@ -18,7 +18,8 @@
  *   - Pointers are DEVICE pointers unless a parameter says "host". The caller
  *     owns every buffer, including the workspace; the library allocates no
  *     device memory and keeps no state besides a per-device cache of the SM
- *     count and architecture check.
+ *     count and architecture check (and the built-in scratch array of
+ *     moe_permute_noalloc, below).
  *   - bf16 data travels as raw 16-bit patterns (moe_bf16). Matrices are dense
  *     and row-major. Integer outputs are int32.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
@@ -79,6 +80,7 @@ typedef enum {
 #define MOE_DEVERR_TIMEOUT      0x1u  /* a pipeline wait gave up after its time limit */
 #define MOE_DEVERR_BAD_EXPERT   0x2u  /* a top-K index outside [0, E) was skipped */
 #define MOE_DEVERR_COUNT_MISMATCH 0x4u /* counts[] disagreed with the recount of topk_idx */
+#define MOE_DEVERR_REPEATED_EXPERT 0x8u /* a token listed one expert twice; the repeat was skipped */
 
 /* Human-readable name of a status code (static string). */
 const char *moe_status_string(int status);
@@ -126,12 +128,16 @@ moe_status_t moe_route_logits(const float *logits, int T, int E, int K, int reno
 
 /* Group the routed slots by expert (SonicMoE page §1 Gather, §2.2 grouping by
  * expert, §3.1 per-expert counts; SpMM page §2 CSR row offsets).
- *   topk_idx [T,K] int32; counts [E] int32 or NULL (when given it is checked
- *   against a recount on the device; a mismatch sets MOE_DEVERR_COUNT_MISMATCH).
+ *   topk_idx [T,K] int32, each row K distinct experts (as the router writes
+ *   it); counts [E] int32 or NULL (when given it is checked against a recount
+ *   on the device; a mismatch sets MOE_DEVERR_COUNT_MISMATCH).
  * Outputs: offsets [E+1]; rows of expert e are offsets[e]..offsets[e+1]-1 in
  *   ascending token order; perm_token [T*K] (token of each grouped row),
  *   perm_slot [T*K] (t*K+k of each row), row_of_slot [T*K] (inverse of
- *   perm_slot; -1 for a slot whose index was out of range);
+ *   perm_slot; -1 for a slot whose index was out of range, which sets
+ *   MOE_DEVERR_BAD_EXPERT, or repeats an expert listed earlier in its token's
+ *   row, which sets MOE_DEVERR_REPEATED_EXPERT; such slots get no row and the
+ *   rows in use end at offsets[E] < T*K);
  *   tiles [(T*K)/128 + E][4] int32 = {expert, first row, rows<=128, 0}, expert
  *   order, and num_tiles [1] (tile_base[E]). ws: workspace of this shape. */
 moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts,
@@ -145,23 +151,27 @@ moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts,
  * and outputs and may not call cudaMalloc, e.g. a plugin inside an inference
  * engine that owns all device memory, or a serving loop whose memory was
  * planned at start-up (cudaMalloc can synchronise the device and can fail once
- * memory is fragmented). Same arguments, outputs and device checks as
- * moe_permute, without the workspace: the grouping scratch is a 4 MiB array
- * built into libmoe.so (every GPU that loads the library holds it until the
- * process exits). The call allocates nothing.
+ * memory is fragmented). Same arguments and outputs as moe_permute, without
+ * the workspace: the grouping scratch is a 4 MiB array built into libmoe.so
+ * (every GPU that loads the library holds it until the process exits). The
+ * call allocates nothing.
  *   - Limit: the shape's grouping scratch, moe_workspace_bytes(T, 0, E, K, 0)
  *     (about 24*T*K + 4*E*ceil(T/32) bytes), must fit in 4 MiB, i.e. T*K up to
  *     about 150000 slots; larger shapes return MOE_ERR_UNSUPPORTED_SHAPE before
  *     anything is enqueued.
- *   - The first call on each device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *   - The first call on each device (in each CUDA context) looks up the
+ *     array's device address with that device current and keeps it for later
+ *     calls in the same context. Under lazy module loading (the CUDA default)
+ *     that first lookup also loads this part of the library onto the device,
+ *     array included: it may need 4 MiB of free device memory and may
+ *     synchronise the device. Make the first call once at start-up, before any
+ *     stream capture, or run with CUDA_MODULE_LOADING=EAGER.
  *   - Every call shares the one array and it keeps the last call's contents;
  *     the call clears what has to start at zero. Calls whose work overlaps on
  *     the GPU (other streams, other threads) race on the array: serialise them.
- *   - The device error word of these calls lives in the array and is not
- *     reported through moe_sync_check; bad expert indices still show up as
- *     row_of_slot == -1. */
+ *   - The device error word of these calls lives in the array and is never
+ *     read back, so passing counts checks nothing here. A slot whose expert is
+ *     out of range or repeated still shows up as row_of_slot == -1. */
 moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const int32_t *counts,
                                  int T, int E, int K,
                                  int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,

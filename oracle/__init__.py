@@ -136,6 +136,41 @@ def topk_softmax(L: np.ndarray, K: int, renorm: bool = True):
     return idx, w
 
 
+def near_ties(X: np.ndarray, Wr: np.ndarray, bias: np.ndarray | None, K: int,
+               tol: float = 1e-5, L32: np.ndarray | None = None) -> dict:
+    """How many routing decisions of a workload sit on a near-tie (a report:
+    nothing fails).
+
+    The float64 logits X Wr (+ bias) come from one library matrix product. A
+    token is a near-tie when its K-th and (K+1)-th largest float64 logits lie
+    within `tol` of each other: its top-K set can then depend on the rounding
+    of the fp32 logits, i.e. on the fixed summation order of the router's fp32
+    definition (router_logits). The report also counts the tokens whose top-K
+    set under that fp32 definition (L32, computed when not given) differs from
+    the float64 one. X uint16 (bf16) [T,d]."""
+    Xf = bf16_bits_to_f64(_c(X, np.uint16))
+    L64 = Xf @ _c(Wr, np.float32).astype(np.float64)
+    if bias is not None:
+        L64 = L64 + _c(bias, np.float32).astype(np.float64)
+    T, E = L64.shape
+    if L32 is None:
+        L32 = router_logits(X, Wr, bias)
+    idx32, _ = topk_softmax(L32, K, True)
+    # float64 top-K set: sort by (-score, expert), the same tie rule
+    order = np.lexsort((np.broadcast_to(np.arange(E), (T, E)), -L64), axis=1)
+    set64 = np.sort(order[:, :K], axis=1)
+    differs = int(np.sum(np.any(np.sort(idx32, axis=1) != set64, axis=1)))
+    if K < E:
+        srt = -np.sort(-L64, axis=1)
+        gap = srt[:, K - 1] - srt[:, K]
+        n_ties = int(np.sum(gap < tol))
+        min_gap = float(gap.min())
+    else:
+        n_ties, min_gap = 0, float("inf")
+    return dict(tokens=T, near_ties=n_ties, tol=tol, min_gap=min_gap,
+                fp32_topk_differs_from_f64=differs)
+
+
 def expert_counts(idx: np.ndarray, E: int) -> np.ndarray:
     idx = _c(idx, np.int32)
     T, K = idx.shape

@@ -1,11 +1,15 @@
 """Whole-layer parity on the GPU for every workload, through the C-ABI.
 
-The step-by-step entry points are checked against the oracle at full size
-(routing, grouping bit-exact; H, Z, Y within tolerance where the oracle can run
-the whole layer in seconds, on sampled tokens otherwise), and moe_forward in
-the configuration the benchmark times must reproduce the step-by-step Y bit for
-bit. Y[t] depends only on X[t] and the weights, so sampled tokens are checked
-against the oracle's token-by-token definition.
+The step-by-step entry points are checked against the oracle at full size:
+routing and grouping bit-exact on every workload; H, Z and Y in full on the
+tiny, SonicMoE- and Mixtral-shaped layers (the Mixtral shape is the benchmarked
+one); on the DeepSeek-V3-shaped layer H and Z on rows of every 128-row tile of
+every expert (its first and last row and two more) and Y on at least 1024
+tokens chosen so that every tile holds a checked row. moe_forward, in the
+configuration the benchmark times, must reproduce the step-by-step result bit
+for bit. Y[t] depends only on X[t] and the weights, and H and Z rows only on
+their token and expert, so checking a subset against the oracle's definition
+on that subset is exact.
 """
 import numpy as np
 import pytest
@@ -17,8 +21,10 @@ from top_routing_grouped_02_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
 
-# tokens the oracle evaluates one by one on the large workloads
-SAMPLE = 48
+# DeepSeek-V3 shape: rows checked per 128-row tile and the least number of
+# tokens whose Y is checked
+ROWS_PER_TILE = 4
+MIN_TOKENS = 1024
 
 
 def _steps(inp, K):
@@ -62,6 +68,35 @@ def _check_grouping(s, idx_r, E):
     return off_r, pt_r, ps_r, ros_r
 
 
+def tile_rows(off, per_tile, rng):
+    """Sorted grouped rows with, from every 128-row tile of every expert, its
+    first and last row and per_tile - 2 more drawn at random."""
+    rows = []
+    M = moe.TILE_M
+    for e in range(len(off) - 1):
+        for r0 in range(int(off[e]), int(off[e + 1]), M):
+            r1 = min(r0 + M, int(off[e + 1]))
+            pick = {r0, r1 - 1}
+            inner = np.arange(r0 + 1, r1 - 1)
+            if inner.size:
+                pick.update(rng.choice(inner, size=min(per_tile - 2, inner.size),
+                                       replace=False).tolist())
+            rows.extend(pick)
+    return np.array(sorted(rows), np.int64)
+
+
+def oracle_rows(X, W1, W3, W2, w_r, pt, ps, off, P):
+    """Oracle H (bf16 bits) and Z (float64) of the grouped rows P (sorted):
+    the same definition run on a grouping that holds only those rows."""
+    E = len(off) - 1
+    e_of = np.searchsorted(off, P, side="right") - 1
+    off_sub = np.zeros(E + 1, np.int32)
+    off_sub[1:] = np.cumsum(np.bincount(e_of, minlength=E))
+    H = oracle.gate_up(X, W1, W3, pt[P], off_sub)
+    Z = oracle.down(H, W2, w_r, ps[P], off_sub)
+    return H, Z
+
+
 def _run_workload(name, full_oracle: bool):
     cfg = synth.WORKLOADS[name]
     T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
@@ -87,12 +122,30 @@ def _run_workload(name, full_oracle: bool):
         check_hz(bits(s["Z"]), Z_ref, "Z")
         Y_ref = oracle.combine(Z_ref, ros_r, K)
         check_y(bits(s["Y"]), Y_ref, "Y")
+        return
     rng = np.random.default_rng(12345)
-    toks = np.sort(rng.choice(T, size=min(SAMPLE, T), replace=False))
-    toks[0], toks[-1] = 0, T - 1
+    # H and Z on rows of every tile
+    P = tile_rows(off_r, ROWS_PER_TILE, rng)
+    H_ref, Z_ref = oracle_rows(X, W1, W3, W2, w_r, pt_r, ps_r, off_r, P)
+    Pt = torch.from_numpy(P).cuda()
+    check_hz(bits(s["H"][Pt]), H_ref, "H (rows of every tile)")
+    check_hz(bits(s["Z"][Pt]), Z_ref, "Z (rows of every tile)")
+    # Y on the token of one row of every tile, topped up to MIN_TOKENS tokens
+    mid = [int(pt_r[(r0 + min(r0 + moe.TILE_M, int(off_r[e + 1]))) // 2])
+           for e in range(E) for r0 in range(int(off_r[e]), int(off_r[e + 1]), moe.TILE_M)]
+    toks = set(mid) | {0, T - 1}
+    rest = np.setdiff1d(np.arange(T), np.fromiter(toks, np.int64))
+    extra = max(0, MIN_TOKENS - len(toks))
+    toks.update(rng.choice(rest, size=min(extra, rest.size), replace=False).tolist())
+    toks = np.array(sorted(toks), np.int64)
+    assert len(toks) >= min(MIN_TOKENS, T)
+    covered = np.isin(pt_r, toks)
+    for e in range(E):
+        for r0 in range(int(off_r[e]), int(off_r[e + 1]), moe.TILE_M):
+            assert covered[r0:min(r0 + moe.TILE_M, int(off_r[e + 1]))].any()
     Y_rows, idx_rows, w_rows = oracle.forward_tokens(X, Wr, bias, W1, W3, W2, K, toks)
     assert np.array_equal(idx_rows, idx_r[toks])
-    check_y(bits(s["Y"])[toks], Y_rows, "Y (sampled tokens)")
+    check_y(bits(s["Y"])[toks], Y_rows, "Y (tokens covering every tile)")
 
 
 def test_tiny_workload():
@@ -104,7 +157,8 @@ def test_sonic_workload():
 
 
 def test_mixtral_workload():
-    _run_workload("mixtral", full_oracle=False)
+    # the benchmarked configuration: H, Z and Y of all 8192 rows / 4096 tokens
+    _run_workload("mixtral", full_oracle=True)
 
 
 def test_dsv3_workload():

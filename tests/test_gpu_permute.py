@@ -79,3 +79,36 @@ def test_permute_flags_bad_expert_and_count_mismatch():
     assert int(out["offsets"][-1]) == T * K - 1
     status, word = moe.moe_sync_check(ws)                # cleared by the previous read
     assert status == 0 and word == 0
+
+
+def test_permute_skips_and_flags_a_repeated_expert():
+    # Each top-K row names K distinct experts. A row that repeats an expert
+    # would give both slots one rank (one bit per token and expert), so the
+    # repeat is skipped (row_of_slot -1) and flagged. The rest must equal the
+    # oracle's grouping with the repeated slot sent to an extra last expert,
+    # which takes no row before offsets[E].
+    T, E, K = 200, 8, 3
+    idx = _routing(T, E, K, seed=11)
+    idx[7] = [3, 3, 5]                                   # slot 7*K+1 repeats expert 3
+    idx[40] = [6, 1, 6]                                  # slot 40*K+2 repeats expert 6
+    rep = [7 * K + 1, 40 * K + 2]
+    ws = moe.workspace(T, 0, E, K, 0)
+    out = moe.moe_permute(torch.from_numpy(idx).cuda(), E, ws=ws)
+    status, word = moe.moe_sync_check(ws)
+    assert status == 7 and (word & 0x8) and not (word & 0x2), word
+    ref_idx = idx.copy().reshape(-1)
+    ref_idx[rep] = E
+    off_r, pt_r, ps_r, ros_r = oracle.permute(ref_idx.reshape(T, K), E + 1)
+    used = int(off_r[E])
+    assert used == T * K - len(rep)
+    assert np.array_equal(out["offsets"].cpu().numpy(), off_r[:E + 1])
+    assert np.array_equal(out["perm_token"].cpu().numpy()[:used], pt_r[:used])
+    assert np.array_equal(out["perm_slot"].cpu().numpy()[:used], ps_r[:used])
+    ros = out["row_of_slot"].cpu().numpy()
+    assert np.all(ros[rep] == -1)
+    keep = np.setdiff1d(np.arange(T * K), rep)
+    assert np.array_equal(ros[keep], ros_r[keep])
+    tiles_r = oracle.tile_schedule(off_r[:E + 1], moe.TILE_M)
+    nt = int(out["num_tiles"].item())
+    assert nt == len(tiles_r)
+    assert np.array_equal(out["tiles"].cpu().numpy()[:nt], tiles_r)

@@ -36,14 +36,6 @@ const DeviceInfo *device_info() {
     return &di;
 }
 
-moe_status_t check_arch() {
-    // a failed call made by someone else earlier must not be reported as ours
-    (void)cudaGetLastError();
-    const DeviceInfo *di = device_info();
-    if (di == nullptr) return MOE_ERR_CUDA;
-    return di->arch_ok ? MOE_OK : MOE_ERR_ARCH;
-}
-
 moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Router-level shape rules.
@@ -84,6 +76,14 @@ T *at(void *ws, size_t off) {
 }
 
 }  // namespace
+
+moe_status_t check_arch() {
+    // a failed call made by someone else earlier must not be reported as ours
+    (void)cudaGetLastError();
+    const DeviceInfo *di = device_info();
+    if (di == nullptr) return MOE_ERR_CUDA;
+    return di->arch_ok ? MOE_OK : MOE_ERR_ARCH;
+}
 
 bool pdl_enabled() {
     static const bool on = [] {

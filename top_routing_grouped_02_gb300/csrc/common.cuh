@@ -166,5 +166,9 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// MOE_OK when the current device is sm_103 (cached per device), MOE_ERR_ARCH
+// otherwise, MOE_ERR_CUDA when the device cannot be queried. Clears a CUDA error
+// left pending by an earlier, unrelated call first.
+moe_status_t check_arch();
 
 }  // namespace moe

@@ -9,6 +9,8 @@
 // fragmented, so such loops forbid it).
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -20,31 +22,65 @@ constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
 
 static __device__ __align__(256) unsigned char g_permute_scratch[kNoAllocScratchBytes];
 
-// Device address of g_permute_scratch, looked up once per device. In host code
-// the symbol is only a host-side stand-in, so the kernels must be given this.
-void *g_scratch_addr[64] = {};
+// Device address of g_permute_scratch per device, looked up with that device
+// current. In host code the symbol is only a host-side stand-in, so the kernels
+// must be given this address. The address belongs to the CUDA context it was
+// looked up in: each entry remembers that context's unique id (never reused,
+// unlike a context handle), so after cudaDeviceReset or under another context
+// the lookup runs again instead of handing out a stale address. A mutex per
+// device serialises host threads.
+struct ScratchSlot {
+    std::mutex m;
+    unsigned long long ctx_id = 0;
+    void *addr = nullptr;
+};
+ScratchSlot g_slots[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the context current on this thread; false when there is none
+// yet (or the driver cannot say).
+bool current_context_id(unsigned long long *id) {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 moe_status_t scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
-            return MOE_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+    ScratchSlot &slot = g_slots[dev];
+    std::lock_guard<std::mutex> lock(slot.m);
+    unsigned long long id = 0;
+    bool known = current_context_id(&id);
+    if (known && slot.addr != nullptr && slot.ctx_id == id) {
+        *out = slot.addr;
+        return MOE_OK;
     }
-    *out = g_scratch_addr[dev];
-    return MOE_OK;
-}
-
-moe_status_t current_device_is_sm103() {
-    (void)cudaGetLastError();
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    // first use in this context: the lookup also loads this part of the library
+    // (and its array) onto the device under lazy module loading
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
         return MOE_ERR_CUDA;
-    return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_ARCH;
+    if (!known) known = current_context_id(&id);  // the lookup made the context current
+    slot.addr = known ? p : nullptr;              // cache only under a known context
+    slot.ctx_id = known ? id : 0;
+    *out = p;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -64,7 +100,7 @@ extern "C" moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const int32
     if ((reinterpret_cast<uintptr_t>(tiles) & 15u) != 0) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, 0, E, K, 0);
     if (L.grouping_end > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;  // beyond the built-in scratch
-    moe_status_t s = current_device_is_sm103();
+    moe_status_t s = check_arch();
     if (s != MOE_OK) return s;
     void *scratch = nullptr;
     if ((s = scratch_for_current_device(&scratch)) != MOE_OK) return s;

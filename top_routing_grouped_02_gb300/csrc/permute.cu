@@ -13,7 +13,9 @@
 //  1. rank:    one warp per chunk of 32 tokens builds, for every expert, a
 //              32-bit mask of the chunk's tokens that chose it; a slot's rank in
 //              its chunk is the popcount of the mask below its lane, and the
-//              chunk's count per expert is the mask's popcount.
+//              chunk's count per expert is the mask's popcount. A slot whose
+//              expert is out of range, or repeats an expert listed earlier in
+//              its token's row, gets no row (rank -1) and is flagged.
 //  2. scan:    one block per expert turns the chunk counts into exclusive
 //              prefix sums; the last block to finish (ticket counter) scans the
 //              expert totals into offsets, tile bases and the tile list.
@@ -49,8 +51,17 @@ rank_kernel(const int32_t *__restrict__ idx, int T, int E, int K, int nchunks,
         if (k < K && valid) {
             int e = idx[t * K + k];
             if (e >= 0 && e < E) {
-                ek[k] = e;
-                atomicOr(&m[e], 1u << lane);
+                // a token owns one bit per expert, so a repeat of an expert in
+                // its row would share the first slot's rank and row: skip it
+                bool repeat = false;
+#pragma unroll
+                for (int k2 = 0; k2 < k; ++k2) repeat |= ek[k2] == e;
+                if (repeat) {
+                    atomicOr(&ctrl[kWordErr], MOE_DEVERR_REPEATED_EXPERT);
+                } else {
+                    ek[k] = e;
+                    atomicOr(&m[e], 1u << lane);
+                }
             } else {
                 atomicOr(&ctrl[kWordErr], MOE_DEVERR_BAD_EXPERT);
             }
