@@ -88,30 +88,59 @@ ROUTE_CASES = [
     (100, 256, 100, 4, True),     # E not a multiple of 64: partial expert tile
     (40, 1024, 33, 2, False),     # smallest tiled E, scalar weight loads
     (1000, 512, 32, 4, False),    # largest per-thread-chain E
-    (3000, 1000, 12, 3, False),   # chain kernel, d not a multiple of its stage
-    # E <= 32 sums in 1024-step blocks, one thread group per block
-    (600, 3000, 32, 4, True),     # 3 blocks, 2 groups: group 0 also runs block 2; partial last block
-    (200, 9216, 8, 2, False),     # 9 blocks, 8 groups
-    (64, 16392, 8, 2, False),     # 17 blocks: beyond the chain kernel, the small kernel folds them
+    (3000, 1000, 12, 3, False),   # E <= 32 kernel, d not a multiple of its stage
+    # E <= 32: logits in 1024-step blocks and selection in one kernel, a warp per
+    # (token group, block) item
+    (600, 3000, 32, 4, True),     # 3 blocks: 3 warps per CTA, partial last block
+    (200, 9216, 8, 2, False),     # 9 blocks: warps take 3, 2, 2, 2 items
+    (64, 16392, 8, 2, False),     # 17 blocks
     (130, 2056, 20, 3, True),     # E padded to 32, a last block of 8 steps
+    (37, 32776, 8, 2, False),     # 33 blocks: beyond the one-kernel router, the small kernel
+    (5000, 2048, 16, 4, False),   # 2 blocks: 2 token groups per CTA
+    (4100, 1024, 8, 2, True),     # 1 block: up to 4 token groups per CTA, partial last group
+    (9, 520, 4, 4, False),        # E = K = 4 padded to 8, one partial group
+    (333, 4096, 24, 8, True),     # E padded to 32, K = 8
 ]
 
 
-@pytest.mark.parametrize("T,d,E,K,zipf", ROUTE_CASES)
-def test_route_from_activations(T, d, E, K, zipf):
+def _route_case(T, d, E, K, zipf, renorm):
     X = synth.normal("X", (T, d), 1.0, torch.bfloat16, "cuda")
     Wr = synth.normal("Wr", (d, E), 1.0 / math.sqrt(d), torch.float32, "cuda")
     bias = synth.zipf_bias(E).cuda() if zipf else None
     logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
-    idx, w, counts = moe.moe_route(X, Wr, K, bias, logits=logits)
+    idx, w, counts = moe.moe_route(X, Wr, K, bias, renorm=renorm, logits=logits)
     torch.cuda.synchronize()
     Xn, Wn = bits(X), Wr.cpu().numpy()
     bn = None if bias is None else bias.cpu().numpy()
     L = oracle.router_logits(Xn, Wn, bn)
     # the logits themselves are the sequential fp32 chain: identical bits
     assert np.array_equal(logits.cpu().numpy().view(np.uint32), L.view(np.uint32))
-    idx_r, w_r = oracle.topk_softmax(L, K, True)
+    idx_r, w_r = oracle.topk_softmax(L, K, renorm)
     _check_routing(idx, w, counts, idx_r, w_r, E)
+
+
+@pytest.mark.parametrize("T,d,E,K,zipf", ROUTE_CASES)
+def test_route_from_activations(T, d, E, K, zipf):
+    _route_case(T, d, E, K, zipf, True)
+
+
+@pytest.mark.parametrize("T,d,E,K,zipf", [(4096, 4096, 8, 2, False), (600, 3000, 32, 4, True),
+                                          (9, 520, 4, 4, False), (1000, 512, 32, 4, False),
+                                          (300, 96, 64, 6, False)])
+def test_route_from_activations_without_renormalisation(T, d, E, K, zipf):
+    _route_case(T, d, E, K, zipf, False)
+
+
+def test_route_exact_ties_from_activations():
+    # X = 0 gives all-zero logits: the first K experts win, each with weight 1/K
+    T, d, E, K = 100, 2048, 8, 3
+    X = torch.zeros((T, d), dtype=torch.bfloat16, device="cuda")
+    Wr = synth.normal("Wr", (d, E), 1.0 / math.sqrt(d), torch.float32, "cuda")
+    idx, w, counts = moe.moe_route(X, Wr, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), np.tile(np.arange(K, dtype=np.int32), (T, 1)))
+    assert np.array_equal(w.cpu().numpy(), np.full((T, K), 1.0 / K, np.float32))
+    assert np.array_equal(counts.cpu().numpy(), np.array([T] * K + [0] * (E - K), np.int32))
 
 
 @pytest.mark.parametrize("pairs", ["4", "5", "6", "7", "8", None])

@@ -9,25 +9,26 @@
 // and the sum of exp(s - max); here the maximum is the top-1 score, so one pass
 // over the scores suffices).
 //
-// Two kernels:
-//  1. logits: L[t,e] in fp32, then one fp32 add of bias[e]. With E > 32 the sum
-//     is one fused multiply-add chain over j = 0..d-1 in ascending order from
-//     +0.0f; with E <= 32 it runs in blocks of 1024 steps, one such chain per
-//     block, the block sums added in ascending block order (a few-expert router
-//     has too few (token, expert) chains to hide a d-long dependency). That
-//     order is the definition the results are pinned to, so L (and hence the
-//     top-K indices) is bit-identical to a sequential evaluation of it. A chain
-//     cannot be split over threads or tensor-core instructions without changing
-//     the rounding, so every chain stays in one thread:
-//       - E <= 32: four (token, expert) chains per thread, one thread group per
-//         block of the reduction, fed from cp.async shared-memory pipelines; the
-//         groups' block sums are added in order at the end.
-//       - E > 32: two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
-//         micro-tiles fed by conflict-free float4 shared-memory reads.
-//       - E >= 128 with many tokens: one 8-warp block per SM, two warps per
-//         scheduler, each lane 2*PA or 2*PB tokens x 8 experts with x widened to
-//         fp32 pairs once per stage, so the FP32 FMA pipe is the limit.
-//  2. select: one warp per token reads its E logits, picks K by repeated warp
+// Logits: L[t,e] in fp32, then one fp32 add of bias[e]. With E > 32 the sum is
+// one fused multiply-add chain over j = 0..d-1 in ascending order from +0.0f;
+// with E <= 32 it runs in blocks of 1024 steps, one such chain per block, the
+// block sums added in ascending block order (a few-expert router has too few
+// (token, expert) chains to hide a d-long dependency). That order is the
+// definition the results are pinned to, so L (and hence the top-K indices) is
+// bit-identical to a sequential evaluation of it. A chain cannot be split over
+// threads or tensor-core instructions without changing the rounding, so every
+// chain stays in one thread.
+//  - E <= 32 (E % 4 == 0): ONE kernel computes the logits and selects: each
+//    lane runs 4 tokens x 2 experts of one 1024-step block (packed FMAs over
+//    token pairs, operands from cp.async shared-memory rings), the CTA adds
+//    the block sums in order and a thread per token ranks its experts.
+//  - E > 32: a logits kernel, then the select kernel below:
+//      - two-warp blocks on 32-token x 64-expert tiles, 4 x 8 register
+//        micro-tiles fed by conflict-free float4 shared-memory reads;
+//      - E >= 128 with many tokens: one 8-warp block per SM, two warps per
+//        scheduler, each lane 2*PA or 2*PB tokens x 8 experts with x widened to
+//        fp32 pairs once per stage, so the FP32 FMA pipe is the limit.
+//  - Select (given logits, or after the E > 32 logits): one warp per token reads its E logits, picks K by repeated warp
 //     argmax over order-preserving keys (ties -> lower index), writes indices
 //     and weights, and counts per expert in a block histogram flushed with one
 //     atomic per (block, expert). The softmax needs no separate maximum pass: the
@@ -37,6 +38,8 @@
 //     and writes the counts directly, so no memset is needed.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <algorithm>
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -48,6 +51,20 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
 }
+// 8-byte copy, or 8 zero bytes when !ok (the source is then not read)
+__device__ __forceinline__ void cp_async8_zfill(void *smem_dst, const void *gmem_src, bool ok) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(d), "l"(gmem_src),
+                 "r"(ok ? 8 : 0)
+                 : "memory");
+}
+// 16-byte copy, or 16 zero bytes when !ok (the source is then not read)
+__device__ __forceinline__ void cp_async16_zfill(void *smem_dst, const void *gmem_src, bool ok) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src),
+                 "r"(ok ? 16 : 0)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -56,163 +73,264 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // With E <= 32 the logits' reduction runs in blocks of kLogitBlock steps: one
 // fma chain per block, the block sums added in ascending block order (with
-// d <= kLogitBlock the single chain over j). The E <= 32 kernels' stage lengths
-// divide kLogitBlock.
+// d <= kLogitBlock the single chain over j). The E <= 32 kernel's stage length
+// divides kLogitBlock.
 constexpr int kLogitBlock = 1024;
 
-// ---- E <= 32: four (token, expert) chains per thread, one group per block ----
-// A thread group covers 16 tokens x EP experts, one thread per (token slot,
-// expert pair) with the tokens of slots tl and tl + 8, so 4*EP threads; a CTA
-// holds NG groups, and group g runs the chains of blocks g, g + NG, ... of the
-// reduction, so the blocks of one logit run side by side. Each group streams
-// its block through its own ring of 64-step stages (3 deep, cp.async): the 16
-// rows of X (bf16, 16-byte chunks XOR-swizzled by row) and the rows of Wr. Per
-// 4 steps a thread reads 8 bytes of bf16 x for each of its two tokens (widened
-// in registers) and four float2 of weights for 16 fused multiply-adds on its
-// four chains. At the end each group's block sums go to
-// shared memory and the first group adds them in ascending block order.
-// Requires d % 8 == 0, E % 4 == 0, a 16-byte-aligned Wr and at most
-// kChainMaxBlocks blocks.
-constexpr int kChainSlots = 8;   // token slots of a group; a thread takes slots tl and tl + 8
-constexpr int kChainTok = 16;    // tokens of a group
-constexpr int kChainStages = 3;
-constexpr int kChainJC = 64;
-constexpr int kChainMaxBlocks = 16;
+// ---- E <= 32: logits and selection in one kernel ------------------------------
+// Lane (q, p) of a warp owns the chains of 4 tokens (rows q, q + QPW, q + 2QPW,
+// q + 3QPW of its token group) x 2 experts (expert pair p) over one 1024-step
+// block of the reduction: EP/2 lanes per token quad, so a warp covers TPW =
+// 256/EP tokens (32, 16 or 8). A work item is (token group of TPW tokens,
+// block); a CTA holds `tg` token groups and all their blocks, its warps taking
+// the items in turn, so the blocks of one logit run side by side. Each warp
+// streams its item through its own ring of 64-step stages (cp.async): the TPW
+// rows of X (bf16, rows padded to 144 bytes) and, per expert pair, the pair's
+// 64 weights as (w[j][2p], w[j][2p+1]) rows (padded to 528 bytes). The
+// paddings put the rows a warp reads at once in distinct banks, so every load
+// address is the lane's base plus a constant. Per 8 steps a lane loads 16
+// bytes of x per token and four 128-bit weight words, one 8-step group ahead
+// of its use, and issues 4 packed FMAs per step over token pairs (each
+// component rounds like __fmaf_rn, so every block sum is one sequential fma
+// chain): 16 bytes of operands per 8 FMAs. Steps past d are zero-filled, which
+// leaves a chain unchanged (fmaf(0, w, acc) = acc for the +0-started chains).
+// At the end the block sums go to shared memory, one thread per token adds
+// them in ascending block order, adds the bias, stores the logits and runs the
+// selection below on its token, and the CTA's per-expert counts are added into
+// counts (zeroed before the launch).
+// What bounds it (Mixtral shape, 4096 tokens, d = 4096, E = 8): the definition
+// gives 131072 independent chains of 1024 steps, one warp per scheduler at 8
+// chains per lane, so each step's operand latency and the packed-FMA dispatch
+// (about 10 cycles per step for 4 packed FMAs) are exposed; X streams at about
+// half of HBM bandwidth behind them.
+// Requires E % 4 == 0, a 16-byte-aligned Wr and at most kRouteMaxBlocks blocks.
+constexpr int kRouteJS = 64;         // steps per stage
+constexpr int kRouteStages = 4;
+constexpr int kRouteMaxBlocks = 32;  // d <= 32768
+constexpr int kRouteWarps = 4;       // most warps per CTA
 
 template <int EP>
-struct ChainCfg {
-    static constexpr int THREADS = kChainSlots * EP / 2;      // one group
-    static constexpr int RXBYTES = kChainTok * kChainJC * 2;  // raw X rows (bf16)
-    static constexpr int RWBYTES = kChainJC * EP * 4;         // raw Wr rows (EP floats each)
-    static constexpr int RSTAGE = RXBYTES + RWBYTES;
-    static constexpr int GROUP_SMEM = kChainStages * RSTAGE;
-    static constexpr int MAXG = EP == 8 ? 8 : (EP == 16 ? 4 : 2);  // groups per CTA
-    static constexpr int MAX_SMEM = MAXG * GROUP_SMEM + kChainMaxBlocks * THREADS * 16;
+struct RouteCfg {
+    static constexpr int PAIRS = EP / 2;               // lanes per token quad
+    static constexpr int QPW = 32 / PAIRS;             // token quads per warp
+    static constexpr int TPW = 4 * QPW;                // tokens per warp
+    static constexpr int XROW = kRouteJS * 2 + 16;     // x row pitch: 64 bf16 + 16 bytes
+    static constexpr int XB = TPW * XROW;              // x rows of a stage
+    static constexpr int WROW = kRouteJS * 8 + 16;     // one expert pair's 64 steps + 16 bytes
+    static constexpr int WB = PAIRS * WROW;            // weights of a stage
+    static constexpr int SB = XB + WB;
+    static constexpr int WARP_SMEM = kRouteStages * SB;
+    static constexpr int PART = TPW * EP * 4;          // block sums of one item
 };
 
+// Selection for one token with its EP scores in registers (entries >= E are
+// ignored): the maximum, then K passes (higher score wins, equal scores: lower
+// index), weights exp(L_k - max) over their sum (renorm) or over a compensated
+// (Kahan) sum of exp(L_e - max) over every expert. Writes idx/w of token t and
+// counts the choices in the shared histogram.
 template <int EP>
-__global__ void __launch_bounds__(ChainCfg<EP>::THREADS * ChainCfg<EP>::MAXG)
-logits_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
-                    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
+__device__ __forceinline__ void select_token(const float (&v)[EP], int E, int K, int renorm,
+                                             int64_t t, int32_t *__restrict__ idx_out,
+                                             float *__restrict__ w_out, int *hist) {
+    float m = v[0];
+#pragma unroll
+    for (int e = 1; e < EP; ++e)
+        if (e < E) m = fmaxf(m, v[e]);
+    uint32_t taken = 0;
+    int sel[kMaxK];
+    float kept = 0.f, ex[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k < K) {
+            int bi = -1;
+            float bv = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < EP; ++e)
+                if (e < E && !(taken >> e & 1u) && (bi < 0 || v[e] > bv)) {
+                    bv = v[e];
+                    bi = e;
+                }
+            taken |= 1u << bi;
+            sel[k] = bi;
+            ex[k] = expf(bv - m);
+            kept += ex[k];
+        }
+    }
+    float denom = kept;
+    if (!renorm) {
+        float sum = 0.f, comp = 0.f;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            if (e < E) {
+                const float y = expf(v[e] - m) - comp;
+                const float tt = sum + y;
+                comp = (tt - sum) - y;
+                sum = tt;
+            }
+        }
+        denom = sum;
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k < K) {
+            idx_out[t * K + k] = sel[k];
+            w_out[t * K + k] = ex[k] / denom;
+            atomicAdd(&hist[sel[k]], 1);
+        }
+    }
+}
+
+template <int EP>
+__global__ void __launch_bounds__(32 * kRouteWarps)
+route_chain_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ Wr,
+                   const float *__restrict__ bias, int T, int d, int E, int K, int renorm,
+                   int tg, float *__restrict__ L, int32_t *__restrict__ idx_out,
+                   float *__restrict__ w_out, int32_t *__restrict__ counts) {
+    using C = RouteCfg<EP>;
+    constexpr int TPW = C::TPW;
     pdl_wait();
     pdl_trigger();
-    using C = ChainCfg<EP>;
-    constexpr int NTH = C::THREADS;
     extern __shared__ __align__(16) unsigned char sm[];
-    const int NG = blockDim.x / NTH;
-    const int g = threadIdx.x / NTH, tid = threadIdx.x % NTH;
-    unsigned char *gsm = sm + g * C::GROUP_SMEM;
-    float4 *part = reinterpret_cast<float4 *>(sm + NG * C::GROUP_SMEM);     // [nb][NTH]
-    const int h = tid % (EP / 2), tl = tid / (EP / 2);  // experts 2h, 2h+1 of tokens tl, tl + 8
-    const int64_t t0 = (int64_t)blockIdx.x * kChainTok;
+    __shared__ int hist[EP];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
     const int nb = (d + kLogitBlock - 1) / kLogitBlock;
-    auto group_sync = [&]() {
-        if constexpr (NTH == 32) __syncwarp();
-        else asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "r"(NTH) : "memory");
-    };
+    const int items = tg * nb;
+    const int64_t tcta = (int64_t)blockIdx.x * tg * TPW;
+    unsigned char *ring = sm + warp * C::WARP_SMEM;
+    float *part = reinterpret_cast<float *>(sm + nw * C::WARP_SMEM);  // [items][TPW][EP]
+    const int q = lane / C::PAIRS, p = lane % C::PAIRS;
+    for (int e = threadIdx.x; e < EP; e += blockDim.x) hist[e] = 0;
 
-    for (int b = g; b < nb; b += NG) {
+    for (int it = warp; it < items; it += nw) {
+        const int g = it / nb, b = it % nb;
+        const int64_t t0 = tcta + (int64_t)g * TPW;
         const int jb = b * kLogitBlock;
         const int len = min(kLogitBlock, d - jb);
-        const int nst = (len + kChainJC - 1) / kChainJC;
+        const int nst = (len + kRouteJS - 1) / kRouteJS;
+        // stage st of this item into ring slot st % kRouteStages (zero-filled
+        // beyond T, d and E)
         auto issue = [&](int st) {
-            unsigned char *xs = gsm + (st % kChainStages) * C::RSTAGE;
-            unsigned char *ws = xs + C::RXBYTES;
-            const int j0 = jb + st * kChainJC;
-            for (int q = tid; q < kChainTok * (kChainJC / 8); q += NTH) {
-                const int r = q / (kChainJC / 8), c = q % (kChainJC / 8);
+            unsigned char *xs = ring + (st % kRouteStages) * C::SB;
+            unsigned char *ws = xs + C::XB;
+            const int j0 = jb + st * kRouteJS;
+#pragma unroll
+            for (int i = 0; i < TPW * 8 / 32; ++i) {
+                const int cidx = lane + 32 * i;
+                const int r = cidx >> 3, c = cidx & 7;
                 const int64_t t = t0 + r;
-                const int j = j0 + c * 8;
-                if (t < T && j < jb + len)
-                    cp_async16(xs + r * (kChainJC * 2) + ((c ^ (r & 7)) << 4), X + t * d + j);
+                const int j = j0 + 8 * c;
+                const bool ok = t < T && j < d;
+                cp_async16_zfill(xs + r * C::XROW + c * 16, ok ? X + t * d + j : X, ok);
             }
-            for (int q = tid; q < kChainJC * (EP / 4); q += NTH) {
-                const int jj = q / (EP / 4), c4 = (q % (EP / 4)) * 4;
+#pragma unroll
+            for (int i = 0; i < kRouteJS * C::PAIRS / 32; ++i) {
+                const int cidx = lane + 32 * i;
+                const int jj = cidx / C::PAIRS, pp = cidx % C::PAIRS;
                 const int j = j0 + jj;
-                if (j < jb + len && c4 < E) cp_async16(ws + (jj * EP + c4) * 4, Wr + (int64_t)j * E + c4);
+                const bool ok = j < d && 2 * pp < E;
+                cp_async8_zfill(ws + pp * C::WROW + jj * 8, ok ? Wr + (int64_t)j * E + 2 * pp : Wr, ok);
             }
         };
-        for (int st = 0; st < kChainStages - 1; ++st) {
+#pragma unroll
+        for (int st = 0; st < kRouteStages - 1; ++st) {
             if (st < nst) issue(st);
             cp_async_commit();
         }
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // (tl, 2h), (tl, 2h+1), (tl+8, ...)
+        // chains: a[i][h] = (token pair i of the quad, expert 2p + h)
+        float2 a[2][2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) a[i][0] = a[i][1] = make_float2(0.f, 0.f);
         for (int st = 0; st < nst; ++st) {
-            cp_async_wait<kChainStages - 2>();
-            group_sync();  // raw stage st landed; the group is past the previous stage
-            if (st + kChainStages - 1 < nst) issue(st + kChainStages - 1);
+            cp_async_wait<kRouteStages - 2>();
+            __syncwarp();  // stage st landed for every lane; all lanes are past st - 1
+            if (st + kRouteStages - 1 < nst) issue(st + kRouteStages - 1);
             cp_async_commit();
-            const unsigned char *xs = gsm + (st % kChainStages) * C::RSTAGE;
-            const float2 *w2 = reinterpret_cast<const float2 *>(xs + C::RXBYTES) + h;  // row stride EP/2
-            const int jn = min(kChainJC, len - st * kChainJC);  // a multiple of 8
-            // the thread's two token rows in the stage: 8 bytes (4 steps) per read,
-            // 16-byte chunks XOR-swizzled by row so the reads are conflict-free
-            const unsigned char *xa = xs + tl * (kChainJC * 2);
-            const unsigned char *xb = xs + (tl + kChainSlots) * (kChainJC * 2);
-            auto step4 = [&](int v) {
-                const int off = (((v >> 1) ^ (tl & 7)) << 4) + (v & 1) * 8;
-                const uint2 ra = *reinterpret_cast<const uint2 *>(xa + off);
-                const uint2 rb = *reinterpret_cast<const uint2 *>(xb + off);
-                const float4 xv = make_float4(__uint_as_float(ra.x << 16), __uint_as_float(ra.x & 0xffff0000u),
-                                              __uint_as_float(ra.y << 16), __uint_as_float(ra.y & 0xffff0000u));
-                const float4 xu = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
-                                              __uint_as_float(rb.y << 16), __uint_as_float(rb.y & 0xffff0000u));
-                const float2 wa = w2[(4 * v + 0) * (EP / 2)], wb = w2[(4 * v + 1) * (EP / 2)];
-                const float2 wc = w2[(4 * v + 2) * (EP / 2)], wd = w2[(4 * v + 3) * (EP / 2)];
-                acc0 = __fmaf_rn(xv.x, wa.x, acc0);
-                acc1 = __fmaf_rn(xv.x, wa.y, acc1);
-                acc2 = __fmaf_rn(xu.x, wa.x, acc2);
-                acc3 = __fmaf_rn(xu.x, wa.y, acc3);
-                acc0 = __fmaf_rn(xv.y, wb.x, acc0);
-                acc1 = __fmaf_rn(xv.y, wb.y, acc1);
-                acc2 = __fmaf_rn(xu.y, wb.x, acc2);
-                acc3 = __fmaf_rn(xu.y, wb.y, acc3);
-                acc0 = __fmaf_rn(xv.z, wc.x, acc0);
-                acc1 = __fmaf_rn(xv.z, wc.y, acc1);
-                acc2 = __fmaf_rn(xu.z, wc.x, acc2);
-                acc3 = __fmaf_rn(xu.z, wc.y, acc3);
-                acc0 = __fmaf_rn(xv.w, wd.x, acc0);
-                acc1 = __fmaf_rn(xv.w, wd.y, acc1);
-                acc2 = __fmaf_rn(xu.w, wd.x, acc2);
-                acc3 = __fmaf_rn(xu.w, wd.y, acc3);
+            const unsigned char *xs = ring + (st % kRouteStages) * C::SB;
+            const unsigned char *xq = xs + q * C::XROW;                  // the lane's first token row
+            const unsigned char *wrow = xs + C::XB + p * C::WROW;        // its expert pair's weights
+            // 8-step groups: x words of the 4 tokens and 4 weight words, loaded one
+            // group ahead of their use
+            uint4 xr[2][4];
+            float4 wq[2][4];
+            auto load = [&](int v, int bs) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    xr[bs][i] = *reinterpret_cast<const uint4 *>(xq + i * C::QPW * C::XROW + v * 16);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    wq[bs][m] = *reinterpret_cast<const float4 *>(wrow + (8 * v + 2 * m) * 8);
             };
-            if (jn == kChainJC) {
-#pragma unroll 8
-                for (int v = 0; v < kChainJC / 4; ++v) step4(v);
-            } else {
-                for (int v = 0; v < jn / 4; ++v) step4(v);
+            load(0, 0);
+#pragma unroll
+            for (int v = 0; v < kRouteJS / 8; ++v) {
+                const int cb = v & 1;
+                if (v + 1 < kRouteJS / 8) load(v + 1, cb ^ 1);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    // word u of a row holds steps 8v + 2u (low half) and 8v + 2u + 1 (high)
+                    const uint32_t w0 = (&xr[cb][0].x)[u], w1 = (&xr[cb][1].x)[u];
+                    const uint32_t w2v = (&xr[cb][2].x)[u], w3 = (&xr[cb][3].x)[u];
+                    const float4 wv4 = wq[cb][u];  // (e0, e1) of step 8v + 2u, then of the next step
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float e0 = hh ? wv4.z : wv4.x, e1 = hh ? wv4.w : wv4.y;
+                        const float2 we0 = make_float2(e0, e0), we1 = make_float2(e1, e1);
+                        const float2 x01 =
+                            make_float2(__uint_as_float(hh ? (w0 & 0xffff0000u) : (w0 << 16)),
+                                        __uint_as_float(hh ? (w1 & 0xffff0000u) : (w1 << 16)));
+                        const float2 x23 =
+                            make_float2(__uint_as_float(hh ? (w2v & 0xffff0000u) : (w2v << 16)),
+                                        __uint_as_float(hh ? (w3 & 0xffff0000u) : (w3 << 16)));
+                        a[0][0] = __ffma2_rn(x01, we0, a[0][0]);
+                        a[0][1] = __ffma2_rn(x01, we1, a[0][1]);
+                        a[1][0] = __ffma2_rn(x23, we0, a[1][0]);
+                        a[1][1] = __ffma2_rn(x23, we1, a[1][1]);
+                    }
+                }
             }
         }
         cp_async_wait<0>();
-        group_sync();  // the ring and xf are free for the group's next block
-        part[b * NTH + tid] = make_float4(acc0, acc1, acc2, acc3);
-    }
-    __syncthreads();
-    if (g != 0) return;
-    float4 s = part[tid];
-    for (int b = 1; b < nb; ++b) {
-        const float4 p = part[b * NTH + tid];
-        s.x = __fadd_rn(s.x, p.x);
-        s.y = __fadd_rn(s.y, p.y);
-        s.z = __fadd_rn(s.z, p.z);
-        s.w = __fadd_rn(s.w, p.w);
-    }
-    const int e0 = 2 * h;
+        __syncwarp();  // the ring is free for the warp's next item
+        float *pp = part + (size_t)it * TPW * EP;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int64_t t = t0 + tl + k * kChainSlots;
-        float v0 = k ? s.z : s.x, v1 = k ? s.w : s.y;
-        if (t < T) {
-            if (e0 < E) {
-                if (bias != nullptr) v0 = __fadd_rn(v0, __ldg(bias + e0));
-                L[t * E + e0] = v0;
-            }
-            if (e0 + 1 < E) {
-                if (bias != nullptr) v1 = __fadd_rn(v1, __ldg(bias + e0 + 1));
-                L[t * E + e0 + 1] = v1;
-            }
+        for (int i = 0; i < 2; ++i) {
+            // token pair i of the lane: rows q + 2i*QPW and q + (2i+1)*QPW
+            const int ta = q + 2 * i * C::QPW, tb = ta + C::QPW;
+            pp[ta * EP + 2 * p] = a[i][0].x;
+            pp[ta * EP + 2 * p + 1] = a[i][1].x;
+            pp[tb * EP + 2 * p] = a[i][0].y;
+            pp[tb * EP + 2 * p + 1] = a[i][1].y;
         }
     }
+    __syncthreads();
+    // one thread per token: block sums in ascending block order, bias, logits,
+    // selection
+    for (int tau = threadIdx.x; tau < tg * TPW; tau += blockDim.x) {
+        const int64_t t = tcta + tau;
+        if (t >= T) continue;
+        const int g = tau / TPW, tl = tau % TPW;
+        float v[EP];
+        const float *p0 = part + (size_t)(g * nb) * TPW * EP + tl * EP;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) v[e] = p0[e];
+        for (int b = 1; b < nb; ++b) {
+            const float *pb = p0 + (size_t)b * TPW * EP;
+#pragma unroll
+            for (int e = 0; e < EP; ++e) v[e] = __fadd_rn(v[e], pb[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+            if (e < E) {
+                if (bias != nullptr) v[e] = __fadd_rn(v[e], __ldg(bias + e));
+                L[t * E + e] = v[e];
+            }
+        }
+        select_token<EP>(v, E, K, renorm, t, idx_out, w_out, hist);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
 }
 
 // Fallback for E <= 32 with E % 4 != 0 (or an unaligned Wr): operands straight
@@ -429,12 +547,6 @@ constexpr int kBStage = kBWBytes + kBXBytes;
 constexpr int kBXsBytes = kBK * kBWords * 8;   // transposed x, fp32 pairs: 32 KB
 constexpr int kBSmem = kBStages * kBStage + 2 * kBXsBytes;
 
-__device__ __forceinline__ void cp_async16_zfill(void *smem_dst, const void *gmem_src, bool ok) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src),
-                 "r"(ok ? 16 : 0)
-                 : "memory");
-}
 
 // jn reduction steps of one stage for a lane with N token pairs (acc[0..N-1])
 template <int N, int PMAX, bool FULL>
@@ -739,51 +851,7 @@ select_thread_kernel(const float *__restrict__ logits, int T, int E, int K, int 
 #pragma unroll
             for (int e = 0; e < EP; ++e) v[e] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
         }
-        float m = v[0];
-#pragma unroll
-        for (int e = 1; e < EP; ++e) m = fmaxf(m, v[e]);
-        uint32_t taken = 0;
-        int sel[kMaxK];
-        float kept = 0.f, ex[kMaxK];
-#pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k < K) {
-                int bi = -1;
-                float bv = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < EP; ++e)
-                    if (e < E && !(taken >> e & 1u) && (bi < 0 || v[e] > bv)) {
-                        bv = v[e];
-                        bi = e;
-                    }
-                taken |= 1u << bi;
-                sel[k] = bi;
-                ex[k] = expf(bv - m);
-                kept += ex[k];
-            }
-        }
-        float denom = kept;
-        if (!renorm) {
-            float sum = 0.f, comp = 0.f;
-#pragma unroll
-            for (int e = 0; e < EP; ++e) {
-                if (e < E) {
-                    const float y = expf(v[e] - m) - comp;
-                    const float tt = sum + y;
-                    comp = (tt - sum) - y;
-                    sum = tt;
-                }
-            }
-            denom = sum;
-        }
-#pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k < K) {
-                idx_out[t * K + k] = sel[k];
-                w_out[t * K + k] = ex[k] / denom;
-                atomicAdd(&hist[sel[k]], 1);
-            }
-        }
+        select_token<EP>(v, E, K, renorm, t, idx_out, w_out, hist);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -831,25 +899,39 @@ cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, 
                     counts);
 }
 
+// Token groups per CTA of the fused E <= 32 route kernel: the CTA holds all
+// blocks of its groups, up to kRouteWarps items; with few blocks it takes more
+// groups, unless that leaves SMs idle.
+int route_token_groups(int T, int d, int tpw) {
+    const int nb = (d + kLogitBlock - 1) / kLogitBlock;
+    int tg = nb >= kRouteWarps ? 1 : kRouteWarps / nb;
+    const int64_t groups = (T + tpw - 1) / tpw;
+    while (tg > 1 && (groups + tg - 1) / tg < sm_count()) --tg;
+    return tg;
+}
+
 template <int EP>
-cudaError_t launch_chain(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T, int d,
-                         int E, float *L, cudaStream_t s) {
-    using C = ChainCfg<EP>;
+cudaError_t launch_route_chain(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
+                              int d, int E, int K, int renorm, float *L, int32_t *idx, float *w,
+                              int32_t *counts, cudaStream_t s) {
+    using C = RouteCfg<EP>;
+    const int nb = (d + kLogitBlock - 1) / kLogitBlock;
+    const int tg = route_token_groups(T, d, C::TPW);
+    const int warps = std::min(kRouteWarps, tg * nb);
+    const size_t smem = (size_t)warps * C::WARP_SMEM + (size_t)tg * nb * C::PART;
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(logits_chain_kernel<EP>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::MAX_SMEM);
+        const size_t most = (size_t)kRouteWarps * C::WARP_SMEM + (size_t)kRouteMaxBlocks * C::PART;
+        cudaError_t e = cudaFuncSetAttribute(route_chain_kernel<EP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const int nb = (d + kLogitBlock - 1) / kLogitBlock;
-    const int ng = nb < C::MAXG ? nb : C::MAXG;
-    const size_t smem = (size_t)ng * C::GROUP_SMEM + (size_t)nb * C::THREADS * 16;
-    const unsigned grid = (unsigned)((T + kChainTok - 1) / kChainTok);
-    return launch_k(logits_chain_kernel<EP>, dim3(grid), dim3(ng * C::THREADS), smem, s, X, Wr,
-                    bias, T, d, E, L);
+    const unsigned grid = (unsigned)(((int64_t)T + (int64_t)tg * C::TPW - 1) / ((int64_t)tg * C::TPW));
+    return launch_k(route_chain_kernel<EP>, dim3(grid), dim3(32 * warps), smem, s, X, Wr, bias, T,
+                    d, E, K, renorm, tg, L, idx, w, counts);
 }
 
 template <int PA, int PB>
@@ -868,17 +950,6 @@ cudaError_t launch_big(const __nv_bfloat16 *X, const float *Wr, const float *bia
     const dim3 grid((unsigned)((T + kTok - 1) / kTok), (unsigned)((E + kBE - 1) / kBE));
     return launch_k(logits_big_kernel<PA, PB>, grid, dim3(kBThreads), (size_t)kBSmem, s, X, Wr,
                     bias, T, d, E, L);
-}
-
-int sm_count() {
-    static int count[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (count[dev] == 0 &&
-        cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        count[dev] = 148;
-    return count[dev];
 }
 
 // Token pairs per scheduler (P = PA + PB) of the one-block-per-SM kernel (0: use
@@ -918,11 +989,6 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
             default: break;
         }
     }
-    if (E <= 32 && E % 4 == 0 && wr16 && d <= kChainMaxBlocks * kLogitBlock) {
-        if (E <= 8) return launch_chain<8>(X, Wr, bias, T, d, E, L, s);
-        if (E <= 16) return launch_chain<16>(X, Wr, bias, T, d, E, L, s);
-        return launch_chain<32>(X, Wr, bias, T, d, E, L, s);
-    }
     if (E <= 32) {
         const int ep = E <= 8 ? 8 : (E <= 16 ? 16 : 32);
         auto kern = E <= 8 ? logits_small_kernel<8>
@@ -938,6 +1004,17 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
                          int d, int E, int K, int renorm, float *logits, int32_t *idx, float *w,
                          int32_t *counts, cudaStream_t s) {
+    const bool wr16 = (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
+    if (E <= 32 && E % 4 == 0 && wr16 && d <= kRouteMaxBlocks * kLogitBlock) {
+        // logits and selection in one kernel; its CTAs add into zeroed counts
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+        if (e != cudaSuccess) return e;
+        if (E <= 8)
+            return launch_route_chain<8>(X, Wr, bias, T, d, E, K, renorm, logits, idx, w, counts, s);
+        if (E <= 16)
+            return launch_route_chain<16>(X, Wr, bias, T, d, E, K, renorm, logits, idx, w, counts, s);
+        return launch_route_chain<32>(X, Wr, bias, T, d, E, K, renorm, logits, idx, w, counts, s);
+    }
     const bool zero = select_needs_zero_counts(T, E);
     if (zero) {
         cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
