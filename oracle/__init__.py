@@ -57,6 +57,7 @@ def _load():
                 "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
                 "oracle_bf16_to_double": (ctypes.c_double, [ctypes.c_uint16]),
                 "oracle_router_logits": (None, [P, P, P, I64, I, I, P]),
+                "oracle_gate_up_pre": (None, [P, P, P, P, P, I, I, I, P, P]),
                 "oracle_topk_softmax": (None, [P, I64, I, I, I, P, P]),
                 "oracle_expert_counts": (None, [P, I64, I, I, P]),
                 "oracle_permute": (None, [P, I64, I, I, P, P, P, P]),
@@ -216,6 +217,23 @@ def gate_up(X, W1, W3, perm_token, offsets) -> np.ndarray:
     H = np.empty((R, n), np.uint16)
     _load().oracle_gate_up(_p(X), _p(W1), _p(W3), _p(perm_token), _p(offsets), E, d, n, _p(H))
     return H
+
+
+def gate_up_pre(X, W1, W3, perm_token, offsets):
+    """(A1, A3) float64 [R,n]: the unrounded pre-activations x W1[e], x W3[e]."""
+    X = _c(X, np.uint16)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    perm_token = _c(perm_token, np.int32)
+    offsets = _c(offsets, np.int32)
+    E, d, n = W1.shape
+    assert W3.shape == W1.shape and X.shape[1] == d and offsets.shape[0] == E + 1
+    R = int(offsets[E])
+    A1 = np.empty((R, n), np.float64)
+    A3 = np.empty((R, n), np.float64)
+    _load().oracle_gate_up_pre(_p(X), _p(W1), _p(W3), _p(perm_token), _p(offsets), E, d, n,
+                               _p(A1), _p(A3))
+    return A1, A3
 
 
 def down(H, W2, topk_w, perm_slot, offsets) -> np.ndarray:

@@ -264,6 +264,24 @@ void oracle_gate_up(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
     }
 }
 
+void oracle_gate_up_pre(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                        const int32_t *perm_token, const int32_t *offsets, int E, int d, int n,
+                        double *A1, double *A3) {
+    int32_t R = offsets[E];
+#pragma omp parallel
+    {
+        uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t p = 0; p < R; ++p) {
+            int e = expert_of_row(offsets, E, p);
+            const uint16_t *x = X + (int64_t)perm_token[p] * d;
+            gate_up_row(x, W1 + (int64_t)e * d * n, W3 + (int64_t)e * d * n, d, n,
+                        A1 + (int64_t)p * n, A3 + (int64_t)p * n, h);
+        }
+        free(h);
+    }
+}
+
 void oracle_down(const uint16_t *H, const uint16_t *W2, const float *topk_w,
                  const int32_t *perm_slot, const int32_t *offsets,
                  int E, int n, int d, double *Z) {

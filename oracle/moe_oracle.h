@@ -88,6 +88,12 @@ int oracle_tile_schedule(const int32_t *offsets, int E, int M, int32_t *tiles, i
 void oracle_gate_up(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
                     const int32_t *perm_token, const int32_t *offsets,
                     int E, int d, int n, uint16_t *H);
+/* The pre-activations of the same rows, unrounded: A1[p,:] = x W1[e] and
+ * A3[p,:] = x W3[e] in double ([R,n] each), the two products gate_up rounds
+ * SiLU(A1)*A3 from. A training forward keeps them for the backward pass. */
+void oracle_gate_up_pre(const uint16_t *X, const uint16_t *W1, const uint16_t *W3,
+                        const int32_t *perm_token, const int32_t *offsets, int E, int d, int n,
+                        double *A1, double *A3);
 
 /* Z[p,:] = w[perm_slot[p]] * (H[p,:] W2[e]) in double; W2 is [E,n,d]. */
 void oracle_down(const uint16_t *H, const uint16_t *W2, const float *topk_w,

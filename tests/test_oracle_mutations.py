@@ -3,8 +3,8 @@
 Every mutation below is a plausible slip in the oracle's C source:
 - in the forward pass: a reordered, unfused or unblocked logit chain, the wrong
   tie-break, a dropped renormalisation, a sign error in SiLU, swapped gate/up
-  branches, a dropped routing weight, truncating instead of rounding, a
-  transposed weight, an unstable grouping;
+  branches or pre-activations, a dropped routing weight, truncating instead of
+  rounding, a transposed weight, an unstable grouping;
 - in Token Rounding: a wrong rounding rule, a wrong order in the second sort or
   a dropped renormalisation;
 - in the backward pass: a wrong SiLU derivative, a dropped routing weight or
@@ -44,6 +44,8 @@ MUTATIONS = [
      "for (int64_t t = T - 1; t >= 0; --t)\n        for (int k = 0; k < K; ++k) {\n            int32_t slot"),
     ("gather_ignores_perm", "const uint16_t *x = X + (int64_t)perm_token[p] * d;",
      "const uint16_t *x = X + (int64_t)p * d;"),
+    ("pre_activations_swapped", "A1 + (int64_t)p * n, A3 + (int64_t)p * n, h);",
+     "A3 + (int64_t)p * n, A1 + (int64_t)p * n, h);"),
     # Token Rounding
     ("tr_always_round_down", "(int64_t)M * ((f[e] + M / 2) / M);", "(int64_t)M * (f[e] / M);"),
     ("tr_always_round_up", "(int64_t)M * ((f[e] + M / 2) / M);", "(int64_t)M * ((f[e] + M - 1) / M);"),

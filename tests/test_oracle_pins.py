@@ -314,6 +314,25 @@ def test_single_expert_equals_dense_swiglu(oracle_lib):
     assert ulp_diff(out["Y"], bf16_bits_of_f64_via_torch(y.numpy())).max() <= 1
 
 
+def test_pre_activations_are_the_grouped_rows_times_w1_and_w3(oracle_lib):
+    # A1 = x W1[e], A3 = x W3[e] of each grouped row, against torch float64
+    # matmuls of the gathered rows expert by expert; and SiLU(A1) * A3 rounded
+    # to bf16 gives the oracle's H
+    X, Wr, _, W1, W3, W2 = _small_layer(T=50, d=64, E=4, n=48, seed=21)
+    out = oracle.forward(X, Wr, None, W1, W3, W2, K=2)
+    A1, A3 = oracle.gate_up_pre(X, W1, W3, out["perm_token"], out["offsets"])
+    off = out["offsets"]
+    xs = torch.from_numpy(f64(X))
+    for e in range(4):
+        rows = xs[torch.from_numpy(out["perm_token"][off[e]:off[e + 1]].astype(np.int64))]
+        r1 = (rows @ torch.from_numpy(f64(W1[e]))).numpy()
+        r3 = (rows @ torch.from_numpy(f64(W3[e]))).numpy()
+        assert np.max(np.abs(A1[off[e]:off[e + 1]] - r1)) < 1e-12
+        assert np.max(np.abs(A3[off[e]:off[e + 1]] - r3)) < 1e-12
+    h = torch.nn.functional.silu(torch.from_numpy(A1)) * torch.from_numpy(A3)
+    assert ulp_diff(out["H"], bf16_bits_of_f64_via_torch(h.numpy())).max() <= 1
+
+
 def test_silu_gate_is_w1_not_w3(oracle_lib):
     X, Wr, _, W1, W3, W2 = _small_layer(T=8, d=64, E=1, n=64, seed=12)
     a = oracle.forward(X, Wr, None, W1, W3, W2, K=1)["Y"]
