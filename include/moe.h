@@ -114,8 +114,10 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * Logits are fp32 fused multiply-add chains over j ascending from +0, then
  * + bias[e]: with E > 32 one chain over j = 0..d-1; with E <= 32 one chain per
  * block of 1024 consecutive j, the block sums added in ascending block order.
- * Bit-identical to that sequential definition. Two kernels (logits, then
- * softmax and top-K) and, unless E <= 16 and T <= 2048, a memset of counts. */
+ * Bit-identical to that sequential definition. With E <= 32, E % 4 == 0, a
+ * 16-byte-aligned Wr and d <= 32768: a memset of counts and ONE kernel
+ * (logits and selection). Otherwise two kernels (logits, then softmax and
+ * top-K) and, unless E <= 16 and T <= 2048, a memset of counts. */
 moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias,
                        int T, int d, int E, int K, int renorm, float *logits,
                        int32_t *topk_idx, float *topk_w, int32_t *counts, void *stream);
@@ -200,6 +202,42 @@ moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *t
                            int T, int d, int E, int K, int n, moe_bf16 *Z,
                            void *ws, size_t ws_bytes, void *stream);
 
+/* ---- Backward pass (SonicMoE page §2.2: the gradient of H with the routing
+ * score's gradient dS computed inside it; §4.1: its TMA load pipeline). The
+ * top-K choice is held fixed; the gradients follow, for every grouped row p of
+ * expert e with token t = perm_token[p] and weight w = topk_w[perm_slot[p]]:
+ *   g[p,j]   = sum_c dY[t,c] W2[e][j,c]                      (dH' = dY W2[e]^T)
+ *   dS[p]    = sum_j g[p,j] SiLU(a1[p,j]) a3[p,j]            (dL/dw of that slot)
+ *   dA1[p,j] = w g[p,j] a3[p,j] s (1 + a1[p,j] (1 - s)),  s = sigmoid(a1[p,j])
+ *   dA3[p,j] = w g[p,j] SiLU(a1[p,j])
+ * with a1 = x W1[e], a3 = x W3[e] the forward's pre-activations. */
+
+/* The gate/up GEMM of a training forward: H exactly as moe_gemm_gate_up writes
+ * it, and the pre-activations A1 = x W1[e], A3 = x W3[e] of every grouped row
+ * (fp32 [T*K, n] each: the accumulators as they are, so that the backward's
+ * sums over n do not inherit a bf16 rounding of every term) for
+ * moe_backward_dh. Same arguments and workspace as moe_gemm_gate_up. */
+moe_status_t moe_gemm_gate_up_train(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
+                                    const int32_t *perm_token, const int32_t *offsets, int T,
+                                    int d, int E, int K, int n, moe_bf16 *H, float *A1,
+                                    float *A3, void *ws, size_t ws_bytes, void *stream);
+
+/* The backward's dH step: one grouped GEMM g = dY[perm_token] W2[e]^T (rows
+ * of dY [T,d] bf16 gathered like X; W2 [E,n,d] read with d, the reduction, as
+ * the contiguous dimension) whose epilogue forms, with A1, A3 [T*K,n] fp32
+ * from moe_gemm_gate_up_train and the routing weights topk_w [T*K] fp32:
+ * dA1, dA3 [T*K,n] bf16 (grouped rows) and dS [T*K] fp32 (grouped rows; each
+ * row's sum over j in fp32, 32-column partials added in ascending column
+ * order by a second kernel). Needs n % 256 == 0 and n <= 16*d, else
+ * MOE_ERR_UNSUPPORTED_SHAPE. ws: workspace of this shape (its gathered-rows
+ * region holds the partials). Two kernels; a row index out of range is
+ * skipped and flagged like the forward GEMMs'. */
+moe_status_t moe_backward_dh(const moe_bf16 *dY, const moe_bf16 *W2, const float *A1,
+                             const float *A3, const float *topk_w, const int32_t *perm_token,
+                             const int32_t *perm_slot, const int32_t *offsets, int T, int d,
+                             int E, int K, int n, moe_bf16 *dA1, moe_bf16 *dA3, float *dS,
+                             void *ws, size_t ws_bytes, void *stream);
+
 /* Both expert GEMMs: H as moe_gemm_gate_up writes it, then Z as moe_gemm_down
  * writes it, bit for bit. Two launches (three on CTA pairs); with
  * MOE_GEMM_FUSED=1 and n <= 2048, ONE persistent launch (the SonicMoE page's
@@ -237,10 +275,13 @@ int moe_expert_mlp_launches(int T, int d, int E, int K, int n, int rounded);
 
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
- * Enqueues moe_forward_launches(T, d, E, K, n, 0) kernels: 8, or 9 on CTA
- * pairs, which gather their rows first, or 7 when both expert GEMMs run in one
- * launch (see moe_expert_mlp); and, unless E <= 16 and T <= 2048, one memset
- * of the counts; no host synchronisation. */
+ * Enqueues moe_forward_launches(T, d, E, K, n, 0) kernels: the router (1 with
+ * E <= 32 as moe_route says, else 2), the grouping (3), the expert GEMMs (2, 3
+ * on CTA pairs, which gather their rows first, or 1 when both run in one launch,
+ * see moe_expert_mlp) and the combine (1); and, unless E <= 16 and T <= 2048
+ * with the two-kernel router, one memset of the counts; no host
+ * synchronisation. The grouping here writes no tile list: the expert GEMMs
+ * decode their work units from the offsets. */
 moe_status_t moe_forward(const moe_bf16 *X, const float *Wr, const float *bias,
                          const moe_bf16 *W1, const moe_bf16 *W3, const moe_bf16 *W2,
                          int T, int d, int E, int K, int n, int renorm,

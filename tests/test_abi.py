@@ -49,25 +49,28 @@ def test_workspace_bytes(lib):
 
 
 def test_forward_launch_counts(lib, monkeypatch):
-    # kernels per forward: router 2, grouping (or rounding) 3, combine 1, and the
-    # expert GEMMs: two launches, a row gather more on CTA pairs (experts of at
-    # least 8 row tiles on average), or one fused launch on request
+    # kernels per forward: the router (1 for E <= 32 with E % 4 == 0: logits and
+    # selection in one kernel; else 2), grouping (or rounding) 3, combine 1, and
+    # the expert GEMMs: two launches, a row gather more on CTA pairs (experts of
+    # at least 8 row tiles on average), or one fused launch on request
     for var in ("MOE_GEMM_FUSED", "MOE_GEMM_CTA_PAIR"):
         monkeypatch.delenv(var, raising=False)
-    assert moe.forward_launches(512, 256, 8, 2, 512) == 8            # tiny
+    assert moe.forward_launches(512, 256, 8, 2, 512) == 7            # tiny
     assert moe.forward_launches(16384, 1536, 128, 4, 256) == 8       # SonicMoE
     assert moe.forward_launches(16384, 1536, 128, 4, 256, True) == 8
     assert moe.forward_launches(8192, 7168, 256, 8, 2048) == 8       # DeepSeek-V3
-    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 9        # Mixtral: CTA pairs
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 8        # Mixtral: CTA pairs
+    assert moe.forward_launches(64, 256, 6, 2, 512) == 8             # E % 4 != 0: two router kernels
+    assert moe.forward_launches(64, 33792, 8, 2, 512) == 8           # 33 blocks: two router kernels
     # (whether a fused launch's units fit its rounds depends on the device's SM
     # count, unknown here; these cases do not depend on it)
     assert moe.forward_launches(16384, 1536, 128, 4, 256, part="expert_mlp") == 2
     assert moe.forward_launches(4096, 4096, 8, 2, 14336, part="expert_mlp") == 3
     monkeypatch.setenv("MOE_GEMM_FUSED", "1")
-    assert moe.forward_launches(512, 256, 8, 2, 512) == 7            # 80 units at most
+    assert moe.forward_launches(512, 256, 8, 2, 512) == 6            # 80 units at most
     assert moe.forward_launches(512, 256, 8, 2, 512, part="expert_mlp") == 1
-    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 9        # too wide to fuse
-    assert moe.forward_launches(64, 256, 4, 1, 2176) == 8            # n > 2048
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 8        # too wide to fuse
+    assert moe.forward_launches(64, 256, 4, 1, 2176) == 7            # n > 2048
     monkeypatch.setenv("MOE_GEMM_FUSED", "0")
     assert moe.forward_launches(16384, 1536, 128, 4, 256) == 8
     with pytest.raises(ValueError):

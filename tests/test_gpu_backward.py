@@ -1,0 +1,132 @@
+"""The backward's dH step on the GPU against the oracle (through the C-ABI).
+
+moe_gemm_gate_up_train must give H bit for bit as moe_gemm_gate_up does and
+the pre-activations A1 = x W1[e], A3 = x W3[e] (fp32) within the tolerance
+below of the oracle's unrounded products. moe_backward_dh, fed with those, must give
+dA1, dA3 and the routing-weight gradient dS of every grouped row within the
+tolerance the forward's H and Z are held to, against oracle.backward_rows
+(the gradient of sum(Y * dY) with the top-K choice fixed, in double).
+
+A row's quantities depend only on its token, its expert and the weights, so
+on the SonicMoE shape the oracle runs on the sampled tokens alone (their own
+grouping) and its rows are matched to the full grouping's through the slots.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import check_hz, f64_of_bits, bits, layer_np
+from top_routing_grouped_02_gb300 import moe, synth
+
+pytestmark = pytest.mark.gpu
+
+REL = 2.0 ** -6
+FRO = 5e-3
+
+
+def check_f32(got: np.ndarray, ref: np.ndarray, what: str):
+    """fp32 values against float64 ones: |d| / max(1, |ref|) and relative Frobenius."""
+    got = got.astype(np.float64)
+    worst = float((np.abs(got - ref) / np.maximum(1.0, np.abs(ref))).max())
+    fro = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    assert worst <= REL, f"{what}: max |d|/max(1,|ref|) {worst:.3e} > {REL}"
+    assert fro <= FRO, f"{what}: rel-Frobenius {fro:.3e} > {FRO}"
+
+
+def _gpu_steps(inp, dY, K):
+    T, d = inp["X"].shape
+    E, _, n = inp["W1"].shape
+    ws = moe.workspace(T, d, E, K, n)
+    idx, w, counts = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"])
+    g = moe.moe_permute(idx, E, counts=counts, ws=ws)
+    H0 = moe.moe_gemm_gate_up(inp["X"], inp["W1"], inp["W3"], g["perm_token"], g["offsets"], K, ws=ws)
+    H, A1, A3 = moe.moe_gemm_gate_up_train(inp["X"], inp["W1"], inp["W3"], g["perm_token"],
+                                           g["offsets"], K, ws=ws)
+    dA1, dA3, dS = moe.moe_backward_dh(dY, inp["W2"], A1, A3, w.view(-1), g["perm_token"],
+                                       g["perm_slot"], g["offsets"], K, ws=ws)
+    torch.cuda.synchronize()
+    st, word = moe.moe_sync_check(ws)
+    assert st == 0, (st, word)
+    R = int(g["offsets"][-1].item())
+    # the training gate/up GEMM stores H exactly as the forward one does
+    assert torch.equal(H[:R].view(torch.int16), H0[:R].view(torch.int16))
+    return dict(idx=idx, H=H, A1=A1, A3=A3, dA1=dA1, dA3=dA3, dS=dS, **g)
+
+
+def _f64(a):
+    # fp32 router weights and bias widen to float64 exactly
+    return None if a is None else np.asarray(a, np.float64)
+
+
+def _dY(T, d):
+    return synth.normal("dY", (T, d), 1.0, torch.bfloat16, "cuda", seed=7)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_backward_dh_matches_oracle_in_full(pair, monkeypatch):
+    # the tiny layer, with the training gate/up GEMM on single CTAs and on CTA
+    # pairs (the dH GEMM runs single CTAs either way)
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", pair)
+    cfg = synth.WORKLOADS["tiny"]
+    T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    dY = _dY(T, d)
+    s = _gpu_steps(inp, dY, K)
+    X, Wr, bias, W1, W3, W2 = layer_np(inp)
+    idx_r, _ = oracle.topk_softmax(oracle.router_logits(X, Wr, bias), K, True)
+    assert np.array_equal(s["idx"].cpu().numpy(), idx_r)
+    off_r, pt_r, ps_r, _ = oracle.permute(idx_r, E)
+    A1r, A3r = oracle.gate_up_pre(X, W1, W3, pt_r, off_r)
+    check_f32(s["A1"].cpu().numpy(), A1r, "A1")
+    check_f32(s["A3"].cpu().numpy(), A3r, "A3")
+    ref = oracle.backward_rows(X, _f64(Wr), _f64(bias), W1, W3, W2, idx_r, ps_r,
+                               f64_of_bits(bits(dY)))
+    check_hz(bits(s["dA1"]), ref["dA1"], "dA1")
+    check_hz(bits(s["dA3"]), ref["dA3"], "dA3")
+    check_f32(s["dS"].cpu().numpy(), ref["dS"], "dS")
+
+
+def test_backward_dh_sonic_shape_sampled_tokens():
+    cfg = synth.WORKLOADS["sonic"]
+    T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]
+    inp = synth.layer_inputs(device="cuda", **cfg)
+    dY = _dY(T, d)
+    s = _gpu_steps(inp, dY, K)
+    X, Wr, bias, W1, W3, W2 = layer_np(inp)
+    rng = np.random.default_rng(5)
+    toks = np.sort(rng.choice(T, size=192, replace=False))
+    toks[0], toks[-1] = 0, T - 1
+    idx_full = s["idx"].cpu().numpy()
+    # the oracle's routing of those tokens is the GPU's (checked bit for bit in
+    # the router tests); the sub-problem keeps it fixed
+    L = oracle.router_logits(X[toks], Wr, bias)
+    idx_sub, _ = oracle.topk_softmax(L, K, True)
+    assert np.array_equal(idx_sub, idx_full[toks])
+    _, _, ps_sub, _ = oracle.permute(idx_sub, E)
+    ref = oracle.backward_rows(X[toks], _f64(Wr), _f64(bias), W1, W3, W2, idx_sub, ps_sub,
+                               f64_of_bits(bits(dY))[toks])
+    # sub-problem row p holds slot ps_sub[p] = t' * K + k of token toks[t']; its
+    # row in the full grouping is row_of_slot[toks[t'] * K + k]
+    ros = s["row_of_slot"].cpu().numpy()
+    full_rows = ros[toks[ps_sub // K] * K + ps_sub % K]
+    P = torch.from_numpy(full_rows.astype(np.int64)).cuda()
+    check_hz(bits(s["dA1"][P]), ref["dA1"], "dA1 (sampled tokens)")
+    check_hz(bits(s["dA3"][P]), ref["dA3"], "dA3 (sampled tokens)")
+    check_f32(s["dS"][P].cpu().numpy(), ref["dS"], "dS (sampled tokens)")
+
+
+def test_backward_dh_rejects_n_not_a_multiple_of_256():
+    T, d, E, K, n = 64, 256, 4, 2, 384
+    z = torch.zeros
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_backward_dh(z((T, d), dtype=torch.bfloat16, device="cuda"),
+                            z((E, n, d), dtype=torch.bfloat16, device="cuda"),
+                            z((T * K, n), dtype=torch.float32, device="cuda"),
+                            z((T * K, n), dtype=torch.float32, device="cuda"),
+                            z(T * K, dtype=torch.float32, device="cuda"),
+                            z(T * K, dtype=torch.int32, device="cuda"),
+                            z(T * K, dtype=torch.int32, device="cuda"),
+                            z(E + 1, dtype=torch.int32, device="cuda"), K)
+    assert e.value.status == 2

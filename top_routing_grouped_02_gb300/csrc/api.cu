@@ -189,8 +189,9 @@ int moe_expert_mlp_launches(int T, int d, int E, int K, int n, int rounded) {
 int moe_forward_launches(int T, int d, int E, int K, int n, int rounded) {
     const int gemms = moe_expert_mlp_launches(T, d, E, K, n, rounded);
     if (gemms < 0) return -1;
-    // router 2, grouping or rounding 3, combine 1, and the expert GEMMs
-    return 2 + 3 + gemms + 1;
+    // router 1 or 2 (with 16-byte-aligned router weights), grouping or rounding
+    // 3, combine 1, and the expert GEMMs
+    return (route_is_one_kernel(d, E, true) ? 1 : 2) + 3 + gemms + 1;
 }
 
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n) {
@@ -263,6 +264,53 @@ moe_status_t moe_gemm_gate_up(const moe_bf16 *X, const moe_bf16 *W1, const moe_b
                                          T * K, d, E, n, reinterpret_cast<__nv_bfloat16 *>(H),
                                          at<__nv_bfloat16>(ws, L.xg), at<uint32_t>(ws, L.err),
                                          as_stream(stream)));
+}
+
+moe_status_t moe_gemm_gate_up_train(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
+                                    const int32_t *perm_token, const int32_t *offsets, int T,
+                                    int d, int E, int K, int n, moe_bf16 *H, float *A1,
+                                    float *A3, void *ws, size_t ws_bytes, void *stream) {
+    if (!X || !W1 || !W3 || !perm_token || !offsets || !H || !A1 || !A3 || !ws)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W3) || !aligned16(H) || !aligned16(A1) ||
+        !aligned16(A3))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, K, n);
+    if (ws_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_gemm_gate_up_train(
+        reinterpret_cast<const __nv_bfloat16 *>(X), perm_token, T,
+        reinterpret_cast<const __nv_bfloat16 *>(W1), reinterpret_cast<const __nv_bfloat16 *>(W3),
+        offsets, T * K, d, E, n, reinterpret_cast<__nv_bfloat16 *>(H), A1, A3,
+        at<__nv_bfloat16>(ws, L.xg), at<uint32_t>(ws, L.err), as_stream(stream)));
+}
+
+moe_status_t moe_backward_dh(const moe_bf16 *dY, const moe_bf16 *W2, const float *A1,
+                             const float *A3, const float *topk_w, const int32_t *perm_token,
+                             const int32_t *perm_slot, const int32_t *offsets, int T, int d,
+                             int E, int K, int n, moe_bf16 *dA1, moe_bf16 *dA3, float *dS,
+                             void *ws, size_t ws_bytes, void *stream) {
+    if (!dY || !W2 || !A1 || !A3 || !topk_w || !perm_token || !offsets || !dA1 || !dA3 || !dS ||
+        !ws)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    // 256 hidden columns per unit; the dS partials (n/32 floats per row) live
+    // in the workspace region of the gathered rows (2*d bytes per row)
+    if (n % 256 != 0 || n / 8 > 2 * d) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(dY) || !aligned16(W2) || !aligned16(A1) || !aligned16(A3) || !aligned16(dA1) ||
+        !aligned16(dA3))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, K, n);
+    if (ws_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_backward_dh(
+        reinterpret_cast<const __nv_bfloat16 *>(dY), perm_token, T,
+        reinterpret_cast<const __nv_bfloat16 *>(W2), A1, A3, topk_w, perm_slot, offsets, T * K, d, E, n,
+        reinterpret_cast<__nv_bfloat16 *>(dA1), reinterpret_cast<__nv_bfloat16 *>(dA3),
+        at<float>(ws, L.xg), dS, at<uint32_t>(ws, L.err), as_stream(stream)));
 }
 
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
@@ -358,9 +406,10 @@ moe_status_t moe_forward_traced(const moe_bf16 *X, const float *Wr, const float 
                      st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
-    if (launch_permute(idx, counts, T, E, K, offsets, perm_token, perm_slot, row_of_slot,
-                       at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.num_tiles), L,
-                       static_cast<char *>(ws), st) != cudaSuccess ||
+    // the expert GEMMs decode their units from the offsets, so the tile list is
+    // not written here (moe_permute writes it for callers that schedule tiles)
+    if (launch_permute(idx, counts, T, E, K, offsets, perm_token, perm_slot, row_of_slot, nullptr,
+                       nullptr, L, static_cast<char *>(ws), st) != cudaSuccess ||
         !mark())
         return MOE_ERR_CUDA;
     if (use_fused_mlp(R, d, E, n)) {

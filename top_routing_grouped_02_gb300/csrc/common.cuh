@@ -76,6 +76,9 @@ size_t round_scratch_bytes(int T, int E);
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
                          int d, int E, int K, int renorm, float *logits, int32_t *idx, float *w,
                          int32_t *counts, cudaStream_t s);
+// Whether launch_route runs one kernel (logits and selection together) for
+// this shape and router-weight alignment; otherwise two.
+bool route_is_one_kernel(int d, int E, bool wr16);
 cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const float *bias,
                                  int T, int d, int E, float *L, cudaStream_t s);
 cudaError_t launch_route_logits(const float *logits, int T, int E, int K, int renorm,
@@ -95,6 +98,21 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_toke
                                 const int32_t *offsets, int R, int d, int E, int n,
                                 __nv_bfloat16 *H, __nv_bfloat16 *xg, uint32_t *err,
                                 cudaStream_t s);
+// The gate/up GEMM that also stores the pre-activations A1 = x W1[e] and
+// A3 = x W3[e] (fp32 [R, n] each) beside H.
+cudaError_t launch_gemm_gate_up_train(const __nv_bfloat16 *X, const int32_t *perm_token, int T,
+                                      const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                                      const int32_t *offsets, int R, int d, int E, int n,
+                                      __nv_bfloat16 *H, float *A1, float *A3,
+                                      __nv_bfloat16 *xg, uint32_t *err, cudaStream_t s);
+// Backward dH: dA1, dA3 [R, n] bf16 and dS [R] fp32 from dY [T, d], W2 and the
+// pre-activations; dspart: scratch [R, n/32] fp32 (n % 256 == 0).
+cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_token, int T,
+                               const __nv_bfloat16 *W2, const float *A1,
+                               const float *A3, const float *topk_w,
+                               const int32_t *perm_slot, const int32_t *offsets, int R, int d,
+                               int E, int n, __nv_bfloat16 *dA1, __nv_bfloat16 *dA3,
+                               float *dspart, float *dS, uint32_t *err, cudaStream_t s);
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,

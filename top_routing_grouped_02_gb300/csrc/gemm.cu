@@ -117,12 +117,22 @@ struct Geo {
     static constexpr int kStages = PAIR ? MOE_GEMM_PAIR_STAGES : MOE_GEMM_STAGES;
     static constexpr int kBBoxes = PAIR ? 2 : 4;
     static constexpr uint32_t kStageBytes = kABytes + kBBoxes * kBBox;
-    static constexpr uint32_t kIdesc =
-        ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
 
 };
 
-enum Mode : int { kGateUp = 0, kDown = 1, kFused = 2 };
+// kGateUpPre: gate/up that also keeps the pre-activations A1 = x W1[e] and
+// A3 = x W3[e] (fp32, the accumulators as they are) beside H, for the backward. kDH: the backward's
+// dH' = dY[t_p] W2[e]^T (B = W2[e] read K-major, rows of dY gathered like X),
+// whose epilogue forms dA1, dA3 and the routing-weight gradient's partial sums.
+enum Mode : int { kGateUp = 0, kDown = 1, kFused = 2, kGateUpPre = 3, kDH = 4 };
+
+// Instruction descriptor: B is MN-major (the forward's weights, K rows of N
+// contiguous columns) except for kDH, whose W2[e] rows are n-major with the
+// reduction dimension d contiguous (K-major).
+template <int MODE, bool PAIR>
+constexpr uint32_t idesc_of() {
+    return ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false, /*B MN-major*/ MODE != kDH);
+}
 
 // Single-CTA gate/up A rows are gathered by warps 2 and 3 with 16-byte cp.async.
 // Each lane waits for its own copies and fences them for the async proxy, the
@@ -134,6 +144,17 @@ constexpr int kGatherWarps = 2;
 #define MOE_GEMM_GATHER_LAG 2
 #endif
 constexpr int kGatherLag = MOE_GEMM_GATHER_LAG;
+
+// Work tiles of one expert whose units run column block by column block
+// before the expert's next tiles start.
+#ifndef MOE_GEMM_GROUP_TILES
+#define MOE_GEMM_GROUP_TILES 1000000
+#endif
+constexpr int kGroupTiles = MOE_GEMM_GROUP_TILES;
+// L2 policy of the gathered A-row copies: 1 = evict-last.
+#ifndef MOE_GEMM_GATHER_HINT
+#define MOE_GEMM_GATHER_HINT 0
+#endif
 
 // Most rounds (unit positions / CTAs) a fused launch may have; the host runs
 // the two GEMMs apart when the bound on its units exceeds them.
@@ -190,6 +211,19 @@ struct GemmArgs {
     int out2_ld;
     uint32_t *dep;
     int gap_rounds;
+    // kGateUpPre: the pre-activation outputs A1, A3 [R, n] fp32; kDH: dA3 (dA1
+    // goes to out)
+    float *pre_out1;
+    float *pre_out3;
+    __nv_bfloat16 *out3;
+    // kDH: the pre-activations A1, A3 [R, n] fp32 (row length out_ld), rows of
+    // W2[e] per expert (n), and the per-(row, 32-column chunk) partial sums of
+    // dS [R, ds_ld]
+    const float *pre1;
+    const float *pre3;
+    int bn_rows;
+    float *dspart;
+    int ds_ld;
 };
 
 // Counter words of the fused kernel: the launch's epoch in the high 24 bits, the
@@ -257,8 +291,14 @@ __device__ __forceinline__ void decode_unit(int p, int NB, int E, const int32_t 
     e = lo;
     const int m_e = tb[e + 1] - tb[e];
     const int local = u - tb[e] * NB;
-    nb = local / m_e;
-    const int pt = local - nb * m_e;
+    // groups of kGroupTiles work tiles: a group runs all column blocks before
+    // the next group starts (the last group holds the remainder)
+    const int nfull = m_e / kGroupTiles;
+    const int k = min(local / (kGroupTiles * NB), nfull);
+    const int gs = k < nfull ? kGroupTiles : m_e - nfull * kGroupTiles;
+    const int go = local - k * kGroupTiles * NB;
+    nb = go / gs;
+    const int pt = k * kGroupTiles + (go - nb * gs);
     row0 = off[e] + (pt * per_tile + rank) * BM;
     rows = min(BM, off[e + 1] - row0);
 }
@@ -357,7 +397,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr bool FUSED = MODE == kFused;
     static_assert(!(FUSED && PAIR), "the fused kernel runs single CTAs");
     // A rows gathered in the kernel (single-CTA gate/up units) or loaded by TMA
-    constexpr bool GATHER = (MODE == kGateUp || FUSED) && !PAIR;
+    constexpr bool GATHER = (MODE == kGateUp || MODE == kGateUpPre || MODE == kDH || FUSED) && !PAIR;
+    constexpr bool GATE = MODE == kGateUp || MODE == kGateUpPre;  // gate/up B boxes (W1 | W3)
+    static_assert(!(MODE == kDH && PAIR), "the backward dH GEMM runs single CTAs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -388,8 +430,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0 && lane == 0) {
         if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
-        if (MODE != kDown) ptx::prefetch_tensormap(&tmB1);
+        if (GATE || FUSED) ptx::prefetch_tensormap(&tmB1);
         ptx::prefetch_tensormap(&tmOut);
+        if (MODE == kDH) ptx::prefetch_tensormap(&tmOut2);
         if (FUSED) {
             ptx::prefetch_tensormap(&tmA);
             ptx::prefetch_tensormap(&tmB2);
@@ -582,7 +625,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (leader) ptx::mbar_arrive_expect_tx(full, 2 * kTx);
                     const uint32_t fullc = ptx::mapa(full, 0);
                     ptx::tma_load_2d_pair(sA, &tmA, fullc, kb * BK, row0);
-                    if (MODE == kGateUp) {
+                    if (GATE) {
                         // even CTA: gate columns (W1), odd CTA: up columns (W3)
                         const CUtensorMap *mb = leader ? &tmB0 : &tmB1;
                         ptx::tma_load_2d_pair(sB, mb, fullc, nb * 128, ky);
@@ -601,7 +644,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 } else {
                     ptx::mbar_arrive_expect_tx(full, kTx);
                     if (!GATHER) ptx::tma_load_2d(sA, &tmA, full, kb * BK, row0);
-                    if (MODE != kDown) {
+                    if constexpr (MODE == kDH) {
+                        // W2[e] rows nb*256 .. +255 (n), columns kb*64 .. +63 (d):
+                        // four 64-row boxes stacked into one K-major 256-row tile
+                        const int brow = e * args.bn_rows + nb * BN;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            ptx::tma_load_2d(sB + q * kBBox, &tmB0, full, kb * BK, brow + q * 64);
+                    } else if (MODE != kDown) {
                         ptx::tma_load_2d(sB + 0 * kBBox, &tmB0, full, nb * 128, ky);
                         ptx::tma_load_2d(sB + 1 * kBBox, &tmB0, full, nb * 128 + 64, ky);
                         ptx::tma_load_2d(sB + 2 * kBBox, &tmB1, full, nb * 128, ky);
@@ -647,11 +697,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint64_t adesc = ptx::desc_sw128(sA + k * 32, 16, 1024);
-                    const uint64_t bdesc = ptx::desc_sw128(sB + k * 2048, kBBox, 1024);
+                    // B MN-major: the next 16 k-rows are 2048 bytes on; K-major (kDH):
+                    // the next 16 k-columns are 32 bytes on within each row
+                    const uint64_t bdesc = MODE == kDH ? ptx::desc_sw128(sB + k * 32, 16, 1024)
+                                                       : ptx::desc_sw128(sB + k * 2048, kBBox, 1024);
+                    constexpr uint32_t kId = idesc_of<MODE, PAIR>();
                     if constexpr (PAIR)
-                        ptx::tc_mma_f16_pair(d_tmem, adesc, bdesc, G::kIdesc, (kb | k) != 0);
+                        ptx::tc_mma_f16_pair(d_tmem, adesc, bdesc, kId, (kb | k) != 0);
                     else
-                        ptx::tc_mma_f16(d_tmem, adesc, bdesc, G::kIdesc, (kb | k) != 0);
+                        ptx::tc_mma_f16(d_tmem, adesc, bdesc, kId, (kb | k) != 0);
                 }
                 if constexpr (PAIR)
                     ptx::tc_commit_pair(ptx::smem_addr(&ctl->empty[s]), 0x3);
@@ -697,6 +751,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
         };
         int nxt[16];
+#if MOE_GEMM_GATHER_HINT
+        const uint64_t gpol = ptx::policy_evict_last();
+#endif
         if (first_unit < total_units) load_tok(first_unit, nxt);
         for (int u = first_unit; u < total_units && ok; u += unit_stride) {
             const Unit cur = unit_at(u);
@@ -722,9 +779,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int r = gw * 4 + rr + 8 * i;
-                    if (tok[i] >= 0)
+                    if (tok[i] >= 0) {
+#if MOE_GEMM_GATHER_HINT
+                        ptx::cp_async_16_hint(sA + r * 128 + ((c ^ (r & 7)) << 4),
+                                              args.X + (int64_t)tok[i] * args.Kdim + kb * BK + c * 8,
+                                              gpol);
+#else
                         ptx::cp_async_16(sA + r * 128 + ((c ^ (r & 7)) << 4),
                                          args.X + (int64_t)tok[i] * args.Kdim + kb * BK + c * 8);
+#endif
+                    }
                 }
                 ptx::cp_async_commit_group();
                 if (it >= (uint32_t)kGatherLag) {
@@ -769,7 +833,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // chunk through shared memory and a TMA store (whole 64-byte row
             // segments); otherwise each valid row is stored directly.
             const bool whole = q * 32 + 31 < rows;
-            auto emit = [&](const uint32_t (&packed)[16], __nv_bfloat16 *dst, int col) {
+            auto emit = [&](const uint32_t (&packed)[16], __nv_bfloat16 *dst, int col,
+                            const CUtensorMap *map) {
                 if (whole) {
                     // buffers rotate with the store groups, so the group that last
                     // read this buffer is the kNBuf-th most recent one
@@ -785,7 +850,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::tma_store_2d(omap, buf, col, row0 + q * 32);
+                        ptx::tma_store_2d(map, buf, col, row0 + q * 32);
                         ptx::bulk_commit_group();
                     }
                     ++epi_groups;
@@ -797,7 +862,55 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                            packed[4 * i + 3]);
                 }
             };
-            if (!dn) {
+            if constexpr (MODE == kDH) {
+                // g = dY[t_p] W2[e]^T for 256 columns j of the expert's hidden
+                // layer; with the stored pre-activations a1, a3 of row p:
+                //   dA1 = w g a3 s (1 + a1 (1 - s)), dA3 = w g SiLU(a1), s = sigmoid(a1)
+                // and the routing weight's gradient gets sum_j g SiLU(a1) a3, summed
+                // here per 32-column chunk (ascending j) into dS partials
+                float w = 0.f;
+                if (valid) {
+                    const int slot = args.perm_slot != nullptr ? __ldg(args.perm_slot + p) : (int)p;
+                    if (slot >= 0 && slot < args.R) w = __ldg(args.topk_w + slot);
+                    else atomicOr(args.err, MOE_DEVERR_BAD_EXPERT);
+                }
+                const int64_t rowoff = p * args.out_ld + nb * BN;
+#pragma unroll 1
+                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                    uint32_t gv[32];
+                    ptx::tmem_ld32(taddr + c * 32, gv);
+                    float4 x1[8], x3[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        x1[i] = valid ? __ldg(reinterpret_cast<const float4 *>(args.pre1 + rowoff + c * 32) + i)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                        x3[i] = valid ? __ldg(reinterpret_cast<const float4 *>(args.pre3 + rowoff + c * 32) + i)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    float part = 0.f;
+                    uint32_t pa[16], pb[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float r1[2], r3[2];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const float a1 = (&x1[i >> 1].x)[2 * (i & 1) + hh];
+                            const float a3 = (&x3[i >> 1].x)[2 * (i & 1) + hh];
+                            const float g = __uint_as_float(gv[2 * i + hh]);
+                            const float sg = __fdividef(1.0f, 1.0f + __expf(-a1));
+                            const float silu = a1 * sg;
+                            part += g * (silu * a3);
+                            r1[hh] = w * g * a3 * sg * (1.0f + a1 * (1.0f - sg));
+                            r3[hh] = w * g * silu;
+                        }
+                        pa[i] = pack_bf16x2(r1[0], r1[1]);
+                        pb[i] = pack_bf16x2(r3[0], r3[1]);
+                    }
+                    emit(pa, args.out + rowoff + c * 32, nb * BN + c * 32, &tmOut);
+                    emit(pb, args.out3 + rowoff + c * 32, nb * BN + c * 32, &tmOut2);
+                    if (valid) args.dspart[p * args.ds_ld + nb * (BN / 32) + c] = part;
+                }
+            } else if (!dn) {
                 __nv_bfloat16 *dst = args.out + p * args.out_ld + nb * 128;
 #pragma unroll 1
                 for (int c = half * (4 / nhalf); c < (half + 1) * (4 / nhalf); ++c) {
@@ -813,7 +926,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
                         packed[i] = pack_bf16x2(h0, h1);
                     }
-                    emit(packed, dst + c * 32, nb * 128 + c * 32);
+                    emit(packed, dst + c * 32, nb * 128 + c * 32, omap);
+                    if constexpr (MODE == kGateUpPre) {
+                        // the pre-activations as they are (fp32): A1 (gate), A3 (up);
+                        // each lane writes its row's 128 bytes of the chunk
+                        if (valid) {
+                            const int64_t off = p * args.out_ld + nb * 128 + c * 32;
+                            float4 *d1 = reinterpret_cast<float4 *>(args.pre_out1 + off);
+                            float4 *d3 = reinterpret_cast<float4 *>(args.pre_out3 + off);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                d1[i] = make_float4(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1]),
+                                                    __uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3]));
+                                d3[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                            }
+                        }
+                    }
                 }
             } else {
                 float w = 0.f;
@@ -833,7 +962,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int i = 0; i < 16; ++i)
                         packed[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]),
                                                 w * __uint_as_float(v[2 * i + 1]));
-                    emit(packed, dst + c * 32, nb * BN + c * 32);
+                    emit(packed, dst + c * 32, nb * BN + c * 32, omap);
                 }
             }
             ptx::tc_fence_before();
@@ -1042,6 +1171,106 @@ cudaError_t launch_gemm_gate_up(const __nv_bfloat16 *X, const int32_t *perm_toke
     }
     // single CTAs gather their A rows themselves; the A map argument is not read
     return launch_variant<kGateUp, false>(tb0, tb0, tb1, th, args, tiles * args.NB, s);
+}
+
+namespace {
+// Epilogue warps as launch_variant chooses them, with the extra maps b2/out2.
+template <int MODE, bool PAIR>
+cudaError_t launch_ew_auto(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                           const CUtensorMap &out, const CUtensorMap &b2, const CUtensorMap &out2,
+                           const GemmArgs &args, int max_units, cudaStream_t s) {
+    if (args.Kdim / BK <= 8)
+        return launch_ew<MODE, PAIR, 8>(a, b0, b1, out, b2, out2, args, max_units, s);
+    return launch_ew<MODE, PAIR, 4>(a, b0, b1, out, b2, out2, args, max_units, s);
+}
+
+// dS[p] = sum of the row's partials in ascending column order (rows in use).
+__global__ void __launch_bounds__(256)
+ds_reduce_kernel(const float *__restrict__ part, int ld, int R, const int32_t *__restrict__ rows_used,
+                 float *__restrict__ dS) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= R || p >= __ldg(rows_used)) return;
+    const float *row = part + p * ld;
+    float acc = row[0];
+    for (int i = 1; i < ld; ++i) acc = __fadd_rn(acc, row[i]);
+    dS[p] = acc;
+}
+}  // namespace
+
+cudaError_t launch_gemm_gate_up_train(const __nv_bfloat16 *X, const int32_t *perm_token, int T,
+                                      const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                                      const int32_t *offsets, int R, int d, int E, int n,
+                                      __nv_bfloat16 *H, float *A1, float *A3,
+                                      __nv_bfloat16 *xg, uint32_t *err, cudaStream_t s) {
+    CUtensorMap ta, tb0, tb1, th;
+    if (!make_map(&tb0, W1, n, (uint64_t)E * d, 64, BK) ||
+        !make_map(&tb1, W3, n, (uint64_t)E * d, 64, BK) ||
+        !make_map(&th, H, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    GemmArgs args{};
+    args.X = X;
+    args.perm_token = perm_token;
+    args.T = T;
+    args.offsets = offsets;
+    args.E = E;
+    args.R = R;
+    args.Kdim = d;
+    args.NB = n / 128;
+    args.out = H;
+    args.out_ld = n;
+    args.pre_out1 = A1;
+    args.pre_out3 = A3;
+    args.err = err;
+    const int tiles = R / BM + E;  // upper bound of the 128-row tiles
+    if (use_pair(R, E)) {
+        cudaError_t e = launch_gather_rows(X, perm_token, T, R, offsets + E, d, xg, err, s);
+        if (e != cudaSuccess) return e;
+        if (!make_map(&ta, xg, d, R, 64, BM)) return cudaErrorInvalidValue;
+        return launch_ew_auto<kGateUpPre, true>(ta, tb0, tb1, th, tb0, th, args,
+                                                (tiles / 2 + E) * args.NB, s);
+    }
+    return launch_ew_auto<kGateUpPre, false>(tb0, tb0, tb1, th, tb0, th, args, tiles * args.NB, s);
+}
+
+cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_token, int T,
+                               const __nv_bfloat16 *W2, const float *A1,
+                               const float *A3, const float *topk_w,
+                               const int32_t *perm_slot, const int32_t *offsets, int R, int d,
+                               int E, int n, __nv_bfloat16 *dA1, __nv_bfloat16 *dA3,
+                               float *dspart, float *dS, uint32_t *err, cudaStream_t s) {
+    CUtensorMap tb, t1, t3;
+    // W2 as [E*n rows, d columns]: 64 x 64 boxes, K-major (d contiguous)
+    if (!make_map(&tb, W2, d, (uint64_t)E * n, 64, 64) ||
+        !make_map(&t1, dA1, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&t3, dA3, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    GemmArgs args{};
+    args.X = dY;
+    args.perm_token = perm_token;
+    args.T = T;
+    args.offsets = offsets;
+    args.E = E;
+    args.R = R;
+    args.Kdim = d;
+    args.NB = n / BN;
+    args.out = dA1;
+    args.out_ld = n;
+    args.out3 = dA3;
+    args.topk_w = topk_w;
+    args.perm_slot = perm_slot;
+    args.err = err;
+    args.pre1 = A1;
+    args.pre3 = A3;
+    args.bn_rows = n;
+    args.dspart = dspart;
+    args.ds_ld = n / 32;
+    const int tiles = R / BM + E;
+    cudaError_t e = launch_ew_auto<kDH, false>(tb, tb, tb, t1, tb, t3, args, tiles * args.NB, s);
+    if (e != cudaSuccess) return e;
+    return launch_k(ds_reduce_kernel, dim3((unsigned)((R + 255) / 256)), dim3(256), 0, s,
+                    static_cast<const float *>(dspart), n / 32, R, offsets + E, dS);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {

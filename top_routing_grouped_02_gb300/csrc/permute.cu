@@ -18,7 +18,9 @@
 //              its token's row, gets no row (rank -1) and is flagged.
 //  2. scan:    one block per expert turns the chunk counts into exclusive
 //              prefix sums; the last block to finish (ticket counter) scans the
-//              expert totals into offsets, tile bases and the tile list.
+//              expert totals into offsets, tile bases and the tile list (the
+//              list is skipped when tiles is NULL: the whole-layer call's
+//              GEMMs decode their units from the offsets).
 //  3. scatter: p = offsets[e] + chunk prefix + rank; writes perm_token,
 //              perm_slot and row_of_slot.
 #include "common.cuh"
@@ -145,7 +147,7 @@ scan_kernel(int32_t *__restrict__ chunk_cnt, int nchunks, int E, const int32_t *
         tile_base[ee] = tb;
         if (counts_in != nullptr && counts_in[ee] != c)
             atomicOr(&ctrl[kWordErr], MOE_DEVERR_COUNT_MISMATCH);
-        for (int i = 0; i < ntile; ++i) {
+        for (int i = 0; tiles != nullptr && i < ntile; ++i) {
             int4 tv;
             tv.x = ee;
             tv.y = off + i * kTileM;
@@ -157,7 +159,7 @@ scan_kernel(int32_t *__restrict__ chunk_cnt, int nchunks, int E, const int32_t *
     if (ee == 0) {
         offsets[E] = tot_rows;
         tile_base[E] = tot_tiles;
-        num_tiles[0] = tot_tiles;
+        if (num_tiles != nullptr) num_tiles[0] = tot_tiles;
         ctrl[kWordDone] = 0;
     }
 }

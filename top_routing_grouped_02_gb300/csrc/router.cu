@@ -1001,11 +1001,15 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
     return launch_k(kern, grid, dim3(kWThreads), 0, s, X, Wr, bias, T, d, E, L);
 }
 
+bool route_is_one_kernel(int d, int E, bool wr16) {
+    return E <= 32 && E % 4 == 0 && wr16 && d <= kRouteMaxBlocks * kLogitBlock;
+}
+
 cudaError_t launch_route(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T,
                          int d, int E, int K, int renorm, float *logits, int32_t *idx, float *w,
                          int32_t *counts, cudaStream_t s) {
     const bool wr16 = (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
-    if (E <= 32 && E % 4 == 0 && wr16 && d <= kRouteMaxBlocks * kLogitBlock) {
+    if (route_is_one_kernel(d, E, wr16)) {
         // logits and selection in one kernel; its CTAs add into zeroed counts
         cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
         if (e != cudaSuccess) return e;

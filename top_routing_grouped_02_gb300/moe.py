@@ -26,6 +26,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # when it runs on CTA pairs, and the whole-layer calls depend on the shape
 # (forward_launches).
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
+            "moe_gemm_gate_up_train": 1, "moe_backward_dh": 2,
             "moe_gemm_down": 1, "moe_combine": 1, "moe_round_routing": 3, "moe_combine_rows": 1}
 TILE_M = 128
 
@@ -54,6 +55,10 @@ _SIGS = {
     "moe_permute_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_gemm_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_gemm_down": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_gemm_gate_up_train": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ,
+                                    _P]),
+    "moe_backward_dh": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                             _SZ, _P]),
     "moe_expert_mlp": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
                             _P]),
     "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _P]),
@@ -233,6 +238,41 @@ def moe_gemm_gate_up(X, W1, W3, perm_token, offsets, K: int, ws=None, stream=Non
         _ptr(perm_token, torch.int32), _ptr(offsets, torch.int32), T, d, E, K, n, _ptr(H),
         _ptr(ws), ws.numel(), _stream(stream)))
     return H
+
+
+def moe_gemm_gate_up_train(X, W1, W3, perm_token, offsets, K: int, ws=None, stream=None):
+    """(H [T*K, n] bf16, A1, A3 [T*K, n] fp32): H as moe_gemm_gate_up gives it
+    and the pre-activations x W1[e], x W3[e] of every grouped row."""
+    T, d = X.shape
+    E, _, n = W1.shape
+    if ws is None:
+        ws = workspace(T, d, E, K, n, X.device)
+    H = torch.empty((T * K, n), dtype=torch.bfloat16, device=X.device)
+    A1, A3 = (torch.empty((T * K, n), dtype=torch.float32, device=X.device) for _ in range(2))
+    _check("moe_gemm_gate_up_train", lib().moe_gemm_gate_up_train(
+        _ptr(X, torch.bfloat16, "X"), _ptr(W1, torch.bfloat16, "W1"), _ptr(W3, torch.bfloat16, "W3"),
+        _ptr(perm_token, torch.int32, "perm_token"), _ptr(offsets, torch.int32, "offsets"),
+        T, d, E, K, n, _ptr(H), _ptr(A1), _ptr(A3), _ptr(ws), ws.numel(), _stream(stream)))
+    return H, A1, A3
+
+
+def moe_backward_dh(dY, W2, A1, A3, topk_w, perm_token, perm_slot, offsets, K: int, ws=None,
+                    stream=None):
+    """(dA1, dA3 [T*K, n] bf16, dS [T*K] fp32) of the grouped rows: the backward's
+    dH step with the routing-weight gradient."""
+    T, d = dY.shape
+    E, n, _ = W2.shape
+    if ws is None:
+        ws = workspace(T, d, E, K, n, dY.device)
+    dA1, dA3 = (torch.empty((T * K, n), dtype=torch.bfloat16, device=dY.device) for _ in range(2))
+    dS = torch.zeros(T * K, dtype=torch.float32, device=dY.device)
+    _check("moe_backward_dh", lib().moe_backward_dh(
+        _ptr(dY, torch.bfloat16, "dY"), _ptr(W2, torch.bfloat16, "W2"), _ptr(A1, torch.float32, "A1"),
+        _ptr(A3, torch.float32, "A3"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(perm_token, torch.int32, "perm_token"), _ptr(perm_slot, torch.int32, "perm_slot"),
+        _ptr(offsets, torch.int32, "offsets"), T, d, E, K, n, _ptr(dA1), _ptr(dA3), _ptr(dS),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return dA1, dA3, dS
 
 
 def moe_gemm_down(H, W2, topk_w, perm_slot, offsets, T: int, K: int, ws=None, stream=None):
