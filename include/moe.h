@@ -238,6 +238,20 @@ moe_status_t moe_backward_dh(const moe_bf16 *dY, const moe_bf16 *W2, const float
                              int E, int K, int n, moe_bf16 *dA1, moe_bf16 *dA3, float *dS,
                              void *ws, size_t ws_bytes, void *stream);
 
+/* The backward's dX step for the expert MLPs: one grouped GEMM per row
+ *   dXg[p,:] = dA1[p,:] W1[e]^T + dA3[p,:] W3[e]^T       (reduction 2n, fp32)
+ * stored as bf16 [T*K, d] (grouped rows), then the combine of moe_combine:
+ *   dX[t,:] = bf16( sum over k ascending of dXg[row_of_slot[t*K+k],:] )
+ * dA1, dA3 [T*K, n] bf16 as moe_backward_dh writes them; W1, W3 [E,d,n] bf16
+ * read with n, the reduction, as the contiguous dimension. dX is the experts'
+ * share of the input gradient (the router adds dL Wr^T). ws: any workspace of
+ * >= 64 bytes (its error word flags bad offsets). Two kernels. */
+moe_status_t moe_backward_dx(const moe_bf16 *dA1, const moe_bf16 *dA3, const moe_bf16 *W1,
+                             const moe_bf16 *W3, const int32_t *offsets,
+                             const int32_t *row_of_slot, int T, int d, int E, int K, int n,
+                             moe_bf16 *dXg, moe_bf16 *dX, void *ws, size_t ws_bytes,
+                             void *stream);
+
 /* Both expert GEMMs: H as moe_gemm_gate_up writes it, then Z as moe_gemm_down
  * writes it, bit for bit. Two launches (three on CTA pairs); with
  * MOE_GEMM_FUSED=1 and n <= 2048, ONE persistent launch (the SonicMoE page's

@@ -5,7 +5,9 @@ the pre-activations A1 = x W1[e], A3 = x W3[e] (fp32) within the tolerance
 below of the oracle's unrounded products. moe_backward_dh, fed with those, must give
 dA1, dA3 and the routing-weight gradient dS of every grouped row within the
 tolerance the forward's H and Z are held to, against oracle.backward_rows
-(the gradient of sum(Y * dY) with the top-K choice fixed, in double).
+(the gradient of sum(Y * dY) with the top-K choice fixed, in double), and
+moe_backward_dx, fed with dA1 and dA3, each row's share of dX within that
+tolerance and their sum per token within the Y tolerance.
 
 A row's quantities depend only on its token, its expert and the weights, so
 on the SonicMoE shape the oracle runs on the sampled tokens alone (their own
@@ -17,7 +19,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_common import check_hz, f64_of_bits, bits, layer_np
+from gpu_common import bits, check_hz, check_y, f64_of_bits, layer_np
 from top_routing_grouped_02_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
@@ -46,13 +48,15 @@ def _gpu_steps(inp, dY, K):
                                            g["offsets"], K, ws=ws)
     dA1, dA3, dS = moe.moe_backward_dh(dY, inp["W2"], A1, A3, w.view(-1), g["perm_token"],
                                        g["perm_slot"], g["offsets"], K, ws=ws)
+    dXg, dX = moe.moe_backward_dx(dA1, dA3, inp["W1"], inp["W3"], g["offsets"], g["row_of_slot"],
+                                  K, ws=ws)
     torch.cuda.synchronize()
     st, word = moe.moe_sync_check(ws)
     assert st == 0, (st, word)
     R = int(g["offsets"][-1].item())
     # the training gate/up GEMM stores H exactly as the forward one does
     assert torch.equal(H[:R].view(torch.int16), H0[:R].view(torch.int16))
-    return dict(idx=idx, H=H, A1=A1, A3=A3, dA1=dA1, dA3=dA3, dS=dS, **g)
+    return dict(idx=idx, H=H, A1=A1, A3=A3, dA1=dA1, dA3=dA3, dS=dS, dXg=dXg, dX=dX, **g)
 
 
 def _f64(a):
@@ -86,6 +90,10 @@ def test_backward_dh_matches_oracle_in_full(pair, monkeypatch):
     check_hz(bits(s["dA1"]), ref["dA1"], "dA1")
     check_hz(bits(s["dA3"]), ref["dA3"], "dA3")
     check_f32(s["dS"].cpu().numpy(), ref["dS"], "dS")
+    # dX step: each row's share, then the sum over a token's rows
+    check_hz(bits(s["dXg"]), ref["dXg"], "dXg")
+    _, _, _, ros_r = oracle.permute(idx_r, E)
+    check_y(bits(s["dX"]), oracle.combine(ref["dXg"], ros_r, K), "dX (experts' share)")
 
 
 def test_backward_dh_sonic_shape_sampled_tokens():
@@ -115,6 +123,11 @@ def test_backward_dh_sonic_shape_sampled_tokens():
     check_hz(bits(s["dA1"][P]), ref["dA1"], "dA1 (sampled tokens)")
     check_hz(bits(s["dA3"][P]), ref["dA3"], "dA3 (sampled tokens)")
     check_f32(s["dS"][P].cpu().numpy(), ref["dS"], "dS (sampled tokens)")
+    check_hz(bits(s["dXg"][P]), ref["dXg"], "dXg (sampled tokens)")
+    # the sampled tokens' dX: the oracle's combine over the sub-problem's rows
+    _, _, _, ros_sub = oracle.permute(idx_sub, E)
+    Tt = torch.from_numpy(toks.astype(np.int64)).cuda()
+    check_y(bits(s["dX"][Tt]), oracle.combine(ref["dXg"], ros_sub, K), "dX (sampled tokens)")
 
 
 def test_backward_dh_rejects_n_not_a_multiple_of_256():

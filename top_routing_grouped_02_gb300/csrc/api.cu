@@ -313,6 +313,27 @@ moe_status_t moe_backward_dh(const moe_bf16 *dY, const moe_bf16 *W2, const float
         at<float>(ws, L.xg), dS, at<uint32_t>(ws, L.err), as_stream(stream)));
 }
 
+moe_status_t moe_backward_dx(const moe_bf16 *dA1, const moe_bf16 *dA3, const moe_bf16 *W1,
+                             const moe_bf16 *W3, const int32_t *offsets,
+                             const int32_t *row_of_slot, int T, int d, int E, int K, int n,
+                             moe_bf16 *dXg, moe_bf16 *dX, void *ws, size_t ws_bytes,
+                             void *stream) {
+    if (!dA1 || !dA3 || !W1 || !W3 || !offsets || !row_of_slot || !dXg || !dX || !ws)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (!aligned16(dA1) || !aligned16(dA3) || !aligned16(W1) || !aligned16(W3) ||
+        !aligned16(dXg) || !aligned16(dX))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < 64) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_backward_dx(
+        reinterpret_cast<const __nv_bfloat16 *>(dA1), reinterpret_cast<const __nv_bfloat16 *>(dA3),
+        reinterpret_cast<const __nv_bfloat16 *>(W1), reinterpret_cast<const __nv_bfloat16 *>(W3),
+        offsets, row_of_slot, T, K, T * K, d, E, n, reinterpret_cast<__nv_bfloat16 *>(dXg),
+        reinterpret_cast<__nv_bfloat16 *>(dX), at<uint32_t>(ws, 0), as_stream(stream)));
+}
+
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
                            const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
                            int K, int n, moe_bf16 *Z, void *ws, size_t ws_bytes, void *stream) {

@@ -113,6 +113,13 @@ cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_toke
                                const int32_t *perm_slot, const int32_t *offsets, int R, int d,
                                int E, int n, __nv_bfloat16 *dA1, __nv_bfloat16 *dA3,
                                float *dspart, float *dS, uint32_t *err, cudaStream_t s);
+// Backward dX: dXg [R, d] = dA1 W1[e]^T + dA3 W3[e]^T (bf16), then
+// dX [T, d] = sum over k of dXg[row_of_slot[t*K + k]] (the combine).
+cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA3,
+                               const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                               const int32_t *offsets, const int32_t *row_of_slot, int T, int K,
+                               int R, int d, int E, int n, __nv_bfloat16 *dXg,
+                               __nv_bfloat16 *dX, uint32_t *err, cudaStream_t s);
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,

@@ -129,14 +129,18 @@ struct Geo {
 // A3 = x W3[e] (fp32, the accumulators as they are) beside H, for the backward. kDH: the backward's
 // dH' = dY[t_p] W2[e]^T (B = W2[e] read K-major, rows of dY gathered like X),
 // whose epilogue forms dA1, dA3 and the routing-weight gradient's partial sums.
-enum Mode : int { kGateUp = 0, kDown = 1, kFused = 2, kGateUpPre = 3, kDH = 4 };
+// kDX: the backward's dXg = dA1 W1[e]^T + dA3 W3[e]^T over the grouped rows,
+// one reduction of 2n (dA1 against W1[e], then dA3 against W3[e], both weights
+// read K-major), stored as bf16 like Z.
+enum Mode : int { kGateUp = 0, kDown = 1, kFused = 2, kGateUpPre = 3, kDH = 4, kDX = 5 };
 
 // Instruction descriptor: B is MN-major (the forward's weights, K rows of N
 // contiguous columns) except for kDH, whose W2[e] rows are n-major with the
 // reduction dimension d contiguous (K-major).
 template <int MODE, bool PAIR>
 constexpr uint32_t idesc_of() {
-    return ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false, /*B MN-major*/ MODE != kDH);
+    return ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false,
+                           /*B MN-major*/ MODE != kDH && MODE != kDX);
 }
 
 // Single-CTA gate/up A rows are gathered by warps 2 and 3 with 16-byte cp.async.
@@ -234,7 +238,8 @@ struct GemmArgs {
     // dS [R, ds_ld]
     const float *pre1;
     const float *pre3;
-    int bn_rows;
+    int bn_rows;  // kDH, kDX: rows of the K-major weight per expert
+    int kb_half;  // kDX: k-blocks of the first half of the reduction (n / 64)
     float *dspart;
     int ds_ld;
 };
@@ -412,7 +417,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // A rows gathered in the kernel (single-CTA gate/up units) or loaded by TMA
     constexpr bool GATHER = (MODE == kGateUp || MODE == kGateUpPre || MODE == kDH || FUSED) && !PAIR;
     constexpr bool GATE = MODE == kGateUp || MODE == kGateUpPre;  // gate/up B boxes (W1 | W3)
-    static_assert(!(MODE == kDH && PAIR), "the backward dH GEMM runs single CTAs");
+    static_assert(!((MODE == kDH || MODE == kDX) && PAIR), "the backward GEMMs run single CTAs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -443,7 +448,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0 && lane == 0) {
         if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
-        if (GATE || FUSED) ptx::prefetch_tensormap(&tmB1);
+        if (GATE || FUSED || MODE == kDX) ptx::prefetch_tensormap(&tmB1);
+        if (MODE == kDX) ptx::prefetch_tensormap(&tmB2);
         ptx::prefetch_tensormap(&tmOut);
         if (MODE == kDH) ptx::prefetch_tensormap(&tmOut2);
         if (FUSED) {
@@ -654,6 +660,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         ptx::tma_load_2d(sB + q * kBBox, &tmB2, full, nb * BN + q * 64, ky);
+                } else if constexpr (MODE == kDX) {
+                    // k-blocks 0 .. n/64-1: dA1 rows against W1[e]; then dA3 against W3[e].
+                    // W rows e*d + nb*256 .. +255 (d), columns kx .. kx+63 (n): K-major
+                    ptx::mbar_arrive_expect_tx(full, kTx);
+                    const bool second = kb >= args.kb_half;
+                    const int kx = (second ? kb - args.kb_half : kb) * BK;
+                    ptx::tma_load_2d(sA, second ? &tmB2 : &tmA, full, kx, row0);
+                    const int brow = e * args.bn_rows + nb * BN;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        ptx::tma_load_2d(sB + q * kBBox, second ? &tmB1 : &tmB0, full, kx, brow + q * 64);
                 } else {
                     ptx::mbar_arrive_expect_tx(full, kTx);
                     if (!GATHER) ptx::tma_load_2d(sA, &tmA, full, kb * BK, row0);
@@ -712,8 +729,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint64_t adesc = ptx::desc_sw128(sA + k * 32, 16, 1024);
                     // B MN-major: the next 16 k-rows are 2048 bytes on; K-major (kDH):
                     // the next 16 k-columns are 32 bytes on within each row
-                    const uint64_t bdesc = MODE == kDH ? ptx::desc_sw128(sB + k * 32, 16, 1024)
-                                                       : ptx::desc_sw128(sB + k * 2048, kBBox, 1024);
+                    const uint64_t bdesc = (MODE == kDH || MODE == kDX)
+                                               ? ptx::desc_sw128(sB + k * 32, 16, 1024)
+                                               : ptx::desc_sw128(sB + k * 2048, kBBox, 1024);
                     constexpr uint32_t kId = idesc_of<MODE, PAIR>();
                     if constexpr (PAIR)
                         ptx::tc_mma_f16_pair(d_tmem, adesc, bdesc, kId, (kb | k) != 0);
@@ -833,7 +851,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const Unit un = unit_at(u);
             if (!un.valid) continue;
             const int nb = un.nb, row0 = un.row0, rows = un.rows;
-            const bool dn = MODE == kDown || (FUSED && un.down);
+            const bool dn = MODE == kDown || MODE == kDX || (FUSED && un.down);
             const CUtensorMap *omap = FUSED && un.down ? &tmOut2 : &tmOut;
             const uint32_t a = uc & 1u, aph = (uc >> 1) & 1u;
             ++uc;
@@ -959,7 +977,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             } else {
                 float w = 0.f;
-                if (valid) {
+                if (MODE == kDX) {
+                    w = 1.f;  // dXg carries no routing weight (dA1, dA3 already do)
+                } else if (valid) {
                     const int slot = args.perm_slot != nullptr ? __ldg(args.perm_slot + p) : (int)p;
                     if (slot >= 0 && slot < args.R) w = __ldg(args.topk_w + slot);
                     else atomicOr(args.err, MOE_DEVERR_BAD_EXPERT);
@@ -1284,6 +1304,37 @@ cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_toke
     if (e != cudaSuccess) return e;
     return launch_k(ds_reduce_kernel, dim3((unsigned)((R + 255) / 256)), dim3(256), 0, s,
                     static_cast<const float *>(dspart), n / 32, R, offsets + E, dS);
+}
+
+cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA3,
+                               const __nv_bfloat16 *W1, const __nv_bfloat16 *W3,
+                               const int32_t *offsets, const int32_t *row_of_slot, int T, int K,
+                               int R, int d, int E, int n, __nv_bfloat16 *dXg,
+                               __nv_bfloat16 *dX, uint32_t *err, cudaStream_t s) {
+    CUtensorMap ta1, ta3, tw1, tw3, tout;
+    // A: rows of dA1 / dA3 [R, n], boxes of 64 columns x 128 rows; B: W1 / W3
+    // as [E*d rows, n columns], 64 x 64 boxes (n contiguous: K-major)
+    if (!make_map(&ta1, dA1, n, R, 64, BM) || !make_map(&ta3, dA3, n, R, 64, BM) ||
+        !make_map(&tw1, W1, n, (uint64_t)E * d, 64, 64) ||
+        !make_map(&tw3, W3, n, (uint64_t)E * d, 64, 64) ||
+        !make_map(&tout, dXg, d, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    GemmArgs args{};
+    args.offsets = offsets;
+    args.E = E;
+    args.R = R;
+    args.Kdim = 2 * n;
+    args.NB = d / BN;
+    args.out = dXg;
+    args.out_ld = d;
+    args.err = err;
+    args.bn_rows = d;
+    args.kb_half = n / BK;
+    const int tiles = R / BM + E;
+    cudaError_t e =
+        launch_ew_auto<kDX, false>(ta1, tw1, tw3, tout, ta3, tout, args, tiles * args.NB, s);
+    if (e != cudaSuccess) return e;
+    return launch_combine(dXg, row_of_slot, T, K, d, dX, s);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {

@@ -26,7 +26,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # when it runs on CTA pairs, and the whole-layer calls depend on the shape
 # (forward_launches).
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
-            "moe_gemm_gate_up_train": 1, "moe_backward_dh": 2,
+            "moe_gemm_gate_up_train": 1, "moe_backward_dh": 2, "moe_backward_dx": 2,
             "moe_gemm_down": 1, "moe_combine": 1, "moe_round_routing": 3, "moe_combine_rows": 1}
 TILE_M = 128
 
@@ -59,6 +59,7 @@ _SIGS = {
                                     _P]),
     "moe_backward_dh": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                              _SZ, _P]),
+    "moe_backward_dx": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_expert_mlp": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
                             _P]),
     "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _P]),
@@ -273,6 +274,24 @@ def moe_backward_dh(dY, W2, A1, A3, topk_w, perm_token, perm_slot, offsets, K: i
         _ptr(offsets, torch.int32, "offsets"), T, d, E, K, n, _ptr(dA1), _ptr(dA3), _ptr(dS),
         _ptr(ws), ws.numel(), _stream(stream)))
     return dA1, dA3, dS
+
+
+def moe_backward_dx(dA1, dA3, W1, W3, offsets, row_of_slot, K: int, ws=None, stream=None):
+    """(dXg [T*K, d] bf16 grouped rows, dX [T, d] bf16): the experts' share of the
+    input gradient."""
+    R, n = dA1.shape
+    E, d, _ = W1.shape
+    T = R // K
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=dA1.device)
+    dXg = torch.empty((R, d), dtype=torch.bfloat16, device=dA1.device)
+    dX = torch.empty((T, d), dtype=torch.bfloat16, device=dA1.device)
+    _check("moe_backward_dx", lib().moe_backward_dx(
+        _ptr(dA1, torch.bfloat16, "dA1"), _ptr(dA3, torch.bfloat16, "dA3"),
+        _ptr(W1, torch.bfloat16, "W1"), _ptr(W3, torch.bfloat16, "W3"),
+        _ptr(offsets, torch.int32, "offsets"), _ptr(row_of_slot, torch.int32, "row_of_slot"),
+        T, d, E, K, n, _ptr(dXg), _ptr(dX), _ptr(ws), ws.numel(), _stream(stream)))
+    return dXg, dX
 
 
 def moe_gemm_down(H, W2, topk_w, perm_slot, offsets, T: int, K: int, ws=None, stream=None):
