@@ -252,6 +252,32 @@ moe_status_t moe_backward_dx(const moe_bf16 *dA1, const moe_bf16 *dA3, const moe
                              moe_bf16 *dXg, moe_bf16 *dX, void *ws, size_t ws_bytes,
                              void *stream);
 
+/* The router's backward (SonicMoE page §2.2: from dS, the gradient of the
+ * routing scores' softmax; §3.2: the kept scores renormalised), with the
+ * top-K choice fixed. Per token, with p = softmax(logits[t,:]) over all E
+ * experts, kept = sum of p over the K chosen, w_k = p_k / kept (renorm) or p_k
+ * and dS_k = dS[row_of_slot[t*K+k]] (moe_backward_dh):
+ *   g_e     = (dS_k - sum_k' w_k' dS_k') / kept for e = topk_idx[t,k] with
+ *             renorm, dS_k without; 0 for the other experts
+ *   dL[t,e] = p_e (g_e - sum_e' p_e' g_e')                  fp32 [T, E]
+ * and over the batch
+ *   dbias   = sum over t of dL[t,:]                         fp32 [E]
+ *   dWr     = X^T dL                                        fp32 [d, E]
+ *   dX      = bf16( sum over k ascending of dXg[row_of_slot[t*K+k],:]
+ *                   + (dL Wr^T)[t,:] )                      bf16 [T, d]
+ * i.e. the full input gradient: the experts' rows (dXg from moe_backward_dx)
+ * and the router's share, added in fp32 and rounded once. logits [T,E] as
+ * moe_route wrote them; dWr and dL Wr^T are fp32 fma chains in fixed orders
+ * (t, e ascending), dbias a fixed tree: deterministic. ws: at least
+ * moe_workspace_bytes(T, d, E, K, 0) bytes (a workspace of the layer's shape
+ * serves); its gathered-rows region onwards holds dL Wr^T. Five kernels. */
+moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,
+                                 const int32_t *topk_idx, const float *dS,
+                                 const int32_t *row_of_slot, int T, int d, int E, int K,
+                                 int renorm, const moe_bf16 *dXg, moe_bf16 *dX, float *dL,
+                                 float *dWr, float *dbias, void *ws, size_t ws_bytes,
+                                 void *stream);
+
 /* Both expert GEMMs: H as moe_gemm_gate_up writes it, then Z as moe_gemm_down
  * writes it, bit for bit. Two launches (three on CTA pairs); with
  * MOE_GEMM_FUSED=1 and n <= 2048, ONE persistent launch (the SonicMoE page's

@@ -7,7 +7,10 @@ dA1, dA3 and the routing-weight gradient dS of every grouped row within the
 tolerance the forward's H and Z are held to, against oracle.backward_rows
 (the gradient of sum(Y * dY) with the top-K choice fixed, in double), and
 moe_backward_dx, fed with dA1 and dA3, each row's share of dX within that
-tolerance and their sum per token within the Y tolerance.
+tolerance and their sum per token within the Y tolerance; moe_backward_router
+the logits' gradient dL, dbias and dWr within the fp32 bound below and the full
+input gradient dX (experts' rows plus the router's share) within the Y
+tolerance, against oracle.backward.
 
 A row's quantities depend only on its token, its expert and the weights, so
 on the SonicMoE shape the oracle runs on the sampled tokens alone (their own
@@ -41,7 +44,9 @@ def _gpu_steps(inp, dY, K):
     T, d = inp["X"].shape
     E, _, n = inp["W1"].shape
     ws = moe.workspace(T, d, E, K, n)
-    idx, w, counts = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"])
+    E_ = inp["Wr"].shape[1]
+    logits = torch.empty((T, E_), dtype=torch.float32, device="cuda")
+    idx, w, counts = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"], logits=logits)
     g = moe.moe_permute(idx, E, counts=counts, ws=ws)
     H0 = moe.moe_gemm_gate_up(inp["X"], inp["W1"], inp["W3"], g["perm_token"], g["offsets"], K, ws=ws)
     H, A1, A3 = moe.moe_gemm_gate_up_train(inp["X"], inp["W1"], inp["W3"], g["perm_token"],
@@ -50,13 +55,15 @@ def _gpu_steps(inp, dY, K):
                                        g["perm_slot"], g["offsets"], K, ws=ws)
     dXg, dX = moe.moe_backward_dx(dA1, dA3, inp["W1"], inp["W3"], g["offsets"], g["row_of_slot"],
                                   K, ws=ws)
+    rb = moe.moe_backward_router(inp["X"], inp["Wr"], logits, idx, dS, g["row_of_slot"], dXg, ws=ws)
     torch.cuda.synchronize()
     st, word = moe.moe_sync_check(ws)
     assert st == 0, (st, word)
     R = int(g["offsets"][-1].item())
     # the training gate/up GEMM stores H exactly as the forward one does
     assert torch.equal(H[:R].view(torch.int16), H0[:R].view(torch.int16))
-    return dict(idx=idx, H=H, A1=A1, A3=A3, dA1=dA1, dA3=dA3, dS=dS, dXg=dXg, dX=dX, **g)
+    return dict(idx=idx, H=H, A1=A1, A3=A3, dA1=dA1, dA3=dA3, dS=dS, dXg=dXg, dX_experts=dX,
+                dX=rb["dX"], dL=rb["dL"], dWr=rb["dWr"], dbias=rb["dbias"], **g)
 
 
 def _f64(a):
@@ -93,7 +100,13 @@ def test_backward_dh_matches_oracle_in_full(pair, monkeypatch):
     # dX step: each row's share, then the sum over a token's rows
     check_hz(bits(s["dXg"]), ref["dXg"], "dXg")
     _, _, _, ros_r = oracle.permute(idx_r, E)
-    check_y(bits(s["dX"]), oracle.combine(ref["dXg"], ros_r, K), "dX (experts' share)")
+    check_y(bits(s["dX_experts"]), oracle.combine(ref["dXg"], ros_r, K), "dX (experts' share)")
+    # the router's backward and the full input gradient
+    check_f32(s["dL"].cpu().numpy(), ref["dL"], "dL")
+    full = oracle.backward(X, _f64(Wr), _f64(bias), W1, W3, W2, idx_r, f64_of_bits(bits(dY)))
+    check_f32(s["dbias"].cpu().numpy(), full["dbias"], "dbias")
+    check_f32(s["dWr"].cpu().numpy(), full["dWr"], "dWr")
+    check_y(bits(s["dX"]), full["dX"], "dX")
 
 
 def test_backward_dh_sonic_shape_sampled_tokens():
@@ -127,7 +140,13 @@ def test_backward_dh_sonic_shape_sampled_tokens():
     # the sampled tokens' dX: the oracle's combine over the sub-problem's rows
     _, _, _, ros_sub = oracle.permute(idx_sub, E)
     Tt = torch.from_numpy(toks.astype(np.int64)).cuda()
-    check_y(bits(s["dX"][Tt]), oracle.combine(ref["dXg"], ros_sub, K), "dX (sampled tokens)")
+    check_y(bits(s["dX_experts"][Tt]), oracle.combine(ref["dXg"], ros_sub, K),
+            "dX, experts' share (sampled tokens)")
+    # per-token quantities of the router's backward on the same sub-problem
+    check_f32(s["dL"][Tt].cpu().numpy(), ref["dL"], "dL (sampled tokens)")
+    full = oracle.backward(X[toks], _f64(Wr), _f64(bias), W1, W3, W2, idx_sub,
+                           f64_of_bits(bits(dY))[toks])
+    check_y(bits(s["dX"][Tt]), full["dX"], "dX (sampled tokens)")
 
 
 def test_backward_dh_rejects_n_not_a_multiple_of_256():

@@ -334,6 +334,30 @@ moe_status_t moe_backward_dx(const moe_bf16 *dA1, const moe_bf16 *dA3, const moe
         reinterpret_cast<__nv_bfloat16 *>(dX), at<uint32_t>(ws, 0), as_stream(stream)));
 }
 
+moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,
+                                 const int32_t *topk_idx, const float *dS,
+                                 const int32_t *row_of_slot, int T, int d, int E, int K,
+                                 int renorm, const moe_bf16 *dXg, moe_bf16 *dX, float *dL,
+                                 float *dWr, float *dbias, void *ws, size_t ws_bytes,
+                                 void *stream) {
+    if (!X || !Wr || !logits || !topk_idx || !dS || !row_of_slot || !dXg || !dX || !dL || !dWr ||
+        !dbias || !ws || (renorm != 0 && renorm != 1))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_route_shape(T, d, E, K);
+    if (s != MOE_OK) return s;
+    if (!aligned16(X) || !aligned16(dXg) || !aligned16(dX)) return MOE_ERR_INVALID_ARG;
+    // the router's share dL Wr^T (fp32 [T, d]) lives in the workspace from the
+    // gathered-rows region on (that region and the ones after it hold >= 4*T*d bytes)
+    const WsLayout L = ws_layout(T, d, E, K, 0);
+    const size_t need = L.xg + (size_t)T * d * sizeof(float);
+    if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    return from_cuda(launch_backward_router(
+        reinterpret_cast<const __nv_bfloat16 *>(X), Wr, logits, topk_idx, dS, row_of_slot, T, d, E,
+        K, renorm, reinterpret_cast<const __nv_bfloat16 *>(dXg), dL, dWr, dbias,
+        at<float>(ws, L.xg), reinterpret_cast<__nv_bfloat16 *>(dX), as_stream(stream)));
+}
+
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
                            const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
                            int K, int n, moe_bf16 *Z, void *ws, size_t ws_bytes, void *stream) {

@@ -120,6 +120,14 @@ cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA
                                const int32_t *offsets, const int32_t *row_of_slot, int T, int K,
                                int R, int d, int E, int n, __nv_bfloat16 *dXg,
                                __nv_bfloat16 *dX, uint32_t *err, cudaStream_t s);
+// Router backward (backward.cu): dL [T, E], dbias [E], dWr [d, E] (fp32) and
+// dX [T, d] = bf16(sum_k dXg[row_of_slot[t*K+k]] + dL Wr^T), with dXr [T, d]
+// fp32 scratch for the second term.
+cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, const float *L,
+                                   const int32_t *idx, const float *dS,
+                                   const int32_t *row_of_slot, int T, int d, int E, int K,
+                                   int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
+                                   float *dbias, float *dXr, __nv_bfloat16 *dX, cudaStream_t s);
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,

@@ -27,6 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # (forward_launches).
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
             "moe_gemm_gate_up_train": 1, "moe_backward_dh": 2, "moe_backward_dx": 2,
+            "moe_backward_router": 5,
             "moe_gemm_down": 1, "moe_combine": 1, "moe_round_routing": 3, "moe_combine_rows": 1}
 TILE_M = 128
 
@@ -60,6 +61,8 @@ _SIGS = {
     "moe_backward_dh": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                              _SZ, _P]),
     "moe_backward_dx": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "moe_backward_router": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                 _P, _SZ, _P]),
     "moe_expert_mlp": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
                             _P]),
     "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _P]),
@@ -292,6 +295,29 @@ def moe_backward_dx(dA1, dA3, W1, W3, offsets, row_of_slot, K: int, ws=None, str
         _ptr(offsets, torch.int32, "offsets"), _ptr(row_of_slot, torch.int32, "row_of_slot"),
         T, d, E, K, n, _ptr(dXg), _ptr(dX), _ptr(ws), ws.numel(), _stream(stream)))
     return dXg, dX
+
+
+def moe_backward_router(X, Wr, logits, topk_idx, dS, row_of_slot, dXg, renorm: bool = True,
+                        ws=None, stream=None) -> dict:
+    """The router's backward and the full input gradient: dict of dX [T, d] bf16,
+    dL [T, E], dWr [d, E], dbias [E] fp32."""
+    T, d = X.shape
+    E = Wr.shape[1]
+    K = topk_idx.shape[1]
+    if ws is None:
+        ws = workspace(T, d, E, K, 0, X.device)
+    out = dict(dX=torch.empty((T, d), dtype=torch.bfloat16, device=X.device),
+               dL=torch.empty((T, E), dtype=torch.float32, device=X.device),
+               dWr=torch.empty((d, E), dtype=torch.float32, device=X.device),
+               dbias=torch.empty(E, dtype=torch.float32, device=X.device))
+    _check("moe_backward_router", lib().moe_backward_router(
+        _ptr(X, torch.bfloat16, "X"), _ptr(Wr, torch.float32, "Wr"),
+        _ptr(logits, torch.float32, "logits"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(dS, torch.float32, "dS"), _ptr(row_of_slot, torch.int32, "row_of_slot"),
+        T, d, E, K, int(bool(renorm)), _ptr(dXg, torch.bfloat16, "dXg"), _ptr(out["dX"]),
+        _ptr(out["dL"]), _ptr(out["dWr"]), _ptr(out["dbias"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
 
 
 def moe_gemm_down(H, W2, topk_w, perm_slot, offsets, T: int, K: int, ws=None, stream=None):
