@@ -252,6 +252,26 @@ moe_status_t moe_backward_dx(const moe_bf16 *dA1, const moe_bf16 *dA3, const moe
                              moe_bf16 *dXg, moe_bf16 *dX, void *ws, size_t ws_bytes,
                              void *stream);
 
+/* The backward's weight gradients, with the top-K choice fixed (the sums over
+ * each expert's grouped rows p, t = perm_token[p], w = topk_w[perm_slot[p]]):
+ *   dW1[e] = sum_p X[t]^T dA1[p]      dW3[e] = sum_p X[t]^T dA3[p]    [E,d,n]
+ *   dW2[e] = sum_p H[p]^T (w dY[t])                                   [E,n,d]
+ * all fp32, one fp32 accumulation per output in the tensor cores. H [T*K,n]
+ * bf16 (the forward's), dA1, dA3 [T*K,n] bf16 (moe_backward_dh), X, dY [T,d]
+ * bf16. An expert with no rows gets zero gradients. w dY is rounded to bf16
+ * once per element (an operand of the grouped GEMM). Two grouped GEMMs after
+ * a gather of the rows into a layout where every expert's rows start on a
+ * 64-row boundary. scratch: moe_backward_dw_scratch_bytes(T, d, E, K) bytes,
+ * 256-byte aligned, whose first 4 bytes are a device error word as in a
+ * workspace (zero them once before first use; moe_sync_check reads them). */
+size_t moe_backward_dw_scratch_bytes(int T, int d, int E, int K);
+moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf16 *H,
+                             const moe_bf16 *dA1, const moe_bf16 *dA3, const float *topk_w,
+                             const int32_t *perm_token, const int32_t *perm_slot,
+                             const int32_t *offsets, int T, int d, int E, int K, int n,
+                             float *dW1, float *dW3, float *dW2, void *scratch,
+                             size_t scratch_bytes, void *stream);
+
 /* The router's backward (SonicMoE page §2.2: from dS, the gradient of the
  * routing scores' softmax; §3.2: the kept scores renormalised), with the
  * top-K choice fixed. Per token, with p = softmax(logits[t,:]) over all E

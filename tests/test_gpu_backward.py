@@ -7,7 +7,9 @@ dA1, dA3 and the routing-weight gradient dS of every grouped row within the
 tolerance the forward's H and Z are held to, against oracle.backward_rows
 (the gradient of sum(Y * dY) with the top-K choice fixed, in double), and
 moe_backward_dx, fed with dA1 and dA3, each row's share of dX within that
-tolerance and their sum per token within the Y tolerance; moe_backward_router
+tolerance and their sum per token within the Y tolerance; moe_backward_dw the
+weight gradients dW1, dW3, dW2 within the fp32 bound below (an expert that no
+token chose gets exact zeros); moe_backward_router
 the logits' gradient dL, dbias and dWr within the fp32 bound below and the full
 input gradient dX (experts' rows plus the router's share) within the Y
 tolerance, against oracle.backward.
@@ -162,3 +164,63 @@ def test_backward_dh_rejects_n_not_a_multiple_of_256():
                             z(T * K, dtype=torch.int32, device="cuda"),
                             z(E + 1, dtype=torch.int32, device="cuda"), K)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("T,d,E,K,n,empty", [
+    (512, 256, 8, 2, 512, None),   # the tiny layer
+    (300, 256, 16, 2, 256, 5),     # expert 5 chosen by no token: its gradients are zero
+    (700, 512, 4, 3, 768, None),   # several 64-row k-blocks and 128-row output tiles per expert
+])
+def test_weight_gradients_match_oracle(T, d, E, K, n, empty):
+    inp = synth.layer_inputs(T=T, d=d, E=E, n=n, device="cuda", seed=T)
+    if empty is not None:
+        bias = torch.zeros(E, dtype=torch.float32)
+        bias[empty] = -100.0
+        inp["bias"] = bias.cuda()
+    dY = _dY(T, d)
+    ws = moe.workspace(T, d, E, K, n)
+    idx, w, counts = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"])
+    g = moe.moe_permute(idx, E, counts=counts, ws=ws)
+    H, A1, A3 = moe.moe_gemm_gate_up_train(inp["X"], inp["W1"], inp["W3"], g["perm_token"],
+                                           g["offsets"], K, ws=ws)
+    dA1, dA3, dS = moe.moe_backward_dh(dY, inp["W2"], A1, A3, w.view(-1), g["perm_token"],
+                                       g["perm_slot"], g["offsets"], K, ws=ws)
+    out = moe.moe_backward_dw(inp["X"], dY, H, dA1, dA3, w.view(-1), g["perm_token"],
+                              g["perm_slot"], g["offsets"], K)
+    torch.cuda.synchronize()
+    for buf in (ws, out["scratch"]):
+        st, word = moe.moe_sync_check(buf)
+        assert st == 0, (st, word)
+    X, Wr, bias, W1, W3, W2 = layer_np(inp)
+    idx_r, _ = oracle.topk_softmax(oracle.router_logits(X, Wr, bias), K, True)
+    assert np.array_equal(idx.cpu().numpy(), idx_r)
+    if empty is not None:
+        assert int(counts[empty].item()) == 0
+        for k in ("dW1", "dW3", "dW2"):
+            assert torch.count_nonzero(out[k][empty]).item() == 0
+    full = oracle.backward(X, _f64(Wr), _f64(bias), W1, W3, W2, idx_r, f64_of_bits(bits(dY)))
+    # Each gradient entry is a sum over the expert's rows of products whose GPU
+    # operands are bf16 (dA1, dA3; H and w dY), each within 2^-8 of the exact
+    # value. So |error| <= 2^-8 * sum_p |a_p b_p| plus the fp32 accumulation's
+    # share; the check allows twice that, with the sums of absolute products
+    # taken from the oracle's own operands, and the relative Frobenius bound.
+    off_r, pt_r, ps_r, _ = oracle.permute(idx_r, E)
+    rows = oracle.backward_rows(X, _f64(Wr), _f64(bias), W1, W3, W2, idx_r, ps_r,
+                                f64_of_bits(bits(dY)))
+    A1r, A3r = oracle.gate_up_pre(X, W1, W3, pt_r, off_r)
+    h_r = np.abs(A1r / (1.0 + np.exp(-A1r)) * A3r)
+    _, w_r = oracle.topk_softmax(oracle.router_logits(X, Wr, bias), K, True)
+    wdy = np.abs(w_r.reshape(-1)[ps_r].astype(np.float64)[:, None]
+                 * f64_of_bits(bits(dY))[pt_r])
+    xg = np.abs(oracle.bf16_bits_to_f64(X)[pt_r])
+    for k, a, b in (("dW1", xg, np.abs(rows["dA1"])), ("dW3", xg, np.abs(rows["dA3"])),
+                    ("dW2", h_r, wdy)):
+        got = out[k].cpu().numpy().astype(np.float64)
+        ref = full[k]
+        for e in range(E):
+            r0, r1 = int(off_r[e]), int(off_r[e + 1])
+            bound = 2.0 ** -7 * (a[r0:r1].T @ b[r0:r1]) + 1e-6
+            err = np.abs(got[e] - ref[e])
+            assert np.all(err <= bound), (k, e, float((err / bound).max()))
+        fro = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+        assert fro <= FRO, f"{k}: rel-Frobenius {fro:.3e} > {FRO}"

@@ -358,6 +358,40 @@ moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float
         at<float>(ws, L.xg), reinterpret_cast<__nv_bfloat16 *>(dX), as_stream(stream)));
 }
 
+size_t moe_backward_dw_scratch_bytes(int T, int d, int E, int K) {
+    if (T < 1 || E < 1 || K < 1 || d < 1 || E > kMaxE || K > kMaxK || K > E) return 0;
+    const size_t pad = ((size_t)T * K + 64 * (size_t)E) * d * 2;
+    return 256 + (pad + 255) / 256 * 256 + 4 * (size_t)(E + 1);
+}
+
+moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf16 *H,
+                             const moe_bf16 *dA1, const moe_bf16 *dA3, const float *topk_w,
+                             const int32_t *perm_token, const int32_t *perm_slot,
+                             const int32_t *offsets, int T, int d, int E, int K, int n,
+                             float *dW1, float *dW3, float *dW2, void *scratch,
+                             size_t scratch_bytes, void *stream) {
+    if (!X || !dY || !H || !dA1 || !dA3 || !topk_w || !perm_token || !perm_slot || !offsets ||
+        !dW1 || !dW3 || !dW2 || !scratch)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t s = check_mlp_shape(T, d, E, K, n);
+    if (s != MOE_OK) return s;
+    if (!aligned16(X) || !aligned16(dY) || !aligned16(H) || !aligned16(dA1) || !aligned16(dA3) ||
+        !aligned16(dW1) || !aligned16(dW3) || !aligned16(dW2) ||
+        (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < moe_backward_dw_scratch_bytes(T, d, E, K)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_arch()) != MOE_OK) return s;
+    const size_t pad = ((size_t)T * K + 64 * (size_t)E) * d * 2;
+    char *base = static_cast<char *>(scratch);
+    return from_cuda(launch_backward_dw(
+        reinterpret_cast<const __nv_bfloat16 *>(X), reinterpret_cast<const __nv_bfloat16 *>(dY),
+        reinterpret_cast<const __nv_bfloat16 *>(H), reinterpret_cast<const __nv_bfloat16 *>(dA1),
+        reinterpret_cast<const __nv_bfloat16 *>(dA3), topk_w, perm_token, perm_slot, offsets, T,
+        T * K, d, E, n, dW1, dW3, dW2, reinterpret_cast<__nv_bfloat16 *>(base + 256),
+        reinterpret_cast<int32_t *>(base + 256 + (pad + 255) / 256 * 256),
+        reinterpret_cast<uint32_t *>(base), as_stream(stream)));
+}
+
 moe_status_t moe_gemm_down(const moe_bf16 *H, const moe_bf16 *W2, const float *topk_w,
                            const int32_t *perm_slot, const int32_t *offsets, int T, int d, int E,
                            int K, int n, moe_bf16 *Z, void *ws, size_t ws_bytes, void *stream) {

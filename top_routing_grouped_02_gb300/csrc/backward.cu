@@ -276,7 +276,92 @@ combine_add_kernel(const __nv_bfloat16 *__restrict__ dXg, const int32_t *__restr
     }
 }
 
+// Padded row offsets of the weight gradients: each expert's rows rounded up to
+// a multiple of 64; poff[E] is the padded total. One block (E <= 256).
+__global__ void __launch_bounds__(256)
+pad_offsets_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restrict__ poff) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ int32_t c[kMaxE];
+    const int e = threadIdx.x;
+    if (e < E) {
+        const int32_t n = offsets[e + 1] - offsets[e];
+        c[e] = n > 0 ? (n + 63) / 64 * 64 : 0;
+    }
+    __syncthreads();
+    if (e == 0) {
+        int32_t acc = 0;
+        for (int i = 0; i < E; ++i) {
+            poff[i] = acc;
+            acc += c[i];
+        }
+        poff[E] = acc;
+    }
+}
+
+// dst[q] for padded rows q < poff[E]: the source row of grouped row
+// p = offsets[e] + (q - poff[e]) (src[perm_token[p]], times w[perm_slot[p]]
+// when w is given, rounded to bf16 once), or zeros past the expert's rows. One
+// warp per row; indices out of range give a zero row.
+__global__ void __launch_bounds__(256)
+gather_pad_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restrict__ perm_token,
+                  int T, const int32_t *__restrict__ offsets, const int32_t *__restrict__ poff,
+                  int E, int d, const float *__restrict__ w, const int32_t *__restrict__ perm_slot,
+                  int64_t R, int64_t cap, __nv_bfloat16 *__restrict__ dst) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t q = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (q >= cap || q >= __ldg(poff + E)) return;
+    int lo = 0, hi = E - 1;  // the last expert whose padded rows start at or before q
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(poff + mid) <= q) lo = mid; else hi = mid - 1;
+    }
+    const int64_t local = q - __ldg(poff + lo);
+    const int64_t p = (int64_t)__ldg(offsets + lo) + local;
+    bool ok = local < (int64_t)__ldg(offsets + lo + 1) - __ldg(offsets + lo) && p >= 0 && p < R;
+    int64_t t = ok ? __ldg(perm_token + p) : -1;
+    ok = ok && t >= 0 && t < T;
+    float scale = 1.f;
+    if (ok && w != nullptr) {
+        const int32_t slot = __ldg(perm_slot + p);
+        ok = slot >= 0 && slot < R;
+        scale = ok ? __ldg(w + slot) : 0.f;
+    }
+    uint4 *out = reinterpret_cast<uint4 *>(dst + q * d);
+    for (int c = lane; c < d / 8; c += 32) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (ok) {
+            v = __ldg(reinterpret_cast<const uint4 *>(src + t * d) + c);
+            if (w != nullptr) {
+                __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 f = __bfloat1622float2(h2[u]);
+                    h2[u] = __floats2bfloat162_rn(scale * f.x, scale * f.y);
+                }
+            }
+        }
+        out[c] = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_padded(const __nv_bfloat16 *src, const int32_t *perm_token, int T,
+                                 const int32_t *offsets, int E, int d, const float *w,
+                                 const int32_t *perm_slot, int64_t R, int64_t cap,
+                                 int32_t *poff, __nv_bfloat16 *dst, bool offsets_done,
+                                 cudaStream_t s) {
+    if (!offsets_done) {
+        cudaError_t e = launch_k(pad_offsets_kernel, dim3(1), dim3(256), 0, s, offsets, E, poff);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_k(gather_pad_kernel, dim3((unsigned)((cap + 7) / 8)), dim3(256), 0, s, src,
+                    perm_token, T, offsets, static_cast<const int32_t *>(poff), E, d, w, perm_slot,
+                    R, cap, dst);
+}
 
 cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, const float *L,
                                    const int32_t *idx, const float *dS,

@@ -128,6 +128,24 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
                                    float *dbias, float *dXr, __nv_bfloat16 *dX, cudaStream_t s);
+// Rows of src gathered into the padded grouped layout of the weight gradients
+// (each expert's rows from a 64-row boundary, zeros after them), optionally
+// scaled by w[perm_slot[p]]; poff [E+1] receives (or, offsets_done, holds) the
+// padded offsets. dst: [cap, d] with cap >= R + 64*E.
+cudaError_t launch_gather_padded(const __nv_bfloat16 *src, const int32_t *perm_token, int T,
+                                 const int32_t *offsets, int E, int d, const float *w,
+                                 const int32_t *perm_slot, int64_t R, int64_t cap,
+                                 int32_t *poff, __nv_bfloat16 *dst, bool offsets_done,
+                                 cudaStream_t s);
+// Weight gradients: dW1, dW3 [E, d, n] and dW2 [E, n, d] (fp32). pad: scratch
+// [R + 64*E, d] bf16, poff: scratch [E+1].
+cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
+                               const __nv_bfloat16 *H, const __nv_bfloat16 *dA1,
+                               const __nv_bfloat16 *dA3, const float *topk_w,
+                               const int32_t *perm_token, const int32_t *perm_slot,
+                               const int32_t *offsets, int T, int R, int d, int E, int n,
+                               float *dW1, float *dW3, float *dW2, __nv_bfloat16 *pad,
+                               int32_t *poff, uint32_t *err, cudaStream_t s);
 cudaError_t launch_gemm_down(const __nv_bfloat16 *H, const __nv_bfloat16 *W2,
                              const float *topk_w, const int32_t *perm_slot,
                              const int32_t *offsets, int R, int d, int E, int n,

@@ -132,14 +132,25 @@ struct Geo {
 // kDX: the backward's dXg = dA1 W1[e]^T + dA3 W3[e]^T over the grouped rows,
 // one reduction of 2n (dA1 against W1[e], then dA3 against W3[e], both weights
 // read K-major), stored as bf16 like Z.
-enum Mode : int { kGateUp = 0, kDown = 1, kFused = 2, kGateUpPre = 3, kDH = 4, kDX = 5 };
+// kDW13, kDW2: the weight gradients, one unit per (expert, 128 output rows,
+// output columns) with the expert's rows as the reduction (64 per k-block);
+// both operands MN-major, loaded by TMA:
+//   kDW13: dW1[e] | dW3[e] (d x n, 128 + 128 columns) = Xg^T [dA1 | dA3]
+//   kDW2:  dW2[e] (n x d, 256 columns) = H^T (w dY)g
+// One operand of each is a row-padded copy (each expert's rows start on a
+// 64-row boundary, zeros after its last row): Xg for kDW13, w-scaled dY rows
+// for kDW2, so the k-block past an expert's last row adds nothing although its
+// other operand then reads the next expert's rows. Outputs are fp32.
+enum Mode : int {
+    kGateUp = 0, kDown = 1, kFused = 2, kGateUpPre = 3, kDH = 4, kDX = 5, kDW13 = 6, kDW2 = 7
+};
 
 // Instruction descriptor: B is MN-major (the forward's weights, K rows of N
 // contiguous columns) except for kDH, whose W2[e] rows are n-major with the
 // reduction dimension d contiguous (K-major).
 template <int MODE, bool PAIR>
 constexpr uint32_t idesc_of() {
-    return ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false,
+    return ptx::idesc_bf16(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ MODE == kDW13 || MODE == kDW2,
                            /*B MN-major*/ MODE != kDH && MODE != kDX);
 }
 
@@ -240,6 +251,13 @@ struct GemmArgs {
     const float *pre3;
     int bn_rows;  // kDH, kDX: rows of the K-major weight per expert
     int kb_half;  // kDX: k-blocks of the first half of the reduction (n / 64)
+    // kDW13 / kDW2: 128-row output tiles per expert, the outputs (fp32, [E, wout_rows,
+    // wout_ld]; kDW13 writes dW1 to wout1 and dW3 to wout3)
+    int MT;
+    float *wout1;
+    float *wout3;
+    int wout_rows;
+    int wout_ld;
     float *dspart;
     int ds_ld;
 };
@@ -327,6 +345,8 @@ struct Unit {
     bool valid;  // false: an empty position of the fused sequence
     bool down;
     int e, nb, row0, rows, tile;
+    int kbs;       // k-blocks of the unit's main loop
+    int poff, off;  // weight gradients: the expert's first padded row and first row
 };
 
 // Fused sequence. Each stream (gate/up units, down units) runs expert-major,
@@ -418,6 +438,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr bool GATHER = (MODE == kGateUp || MODE == kGateUpPre || MODE == kDH || FUSED) && !PAIR;
     constexpr bool GATE = MODE == kGateUp || MODE == kGateUpPre;  // gate/up B boxes (W1 | W3)
     static_assert(!((MODE == kDH || MODE == kDX) && PAIR), "the backward GEMMs run single CTAs");
+    constexpr bool WGRAD = MODE == kDW13 || MODE == kDW2;
+    static_assert(!(WGRAD && PAIR), "the weight-gradient GEMMs run single CTAs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -448,7 +470,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0 && lane == 0) {
         if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
-        if (GATE || FUSED || MODE == kDX) ptx::prefetch_tensormap(&tmB1);
+        if (GATE || FUSED || MODE == kDX || MODE == kDW13) ptx::prefetch_tensormap(&tmB1);
         if (MODE == kDX) ptx::prefetch_tensormap(&tmB2);
         ptx::prefetch_tensormap(&tmOut);
         if (MODE == kDH) ptx::prefetch_tensormap(&tmOut2);
@@ -481,7 +503,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
             ctl->offsets[e] = o0;
             bad = o0 < 0 || o1 < o0 || o1 > args.R || (e == 0 && o0 != 0);
-            c = bad ? 0 : (o1 - o0 + BM - 1) / BM;
+            // weight gradients: the expert's 64-row k-blocks (their prefix gives
+            // the padded row offsets); otherwise its 128-row tiles
+            c = bad ? 0 : WGRAD ? (o1 - o0 + BK - 1) / BK : (o1 - o0 + BM - 1) / BM;
             if (PAIR) c = (c + 1) / 2;
         }
         if (e == 0) ctl->offsets[E] = args.offsets[E];
@@ -493,7 +517,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // both streams in one scan: heavy tiles in the low 32 bits, light in the
         // high 32 (the sums stay below 2^31, so the halves never carry)
         // (the fused sequence keeps every expert in one stream)
-        const bool light = !FUSED && c <= light_tiles<PAIR>();
+        const bool light = !FUSED && !WGRAD && c <= light_tiles<PAIR>();
         const uint64_t cs = light ? (uint64_t)c << 32 : (uint64_t)c;
         uint64_t incl = cs;
 #pragma unroll
@@ -586,25 +610,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         __syncthreads();
     }
     const int total_units =
-        FUSED ? ctl->nrounds * (int)gridDim.x
-              : (ctl->tile_base[0][E] + ctl->tile_base[1][E]) * NB;
+        FUSED   ? ctl->nrounds * (int)gridDim.x
+        : WGRAD ? E * args.MT * NB
+                : (ctl->tile_base[0][E] + ctl->tile_base[1][E]) * NB;
     const int per_tile = PAIR ? 2 : 1;
+    // k-blocks of a unit: d / 64 for gate/up, n / 64 for down (weight gradients:
+    // the expert's rows / 64, rounded up)
+    const int KB = args.Kdim / BK;
+    const int KB2 = FUSED ? args.Kdim2 / BK : KB;
     auto unit_at = [&](int u) -> Unit {
         if constexpr (FUSED) {
-            return decode_sched(u, NB, args.NB2, E, ctl->sched, ctl->tile_base[0], ctl->offsets);
+            Unit x = decode_sched(u, NB, args.NB2, E, ctl->sched, ctl->tile_base[0], ctl->offsets);
+            x.kbs = x.down ? KB2 : KB;
+            return x;
+        } else if constexpr (WGRAD) {
+            // expert-major, then 128-row output tile, then output column block
+            Unit x;
+            x.valid = true;
+            x.down = false;
+            x.tile = -1;
+            const int per_e = args.MT * NB;
+            x.e = u / per_e;
+            const int rem = u - x.e * per_e;
+            const int mt = rem / NB;
+            x.nb = rem - mt * NB;
+            x.row0 = mt * BM;
+            x.rows = BM;
+            x.kbs = ctl->tile_base[0][x.e + 1] - ctl->tile_base[0][x.e];
+            x.poff = BK * ctl->tile_base[0][x.e];
+            x.off = ctl->offsets[x.e];
+            return x;
         } else {
             Unit x;
             x.valid = true;
             x.down = MODE == kDown;
             x.tile = -1;
+            x.kbs = KB;
             decode_unit(u, NB, E, ctl->tile_base, ctl->offsets, per_tile, rank, x.e, x.nb, x.row0,
                         x.rows);
             return x;
         }
     };
-    // k-blocks of a unit: d / 64 for gate/up, n / 64 for down
-    const int KB = args.Kdim / BK;
-    const int KB2 = FUSED ? args.Kdim2 / BK : KB;
     // fused: arrivals that complete a row tile's H (epilogue warps x column blocks)
     const uint32_t dep_full = (uint32_t)(NB * EW);
 
@@ -627,7 +673,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 ptx::fence_proxy_async_global();
             }
             const int wrow = e * (fdown ? args.Kdim2 : args.Kdim);
-            const int kbs = fdown ? KB2 : KB;
+            const int kbs = un.kbs;
             for (int kb = 0; kb < kbs; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, args.err)) {
@@ -660,6 +706,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         ptx::tma_load_2d(sB + q * kBBox, &tmB2, full, nb * BN + q * 64, ky);
+                } else if constexpr (WGRAD) {
+                    // A: two 64-column slabs of the 128 output rows, k-rows = the
+                    // expert's rows kb*64 .. +63; B: four 64-column boxes of the same
+                    // k-rows. The padded operand's rows start at poff, the other's at off.
+                    ptx::mbar_arrive_expect_tx(full, kTx);
+                    const int ya = (MODE == kDW13 ? un.poff : un.off) + kb * BK;
+                    const int yb = (MODE == kDW13 ? un.off : un.poff) + kb * BK;
+                    ptx::tma_load_2d(sA, &tmA, full, un.row0, ya);
+                    ptx::tma_load_2d(sA + kBBox, &tmA, full, un.row0 + 64, ya);
+                    if constexpr (MODE == kDW13) {
+                        ptx::tma_load_2d(sB + 0 * kBBox, &tmB0, full, nb * 128, yb);
+                        ptx::tma_load_2d(sB + 1 * kBBox, &tmB0, full, nb * 128 + 64, yb);
+                        ptx::tma_load_2d(sB + 2 * kBBox, &tmB1, full, nb * 128, yb);
+                        ptx::tma_load_2d(sB + 3 * kBBox, &tmB1, full, nb * 128 + 64, yb);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            ptx::tma_load_2d(sB + q * kBBox, &tmB0, full, nb * BN + q * 64, yb);
+                    }
                 } else if constexpr (MODE == kDX) {
                     // k-blocks 0 .. n/64-1: dA1 rows against W1[e]; then dA3 against W3[e].
                     // W rows e*d + nb*256 .. +255 (d), columns kx .. kx+63 (n): K-major
@@ -715,7 +780,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + a * BN;
-            const int kbs = FUSED && un.down ? KB2 : KB;
+            const int kbs = un.kbs;
             for (int kb = 0; kb < kbs; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->full[s]), ph, args.err)) {
@@ -726,7 +791,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t sA = smem_base + s * G::kStageBytes, sB = sA + kABytes;
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
-                    const uint64_t adesc = ptx::desc_sw128(sA + k * 32, 16, 1024);
+                    // A K-major: the next 16 k-columns are 32 bytes on; MN-major (weight
+                    // gradients): the next 16 k-rows are 2048 bytes on, slabs 8 KB apart
+                    const uint64_t adesc = WGRAD ? ptx::desc_sw128(sA + k * 2048, kBBox, 1024)
+                                                 : ptx::desc_sw128(sA + k * 32, 16, 1024);
                     // B MN-major: the next 16 k-rows are 2048 bytes on; K-major (kDH):
                     // the next 16 k-columns are 32 bytes on within each row
                     const uint64_t bdesc = (MODE == kDH || MODE == kDX)
@@ -788,7 +856,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (first_unit < total_units) load_tok(first_unit, nxt);
         for (int u = first_unit; u < total_units && ok; u += unit_stride) {
             const Unit cur = unit_at(u);
-            const int kbs = !cur.valid ? 0 : (FUSED && cur.down ? KB2 : KB);
+            const int kbs = !cur.valid ? 0 : cur.kbs;
             int tok[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -893,7 +961,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                            packed[4 * i + 3]);
                 }
             };
-            if constexpr (MODE == kDH) {
+            if constexpr (WGRAD) {
+                // output row row0 + r of expert e: 32 fp32 columns per chunk; an expert
+                // with no rows ran no MMA, so its gradient is written as zeros
+                const int64_t orow = (int64_t)un.e * args.wout_rows + un.row0 + r;
+#pragma unroll 1
+                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                    uint32_t v[32];
+                    if (un.kbs > 0) {
+                        ptx::tmem_ld32(taddr + c * 32, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+                    float *dst = MODE == kDW13
+                                     ? (c < 4 ? args.wout1 : args.wout3) + orow * args.wout_ld +
+                                           nb * 128 + (c & 3) * 32
+                                     : args.wout1 + orow * args.wout_ld + nb * BN + c * 32;
+                    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                }
+            } else if constexpr (MODE == kDH) {
                 // g = dY[t_p] W2[e]^T for 256 columns j of the expert's hidden
                 // layer; with the stored pre-activations a1, a3 of row p:
                 //   dA1 = w g a3 s (1 + a1 (1 - s)), dA3 = w g SiLU(a1), s = sigmoid(a1)
@@ -1335,6 +1426,55 @@ cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA
         launch_ew_auto<kDX, false>(ta1, tw1, tw3, tout, ta3, tout, args, tiles * args.NB, s);
     if (e != cudaSuccess) return e;
     return launch_combine(dXg, row_of_slot, T, K, d, dX, s);
+}
+
+cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
+                               const __nv_bfloat16 *H, const __nv_bfloat16 *dA1,
+                               const __nv_bfloat16 *dA3, const float *topk_w,
+                               const int32_t *perm_token, const int32_t *perm_slot,
+                               const int32_t *offsets, int T, int R, int d, int E, int n,
+                               float *dW1, float *dW3, float *dW2, __nv_bfloat16 *pad,
+                               int32_t *poff, uint32_t *err, cudaStream_t s) {
+    const int64_t cap = (int64_t)R + 64 * E;
+    // dW1 | dW3 = Xg^T [dA1 | dA3]: padded gathered X rows against dA1, dA3
+    cudaError_t e = launch_gather_padded(X, perm_token, T, offsets, E, d, nullptr, nullptr, R, cap,
+                                         poff, pad, false, s);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tx, t1, t3;
+    if (!make_map(&tx, pad, d, cap, 64, 64) || !make_map(&t1, dA1, n, R, 64, 64) ||
+        !make_map(&t3, dA3, n, R, 64, 64))
+        return cudaErrorInvalidValue;
+    GemmArgs a{};
+    a.offsets = offsets;
+    a.E = E;
+    a.R = R;
+    a.NB = n / 128;
+    a.MT = d / BM;
+    a.wout1 = dW1;
+    a.wout3 = dW3;
+    a.wout_rows = d;
+    a.wout_ld = n;
+    a.err = err;
+    e = launch_ew<kDW13, false, 4>(tx, t1, t3, tx, tx, tx, a, E * a.MT * a.NB, s);
+    if (e != cudaSuccess) return e;
+    // dW2 = H^T (w dY)g: H rows against padded, w-scaled gathered dY rows
+    e = launch_gather_padded(dY, perm_token, T, offsets, E, d, topk_w, perm_slot, R, cap, poff, pad,
+                             true, s);
+    if (e != cudaSuccess) return e;
+    CUtensorMap th, ty;
+    if (!make_map(&th, H, n, R, 64, 64) || !make_map(&ty, pad, d, cap, 64, 64))
+        return cudaErrorInvalidValue;
+    GemmArgs b{};
+    b.offsets = offsets;
+    b.E = E;
+    b.R = R;
+    b.NB = d / BN;
+    b.MT = n / BM;
+    b.wout1 = dW2;
+    b.wout_rows = n;
+    b.wout_ld = d;
+    b.err = err;
+    return launch_ew<kDW2, false, 4>(th, ty, ty, th, th, th, b, E * b.MT * b.NB, s);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {

@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # (forward_launches).
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
             "moe_gemm_gate_up_train": 1, "moe_backward_dh": 2, "moe_backward_dx": 2,
-            "moe_backward_router": 5,
+            "moe_backward_router": 5, "moe_backward_dw": 5,
             "moe_gemm_down": 1, "moe_combine": 1, "moe_round_routing": 3, "moe_combine_rows": 1}
 TILE_M = 128
 
@@ -63,6 +63,9 @@ _SIGS = {
     "moe_backward_dx": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_backward_router": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                  _P, _SZ, _P]),
+    "moe_backward_dw_scratch_bytes": (_SZ, [_I, _I, _I, _I]),
+    "moe_backward_dw": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P,
+                             _P, _SZ, _P]),
     "moe_expert_mlp": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ,
                             _P]),
     "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _P]),
@@ -317,6 +320,29 @@ def moe_backward_router(X, Wr, logits, topk_idx, dS, row_of_slot, dXg, renorm: b
         T, d, E, K, int(bool(renorm)), _ptr(dXg, torch.bfloat16, "dXg"), _ptr(out["dX"]),
         _ptr(out["dL"]), _ptr(out["dWr"]), _ptr(out["dbias"]), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return out
+
+
+def moe_backward_dw(X, dY, H, dA1, dA3, topk_w, perm_token, perm_slot, offsets, K: int,
+                    scratch=None, stream=None) -> dict:
+    """Weight gradients dW1, dW3 [E, d, n] and dW2 [E, n, d], fp32."""
+    T, d = X.shape
+    E = offsets.shape[0] - 1
+    n = dA1.shape[1]
+    if scratch is None:
+        nbytes = int(lib().moe_backward_dw_scratch_bytes(T, d, E, K))
+        scratch = torch.zeros(nbytes, dtype=torch.uint8, device=X.device)
+    out = dict(dW1=torch.empty((E, d, n), dtype=torch.float32, device=X.device),
+               dW3=torch.empty((E, d, n), dtype=torch.float32, device=X.device),
+               dW2=torch.empty((E, n, d), dtype=torch.float32, device=X.device))
+    _check("moe_backward_dw", lib().moe_backward_dw(
+        _ptr(X, torch.bfloat16, "X"), _ptr(dY, torch.bfloat16, "dY"), _ptr(H, torch.bfloat16, "H"),
+        _ptr(dA1, torch.bfloat16, "dA1"), _ptr(dA3, torch.bfloat16, "dA3"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(perm_token, torch.int32, "perm_token"),
+        _ptr(perm_slot, torch.int32, "perm_slot"), _ptr(offsets, torch.int32, "offsets"),
+        T, d, E, K, n, _ptr(out["dW1"]), _ptr(out["dW3"]), _ptr(out["dW2"]), _ptr(scratch),
+        scratch.numel(), _stream(stream)))
+    out["scratch"] = scratch
     return out
 
 
