@@ -21,7 +21,9 @@ Prints ONE JSON line on rank 0:
   extra       tokens/s, per-stage times (from the second region), router and combine
               GB/s, % of peak, routing statistics (tile padding, rows per expert), and
               `sustained`: back-to-back forwards over about 2 s against the sustained
-              bf16 peak (the K-step `value` is a burst figure)
+              bf16 peak (the K-step `value` is a burst figure), and `backward`: the
+              layer's backward (pre-activations, dH with dS, dX, weight gradients,
+              router) timed per call after the forward regions (--no-backward skips it)
 
 --routing rounded runs the layer under Token Rounding (moe_forward_rounded: each
 expert's top-K count rounded to a multiple of the 128-row tile); its value
@@ -237,6 +239,91 @@ def run_reference(args, c, world, rank):
 def _has_cuda():
     import torch
     return torch.cuda.is_available()
+
+
+def measure_backward(args, c, inp, stream, dev):
+    """The layer's backward (top-K choice held fixed) on the same inputs: the
+    five calls a training step makes after the forward's routing and grouping,
+    timed on the launch stream with an event between every two calls, over
+    `args.steps` passes after 2 untimed ones. The routing and grouping are the
+    forward's (computed once, outside the timed passes); dY is synthetic
+    N(0,1). Returns the per-call times and each GEMM's rate against the bf16
+    peak."""
+    import numpy as np
+    import torch
+    from top_routing_grouped_02_gb300 import moe, synth
+
+    T, d, E, K, n = c["T"], c["d"], c["E"], c["K"], c["n"]
+    R = T * K
+    ws = moe.workspace(T, d, E, K, n, dev)
+    dY = synth.normal("dY", (T, d), 1.0, torch.bfloat16, dev, seed=args.seed + 7)
+    names = ["gate_up_train", "dh", "dx", "dw", "router"]
+    with torch.cuda.stream(stream):
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+        idx, w, counts = moe.moe_route(inp["X"], inp["Wr"], K, inp["bias"], logits=logits,
+                                       stream=stream)
+        g = moe.moe_permute(idx, E, counts=counts, ws=ws, stream=stream)
+        scratch = torch.zeros(int(moe.lib().moe_backward_dw_scratch_bytes(T, d, E, K)),
+                              dtype=torch.uint8, device=dev)
+        wv = w.view(-1)
+
+        def one_pass(ev=None):
+            rec = (lambda j: ev[j].record(stream)) if ev is not None else (lambda j: None)
+            rec(0)
+            H, A1, A3 = moe.moe_gemm_gate_up_train(inp["X"], inp["W1"], inp["W3"],
+                                                   g["perm_token"], g["offsets"], K, ws=ws,
+                                                   stream=stream)
+            rec(1)
+            dA1, dA3, dS = moe.moe_backward_dh(dY, inp["W2"], A1, A3, wv, g["perm_token"],
+                                               g["perm_slot"], g["offsets"], K, ws=ws,
+                                               stream=stream)
+            rec(2)
+            dXg, _ = moe.moe_backward_dx(dA1, dA3, inp["W1"], inp["W3"], g["offsets"],
+                                         g["row_of_slot"], K, ws=ws, stream=stream)
+            rec(3)
+            moe.moe_backward_dw(inp["X"], dY, H, dA1, dA3, wv, g["perm_token"], g["perm_slot"],
+                                g["offsets"], K, scratch=scratch, stream=stream)
+            rec(4)
+            moe.moe_backward_router(inp["X"], inp["Wr"], logits, idx, dS, g["row_of_slot"], dXg,
+                                    ws=ws, stream=stream)
+            rec(5)
+
+        for _ in range(2):
+            one_pass()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+               for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            one_pass(evs[i])
+        torch.cuda.synchronize()
+    st, word = moe.moe_sync_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} in the backward region")
+    st, word = moe.moe_sync_check(scratch)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} in the weight-gradient scratch")
+    ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
+          for j, s in enumerate(names)}
+    total = float(np.mean([evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]))
+    peak = load_peaks()["bf16"]
+    gemm_flops = {"gate_up_train": 4.0 * R * d * n, "dh": 2.0 * R * d * n,
+                  "dx": 4.0 * R * d * n, "dw": 6.0 * R * d * n}
+    rates = {k: f / (ms[k] / 1e3) / 1e12 for k, f in gemm_flops.items()}
+    # the router's share: X and dXg read, the fp32 router share of dX written
+    # and read back, dX written (the dL, dWr, dbias terms are E-wide, small)
+    router_bytes = T * d * 2 + R * d * 2 + 2 * T * d * 4 + T * d * 2
+    useful = 12.0 * R * d * n  # dX and the weight gradients of both GEMMs
+    return {
+        "passes": args.steps, "ms_per_pass": round(total, 4),
+        "stage_ms": {k: round(v, 4) for k, v in ms.items()},
+        "gemm_tflops": {k: round(v, 2) for k, v in rates.items()},
+        "gemm_frac_bf16_peak": {k: round(v / peak, 4) for k, v in rates.items()},
+        "router_GBps": round(router_bytes / (ms["router"] / 1e3) / 1e9, 1),
+        "useful_tflops": round(useful / (total / 1e3) / 1e12, 2),
+        "useful_flops_per_pass": useful,
+        "note": "gradients with the top-K choice fixed; the pass recomputes the gate/up "
+                "pre-activations (4*R*d*n flops, counted in gemm_tflops, not in useful)",
+    }
 
 
 def run_gpu(args, c, world, rank, local):
@@ -475,6 +562,8 @@ def run_gpu(args, c, world, rank, local):
             "sustained": sustained,
         },
     }
+    if not args.no_backward and not rounded:
+        line["extra"]["backward"] = measure_backward(args, c, inp, stream, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not rounded:
         import oracle
         oracle.build()
@@ -602,6 +691,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sustained-seconds", type=float, default=2.0,
                     help="length of the sustained region reported in extra.sustained (0: skip)")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward region reported in extra.backward")
     ap.add_argument("--graph", action="store_true",
                     help="time one CUDA graph of the K steps instead of direct calls")
     args = ap.parse_args(argv)

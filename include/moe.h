@@ -287,10 +287,13 @@ moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf
  *                   + (dL Wr^T)[t,:] )                      bf16 [T, d]
  * i.e. the full input gradient: the experts' rows (dXg from moe_backward_dx)
  * and the router's share, added in fp32 and rounded once. logits [T,E] as
- * moe_route wrote them; dWr and dL Wr^T are fp32 fma chains in fixed orders
- * (t, e ascending), dbias a fixed tree: deterministic. ws: at least
- * moe_workspace_bytes(T, d, E, K, 0) bytes (a workspace of the layer's shape
- * serves); its gathered-rows region onwards holds dL Wr^T. Five kernels. */
+ * moe_route wrote them. dWr is summed per chunk of tokens (fp32 fma chains,
+ * t ascending) and the chunks' partials in ascending order; dL Wr^T is one
+ * fp32 fma chain over e ascending per element; dbias a fixed tree: all
+ * deterministic. ws: at least moe_workspace_bytes(T, d, E, K, 0) bytes (a
+ * workspace of the layer's shape serves); T * d floats from its gathered-rows
+ * region on hold the dWr partials and, for E > 32, dL Wr^T. Four kernels for
+ * E <= 32 (five when T needs more than one chunk), else six. */
 moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,
                                  const int32_t *topk_idx, const float *dS,
                                  const int32_t *row_of_slot, int T, int d, int E, int K,

@@ -111,6 +111,30 @@ def test_backward_dh_matches_oracle_in_full(pair, monkeypatch):
     check_y(bits(s["dX"]), full["dX"], "dX")
 
 
+@pytest.mark.parametrize("T,E,K", [
+    (300, 20, 2),    # E <= 32 with a partly used 32-expert block; 10 token chunks
+    (300, 40, 3),    # E > 32: two expert blocks, dL Wr^T in its own kernel; 5 chunks
+    (300, 256, 8),   # E = 256: T too short for chunks, dWr written directly
+    (4100, 8, 2),    # 129 chunks of 32 tokens, the last one ragged
+])
+def test_router_backward_matches_oracle(T, E, K):
+    d, n = 256, 256
+    inp = synth.layer_inputs(T=T, d=d, E=E, n=n, device="cuda", seed=3)
+    dY = _dY(T, d)
+    s = _gpu_steps(inp, dY, K)
+    X, Wr, bias, W1, W3, W2 = layer_np(inp)
+    idx_r, _ = oracle.topk_softmax(oracle.router_logits(X, Wr, bias), K, True)
+    assert np.array_equal(s["idx"].cpu().numpy(), idx_r)
+    _, _, ps_r, _ = oracle.permute(idx_r, E)
+    ref = oracle.backward_rows(X, _f64(Wr), _f64(bias), W1, W3, W2, idx_r, ps_r,
+                               f64_of_bits(bits(dY)))
+    check_f32(s["dL"].cpu().numpy(), ref["dL"], "dL")
+    full = oracle.backward(X, _f64(Wr), _f64(bias), W1, W3, W2, idx_r, f64_of_bits(bits(dY)))
+    check_f32(s["dbias"].cpu().numpy(), full["dbias"], "dbias")
+    check_f32(s["dWr"].cpu().numpy(), full["dWr"], "dWr")
+    check_y(bits(s["dX"]), full["dX"], "dX")
+
+
 def test_backward_dh_sonic_shape_sampled_tokens():
     cfg = synth.WORKLOADS["sonic"]
     T, d, E, K, n = cfg["T"], cfg["d"], cfg["E"], cfg["K"], cfg["n"]

@@ -16,14 +16,18 @@
 // and over the batch: dbias = sum_t dL[t,:], dWr = X^T dL, and the router's
 // share of dX is dL Wr^T, added to the experts' share in the final combine.
 //
-// Five kernels, all deterministic (fixed summation orders, no atomics):
+// Four to six kernels, all deterministic (fixed summation orders, no atomics):
 //  1. dl:       one warp per token (lane l holds experts l, l+32, ...).
 //  2. dbias:    one block per expert, a fixed-shape tree over the tokens.
-//  3. dWr:      64 (j) x 32 (e) output tiles; each output is one fp32 fma
-//               chain over t ascending, operands staged through shared memory.
-//  4. dL Wr^T:  32 (t) x 64 (j) output tiles; one fma chain over e ascending.
+//  3. dWr:      per chunk of tokens, fp32 fma chains over the chunk's tokens in
+//               ascending order; then the chunks' partials added in ascending
+//               order (one kernel when a single chunk covers T).
+//  4. dL Wr^T:  one fma chain over e ascending per output; for E <= 32 inside
+//               the combine, else 32 (t) x 64 (j) output tiles of its own.
 //  5. combine:  dX[t,:] = bf16( sum over k ascending of dXg[row_of_slot[t,k],:]
 //               (fp32) + (dL Wr^T)[t,:] ), one rounding.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -129,57 +133,106 @@ col_sum_kernel(const float *__restrict__ dL, int T, int E, float *__restrict__ d
     if (threadIdx.x == 0) dbias[e] = part[0];
 }
 
-// dWr[j, e] = sum over t ascending of x[t, j] dL[t, e] (one fma chain each).
-// Block: 64 j x 32 e, 128 threads of 4 x 4 outputs; 32 tokens per stage.
-constexpr int kWJ = 64, kWE = 32, kWT = 32;
-__global__ void __launch_bounds__(128)
-router_dwr_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ dL, int T, int d,
-                  int E, float *__restrict__ dWr) {
+// dWr[j, e] = sum over t of x[t, j] dL[t, e], in two fixed orders: chunk c of
+// TC tokens gives the partial P[c][j][e], one fma chain over its tokens in
+// ascending order; dwr_reduce_kernel adds the partials in ascending c. (With
+// one chunk the partial is dWr itself.) A thread holds JPT = 64 / EB
+// consecutive j and EB experts: one JPT-wide vector load of x per token, EB/4
+// broadcast shared-memory loads of dL and 64 fmas. Block: 128 threads, i.e.
+// 128 * JPT columns j; grid (j blocks, chunks, expert blocks of EB).
+constexpr int kPThreads = 128, kPStage = 64;
+template <int EB>
+__global__ void __launch_bounds__(kPThreads)
+router_dwr_part_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ dL, int T,
+                       int d, int E, int TC, float *__restrict__ P) {
+    constexpr int JPT = 64 / EB;
     pdl_wait();
     pdl_trigger();
-    __shared__ float xs[kWT][kWJ];
-    __shared__ float ls[kWT][kWE];
+    __shared__ __align__(16) float ls[kPStage][EB];
     const int tid = threadIdx.x;
-    const int jg = tid % 16, eg = tid / 16;  // outputs j0 + 4jg .. +3, e0 + 4eg .. +3
-    const int j0 = blockIdx.x * kWJ, e0 = blockIdx.y * kWE;
-    float acc[4][4] = {};
-    for (int t0 = 0; t0 < T; t0 += kWT) {
-        for (int q = tid; q < kWT * kWJ; q += 128) {
-            const int tt = q / kWJ, jj = q % kWJ;
-            const int64_t t = t0 + tt;
-            xs[tt][jj] = (t < T && j0 + jj < d) ? __bfloat162float(X[t * d + j0 + jj]) : 0.f;
-        }
-        for (int q = tid; q < kWT * kWE; q += 128) {
-            const int tt = q / kWE, ee = q % kWE;
-            const int64_t t = t0 + tt;
-            ls[tt][ee] = (t < T && e0 + ee < E) ? __ldg(dL + t * E + e0 + ee) : 0.f;
+    const int j0 = (blockIdx.x * kPThreads + tid) * JPT;
+    const int e0 = blockIdx.z * EB;
+    const int64_t tb = (int64_t)blockIdx.y * TC;
+    const int64_t te = min((int64_t)T, tb + TC);
+    const bool active = j0 < d;  // d % 8 == 0, so j0 < d means all JPT columns exist
+    float acc[JPT][EB];
+#pragma unroll
+    for (int a = 0; a < JPT; ++a)
+#pragma unroll
+        for (int b = 0; b < EB; ++b) acc[a][b] = 0.f;
+    for (int64_t t0 = tb; t0 < te; t0 += kPStage) {
+        const int tn = (int)min((int64_t)kPStage, te - t0);
+        __syncthreads();
+        for (int q = tid; q < kPStage * EB; q += kPThreads) {
+            const int tt = q / EB, ee = q % EB;
+            ls[tt][ee] = (tt < tn && e0 + ee < E) ? __ldg(dL + (t0 + tt) * E + e0 + ee) : 0.f;
         }
         __syncthreads();
-        const int tn = min(kWT, T - t0);
-        for (int tt = 0; tt < tn; ++tt) {
-            float xv[4], lv[4];
+        if (!active) continue;
+        const __nv_bfloat16 *xp = X + t0 * d + j0;
+#pragma unroll 4
+        for (int tt = 0; tt < tn; ++tt, xp += d) {
+            float xv[JPT];
+            if constexpr (JPT == 8) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(xp));
+                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) xv[a] = xs[tt][4 * jg + a];
+                for (int u = 0; u < 4; ++u) {
+                    const float2 f = __bfloat1622float2(h[u]);
+                    xv[2 * u] = f.x;
+                    xv[2 * u + 1] = f.y;
+                }
+            } else if constexpr (JPT == 4) {
+                const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(xp));
+                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-            for (int b = 0; b < 4; ++b) lv[b] = ls[tt][4 * eg + b];
+                for (int u = 0; u < 2; ++u) {
+                    const float2 f = __bfloat1622float2(h[u]);
+                    xv[2 * u] = f.x;
+                    xv[2 * u + 1] = f.y;
+                }
+            } else {
+                const float2 f = __bfloat1622float2(
+                    *reinterpret_cast<const __nv_bfloat162 *>(xp));
+                xv[0] = f.x;
+                xv[1] = f.y;
+            }
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int b4 = 0; b4 < EB; b4 += 4) {
+                const float4 l = *reinterpret_cast<const float4 *>(&ls[tt][b4]);
+                const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-                for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xv[a], lv[b], acc[a][b]);
+                for (int a = 0; a < JPT; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        acc[a][b4 + b] = __fmaf_rn(xv[a], lv[b], acc[a][b4 + b]);
+            }
         }
-        __syncthreads();
     }
+    if (!active) return;
+    float *out = P + (int64_t)blockIdx.y * d * E;
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < JPT; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int j = j0 + 4 * jg + a, e = e0 + 4 * eg + b;
-            if (j < d && e < E) dWr[(int64_t)j * E + e] = acc[a][b];
-        }
+        for (int b = 0; b < EB; ++b)
+            if (e0 + b < E) out[(int64_t)(j0 + a) * E + e0 + b] = acc[a][b];
+}
+
+// dWr[i] = sum over chunks c ascending of P[c][i], i < d * E.
+__global__ void __launch_bounds__(256)
+dwr_reduce_kernel(const float *__restrict__ P, int64_t n, int chunks, float *__restrict__ dWr) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= n) return;
+    float s = 0.f;
+    for (int c = 0; c < chunks; ++c) s = __fadd_rn(s, __ldg(P + c * n + i));
+    dWr[i] = s;
 }
 
 // dXr[t, j] = sum over e ascending of dL[t, e] Wr[j, e] (one fma chain each).
 // Block: 32 t x 64 j, 128 threads of 4 x 4 outputs; 32 experts per stage.
+// Grid: (token blocks, column blocks).
 constexpr int kXT = 32, kXJ = 64, kXE = 32;
 __global__ void __launch_bounds__(128)
 router_dx_kernel(const float *__restrict__ dL, const float *__restrict__ Wr, int T, int d, int E,
@@ -190,8 +243,8 @@ router_dx_kernel(const float *__restrict__ dL, const float *__restrict__ Wr, int
     __shared__ float ws[kXJ][kXE + 1];
     const int tid = threadIdx.x;
     const int jg = tid % 16, tg = tid / 16;  // outputs t0 + 4tg .. +3, j0 + 4jg .. +3
-    const int64_t t0 = (int64_t)blockIdx.y * kXT;
-    const int j0 = blockIdx.x * kXJ;
+    const int64_t t0 = (int64_t)blockIdx.x * kXT;
+    const int j0 = blockIdx.y * kXJ;
     float acc[4][4] = {};
     for (int e0 = 0; e0 < E; e0 += kXE) {
         for (int q = tid; q < kXT * kXE; q += 128) {
@@ -273,6 +326,82 @@ combine_add_kernel(const __nv_bfloat16 *__restrict__ dXg, const int32_t *__restr
             o2[u] = __floats2bfloat162_rn(__fadd_rn(acc[2 * u], add[2 * u]),
                                           __fadd_rn(acc[2 * u + 1], add[2 * u + 1]));
         reinterpret_cast<uint4 *>(dX + t * d)[c] = out;
+    }
+}
+
+// E <= 32: the router's share computed in the combine. Block: 8 warps, 32
+// tokens (4 per warp) x 256 columns (8 per lane). Wr's 256 x EB slice is
+// staged transposed in shared memory, dL's 32 x EB slice as is. For each
+// output, r = one fma chain over e ascending of dL[t,e] Wr[j,e], then
+// dX = bf16((sum over k ascending of dXg rows) + r): the same operations, in the
+// same order, as router_dx_kernel followed by combine_add_kernel. Grid: (token
+// blocks, column blocks).
+constexpr int kFTok = 32, kFCols = 256, kFWrLd = kFCols + 4;
+template <int EB>
+__global__ void __launch_bounds__(256)
+combine_router_kernel(const __nv_bfloat16 *__restrict__ dXg,
+                      const int32_t *__restrict__ row_of_slot, const float *__restrict__ dL,
+                      const float *__restrict__ Wr, int T, int K, int d, int E, int64_t R,
+                      __nv_bfloat16 *__restrict__ dX) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ __align__(16) float ws[EB][kFWrLd];
+    __shared__ float lsm[kFTok][EB];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c0 = blockIdx.y * kFCols;
+    const int64_t t0 = (int64_t)blockIdx.x * kFTok;
+    for (int q = tid; q < kFCols * EB; q += 256) {
+        const int jj = q / EB, ee = q % EB;
+        ws[ee][jj] = (c0 + jj < d && ee < E) ? __ldg(Wr + (int64_t)(c0 + jj) * E + ee) : 0.f;
+    }
+    for (int q = tid; q < kFTok * EB; q += 256) {
+        const int tt = q / EB, ee = q % EB;
+        lsm[tt][ee] = (t0 + tt < T && ee < E) ? __ldg(dL + (t0 + tt) * E + ee) : 0.f;
+    }
+    __syncthreads();
+    const int j = c0 + lane * 8;
+    if (j >= d) return;
+    constexpr int TPW = kFTok / 8;  // tokens per warp
+    float r[TPW][8];
+#pragma unroll
+    for (int a = 0; a < TPW; ++a)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r[a][u] = 0.f;
+    for (int e = 0; e < E; ++e) {
+        const float4 w0 = *reinterpret_cast<const float4 *>(&ws[e][lane * 8]);
+        const float4 w1 = *reinterpret_cast<const float4 *>(&ws[e][lane * 8 + 4]);
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int a = 0; a < TPW; ++a) {
+            const float l = lsm[warp * TPW + a][e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) r[a][u] = __fmaf_rn(l, wv[u], r[a][u]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < TPW; ++a) {
+        const int64_t t = t0 + warp * TPW + a;
+        if (t >= T) break;
+        float acc[8] = {};
+        for (int k = 0; k < K; ++k) {
+            const int row = __ldg(row_of_slot + t * K + k);
+            if (row < 0 || row >= R) continue;
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(dXg + (int64_t)row * d + j));
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                acc[2 * u] = __fadd_rn(acc[2 * u], f.x);
+                acc[2 * u + 1] = __fadd_rn(acc[2 * u + 1], f.y);
+            }
+        }
+        uint4 out;
+        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            o2[u] = __floats2bfloat162_rn(__fadd_rn(acc[2 * u], r[a][2 * u]),
+                                          __fadd_rn(acc[2 * u + 1], r[a][2 * u + 1]));
+        *reinterpret_cast<uint4 *>(dX + t * d + j) = out;
     }
 }
 
@@ -380,10 +509,37 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
     e = launch_k(col_sum_kernel, dim3(E), dim3(kColThreads), 0, s, static_cast<const float *>(dL), T,
                  E, dbias);
     if (e != cudaSuccess) return e;
-    e = launch_k(router_dwr_kernel, dim3((d + kWJ - 1) / kWJ, (E + kWE - 1) / kWE), dim3(128), 0, s,
-                 X, static_cast<const float *>(dL), T, d, E, dWr);
+    // dWr: chunks of TC tokens, their partials in the dXr region (T * d floats;
+    // TC grows until the chunks' d x E partials fit), then the reduce
+    int64_t TC = 32;
+    while (TC < T && (((T + TC - 1) / TC) * E > T || (T + TC - 1) / TC > 65535)) TC *= 2;
+    TC = std::min<int64_t>(TC, T);
+    const int chunks = (int)((T + TC - 1) / TC);
+    float *part = chunks > 1 ? dXr : dWr;
+    auto part_k = E <= 8 ? router_dwr_part_kernel<8>
+                  : E <= 16 ? router_dwr_part_kernel<16>
+                            : router_dwr_part_kernel<32>;
+    const int eb = E <= 8 ? 8 : E <= 16 ? 16 : 32;
+    const int jb = kPThreads * (64 / eb);
+    e = launch_k(part_k, dim3((d + jb - 1) / jb, chunks, (E + eb - 1) / eb), dim3(kPThreads), 0, s,
+                 X, static_cast<const float *>(dL), T, d, E, (int)TC, part);
     if (e != cudaSuccess) return e;
-    e = launch_k(router_dx_kernel, dim3((d + kXJ - 1) / kXJ, (unsigned)((T + kXT - 1) / kXT)),
+    if (chunks > 1) {
+        const int64_t n = (int64_t)d * E;
+        e = launch_k(dwr_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                     static_cast<const float *>(part), n, chunks, dWr);
+        if (e != cudaSuccess) return e;
+    }
+    // the router's share dL Wr^T and the final combine: fused for E <= 32
+    if (E <= 32) {
+        auto ck = E <= 8 ? combine_router_kernel<8>
+                  : E <= 16 ? combine_router_kernel<16>
+                            : combine_router_kernel<32>;
+        return launch_k(ck, dim3((unsigned)((T + kFTok - 1) / kFTok), (d + kFCols - 1) / kFCols),
+                        dim3(256), 0, s, dXg, row_of_slot, static_cast<const float *>(dL), Wr, T,
+                        K, d, E, R, dX);
+    }
+    e = launch_k(router_dx_kernel, dim3((unsigned)((T + kXT - 1) / kXT), (d + kXJ - 1) / kXJ),
                  dim3(128), 0, s, static_cast<const float *>(dL), Wr, T, d, E, dXr);
     if (e != cudaSuccess) return e;
     return launch_k(combine_add_kernel, dim3((unsigned)((T + kCThreads / 32 - 1) / (kCThreads / 32))),

@@ -251,13 +251,10 @@ struct GemmArgs {
     const float *pre3;
     int bn_rows;  // kDH, kDX: rows of the K-major weight per expert
     int kb_half;  // kDX: k-blocks of the first half of the reduction (n / 64)
-    // kDW13 / kDW2: 128-row output tiles per expert, the outputs (fp32, [E, wout_rows,
-    // wout_ld]; kDW13 writes dW1 to wout1 and dW3 to wout3)
+    // kDW13 / kDW2: 128-row output tiles per expert and the output rows per
+    // expert (the outputs go through the output tensor maps)
     int MT;
-    float *wout1;
-    float *wout3;
     int wout_rows;
-    int wout_ld;
     float *dspart;
     int ds_ld;
 };
@@ -473,7 +470,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (GATE || FUSED || MODE == kDX || MODE == kDW13) ptx::prefetch_tensormap(&tmB1);
         if (MODE == kDX) ptx::prefetch_tensormap(&tmB2);
         ptx::prefetch_tensormap(&tmOut);
-        if (MODE == kDH) ptx::prefetch_tensormap(&tmOut2);
+        if (MODE == kDH || MODE == kDW13) ptx::prefetch_tensormap(&tmOut2);
         if (FUSED) {
             ptx::prefetch_tensormap(&tmA);
             ptx::prefetch_tensormap(&tmB2);
@@ -932,27 +929,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // chunk through shared memory and a TMA store (whole 64-byte row
             // segments); otherwise each valid row is stored directly.
             const bool whole = q * 32 + 31 < rows;
+            // 32 rows x 64 bytes (each lane's 16 words) through a staging buffer
+            // (64-byte swizzle) and one TMA store at (x, y)
+            auto store_box = [&](const uint32_t (&packed)[16], int x, int y,
+                                 const CUtensorMap *map) {
+                // buffers rotate with the store groups, so the group that last
+                // read this buffer is the kNBuf-th most recent one
+                const uint32_t buf = epi_base + (epi_groups % kNBuf) * kEpiBuf;
+                if (lane == 0 && epi_groups >= (uint32_t)kNBuf)
+                    ptx::bulk_wait_group_read<kNBuf - 1>();
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    ptx::st_shared_v4(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4),
+                                      packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                      packed[4 * i + 3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(map, buf, x, y);
+                    ptx::bulk_commit_group();
+                }
+                ++epi_groups;
+            };
             auto emit = [&](const uint32_t (&packed)[16], __nv_bfloat16 *dst, int col,
                             const CUtensorMap *map) {
                 if (whole) {
-                    // buffers rotate with the store groups, so the group that last
-                    // read this buffer is the kNBuf-th most recent one
-                    const uint32_t buf = epi_base + (epi_groups % kNBuf) * kEpiBuf;
-                    if (lane == 0 && epi_groups >= (uint32_t)kNBuf)
-                        ptx::bulk_wait_group_read<kNBuf - 1>();
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        ptx::st_shared_v4(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4),
-                                          packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                          packed[4 * i + 3]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(map, buf, col, row0 + q * 32);
-                        ptx::bulk_commit_group();
-                    }
-                    ++epi_groups;
+                    store_box(packed, col, row0 + q * 32, map);
                 } else if (valid) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
@@ -962,27 +965,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             };
             if constexpr (WGRAD) {
-                // output row row0 + r of expert e: 32 fp32 columns per chunk; an expert
-                // with no rows ran no MMA, so its gradient is written as zeros
-                const int64_t orow = (int64_t)un.e * args.wout_rows + un.row0 + r;
+                // output rows row0 + 32q .. +31 of expert e (fp32 [E * wout_rows,
+                // wout_ld]; kDW13: dW1 by tmOut, dW3 by tmOut2): each 32-column chunk
+                // as two 16-column TMA boxes. An expert with no rows ran no MMA, so
+                // its gradient is written as zeros.
+                const int oy = un.e * args.wout_rows + un.row0 + q * 32;
 #pragma unroll 1
                 for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
-                    uint32_t v[32];
+                    uint32_t v[32], lo[16], hi[16];
                     if (un.kbs > 0) {
                         ptx::tmem_ld32(taddr + c * 32, v);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0u;
                     }
-                    float *dst = MODE == kDW13
-                                     ? (c < 4 ? args.wout1 : args.wout3) + orow * args.wout_ld +
-                                           nb * 128 + (c & 3) * 32
-                                     : args.wout1 + orow * args.wout_ld + nb * BN + c * 32;
-                    float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                    for (int i = 0; i < 16; ++i) {
+                        lo[i] = v[i];
+                        hi[i] = v[16 + i];
+                    }
+                    const CUtensorMap *map = MODE == kDW13 && c >= 4 ? &tmOut2 : &tmOut;
+                    const int x0 = MODE == kDW13 ? nb * 128 + (c & 3) * 32 : nb * BN + c * 32;
+                    store_box(lo, x0, oy, map);
+                    store_box(hi, x0 + 16, oy, map);
                 }
             } else if constexpr (MODE == kDH) {
                 // g = dY[t_p] W2[e]^T for 256 columns j of the expert's hidden
@@ -1180,6 +1185,20 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, 
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 [rows, cols] row-major (the weight gradients' TMA stores)
+bool make_map_f32(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                  uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1440,9 +1459,12 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     cudaError_t e = launch_gather_padded(X, perm_token, T, offsets, E, d, nullptr, nullptr, R, cap,
                                          poff, pad, false, s);
     if (e != cudaSuccess) return e;
-    CUtensorMap tx, t1, t3;
+    // outputs: fp32 boxes of 16 columns x 32 rows (one epilogue warp's rows)
+    CUtensorMap tx, t1, t3, to1, to3;
     if (!make_map(&tx, pad, d, cap, 64, 64) || !make_map(&t1, dA1, n, R, 64, 64) ||
-        !make_map(&t3, dA3, n, R, 64, 64))
+        !make_map(&t3, dA3, n, R, 64, 64) ||
+        !make_map_f32(&to1, dW1, n, (uint64_t)E * d, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_f32(&to3, dW3, n, (uint64_t)E * d, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     GemmArgs a{};
     a.offsets = offsets;
@@ -1450,19 +1472,17 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     a.R = R;
     a.NB = n / 128;
     a.MT = d / BM;
-    a.wout1 = dW1;
-    a.wout3 = dW3;
     a.wout_rows = d;
-    a.wout_ld = n;
     a.err = err;
-    e = launch_ew<kDW13, false, 4>(tx, t1, t3, tx, tx, tx, a, E * a.MT * a.NB, s);
+    e = launch_ew<kDW13, false, 4>(tx, t1, t3, to1, tx, to3, a, E * a.MT * a.NB, s);
     if (e != cudaSuccess) return e;
     // dW2 = H^T (w dY)g: H rows against padded, w-scaled gathered dY rows
     e = launch_gather_padded(dY, perm_token, T, offsets, E, d, topk_w, perm_slot, R, cap, poff, pad,
                              true, s);
     if (e != cudaSuccess) return e;
-    CUtensorMap th, ty;
-    if (!make_map(&th, H, n, R, 64, 64) || !make_map(&ty, pad, d, cap, 64, 64))
+    CUtensorMap th, ty, to2;
+    if (!make_map(&th, H, n, R, 64, 64) || !make_map(&ty, pad, d, cap, 64, 64) ||
+        !make_map_f32(&to2, dW2, d, (uint64_t)E * n, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     GemmArgs b{};
     b.offsets = offsets;
@@ -1470,11 +1490,9 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     b.R = R;
     b.NB = d / BN;
     b.MT = n / BM;
-    b.wout1 = dW2;
     b.wout_rows = n;
-    b.wout_ld = d;
     b.err = err;
-    return launch_ew<kDW2, false, 4>(th, ty, ty, th, th, th, b, E * b.MT * b.NB, s);
+    return launch_ew<kDW2, false, 4>(th, ty, ty, to2, th, to2, b, E * b.MT * b.NB, s);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {
