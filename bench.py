@@ -693,6 +693,8 @@ def main(argv=None):
                     help="length of the sustained region reported in extra.sustained (0: skip)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward region reported in extra.backward")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count T (0: the workload's own)")
     ap.add_argument("--graph", action="store_true",
                     help="time one CUDA graph of the K steps instead of direct calls")
     args = ap.parse_args(argv)
@@ -704,6 +706,8 @@ def main(argv=None):
         run_router_only(args, world, rank, local)
         return
     c = dict(synth.WORKLOADS[args.workload])
+    if args.tokens:  # a smaller (or larger) case of the same layer, e.g. for ncu captures
+        c["T"] = args.tokens
     if args.impl == "reference":
         run_reference(args, c, world, rank)
     else:

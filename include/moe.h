@@ -292,8 +292,8 @@ moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf
  * fp32 fma chain over e ascending per element; dbias a fixed tree: all
  * deterministic. ws: at least moe_workspace_bytes(T, d, E, K, 0) bytes (a
  * workspace of the layer's shape serves); T * d floats from its gathered-rows
- * region on hold the dWr partials and, for E > 32, dL Wr^T. Four kernels for
- * E <= 32 (five when T needs more than one chunk), else six. */
+ * region on hold the dWr partials. Five kernels (four when T is too short to
+ * split into chunks); dL Wr^T is computed inside the last, the combine. */
 moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,
                                  const int32_t *topk_idx, const float *dS,
                                  const int32_t *row_of_slot, int T, int d, int E, int K,

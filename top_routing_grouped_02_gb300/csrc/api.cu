@@ -346,8 +346,8 @@ moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float
     moe_status_t s = check_route_shape(T, d, E, K);
     if (s != MOE_OK) return s;
     if (!aligned16(X) || !aligned16(dXg) || !aligned16(dX)) return MOE_ERR_INVALID_ARG;
-    // the router's share dL Wr^T (fp32 [T, d]) lives in the workspace from the
-    // gathered-rows region on (that region and the ones after it hold >= 4*T*d bytes)
+    // the partial sums of dWr (at most T * d floats) live in the workspace from
+    // the gathered-rows region on (that region and the ones after it hold >= 4*T*d bytes)
     const WsLayout L = ws_layout(T, d, E, K, 0);
     const size_t need = L.xg + (size_t)T * d * sizeof(float);
     if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;

@@ -16,22 +16,22 @@
 // and over the batch: dbias = sum_t dL[t,:], dWr = X^T dL, and the router's
 // share of dX is dL Wr^T, added to the experts' share in the final combine.
 //
-// Four to six kernels, all deterministic (fixed summation orders, no atomics):
+// Four or five kernels, all deterministic (fixed summation orders, no atomics):
 //  1. dl:       one warp per token (lane l holds experts l, l+32, ...).
 //  2. dbias:    one block per expert, a fixed-shape tree over the tokens.
 //  3. dWr:      per chunk of tokens, fp32 fma chains over the chunk's tokens in
 //               ascending order; then the chunks' partials added in ascending
-//               order (one kernel when a single chunk covers T).
-//  4. dL Wr^T:  one fma chain over e ascending per output; for E <= 32 inside
-//               the combine, else 32 (t) x 64 (j) output tiles of its own.
-//  5. combine:  dX[t,:] = bf16( sum over k ascending of dXg[row_of_slot[t,k],:]
-//               (fp32) + (dL Wr^T)[t,:] ), one rounding.
+//               order (no second kernel when a single chunk covers T).
+//  4. combine:  dX[t,:] = bf16( sum over k ascending of dXg[row_of_slot[t,k],:]
+//               (fp32) + (dL Wr^T)[t,:] ), one rounding, with dL Wr^T one fma
+//               chain over e ascending per element, computed in the kernel.
 #include <algorithm>
 
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -137,79 +137,121 @@ col_sum_kernel(const float *__restrict__ dL, int T, int E, float *__restrict__ d
 // TC tokens gives the partial P[c][j][e], one fma chain over its tokens in
 // ascending order; dwr_reduce_kernel adds the partials in ascending c. (With
 // one chunk the partial is dWr itself.) A thread holds JPT = 64 / EB
-// consecutive j and EB experts: one JPT-wide vector load of x per token, EB/4
-// broadcast shared-memory loads of dL and 64 fmas. Block: 128 threads, i.e.
-// 128 * JPT columns j; grid (j blocks, chunks, expert blocks of EB).
-constexpr int kPThreads = 128, kPStage = 64;
+// consecutive j and EB experts; block: 128 threads, i.e. JB = 128 * JPT
+// columns j; grid (j blocks, chunks, expert blocks of EB). The chunk's tokens
+// go through shared memory in stages of ST tokens (ST x JB bf16 of X = 16 KB,
+// and ST x EB of dL), copied by cp.async into two buffers, the next stage's
+// copies in flight while the current one is used: per token a thread reads its
+// JPT x values (one conflict-free load), EB/4 broadcast loads of dL, 64 fmas.
+constexpr int kPThreads = 128;
+template <int EB>
+struct DwrCfg {
+    static constexpr int JPT = 64 / EB;
+    static constexpr int JB = kPThreads * JPT;
+    static constexpr int ST = 8192 / JB;               // tokens per stage
+    static constexpr int XBYTES = ST * JB * 2;         // 16 KB
+    static constexpr int LBYTES = ST * EB * 4;
+    static constexpr int SMEM = 2 * (XBYTES + LBYTES);
+};
 template <int EB>
 __global__ void __launch_bounds__(kPThreads)
 router_dwr_part_kernel(const __nv_bfloat16 *__restrict__ X, const float *__restrict__ dL, int T,
                        int d, int E, int TC, float *__restrict__ P) {
-    constexpr int JPT = 64 / EB;
+    using C = DwrCfg<EB>;
+    constexpr int JPT = C::JPT, ST = C::ST;
     pdl_wait();
     pdl_trigger();
-    __shared__ __align__(16) float ls[kPStage][EB];
+    extern __shared__ __align__(16) uint8_t dsm[];
     const int tid = threadIdx.x;
-    const int j0 = (blockIdx.x * kPThreads + tid) * JPT;
+    const int jb0 = blockIdx.x * C::JB;
+    const int j0 = jb0 + tid * JPT;
     const int e0 = blockIdx.z * EB;
     const int64_t tb = (int64_t)blockIdx.y * TC;
     const int64_t te = min((int64_t)T, tb + TC);
-    const bool active = j0 < d;  // d % 8 == 0, so j0 < d means all JPT columns exist
+    const int nst = (int)((te - tb + ST - 1) / ST);
+    const uint32_t sbase = ptx::smem_addr(dsm);
+    auto xbuf = [&](int b) { return sbase + b * (C::XBYTES + C::LBYTES); };
+    // stage k's copies: rows tb + k*ST + r (zeros past te), columns jb0.. of X in
+    // 16-byte chunks (zeros past d), and dL's EB experts from e0 (zeros past E)
+    auto issue = [&](int k) {
+        const int64_t t0 = tb + (int64_t)k * ST;
+        const uint32_t xs = xbuf(k & 1), ls = xs + C::XBYTES;
+        constexpr int XCH = ST * C::JB / 8;
+        for (int q = tid; q < XCH; q += kPThreads) {
+            const int r = q / (C::JB / 8), c = q % (C::JB / 8);
+            const int64_t t = t0 + r;
+            const int j = jb0 + c * 8;
+            const bool ok = t < te && j < d;
+            ptx::cp_async_16_zfill(xs + q * 16, ok ? X + t * d + j : X, ok);
+        }
+        for (int q = tid; q < ST * EB; q += kPThreads) {
+            const int r = q / EB, ee = q % EB;
+            const int64_t t = t0 + r;
+            const bool ok = t < te && e0 + ee < E;
+            ptx::cp_async_4_zfill(ls + q * 4, ok ? dL + t * E + e0 + ee : dL, ok);
+        }
+        ptx::cp_async_commit_group();
+    };
     float acc[JPT][EB];
 #pragma unroll
     for (int a = 0; a < JPT; ++a)
 #pragma unroll
         for (int b = 0; b < EB; ++b) acc[a][b] = 0.f;
-    for (int64_t t0 = tb; t0 < te; t0 += kPStage) {
-        const int tn = (int)min((int64_t)kPStage, te - t0);
-        __syncthreads();
-        for (int q = tid; q < kPStage * EB; q += kPThreads) {
-            const int tt = q / EB, ee = q % EB;
-            ls[tt][ee] = (tt < tn && e0 + ee < E) ? __ldg(dL + (t0 + tt) * E + e0 + ee) : 0.f;
+    if (nst > 0) issue(0);
+    for (int k = 0; k < nst; ++k) {
+        if (k + 1 < nst) {
+            issue(k + 1);
+            ptx::cp_async_wait_group<1>();
+        } else {
+            ptx::cp_async_wait_group<0>();
         }
         __syncthreads();
-        if (!active) continue;
-        const __nv_bfloat16 *xp = X + t0 * d + j0;
-#pragma unroll 4
-        for (int tt = 0; tt < tn; ++tt, xp += d) {
-            float xv[JPT];
-            if constexpr (JPT == 8) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(xp));
-                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        const uint8_t *xs = dsm + (k & 1) * (C::XBYTES + C::LBYTES);
+        const float *ls = reinterpret_cast<const float *>(xs + C::XBYTES);
+        const int tn = (int)min((int64_t)ST, te - (tb + (int64_t)k * ST));
+        if (j0 < d) {
+#pragma unroll 2
+            for (int tt = 0; tt < tn; ++tt) {
+                float xv[JPT];
+                const uint8_t *xp = xs + (tt * C::JB + tid * JPT) * 2;
+                if constexpr (JPT == 8) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(xp);
+                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 f = __bfloat1622float2(h[u]);
-                    xv[2 * u] = f.x;
-                    xv[2 * u + 1] = f.y;
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 f = __bfloat1622float2(h[u]);
+                        xv[2 * u] = f.x;
+                        xv[2 * u + 1] = f.y;
+                    }
+                } else if constexpr (JPT == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(xp);
+                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float2 f = __bfloat1622float2(h[u]);
+                        xv[2 * u] = f.x;
+                        xv[2 * u + 1] = f.y;
+                    }
+                } else {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(xp));
+                    xv[0] = f.x;
+                    xv[1] = f.y;
                 }
-            } else if constexpr (JPT == 4) {
-                const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(xp));
-                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float2 f = __bfloat1622float2(h[u]);
-                    xv[2 * u] = f.x;
-                    xv[2 * u + 1] = f.y;
+                for (int b4 = 0; b4 < EB; b4 += 4) {
+                    const float4 l = *reinterpret_cast<const float4 *>(ls + tt * EB + b4);
+                    const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int a = 0; a < JPT; ++a)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            acc[a][b4 + b] = __fmaf_rn(xv[a], lv[b], acc[a][b4 + b]);
                 }
-            } else {
-                const float2 f = __bfloat1622float2(
-                    *reinterpret_cast<const __nv_bfloat162 *>(xp));
-                xv[0] = f.x;
-                xv[1] = f.y;
-            }
-#pragma unroll
-            for (int b4 = 0; b4 < EB; b4 += 4) {
-                const float4 l = *reinterpret_cast<const float4 *>(&ls[tt][b4]);
-                const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-                for (int a = 0; a < JPT; ++a)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        acc[a][b4 + b] = __fmaf_rn(xv[a], lv[b], acc[a][b4 + b]);
             }
         }
+        __syncthreads();  // the buffer is refilled by the issue two stages on
     }
-    if (!active) return;
+    if (j0 >= d) return;  // d % 8 == 0: j0 < d means all JPT columns exist
     float *out = P + (int64_t)blockIdx.y * d * E;
 #pragma unroll
     for (int a = 0; a < JPT; ++a)
@@ -230,178 +272,128 @@ dwr_reduce_kernel(const float *__restrict__ P, int64_t n, int chunks, float *__r
     dWr[i] = s;
 }
 
-// dXr[t, j] = sum over e ascending of dL[t, e] Wr[j, e] (one fma chain each).
-// Block: 32 t x 64 j, 128 threads of 4 x 4 outputs; 32 experts per stage.
-// Grid: (token blocks, column blocks).
-constexpr int kXT = 32, kXJ = 64, kXE = 32;
-__global__ void __launch_bounds__(128)
-router_dx_kernel(const float *__restrict__ dL, const float *__restrict__ Wr, int T, int d, int E,
-                 float *__restrict__ dXr) {
-    pdl_wait();
-    pdl_trigger();
-    __shared__ float ls[kXT][kXE + 1];
-    __shared__ float ws[kXJ][kXE + 1];
-    const int tid = threadIdx.x;
-    const int jg = tid % 16, tg = tid / 16;  // outputs t0 + 4tg .. +3, j0 + 4jg .. +3
-    const int64_t t0 = (int64_t)blockIdx.x * kXT;
-    const int j0 = blockIdx.y * kXJ;
-    float acc[4][4] = {};
-    for (int e0 = 0; e0 < E; e0 += kXE) {
-        for (int q = tid; q < kXT * kXE; q += 128) {
-            const int tt = q / kXE, ee = q % kXE;
-            const int64_t t = t0 + tt;
-            ls[tt][ee] = (t < T && e0 + ee < E) ? __ldg(dL + t * E + e0 + ee) : 0.f;
-        }
-        for (int q = tid; q < kXJ * kXE; q += 128) {
-            const int jj = q / kXE, ee = q % kXE;
-            ws[jj][ee] = (j0 + jj < d && e0 + ee < E) ? __ldg(Wr + (int64_t)(j0 + jj) * E + e0 + ee) : 0.f;
-        }
-        __syncthreads();
-        const int en = min(kXE, E - e0);
-        for (int ee = 0; ee < en; ++ee) {
-            float lv[4], wv[4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) lv[a] = ls[4 * tg + a][ee];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) wv[b] = ws[4 * jg + b][ee];
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(lv[a], wv[b], acc[a][b]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int64_t t = t0 + 4 * tg + a;
-            const int j = j0 + 4 * jg + b;
-            if (t < T && j < d) dXr[t * d + j] = acc[a][b];
-        }
-}
-
-// dX[t, :] = bf16( sum over k ascending of dXg[row_of_slot[t*K+k], :] + dXr[t, :] ):
-// one warp per token, 8 columns per lane and step.
-constexpr int kCThreads = 256;
-__global__ void __launch_bounds__(kCThreads)
-combine_add_kernel(const __nv_bfloat16 *__restrict__ dXg, const int32_t *__restrict__ row_of_slot,
-                   const float *__restrict__ dXr, int T, int K, int d, int64_t R,
-                   __nv_bfloat16 *__restrict__ dX) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t t = (int64_t)blockIdx.x * (kCThreads / 32) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const int lane = threadIdx.x & 31;
-    int rows[kMaxK];
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        rows[k] = -1;
-        if (k < K) {
-            const int r = __ldg(row_of_slot + t * K + k);
-            rows[k] = (r >= 0 && r < R) ? r : -1;
-        }
-    }
-    for (int c = lane; c < d / 8; c += 32) {
-        float acc[8] = {};
-#pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (rows[k] < 0) continue;
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(dXg + (int64_t)rows[k] * d) + c);
-            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 f = __bfloat1622float2(h2[u]);
-                acc[2 * u] = __fadd_rn(acc[2 * u], f.x);
-                acc[2 * u + 1] = __fadd_rn(acc[2 * u + 1], f.y);
-            }
-        }
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(dXr + t * d) + 2 * c);
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(dXr + t * d) + 2 * c + 1);
-        const float add[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint4 out;
-        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&out);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            o2[u] = __floats2bfloat162_rn(__fadd_rn(acc[2 * u], add[2 * u]),
-                                          __fadd_rn(acc[2 * u + 1], add[2 * u + 1]));
-        reinterpret_cast<uint4 *>(dX + t * d)[c] = out;
-    }
-}
-
-// E <= 32: the router's share computed in the combine. Block: 8 warps, 32
-// tokens (4 per warp) x 256 columns (8 per lane). Wr's 256 x EB slice is
-// staged transposed in shared memory, dL's 32 x EB slice as is. For each
-// output, r = one fma chain over e ascending of dL[t,e] Wr[j,e], then
-// dX = bf16((sum over k ascending of dXg rows) + r): the same operations, in the
-// same order, as router_dx_kernel followed by combine_add_kernel. Grid: (token
-// blocks, column blocks).
-constexpr int kFTok = 32, kFCols = 256, kFWrLd = kFCols + 4;
-template <int EB>
-__global__ void __launch_bounds__(256)
+// The router's share of dX computed in the final combine, for any E. Block: 8
+// warps of 8 tokens (64 tokens) x 256 columns (8 per lane). Experts go in
+// chunks of 32: Wr's 256 x 32 slice staged transposed in shared memory and
+// dL's 64 x 32 slice as [e][token], by cp.async into two buffers (the next
+// chunk's copies in flight while the current one is used). For each output,
+// r = one fma chain over e ascending of dL[t,e] Wr[j,e]; then
+// dX = bf16((sum over k ascending of the token's dXg rows, fp32) + r), one
+// rounding. Per expert a warp reads 8 Wr values per lane and 8 dL values (two
+// broadcast loads) for 64 fmas. Grid: (token blocks, column blocks).
+constexpr int kFTok = 64, kFCols = 256, kFE = 32, kFWrLd = kFCols + 4, kFLLd = kFTok + 4;
+constexpr int kFTpw = kFTok / 8;  // tokens per warp
+constexpr int kFBufFloats = kFE * kFWrLd + kFE * kFLLd;  // one chunk's Wr and dL slices
+constexpr int kFSmem = 2 * kFBufFloats * 4;
+__global__ void __launch_bounds__(256, 2)
 combine_router_kernel(const __nv_bfloat16 *__restrict__ dXg,
                       const int32_t *__restrict__ row_of_slot, const float *__restrict__ dL,
                       const float *__restrict__ Wr, int T, int K, int d, int E, int64_t R,
                       __nv_bfloat16 *__restrict__ dX) {
     pdl_wait();
     pdl_trigger();
-    __shared__ __align__(16) float ws[EB][kFWrLd];
-    __shared__ float lsm[kFTok][EB];
+    extern __shared__ __align__(16) float fsm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c0 = blockIdx.y * kFCols;
     const int64_t t0 = (int64_t)blockIdx.x * kFTok;
-    for (int q = tid; q < kFCols * EB; q += 256) {
-        const int jj = q / EB, ee = q % EB;
-        ws[ee][jj] = (c0 + jj < d && ee < E) ? __ldg(Wr + (int64_t)(c0 + jj) * E + ee) : 0.f;
-    }
-    for (int q = tid; q < kFTok * EB; q += 256) {
-        const int tt = q / EB, ee = q % EB;
-        lsm[tt][ee] = (t0 + tt < T && ee < E) ? __ldg(dL + (t0 + tt) * E + ee) : 0.f;
-    }
-    __syncthreads();
     const int j = c0 + lane * 8;
-    if (j >= d) return;
-    constexpr int TPW = kFTok / 8;  // tokens per warp
-    float r[TPW][8];
+    // chunk k's copies into buffer k & 1: Wr[c0 + jj, e0 + ee] at ws[ee][jj] and
+    // dL[t0 + tt, e0 + ee] at ls[ee][tt] (zeros outside), 4-byte cp.async with
+    // consecutive threads on consecutive experts (coalesced reads)
+    auto issue = [&](int k) {
+        const int e0 = k * kFE;
+        float *ws = fsm + (k & 1) * kFBufFloats, *ls = ws + kFE * kFWrLd;
+        for (int q = tid; q < kFCols * kFE; q += 256) {
+            const int jj = q / kFE, ee = q % kFE;
+            const bool ok = c0 + jj < d && e0 + ee < E;
+            ptx::cp_async_4_zfill(ptx::smem_addr(ws + ee * kFWrLd + jj),
+                                  ok ? Wr + (int64_t)(c0 + jj) * E + e0 + ee : Wr, ok);
+        }
+        for (int q = tid; q < kFTok * kFE; q += 256) {
+            const int tt = q / kFE, ee = q % kFE;
+            const bool ok = t0 + tt < T && e0 + ee < E;
+            ptx::cp_async_4_zfill(ptx::smem_addr(ls + ee * kFLLd + tt),
+                                  ok ? dL + (t0 + tt) * E + e0 + ee : dL, ok);
+        }
+        ptx::cp_async_commit_group();
+    };
+    float r[kFTpw][8];
 #pragma unroll
-    for (int a = 0; a < TPW; ++a)
+    for (int a = 0; a < kFTpw; ++a)
 #pragma unroll
         for (int u = 0; u < 8; ++u) r[a][u] = 0.f;
-    for (int e = 0; e < E; ++e) {
-        const float4 w0 = *reinterpret_cast<const float4 *>(&ws[e][lane * 8]);
-        const float4 w1 = *reinterpret_cast<const float4 *>(&ws[e][lane * 8 + 4]);
-        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int a = 0; a < TPW; ++a) {
-            const float l = lsm[warp * TPW + a][e];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) r[a][u] = __fmaf_rn(l, wv[u], r[a][u]);
+    const int nch = (E + kFE - 1) / kFE;
+    issue(0);
+    for (int k = 0; k < nch; ++k) {
+        if (k + 1 < nch) {
+            issue(k + 1);
+            ptx::cp_async_wait_group<1>();
+        } else {
+            ptx::cp_async_wait_group<0>();
         }
-    }
+        __syncthreads();
+        const float *ws = fsm + (k & 1) * kFBufFloats, *ls = ws + kFE * kFWrLd;
+        const int en = min(kFE, E - k * kFE);
+        if (j < d) {
+            for (int ee = 0; ee < en; ++ee) {
+                const float4 w0 = *reinterpret_cast<const float4 *>(ws + ee * kFWrLd + lane * 8);
+                const float4 w1 = *reinterpret_cast<const float4 *>(ws + ee * kFWrLd + lane * 8 + 4);
+                const float4 l0 = *reinterpret_cast<const float4 *>(ls + ee * kFLLd + warp * kFTpw);
+                const float4 l1 = *reinterpret_cast<const float4 *>(ls + ee * kFLLd + warp * kFTpw + 4);
+                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-    for (int a = 0; a < TPW; ++a) {
-        const int64_t t = t0 + warp * TPW + a;
-        if (t >= T) break;
-        float acc[8] = {};
-        for (int k = 0; k < K; ++k) {
-            const int row = __ldg(row_of_slot + t * K + k);
-            if (row < 0 || row >= R) continue;
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(dXg + (int64_t)row * d + j));
-            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                for (int a = 0; a < kFTpw; ++a)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 f = __bfloat1622float2(h2[u]);
-                acc[2 * u] = __fadd_rn(acc[2 * u], f.x);
-                acc[2 * u + 1] = __fadd_rn(acc[2 * u + 1], f.y);
+                    for (int u = 0; u < 8; ++u) r[a][u] = __fmaf_rn(lv[a], wv[u], r[a][u]);
             }
         }
-        uint4 out;
-        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&out);
+        __syncthreads();  // the buffer is refilled by the issue two chunks on
+    }
+    if (j >= d) return;
+    // the experts' rows, four tokens at a time: their k-th rows in flight at once
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            o2[u] = __floats2bfloat162_rn(__fadd_rn(acc[2 * u], r[a][2 * u]),
-                                          __fadd_rn(acc[2 * u + 1], r[a][2 * u + 1]));
-        *reinterpret_cast<uint4 *>(dX + t * d + j) = out;
+    for (int h = 0; h < kFTpw; h += 4) {
+        float acc[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[a][u] = 0.f;
+        for (int k = 0; k < K; ++k) {
+            uint4 raw[4];
+            bool ok[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int64_t t = t0 + warp * kFTpw + h + a;
+                const int row = t < T ? __ldg(row_of_slot + t * K + k) : -1;
+                ok[a] = row >= 0 && row < R;
+                raw[a] = ok[a] ? __ldg(reinterpret_cast<const uint4 *>(dXg + (int64_t)row * d + j))
+                               : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                if (!ok[a]) continue;
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw[a]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 f = __bfloat1622float2(h2[u]);
+                    acc[a][2 * u] = __fadd_rn(acc[a][2 * u], f.x);
+                    acc[a][2 * u + 1] = __fadd_rn(acc[a][2 * u + 1], f.y);
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int64_t t = t0 + warp * kFTpw + h + a;
+            if (t >= T) break;
+            uint4 out;
+            __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                o2[u] = __floats2bfloat162_rn(__fadd_rn(acc[a][2 * u], r[h + a][2 * u]),
+                                              __fadd_rn(acc[a][2 * u + 1], r[h + a][2 * u + 1]));
+            *reinterpret_cast<uint4 *>(dX + t * d + j) = out;
+        }
     }
 }
 
@@ -478,6 +470,26 @@ gather_pad_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restri
 
 }  // namespace
 
+namespace {
+template <int EB>
+cudaError_t launch_dwr_part(const __nv_bfloat16 *X, const float *dL, int T, int d, int E, int TC,
+                            int chunks, float *part, cudaStream_t s) {
+    using C = DwrCfg<EB>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(router_dwr_part_kernel<EB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    return launch_k(router_dwr_part_kernel<EB>,
+                    dim3((d + C::JB - 1) / C::JB, chunks, (E + EB - 1) / EB), dim3(kPThreads),
+                    C::SMEM, s, X, dL, T, d, E, TC, part);
+}
+}  // namespace
+
 cudaError_t launch_gather_padded(const __nv_bfloat16 *src, const int32_t *perm_token, int T,
                                  const int32_t *offsets, int E, int d, const float *w,
                                  const int32_t *perm_slot, int64_t R, int64_t cap,
@@ -496,7 +508,7 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                                    const int32_t *idx, const float *dS,
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
-                                   float *dbias, float *dXr, __nv_bfloat16 *dX, cudaStream_t s) {
+                                   float *dbias, float *scratch, __nv_bfloat16 *dX, cudaStream_t s) {
     const int64_t R = (int64_t)T * K;
     const unsigned tb = (unsigned)((T + kDlThreads / 32 - 1) / (kDlThreads / 32));
     auto dl = E <= 32    ? router_dl_kernel<1>
@@ -509,20 +521,19 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
     e = launch_k(col_sum_kernel, dim3(E), dim3(kColThreads), 0, s, static_cast<const float *>(dL), T,
                  E, dbias);
     if (e != cudaSuccess) return e;
-    // dWr: chunks of TC tokens, their partials in the dXr region (T * d floats;
-    // TC grows until the chunks' d x E partials fit), then the reduce
+    // dWr: chunks of TC tokens, their partials in the scratch region (T * d
+    // floats; TC grows until the chunks' d x E partials fit), then the reduce
     int64_t TC = 32;
     while (TC < T && (((T + TC - 1) / TC) * E > T || (T + TC - 1) / TC > 65535)) TC *= 2;
     TC = std::min<int64_t>(TC, T);
     const int chunks = (int)((T + TC - 1) / TC);
-    float *part = chunks > 1 ? dXr : dWr;
-    auto part_k = E <= 8 ? router_dwr_part_kernel<8>
-                  : E <= 16 ? router_dwr_part_kernel<16>
-                            : router_dwr_part_kernel<32>;
-    const int eb = E <= 8 ? 8 : E <= 16 ? 16 : 32;
-    const int jb = kPThreads * (64 / eb);
-    e = launch_k(part_k, dim3((d + jb - 1) / jb, chunks, (E + eb - 1) / eb), dim3(kPThreads), 0, s,
-                 X, static_cast<const float *>(dL), T, d, E, (int)TC, part);
+    float *part = chunks > 1 ? scratch : dWr;
+    if (E <= 8)
+        e = launch_dwr_part<8>(X, dL, T, d, E, (int)TC, chunks, part, s);
+    else if (E <= 16)
+        e = launch_dwr_part<16>(X, dL, T, d, E, (int)TC, chunks, part, s);
+    else
+        e = launch_dwr_part<32>(X, dL, T, d, E, (int)TC, chunks, part, s);
     if (e != cudaSuccess) return e;
     if (chunks > 1) {
         const int64_t n = (int64_t)d * E;
@@ -530,21 +541,20 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                      static_cast<const float *>(part), n, chunks, dWr);
         if (e != cudaSuccess) return e;
     }
-    // the router's share dL Wr^T and the final combine: fused for E <= 32
-    if (E <= 32) {
-        auto ck = E <= 8 ? combine_router_kernel<8>
-                  : E <= 16 ? combine_router_kernel<16>
-                            : combine_router_kernel<32>;
-        return launch_k(ck, dim3((unsigned)((T + kFTok - 1) / kFTok), (d + kFCols - 1) / kFCols),
-                        dim3(256), 0, s, dXg, row_of_slot, static_cast<const float *>(dL), Wr, T,
-                        K, d, E, R, dX);
+    // the router's share dL Wr^T and the final combine, in one kernel
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(combine_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kFSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
     }
-    e = launch_k(router_dx_kernel, dim3((unsigned)((T + kXT - 1) / kXT), (d + kXJ - 1) / kXJ),
-                 dim3(128), 0, s, static_cast<const float *>(dL), Wr, T, d, E, dXr);
-    if (e != cudaSuccess) return e;
-    return launch_k(combine_add_kernel, dim3((unsigned)((T + kCThreads / 32 - 1) / (kCThreads / 32))),
-                    dim3(kCThreads), 0, s, dXg, row_of_slot, static_cast<const float *>(dXr), T, K,
-                    d, R, dX);
+    return launch_k(combine_router_kernel,
+                    dim3((unsigned)((T + kFTok - 1) / kFTok), (d + kFCols - 1) / kFCols),
+                    dim3(256), kFSmem, s, dXg, row_of_slot, static_cast<const float *>(dL), Wr, T,
+                    K, d, E, R, dX);
 }
 
 }  // namespace moe

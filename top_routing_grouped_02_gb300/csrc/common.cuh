@@ -121,13 +121,13 @@ cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA
                                int R, int d, int E, int n, __nv_bfloat16 *dXg,
                                __nv_bfloat16 *dX, uint32_t *err, cudaStream_t s);
 // Router backward (backward.cu): dL [T, E], dbias [E], dWr [d, E] (fp32) and
-// dX [T, d] = bf16(sum_k dXg[row_of_slot[t*K+k]] + dL Wr^T), with dXr [T, d]
-// fp32 scratch for the second term.
+// dX [T, d] = bf16(sum_k dXg[row_of_slot[t*K+k]] + dL Wr^T), with `scratch`
+// (T * d floats) for the partial sums of dWr.
 cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, const float *L,
                                    const int32_t *idx, const float *dS,
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
-                                   float *dbias, float *dXr, __nv_bfloat16 *dX, cudaStream_t s);
+                                   float *dbias, float *scratch, __nv_bfloat16 *dX, cudaStream_t s);
 // Rows of src gathered into the padded grouped layout of the weight gradients
 // (each expert's rows from a 64-row boundary, zeros after them), optionally
 // scaled by w[perm_slot[p]]; poff [E+1] receives (or, offsets_done, holds) the

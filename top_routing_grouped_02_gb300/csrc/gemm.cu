@@ -920,10 +920,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const CUtensorMap *omap = FUSED && un.down ? &tmOut2 : &tmOut;
             const uint32_t a = uc & 1u, aph = (uc >> 1) & 1u;
             ++uc;
-            if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->tfull[a]), aph, args.err)) break;
-            ptx::tc_fence_after();
             const bool valid = r < rows;
             const int64_t p = (int64_t)row0 + r;
+            // kDH: the row's stored pre-activations, one 32-column chunk ahead of
+            // their use; the first chunk's loads go out before the accumulator wait
+            const int c_lo = half * (BN / 32 / nhalf), c_hi = (half + 1) * (BN / 32 / nhalf);
+            float4 x1[8], x3[8];
+            auto load_pre = [&](int c, float4 (&l1)[8], float4 (&l3)[8]) {
+                const int64_t off = p * args.out_ld + nb * BN + c * 32;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    l1[i] = valid ? __ldg(reinterpret_cast<const float4 *>(args.pre1 + off) + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    l3[i] = valid ? __ldg(reinterpret_cast<const float4 *>(args.pre3 + off) + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            };
+            if constexpr (MODE == kDH) load_pre(c_lo, x1, x3);
+            if (!bounded_wait<PAIR>(ptx::smem_addr(&ctl->tfull[a]), aph, args.err)) break;
+            ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
             // A warp whose 32 rows all belong to the tile writes each 32-column
             // chunk through shared memory and a TMA store (whole 64-byte row
@@ -1003,17 +1018,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 const int64_t rowoff = p * args.out_ld + nb * BN;
 #pragma unroll 1
-                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                for (int c = c_lo; c < c_hi; ++c) {
+                    float4 n1[8], n3[8];
+                    if (c + 1 < c_hi) load_pre(c + 1, n1, n3);
                     uint32_t gv[32];
                     ptx::tmem_ld32(taddr + c * 32, gv);
-                    float4 x1[8], x3[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        x1[i] = valid ? __ldg(reinterpret_cast<const float4 *>(args.pre1 + rowoff + c * 32) + i)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                        x3[i] = valid ? __ldg(reinterpret_cast<const float4 *>(args.pre3 + rowoff + c * 32) + i)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
                     float part = 0.f;
                     uint32_t pa[16], pb[16];
 #pragma unroll
@@ -1036,6 +1045,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     emit(pa, args.out + rowoff + c * 32, nb * BN + c * 32, &tmOut);
                     emit(pb, args.out3 + rowoff + c * 32, nb * BN + c * 32, &tmOut2);
                     if (valid) args.dspart[p * args.ds_ld + nb * (BN / 32) + c] = part;
+                    if (c + 1 < c_hi) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            x1[i] = n1[i];
+                            x3[i] = n3[i];
+                        }
+                    }
                 }
             } else if (!dn) {
                 __nv_bfloat16 *dst = args.out + p * args.out_ld + nb * 128;
@@ -1327,18 +1343,25 @@ cudaError_t launch_ew_auto(const CUtensorMap &a, const CUtensorMap &b0, const CU
     return launch_ew<MODE, PAIR, 4>(a, b0, b1, out, b2, out2, args, max_units, s);
 }
 
-// dS[p] = sum of the row's partials in ascending column order (rows in use).
+// dS[p] = sum of the row's partials (rows in use) in a fixed order: g lanes per
+// row (a power of two, from the row length), lane i of the group adding
+// partials i, i + g, ... ascending, then a butterfly of fixed shape over the
+// group. Reads are coalesced along the row.
 __global__ void __launch_bounds__(256)
 ds_reduce_kernel(const float *__restrict__ part, int ld, int R, const int32_t *__restrict__ rows_used,
-                 float *__restrict__ dS) {
+                 int g, float *__restrict__ dS) {
     pdl_wait();
     pdl_trigger();
-    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (p >= R || p >= __ldg(rows_used)) return;
-    const float *row = part + p * ld;
-    float acc = row[0];
-    for (int i = 1; i < ld; ++i) acc = __fadd_rn(acc, row[i]);
-    dS[p] = acc;
+    const int64_t p = ((int64_t)blockIdx.x * 256 + threadIdx.x) / g;
+    const int sub = threadIdx.x & (g - 1);
+    const bool valid = p < R && p < __ldg(rows_used);
+    float acc = 0.f;
+    if (valid) {
+        const float *row = part + p * ld;
+        for (int i = sub; i < ld; i += g) acc = __fadd_rn(acc, __ldg(row + i));
+    }
+    for (int o = g >> 1; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    if (valid && sub == 0) dS[p] = acc;
 }
 }  // namespace
 
@@ -1412,8 +1435,12 @@ cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_toke
     const int tiles = R / BM + E;
     cudaError_t e = launch_ew_auto<kDH, false>(tb, tb, tb, t1, tb, t3, args, tiles * args.NB, s);
     if (e != cudaSuccess) return e;
-    return launch_k(ds_reduce_kernel, dim3((unsigned)((R + 255) / 256)), dim3(256), 0, s,
-                    static_cast<const float *>(dspart), n / 32, R, offsets + E, dS);
+    // lanes per row: about 8 partials each, 1 .. 32
+    const int ld = n / 32;
+    int g = 1;
+    while (g < 32 && g * 8 < ld) g *= 2;
+    return launch_k(ds_reduce_kernel, dim3((unsigned)(((int64_t)R * g + 255) / 256)), dim3(256), 0,
+                    s, static_cast<const float *>(dspart), ld, R, offsets + E, g, dS);
 }
 
 cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA3,

@@ -69,6 +69,17 @@ __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, 
                  "l"(policy)
                  : "memory");
 }
+// 16- / 4-byte copies that write zeros instead (the source is not read) when !ok.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(ok ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_4_zfill(uint32_t dst, const void *src, bool ok) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(ok ? 4 : 0)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit_group() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
