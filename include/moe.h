@@ -98,7 +98,9 @@ int moe_abi_version(void);
  * Before first use the caller zeroes it once (moe_workspace_init). */
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n);
 
-/* Zero the workspace's error word and control words (enqueued on `stream`). */
+/* Zero the workspace's error word, control words and the one-kernel
+ * grouping's block flags: its first min(ws_bytes, 512) bytes (enqueued on
+ * `stream`). */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Router from activations (page "Triton优化MoE模型：topk_gating算子融合实战",
@@ -141,7 +143,12 @@ moe_status_t moe_route_logits(const float *logits, int T, int E, int K, int reno
  *   row, which sets MOE_DEVERR_REPEATED_EXPERT; such slots get no row and the
  *   rows in use end at offsets[E] < T*K);
  *   tiles [(T*K)/128 + E][4] int32 = {expert, first row, rows<=128, 0}, expert
- *   order, and num_tiles [1] (tile_base[E]). ws: workspace of this shape. */
+ *   order, and num_tiles [1] (tile_base[E]). ws: workspace of this shape.
+ * Kernels: for T <= 65536 ONE (each block counts its run of 32-token chunks
+ * per expert, publishes the counts with a flag and, behind bounded waits on
+ * every block's flag, takes the offsets from the expert totals and its start
+ * within each expert from the blocks before it, then scatters); otherwise three
+ * (rank, scan, scatter). The result is the same either way. */
 moe_status_t moe_permute(const int32_t *topk_idx, const int32_t *counts,
                          int T, int E, int K,
                          int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
@@ -339,7 +346,8 @@ int moe_expert_mlp_launches(int T, int d, int E, int K, int n, int rounded);
 /* The whole layer: route -> permute -> gate/up+SwiGLU -> down+weight -> combine.
  * topk_idx_out / topk_w_out [T,K] may be NULL (kept in the workspace then).
  * Enqueues moe_forward_launches(T, d, E, K, n, 0) kernels: the router (1 with
- * E <= 32 as moe_route says, else 2), the grouping (3), the expert GEMMs (2, 3
+ * E <= 32 as moe_route says, else 2), the grouping (1 for T <= 65536, see
+ * moe_permute; else 3), the expert GEMMs (2, 3
  * on CTA pairs, which gather their rows first, or 1 when both run in one launch,
  * see moe_expert_mlp) and the combine (1); and, unless E <= 16 and T <= 2048
  * with the two-kernel router, one memset of the counts; no host

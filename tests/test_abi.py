@@ -50,29 +50,31 @@ def test_workspace_bytes(lib):
 
 def test_forward_launch_counts(lib, monkeypatch):
     # kernels per forward: the router (1 for E <= 32 with E % 4 == 0: logits and
-    # selection in one kernel; else 2), grouping (or rounding) 3, combine 1, and
+    # selection in one kernel; else 2), grouping 1 (3 above 65536 tokens; rounding
+    # 3), combine 1, and
     # the expert GEMMs: two launches, a row gather more on CTA pairs (experts of
     # at least 8 row tiles on average), or one fused launch on request
     for var in ("MOE_GEMM_FUSED", "MOE_GEMM_CTA_PAIR"):
         monkeypatch.delenv(var, raising=False)
-    assert moe.forward_launches(512, 256, 8, 2, 512) == 7            # tiny
-    assert moe.forward_launches(16384, 1536, 128, 4, 256) == 8       # SonicMoE
+    assert moe.forward_launches(512, 256, 8, 2, 512) == 5            # tiny
+    assert moe.forward_launches(16384, 1536, 128, 4, 256) == 6       # SonicMoE
     assert moe.forward_launches(16384, 1536, 128, 4, 256, True) == 8
-    assert moe.forward_launches(8192, 7168, 256, 8, 2048) == 8       # DeepSeek-V3
-    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 8        # Mixtral: CTA pairs
-    assert moe.forward_launches(64, 256, 6, 2, 512) == 8             # E % 4 != 0: two router kernels
-    assert moe.forward_launches(64, 33792, 8, 2, 512) == 8           # 33 blocks: two router kernels
+    assert moe.forward_launches(8192, 7168, 256, 8, 2048) == 6       # DeepSeek-V3
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 6        # Mixtral: CTA pairs
+    assert moe.forward_launches(64, 256, 6, 2, 512) == 6             # E % 4 != 0: two router kernels
+    assert moe.forward_launches(64, 33792, 8, 2, 512) == 6           # 33 blocks: two router kernels
+    assert moe.forward_launches(70000, 256, 8, 2, 512) == 8          # T > 65536: three grouping kernels (and pairs)
     # (whether a fused launch's units fit its rounds depends on the device's SM
     # count, unknown here; these cases do not depend on it)
     assert moe.forward_launches(16384, 1536, 128, 4, 256, part="expert_mlp") == 2
     assert moe.forward_launches(4096, 4096, 8, 2, 14336, part="expert_mlp") == 3
     monkeypatch.setenv("MOE_GEMM_FUSED", "1")
-    assert moe.forward_launches(512, 256, 8, 2, 512) == 6            # 80 units at most
+    assert moe.forward_launches(512, 256, 8, 2, 512) == 4            # 80 units at most
     assert moe.forward_launches(512, 256, 8, 2, 512, part="expert_mlp") == 1
-    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 8        # too wide to fuse
-    assert moe.forward_launches(64, 256, 4, 1, 2176) == 7            # n > 2048
+    assert moe.forward_launches(4096, 4096, 8, 2, 14336) == 6        # too wide to fuse
+    assert moe.forward_launches(64, 256, 4, 1, 2176) == 5            # n > 2048
     monkeypatch.setenv("MOE_GEMM_FUSED", "0")
-    assert moe.forward_launches(16384, 1536, 128, 4, 256) == 8
+    assert moe.forward_launches(16384, 1536, 128, 4, 256) == 6
     with pytest.raises(ValueError):
         moe.forward_launches(512, 200, 8, 2, 512)
     assert lib.moe_forward_launches(512, 256, 8, 2, 512, 2) == -1

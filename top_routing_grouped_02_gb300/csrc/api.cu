@@ -117,6 +117,11 @@ WsLayout layout_impl(int T, int d, int E, int K, int n, size_t R, bool rounded) 
         return o;
     };
     L.err = take(64);
+    // right after the control words at the same offset in every shape: only the
+    // one-kernel grouping writes these flags (a call's tag could otherwise meet a
+    // stale value another kernel left there)
+    L.group_flags = take(4 * (size_t)kGroupMaxBlocks);
+    L.group_agg = take(4 * (size_t)kGroupMaxBlocks * E);
     L.counts = take(4 * (size_t)E);
     L.offsets = take(4 * (size_t)(E + 1));
     L.tile_base = take(4 * (size_t)(E + 1));
@@ -189,9 +194,10 @@ int moe_expert_mlp_launches(int T, int d, int E, int K, int n, int rounded) {
 int moe_forward_launches(int T, int d, int E, int K, int n, int rounded) {
     const int gemms = moe_expert_mlp_launches(T, d, E, K, n, rounded);
     if (gemms < 0) return -1;
-    // router 1 or 2 (with 16-byte-aligned router weights), grouping or rounding
-    // 3, combine 1, and the expert GEMMs
-    return (route_is_one_kernel(d, E, true) ? 1 : 2) + 3 + gemms + 1;
+    // router 1 or 2 (with 16-byte-aligned router weights), grouping 1 (3 for
+    // T > 65536) or rounding 3, combine 1, and the expert GEMMs
+    const int grouping = rounded ? 3 : permute_launch_count(T);
+    return (route_is_one_kernel(d, E, true) ? 1 : 2) + grouping + gemms + 1;
 }
 
 size_t moe_workspace_bytes(int T, int d, int E, int K, int n) {
@@ -201,7 +207,10 @@ size_t moe_workspace_bytes(int T, int d, int E, int K, int n) {
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
     if (ws == nullptr || ws_bytes < 64) return MOE_ERR_INVALID_ARG;
-    return from_cuda(cudaMemsetAsync(ws, 0, 64, as_stream(stream)));
+    // the control words and the one-kernel grouping's block flags, which sit at
+    // the same offset in every shape (the first 512 bytes)
+    const size_t n = ws_bytes < 512 ? ws_bytes : 512;
+    return from_cuda(cudaMemsetAsync(ws, 0, n, as_stream(stream)));
 }
 
 moe_status_t moe_route(const moe_bf16 *X, const float *Wr, const float *bias, int T, int d, int E,

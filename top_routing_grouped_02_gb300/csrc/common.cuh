@@ -23,10 +23,16 @@ constexpr int kTokCap = 16;
 constexpr int kMaxRoundM = 1 << 16;
 // Tokens per grouping chunk (one warp, one bit per token).
 constexpr int kChunk = 32;
+// One-kernel grouping: at most this many blocks (all resident at once), each of
+// at most kGroupMaxCpb chunks; larger T takes the three-kernel grouping.
+constexpr int kGroupMaxBlocks = 64;
+constexpr int kGroupMaxCpb = 32;
 
 // Byte offsets of the workspace regions for one layer shape (all 256-aligned).
 struct WsLayout {
     size_t err;         // uint32 error word + control words (64 B)
+    size_t group_flags; // uint32 [kGroupMaxBlocks] one-kernel grouping: block flags (fixed offset)
+    size_t group_agg;   // int32 [kGroupMaxBlocks * E] one-kernel grouping: block counts
     size_t counts;      // int32 [E]
     size_t offsets;     // int32 [E+1]
     size_t tile_base;   // int32 [E+1]
@@ -61,7 +67,8 @@ struct WsLayout {
 // Control words at the start of the workspace (uint32 each): the error word,
 // the grouping scan's ticket, and the fused expert MLP's launch epoch and
 // ticket (its row-tile counters carry the epoch, so they need no clearing).
-enum : int { kWordErr = 0, kWordDone = 1, kWordEpoch = 2, kWordTicket = 3 };
+enum : int { kWordErr = 0, kWordDone = 1, kWordEpoch = 2, kWordTicket = 3, kWordGroupEpoch = 4,
+             kWordGroupTicket = 5 };
 
 WsLayout ws_layout(int T, int d, int E, int K, int n);
 // Layout for the Token Rounding forward: grouped buffers sized for the largest
@@ -83,10 +90,13 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *X, const float *Wr, const 
                                  int T, int d, int E, float *L, cudaStream_t s);
 cudaError_t launch_route_logits(const float *logits, int T, int E, int K, int renorm,
                                 int32_t *idx, float *w, int32_t *counts, cudaStream_t s);
+// Kernels launch_permute enqueues: 1 for T <= 65536 (the one-kernel grouping),
+// else 3.
+int permute_launch_count(int T);
 cudaError_t launch_permute(const int32_t *idx, const int32_t *counts_in, int T, int E, int K,
                            int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
                            int32_t *row_of_slot, int32_t *tiles, int32_t *num_tiles,
-                           const WsLayout &L, char *ws, cudaStream_t s);
+                           const WsLayout &L, char *ws, cudaStream_t s, bool one_kernel = true);
 // Rows p < min(R, *rows_used) (rows_used: device, nullable); a token index out of
 // range gives a zero row and sets MOE_DEVERR_BAD_EXPERT in *err.
 cudaError_t launch_gather_rows(const __nv_bfloat16 *X, const int32_t *perm_token, int T, int R,

@@ -108,8 +108,11 @@ extern "C" moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const int32
     // the control words (error word, completion ticket) must start at zero
     if (cudaMemsetAsync(static_cast<char *>(scratch) + L.err, 0, 64, st) != cudaSuccess)
         return MOE_ERR_CUDA;
+    // (three kernels: the one-kernel grouping's call tags live in the control
+    // words, which this call clears every time)
     if (launch_permute(topk_idx, counts, T, E, K, offsets, perm_token, perm_slot, row_of_slot,
-                       tiles, num_tiles, L, static_cast<char *>(scratch), st) != cudaSuccess)
+                       tiles, num_tiles, L, static_cast<char *>(scratch), st,
+                       /*one_kernel=*/false) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -24,7 +24,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_CHECK"}
 # Kernels each call enqueues; the gate/up GEMM launches one more (a row gather)
 # when it runs on CTA pairs, the router's backward one fewer when T is too
-# short to split into chunks, and the whole-layer calls depend on the shape
+# short to split into chunks, moe_permute one kernel instead of three for
+# T <= 65536, and the whole-layer calls depend on the shape
 # (forward_launches).
 LAUNCHES = {"moe_route": 2, "moe_route_logits": 1, "moe_permute": 3, "moe_gemm_gate_up": 1,
             "moe_gemm_gate_up_train": 1, "moe_backward_dh": 2, "moe_backward_dx": 2,
