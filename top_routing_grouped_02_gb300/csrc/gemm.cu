@@ -434,7 +434,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // A rows gathered in the kernel (single-CTA gate/up units) or loaded by TMA
     constexpr bool GATHER = (MODE == kGateUp || MODE == kGateUpPre || MODE == kDH || FUSED) && !PAIR;
     constexpr bool GATE = MODE == kGateUp || MODE == kGateUpPre;  // gate/up B boxes (W1 | W3)
-    static_assert(!((MODE == kDH || MODE == kDX) && PAIR), "the backward GEMMs run single CTAs");
+    static_assert(!(MODE == kDH && PAIR), "the dH GEMM runs single CTAs");
     constexpr bool WGRAD = MODE == kDW13 || MODE == kDW2;
     static_assert(!(WGRAD && PAIR), "the weight-gradient GEMMs run single CTAs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -686,6 +686,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     // both CTAs' loads complete on the even CTA's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full, 2 * kTx);
                     const uint32_t fullc = ptx::mapa(full, 0);
+                    if constexpr (MODE == kDX) {
+                        // A: this CTA's 128 rows of dA1 (first n/64 k-blocks) or dA3;
+                        // B: its 128 of the tile's 256 output columns, W1[e] or W3[e]
+                        // rows (K-major), two 64-row boxes
+                        const bool second = kb >= args.kb_half;
+                        const int kx = (second ? kb - args.kb_half : kb) * BK;
+                        ptx::tma_load_2d_pair(sA, second ? &tmB2 : &tmA, fullc, kx, row0);
+                        const int brow = e * args.bn_rows + nb * BN + (int)rank * 128;
+                        const CUtensorMap *mb = second ? &tmB1 : &tmB0;
+                        ptx::tma_load_2d_pair(sB, mb, fullc, kx, brow);
+                        ptx::tma_load_2d_pair(sB + kBBox, mb, fullc, kx, brow + 64);
+                        continue;
+                    }
                     ptx::tma_load_2d_pair(sA, &tmA, fullc, kb * BK, row0);
                     if (GATE) {
                         // even CTA: gate columns (W1), odd CTA: up columns (W3)
@@ -1468,8 +1481,12 @@ cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA
     args.bn_rows = d;
     args.kb_half = n / BK;
     const int tiles = R / BM + E;
+    // CTA pairs (M = 256, each CTA half of B) where the forward GEMMs use them
     cudaError_t e =
-        launch_ew_auto<kDX, false>(ta1, tw1, tw3, tout, ta3, tout, args, tiles * args.NB, s);
+        use_pair(R, E)
+            ? launch_ew_auto<kDX, true>(ta1, tw1, tw3, tout, ta3, tout, args,
+                                        (tiles / 2 + E) * args.NB, s)
+            : launch_ew_auto<kDX, false>(ta1, tw1, tw3, tout, ta3, tout, args, tiles * args.NB, s);
     if (e != cudaSuccess) return e;
     return launch_combine(dXg, row_of_slot, T, K, d, dX, s);
 }
