@@ -234,10 +234,11 @@ moe_status_t moe_gemm_gate_up_train(const moe_bf16 *X, const moe_bf16 *W1, const
  * the contiguous dimension) whose epilogue forms, with A1, A3 [T*K,n] fp32
  * from moe_gemm_gate_up_train and the routing weights topk_w [T*K] fp32:
  * dA1, dA3 [T*K,n] bf16 (grouped rows) and dS [T*K] fp32 (grouped rows; each
- * row's sum over j in fp32, 32-column partials added in ascending column
- * order by a second kernel). Needs n % 256 == 0 and n <= 16*d, else
- * MOE_ERR_UNSUPPORTED_SHAPE. ws: workspace of this shape (its gathered-rows
- * region holds the partials). Two kernels; a row index out of range is
+ * row's sum over j in fp32: 32-column partials, added in a fixed order by a
+ * second kernel). Needs n % 256 == 0, else MOE_ERR_UNSUPPORTED_SHAPE. ws:
+ * workspace of this shape (its H region holds the partials; on CTA pairs its
+ * gathered-rows region the dY rows). Two kernels, three on CTA pairs (experts of
+ * >= 8 row tiles on average: a row gather first); a row index out of range is
  * skipped and flagged like the forward GEMMs'. */
 moe_status_t moe_backward_dh(const moe_bf16 *dY, const moe_bf16 *W2, const float *A1,
                              const float *A3, const float *topk_w, const int32_t *perm_token,

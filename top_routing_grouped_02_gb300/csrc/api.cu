@@ -306,20 +306,22 @@ moe_status_t moe_backward_dh(const moe_bf16 *dY, const moe_bf16 *W2, const float
         return MOE_ERR_INVALID_ARG;
     moe_status_t s = check_mlp_shape(T, d, E, K, n);
     if (s != MOE_OK) return s;
-    // 256 hidden columns per unit; the dS partials (n/32 floats per row) live
-    // in the workspace region of the gathered rows (2*d bytes per row)
-    if (n % 256 != 0 || n / 8 > 2 * d) return MOE_ERR_UNSUPPORTED_SHAPE;
+    // 256 hidden columns per unit; the dS partials (n/32 floats per row) live in
+    // the workspace's H region (2*n bytes per row), the gathered dY rows of the
+    // CTA-pair path in its gathered-rows region
+    if (n % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(dY) || !aligned16(W2) || !aligned16(A1) || !aligned16(A3) || !aligned16(dA1) ||
         !aligned16(dA3))
         return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, d, E, K, n);
-    if (ws_bytes < L.h) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < L.z) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_arch()) != MOE_OK) return s;
     return from_cuda(launch_backward_dh(
         reinterpret_cast<const __nv_bfloat16 *>(dY), perm_token, T,
         reinterpret_cast<const __nv_bfloat16 *>(W2), A1, A3, topk_w, perm_slot, offsets, T * K, d, E, n,
         reinterpret_cast<__nv_bfloat16 *>(dA1), reinterpret_cast<__nv_bfloat16 *>(dA3),
-        at<float>(ws, L.xg), dS, at<uint32_t>(ws, L.err), as_stream(stream)));
+        at<__nv_bfloat16>(ws, L.xg), at<float>(ws, L.h), dS, at<uint32_t>(ws, L.err),
+        as_stream(stream)));
 }
 
 moe_status_t moe_backward_dx(const moe_bf16 *dA1, const moe_bf16 *dA3, const moe_bf16 *W1,

@@ -116,13 +116,15 @@ cudaError_t launch_gemm_gate_up_train(const __nv_bfloat16 *X, const int32_t *per
                                       __nv_bfloat16 *H, float *A1, float *A3,
                                       __nv_bfloat16 *xg, uint32_t *err, cudaStream_t s);
 // Backward dH: dA1, dA3 [R, n] bf16 and dS [R] fp32 from dY [T, d], W2 and the
-// pre-activations; dspart: scratch [R, n/32] fp32 (n % 256 == 0).
+// pre-activations; xg: scratch [R, d] bf16 for the gathered dY rows (CTA-pair
+// path), dspart: scratch [R, n/32] fp32 (n % 256 == 0).
 cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_token, int T,
                                const __nv_bfloat16 *W2, const float *A1,
                                const float *A3, const float *topk_w,
                                const int32_t *perm_slot, const int32_t *offsets, int R, int d,
                                int E, int n, __nv_bfloat16 *dA1, __nv_bfloat16 *dA3,
-                               float *dspart, float *dS, uint32_t *err, cudaStream_t s);
+                               __nv_bfloat16 *xg, float *dspart, float *dS, uint32_t *err,
+                               cudaStream_t s);
 // Backward dX: dXg [R, d] = dA1 W1[e]^T + dA3 W3[e]^T (bf16), then
 // dX [T, d] = sum over k of dXg[row_of_slot[t*K + k]] (the combine).
 cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA3,

@@ -434,7 +434,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // A rows gathered in the kernel (single-CTA gate/up units) or loaded by TMA
     constexpr bool GATHER = (MODE == kGateUp || MODE == kGateUpPre || MODE == kDH || FUSED) && !PAIR;
     constexpr bool GATE = MODE == kGateUp || MODE == kGateUpPre;  // gate/up B boxes (W1 | W3)
-    static_assert(!(MODE == kDH && PAIR), "the dH GEMM runs single CTAs");
     constexpr bool WGRAD = MODE == kDW13 || MODE == kDW2;
     static_assert(!(WGRAD && PAIR), "the weight-gradient GEMMs run single CTAs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -700,7 +699,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         continue;
                     }
                     ptx::tma_load_2d_pair(sA, &tmA, fullc, kb * BK, row0);
-                    if (GATE) {
+                    if constexpr (MODE == kDH) {
+                        // its 128 of the tile's 256 hidden columns: W2[e] rows (K-major,
+                        // d contiguous), two 64-row boxes
+                        const int brow = e * args.bn_rows + nb * BN + (int)rank * 128;
+                        ptx::tma_load_2d_pair(sB, &tmB0, fullc, kb * BK, brow);
+                        ptx::tma_load_2d_pair(sB + kBBox, &tmB0, fullc, kb * BK, brow + 64);
+                    } else if (GATE) {
                         // even CTA: gate columns (W1), odd CTA: up columns (W3)
                         const CUtensorMap *mb = leader ? &tmB0 : &tmB1;
                         ptx::tma_load_2d_pair(sB, mb, fullc, nb * 128, ky);
@@ -1418,8 +1423,9 @@ cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_toke
                                const float *A3, const float *topk_w,
                                const int32_t *perm_slot, const int32_t *offsets, int R, int d,
                                int E, int n, __nv_bfloat16 *dA1, __nv_bfloat16 *dA3,
-                               float *dspart, float *dS, uint32_t *err, cudaStream_t s) {
-    CUtensorMap tb, t1, t3;
+                               __nv_bfloat16 *xg, float *dspart, float *dS, uint32_t *err,
+                               cudaStream_t s) {
+    CUtensorMap ta, tb, t1, t3;
     // W2 as [E*n rows, d columns]: 64 x 64 boxes, K-major (d contiguous)
     if (!make_map(&tb, W2, d, (uint64_t)E * n, 64, 64) ||
         !make_map(&t1, dA1, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
@@ -1446,7 +1452,18 @@ cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_toke
     args.dspart = dspart;
     args.ds_ld = n / 32;
     const int tiles = R / BM + E;
-    cudaError_t e = launch_ew_auto<kDH, false>(tb, tb, tb, t1, tb, t3, args, tiles * args.NB, s);
+    cudaError_t e;
+    if (use_pair(R, E)) {
+        // CTA pairs, where the forward uses them: dY rows gathered into xg first
+        // (the grouped rows in use end at offsets[E]), then loaded by TMA
+        e = launch_gather_rows(dY, perm_token, T, R, offsets + E, d, xg, err, s);
+        if (e != cudaSuccess) return e;
+        if (!make_map(&ta, xg, d, R, 64, BM)) return cudaErrorInvalidValue;
+        e = launch_ew_auto<kDH, true>(ta, tb, tb, t1, tb, t3, args, (tiles / 2 + E) * args.NB, s);
+    } else {
+        // single CTAs gather their dY rows themselves
+        e = launch_ew_auto<kDH, false>(tb, tb, tb, t1, tb, t3, args, tiles * args.NB, s);
+    }
     if (e != cudaSuccess) return e;
     // lanes per row: about 8 partials each, 1 .. 32
     const int ld = n / 32;
