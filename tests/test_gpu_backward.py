@@ -204,7 +204,10 @@ def test_backward_dh_rejects_n_not_a_multiple_of_256():
     (300, 256, 16, 2, 256, 5),     # expert 5 chosen by no token: its gradients are zero
     (700, 512, 4, 3, 768, None),   # several 64-row k-blocks and 128-row output tiles per expert
 ])
-def test_weight_gradients_match_oracle(T, d, E, K, n, empty):
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_weight_gradients_match_oracle(T, d, E, K, n, empty, pair, monkeypatch):
+    # single CTAs, and CTA pairs (two 128-row output tiles a unit)
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", pair)
     inp = synth.layer_inputs(T=T, d=d, E=E, n=n, device="cuda", seed=T)
     if empty is not None:
         bias = torch.zeros(E, dtype=torch.float32)

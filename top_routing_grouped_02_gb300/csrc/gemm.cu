@@ -435,7 +435,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr bool GATHER = (MODE == kGateUp || MODE == kGateUpPre || MODE == kDH || FUSED) && !PAIR;
     constexpr bool GATE = MODE == kGateUp || MODE == kGateUpPre;  // gate/up B boxes (W1 | W3)
     constexpr bool WGRAD = MODE == kDW13 || MODE == kDW2;
-    static_assert(!(WGRAD && PAIR), "the weight-gradient GEMMs run single CTAs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -502,7 +501,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // weight gradients: the expert's 64-row k-blocks (their prefix gives
             // the padded row offsets); otherwise its 128-row tiles
             c = bad ? 0 : WGRAD ? (o1 - o0 + BK - 1) / BK : (o1 - o0 + BM - 1) / BM;
-            if (PAIR) c = (c + 1) / 2;
+            if (PAIR && !WGRAD) c = (c + 1) / 2;  // tile pairs (k-blocks stay k-blocks)
         }
         if (e == 0) ctl->offsets[E] = args.offsets[E];
         // offsets must be a non-decreasing split of [0, R); otherwise do no work
@@ -607,7 +606,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     const int total_units =
         FUSED   ? ctl->nrounds * (int)gridDim.x
-        : WGRAD ? E * args.MT * NB
+        : WGRAD ? E * (PAIR ? args.MT / 2 : args.MT) * NB
                 : (ctl->tile_base[0][E] + ctl->tile_base[1][E]) * NB;
     const int per_tile = PAIR ? 2 : 1;
     // k-blocks of a unit: d / 64 for gate/up, n / 64 for down (weight gradients:
@@ -620,17 +619,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             x.kbs = x.down ? KB2 : KB;
             return x;
         } else if constexpr (WGRAD) {
-            // expert-major, then 128-row output tile, then output column block
+            // expert-major, then 128-row output tile (a pair of them on CTA pairs,
+            // CTA `rank` taking the pair's tile 2*mt + rank), then output column block
             Unit x;
             x.valid = true;
             x.down = false;
             x.tile = -1;
-            const int per_e = args.MT * NB;
+            const int per_e = (PAIR ? args.MT / 2 : args.MT) * NB;
             x.e = u / per_e;
             const int rem = u - x.e * per_e;
             const int mt = rem / NB;
             x.nb = rem - mt * NB;
-            x.row0 = mt * BM;
+            x.row0 = (PAIR ? 2 * mt + (int)rank : mt) * BM;
             x.rows = BM;
             x.kbs = ctl->tile_base[0][x.e + 1] - ctl->tile_base[0][x.e];
             x.poff = BK * ctl->tile_base[0][x.e];
@@ -685,6 +685,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     // both CTAs' loads complete on the even CTA's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full, 2 * kTx);
                     const uint32_t fullc = ptx::mapa(full, 0);
+                    if constexpr (WGRAD) {
+                        // A (MN-major): this CTA's 128 output rows, two 64-column slabs;
+                        // B: its half of the 256 output columns (dW1|dW3: dA1 on the even
+                        // CTA, dA3 on the odd; dW2: 128 of the w dY columns)
+                        const int ya = (MODE == kDW13 ? un.poff : un.off) + kb * BK;
+                        const int yb = (MODE == kDW13 ? un.off : un.poff) + kb * BK;
+                        ptx::tma_load_2d_pair(sA, &tmA, fullc, row0, ya);
+                        ptx::tma_load_2d_pair(sA + kBBox, &tmA, fullc, row0 + 64, ya);
+                        const CUtensorMap *mb =
+                            MODE == kDW13 ? (leader ? &tmB0 : &tmB1) : &tmB0;
+                        const int x0 = MODE == kDW13 ? nb * 128 : nb * BN + (int)rank * 128;
+                        ptx::tma_load_2d_pair(sB, mb, fullc, x0, yb);
+                        ptx::tma_load_2d_pair(sB + kBBox, mb, fullc, x0 + 64, yb);
+                        continue;
+                    }
                     if constexpr (MODE == kDX) {
                         // A: this CTA's 128 rows of dA1 (first n/64 k-blocks) or dA3;
                         // B: its 128 of the tile's 256 output columns, W1[e] or W3[e]
@@ -1535,7 +1550,10 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     a.MT = d / BM;
     a.wout_rows = d;
     a.err = err;
-    e = launch_ew<kDW13, false, 4>(tx, t1, t3, to1, tx, to3, a, E * a.MT * a.NB, s);
+    // CTA pairs (256 output rows a unit) where the forward uses them
+    const bool pair13 = use_pair(R, E) && a.MT % 2 == 0;
+    e = pair13 ? launch_ew<kDW13, true, 4>(tx, t1, t3, to1, tx, to3, a, E * (a.MT / 2) * a.NB, s)
+               : launch_ew<kDW13, false, 4>(tx, t1, t3, to1, tx, to3, a, E * a.MT * a.NB, s);
     if (e != cudaSuccess) return e;
     // dW2 = H^T (w dY)g: H rows against padded, w-scaled gathered dY rows
     e = launch_gather_padded(dY, perm_token, T, offsets, E, d, topk_w, perm_slot, R, cap, poff, pad,
@@ -1553,7 +1571,9 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     b.MT = n / BM;
     b.wout_rows = n;
     b.err = err;
-    return launch_ew<kDW2, false, 4>(th, ty, ty, to2, th, to2, b, E * b.MT * b.NB, s);
+    const bool pair2 = use_pair(R, E) && b.MT % 2 == 0;
+    return pair2 ? launch_ew<kDW2, true, 4>(th, ty, ty, to2, th, to2, b, E * (b.MT / 2) * b.NB, s)
+                 : launch_ew<kDW2, false, 4>(th, ty, ty, to2, th, to2, b, E * b.MT * b.NB, s);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {
