@@ -466,7 +466,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!GATHER) ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
         if (GATE || FUSED || MODE == kDX || MODE == kDW13) ptx::prefetch_tensormap(&tmB1);
-        if (MODE == kDX) ptx::prefetch_tensormap(&tmB2);
+        if (MODE == kDX || MODE == kGateUpPre) ptx::prefetch_tensormap(&tmB2);
+        if (MODE == kGateUpPre) ptx::prefetch_tensormap(&tmOut2);
         ptx::prefetch_tensormap(&tmOut);
         if (MODE == kDH || MODE == kDW13) ptx::prefetch_tensormap(&tmOut2);
         if (FUSED) {
@@ -1104,9 +1105,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     emit(packed, dst + c * 32, nb * 128 + c * 32, omap);
                     if constexpr (MODE == kGateUpPre) {
-                        // the pre-activations as they are (fp32): A1 (gate), A3 (up);
-                        // each lane writes its row's 128 bytes of the chunk
-                        if (valid) {
+                        // the pre-activations as they are (fp32): A1 (gate), A3 (up).
+                        // Whole 32-row warps: four 16-column TMA boxes through the
+                        // staging buffers (maps in tmB2, tmOut2); else each valid lane
+                        // writes its row's 128 bytes of the chunk
+                        if (whole) {
+                            uint32_t lo[16], hi[16];
+                            const int x0 = nb * 128 + c * 32, y0 = row0 + q * 32;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                lo[i] = g[i];
+                                hi[i] = g[16 + i];
+                            }
+                            store_box(lo, x0, y0, &tmB2);
+                            store_box(hi, x0 + 16, y0, &tmB2);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                lo[i] = v[i];
+                                hi[i] = v[16 + i];
+                            }
+                            store_box(lo, x0, y0, &tmOut2);
+                            store_box(hi, x0 + 16, y0, &tmOut2);
+                        } else if (valid) {
                             const int64_t off = p * args.out_ld + nb * 128 + c * 32;
                             float4 *d1 = reinterpret_cast<float4 *>(args.pre_out1 + off);
                             float4 *d3 = reinterpret_cast<float4 *>(args.pre_out3 + off);
@@ -1403,10 +1423,13 @@ cudaError_t launch_gemm_gate_up_train(const __nv_bfloat16 *X, const int32_t *per
                                       const int32_t *offsets, int R, int d, int E, int n,
                                       __nv_bfloat16 *H, float *A1, float *A3,
                                       __nv_bfloat16 *xg, uint32_t *err, cudaStream_t s) {
-    CUtensorMap ta, tb0, tb1, th;
+    // (A1, A3: fp32 boxes of 16 columns x 32 rows, one epilogue warp's rows)
+    CUtensorMap ta, tb0, tb1, th, tp1, tp3;
     if (!make_map(&tb0, W1, n, (uint64_t)E * d, 64, BK) ||
         !make_map(&tb1, W3, n, (uint64_t)E * d, 64, BK) ||
-        !make_map(&th, H, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_map(&th, H, n, R, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_f32(&tp1, A1, n, R, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_f32(&tp3, A3, n, R, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     GemmArgs args{};
     args.X = X;
@@ -1427,10 +1450,10 @@ cudaError_t launch_gemm_gate_up_train(const __nv_bfloat16 *X, const int32_t *per
         cudaError_t e = launch_gather_rows(X, perm_token, T, R, offsets + E, d, xg, err, s);
         if (e != cudaSuccess) return e;
         if (!make_map(&ta, xg, d, R, 64, BM)) return cudaErrorInvalidValue;
-        return launch_ew_auto<kGateUpPre, true>(ta, tb0, tb1, th, tb0, th, args,
+        return launch_ew_auto<kGateUpPre, true>(ta, tb0, tb1, th, tp1, tp3, args,
                                                 (tiles / 2 + E) * args.NB, s);
     }
-    return launch_ew_auto<kGateUpPre, false>(tb0, tb0, tb1, th, tb0, th, args, tiles * args.NB, s);
+    return launch_ew_auto<kGateUpPre, false>(tb0, tb0, tb1, th, tp1, tp3, args, tiles * args.NB, s);
 }
 
 cudaError_t launch_backward_dh(const __nv_bfloat16 *dY, const int32_t *perm_token, int T,
