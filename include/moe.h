@@ -296,12 +296,15 @@ moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf
  * i.e. the full input gradient: the experts' rows (dXg from moe_backward_dx)
  * and the router's share, added in fp32 and rounded once. logits [T,E] as
  * moe_route wrote them. dWr is summed per chunk of tokens (fp32 fma chains,
- * t ascending) and the chunks' partials in ascending order; dL Wr^T is one
+ * t ascending; for E % 128 == 0, T % 1024 == 0 and d % 256 == 0 a tensor-core
+ * GEMM over 1024-token chunks with dL split into bf16 high and low parts, fp32
+ * accumulation) and the chunks' partials in ascending order; dL Wr^T is one
  * fp32 fma chain over e ascending per element; dbias a fixed tree: all
  * deterministic. ws: at least moe_workspace_bytes(T, d, E, K, 0) bytes (a
  * workspace of the layer's shape serves); T * d floats from its gathered-rows
- * region on hold the dWr partials. Five kernels (four when T is too short to
- * split into chunks); dL Wr^T is computed inside the last, the combine. */
+ * region on hold the dWr partials (and the split dL). Five kernels (four when T
+ * is too short to split into chunks, six on the tensor-core path); dL Wr^T is
+ * computed inside the last, the combine. */
 moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,
                                  const int32_t *topk_idx, const float *dS,
                                  const int32_t *row_of_slot, int T, int d, int E, int K,

@@ -112,14 +112,16 @@ def test_backward_dh_matches_oracle_in_full(pair, monkeypatch):
     check_y(bits(s["dX"]), full["dX"], "dX")
 
 
-@pytest.mark.parametrize("T,E,K", [
-    (300, 20, 2),    # E <= 32 with a partly used 32-expert block; 10 token chunks
-    (300, 40, 3),    # E > 32: two expert blocks, dL Wr^T in its own kernel; 5 chunks
-    (300, 256, 8),   # E = 256: T too short for chunks, dWr written directly
-    (4100, 8, 2),    # 129 chunks of 32 tokens, the last one ragged
+@pytest.mark.parametrize("T,E,K,d", [
+    (300, 20, 2, 256),    # E <= 32 with a partly used 32-expert block; 10 token chunks
+    (300, 40, 3, 256),    # E > 32: two expert blocks; 5 chunks
+    (300, 256, 8, 256),   # E = 256: T too short for chunks, dWr written directly
+    (4100, 8, 2, 256),    # 129 chunks of 32 tokens, the last one ragged
+    (2048, 128, 4, 256),  # dWr on the tensor cores: 2 chunks of 1024 tokens
+    (1024, 256, 8, 768),  # the same with E = 256 (two 256-column blocks) and 6 row tiles
 ])
-def test_router_backward_matches_oracle(T, E, K):
-    d, n = 256, 256
+def test_router_backward_matches_oracle(T, E, K, d):
+    n = 256
     inp = synth.layer_inputs(T=T, d=d, E=E, n=n, device="cuda", seed=3)
     dY = _dY(T, d)
     s = _gpu_steps(inp, dY, K)

@@ -366,7 +366,8 @@ moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float
     return from_cuda(launch_backward_router(
         reinterpret_cast<const __nv_bfloat16 *>(X), Wr, logits, topk_idx, dS, row_of_slot, T, d, E,
         K, renorm, reinterpret_cast<const __nv_bfloat16 *>(dXg), dL, dWr, dbias,
-        at<float>(ws, L.xg), reinterpret_cast<__nv_bfloat16 *>(dX), as_stream(stream)));
+        at<float>(ws, L.xg), reinterpret_cast<__nv_bfloat16 *>(dX), at<uint32_t>(ws, L.err),
+        as_stream(stream)));
 }
 
 size_t moe_backward_dw_scratch_bytes(int T, int d, int E, int K) {

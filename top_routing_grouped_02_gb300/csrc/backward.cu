@@ -272,6 +272,47 @@ dwr_reduce_kernel(const float *__restrict__ P, int64_t n, int chunks, float *__r
     dWr[i] = s;
 }
 
+// Tensor-core dWr (E % 128 == 0, T % 1024 == 0): dL as bf16 high and low parts
+// side by side, dLc[t][e] = bf16(dL[t][e]) and dLc[t][E + e] = bf16(dL[t][e] -
+// high), so that x dL = x high + x low to within 2^-16 of |x dL| (x is bf16
+// already, so each product is exact in the fp32 accumulators). Block 0 also
+// writes the token chunks' offsets c * chunk for the grouped GEMM.
+__global__ void __launch_bounds__(256)
+router_split_kernel(const float *__restrict__ dL, int64_t n, int E, __nv_bfloat16 *__restrict__ dLc,
+                    int32_t *__restrict__ offsets, int nchunks, int chunk) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (blockIdx.x == 0 && (int)threadIdx.x <= nchunks) offsets[threadIdx.x] = threadIdx.x * chunk;
+    if (i >= n) return;
+    const int64_t t = i / E;
+    const int e = (int)(i - t * E);
+    const float v = __ldg(dL + i);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi)));
+    dLc[t * 2 * E + e] = hi;
+    dLc[t * 2 * E + E + e] = lo;
+}
+
+// dWr[j][e] = sum over chunks c ascending of (P[c][j][e] + P[c][j][E + e]): the
+// token chunks' partial products with the high and low parts, fixed order.
+__global__ void __launch_bounds__(256)
+dwr_reduce_halves_kernel(const float *__restrict__ P, int d, int E, int chunks,
+                         float *__restrict__ dWr) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= (int64_t)d * E) return;
+    const int64_t j = i / E;
+    const int e = (int)(i - j * E);
+    float s = 0.f;
+    for (int c = 0; c < chunks; ++c) {
+        const float *row = P + ((int64_t)c * d + j) * 2 * E;
+        s = __fadd_rn(s, __fadd_rn(__ldg(row + e), __ldg(row + E + e)));
+    }
+    dWr[i] = s;
+}
+
 // The router's share of dX computed in the final combine, for any E. Block: 8
 // warps of 8 tokens (64 tokens) x 256 columns (8 per lane). Experts go in
 // chunks of 32: Wr's 256 x 32 slice staged transposed in shared memory and
@@ -488,6 +529,22 @@ cudaError_t launch_dwr_part(const __nv_bfloat16 *X, const float *dL, int T, int 
                     dim3((d + C::JB - 1) / C::JB, chunks, (E + EB - 1) / EB), dim3(kPThreads),
                     C::SMEM, s, X, dL, T, d, E, TC, part);
 }
+cudaError_t launch_combine_router(const __nv_bfloat16 *dXg, const int32_t *row_of_slot,
+                                  const float *dL, const float *Wr, int T, int K, int d, int E,
+                                  int64_t R, __nv_bfloat16 *dX, cudaStream_t s) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(combine_router_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    return launch_k(combine_router_kernel,
+                    dim3((unsigned)((T + kFTok - 1) / kFTok), (d + kFCols - 1) / kFCols),
+                    dim3(256), kFSmem, s, dXg, row_of_slot, dL, Wr, T, K, d, E, R, dX);
+}
 }  // namespace
 
 cudaError_t launch_gather_padded(const __nv_bfloat16 *src, const int32_t *perm_token, int T,
@@ -508,7 +565,8 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                                    const int32_t *idx, const float *dS,
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
-                                   float *dbias, float *scratch, __nv_bfloat16 *dX, cudaStream_t s) {
+                                   float *dbias, float *scratch, __nv_bfloat16 *dX, uint32_t *err,
+                                   cudaStream_t s) {
     const int64_t R = (int64_t)T * K;
     const unsigned tb = (unsigned)((T + kDlThreads / 32 - 1) / (kDlThreads / 32));
     auto dl = E <= 32    ? router_dl_kernel<1>
@@ -521,8 +579,33 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
     e = launch_k(col_sum_kernel, dim3(E), dim3(kColThreads), 0, s, static_cast<const float *>(dL), T,
                  E, dbias);
     if (e != cudaSuccess) return e;
-    // dWr: chunks of TC tokens, their partials in the scratch region (T * d
-    // floats; TC grows until the chunks' d x E partials fit), then the reduce
+    // dWr on the tensor cores where the shape allows: chunks of 1024 tokens as the
+    // grouped GEMM's groups (the weight-gradient mode), partials [chunk][d][2E]
+    // fp32, then dL's split [T][2E] bf16 and the chunk offsets, all in the scratch
+    const int tc_chunk = 1024;
+    const int tc_chunks = T / tc_chunk;
+    const size_t tc_part = (size_t)tc_chunks * d * 2 * E * 4;
+    const size_t tc_split = (size_t)T * 2 * E * 2;
+    if (E % 128 == 0 && T % tc_chunk == 0 && d % 256 == 0 && tc_chunks >= 1 && tc_chunks <= 255 &&
+        tc_part + tc_split + 4 * (size_t)(tc_chunks + 1) <= (size_t)T * d * 4) {
+        float *P = scratch;
+        __nv_bfloat16 *dLc = reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<char *>(scratch) + tc_part);
+        int32_t *coff = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dLc) + tc_split);
+        const int64_t n = (int64_t)T * E;
+        e = launch_k(router_split_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                     static_cast<const float *>(dL), n, E, dLc, coff, tc_chunks, tc_chunk);
+        if (e != cudaSuccess) return e;
+        e = launch_router_dwr_tc(X, dLc, coff, T, d, E, tc_chunks, P, err, s);
+        if (e != cudaSuccess) return e;
+        const int64_t m = (int64_t)d * E;
+        e = launch_k(dwr_reduce_halves_kernel, dim3((unsigned)((m + 255) / 256)), dim3(256), 0, s,
+                     static_cast<const float *>(P), d, E, tc_chunks, dWr);
+        if (e != cudaSuccess) return e;
+        return launch_combine_router(dXg, row_of_slot, dL, Wr, T, K, d, E, R, dX, s);
+    }
+    // dWr on the FP32 pipe: chunks of TC tokens, their partials in the scratch
+    // region (T * d floats; TC grows until the chunks' d x E partials fit), then
+    // the reduce
     int64_t TC = 32;
     while (TC < T && (((T + TC - 1) / TC) * E > T || (T + TC - 1) / TC > 65535)) TC *= 2;
     TC = std::min<int64_t>(TC, T);
@@ -542,19 +625,7 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
         if (e != cudaSuccess) return e;
     }
     // the router's share dL Wr^T and the final combine, in one kernel
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(combine_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kFSmem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    return launch_k(combine_router_kernel,
-                    dim3((unsigned)((T + kFTok - 1) / kFTok), (d + kFCols - 1) / kFCols),
-                    dim3(256), kFSmem, s, dXg, row_of_slot, static_cast<const float *>(dL), Wr, T,
-                    K, d, E, R, dX);
+    return launch_combine_router(dXg, row_of_slot, dL, Wr, T, K, d, E, R, dX, s);
 }
 
 }  // namespace moe

@@ -139,7 +139,14 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                                    const int32_t *idx, const float *dS,
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
-                                   float *dbias, float *scratch, __nv_bfloat16 *dX, cudaStream_t s);
+                                   float *dbias, float *scratch, __nv_bfloat16 *dX, uint32_t *err,
+                                   cudaStream_t s);
+// dWr partials on the tensor cores: P[c][j][col] = sum over the tokens t of chunk c
+// of X[t][j] dLc[t][col] (fp32 [nchunks*d, 2E]), chunk c = tokens offsets[c] ..
+// offsets[c+1] - 1 (multiples of 64); dLc [T, 2E] bf16. E % 128 == 0, d % 128 == 0.
+cudaError_t launch_router_dwr_tc(const __nv_bfloat16 *X, const __nv_bfloat16 *dLc,
+                                 const int32_t *offsets, int T, int d, int E, int nchunks,
+                                 float *P, uint32_t *err, cudaStream_t s);
 // Rows of src gathered into the padded grouped layout of the weight gradients
 // (each expert's rows from a 64-row boundary, zeros after them), optionally
 // scaled by w[perm_slot[p]]; poff [E+1] receives (or, offsets_done, holds) the

@@ -1599,6 +1599,27 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
                  : launch_ew<kDW2, false, 4>(th, ty, ty, to2, th, to2, b, E * b.MT * b.NB, s);
 }
 
+cudaError_t launch_router_dwr_tc(const __nv_bfloat16 *X, const __nv_bfloat16 *dLc,
+                                 const int32_t *offsets, int T, int d, int E, int nchunks,
+                                 float *P, uint32_t *err, cudaStream_t s) {
+    // the weight-gradient GEMM with the token chunks as its groups: A = X rows
+    // (MN-major over d), B = dLc rows (2E columns), outputs [chunk][d][2E] fp32
+    CUtensorMap ta, tb, to;
+    if (!make_map(&ta, X, d, T, 64, 64) || !make_map(&tb, dLc, 2 * (uint64_t)E, T, 64, 64) ||
+        !make_map_f32(&to, P, 2 * (uint64_t)E, (uint64_t)nchunks * d, 16, 32,
+                      CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    GemmArgs b{};
+    b.offsets = offsets;
+    b.E = nchunks;
+    b.R = T;
+    b.NB = 2 * E / BN;
+    b.MT = d / BM;
+    b.wout_rows = d;
+    b.err = err;
+    return launch_ew<kDW2, false, 4>(ta, tb, tb, to, ta, to, b, nchunks * b.MT * b.NB, s);
+}
+
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {
     wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err);
     return cudaGetLastError();
