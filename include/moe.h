@@ -303,8 +303,11 @@ moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf
  * deterministic. ws: at least moe_workspace_bytes(T, d, E, K, 0) bytes (a
  * workspace of the layer's shape serves); T * d floats from its gathered-rows
  * region on hold the dWr partials (and the split dL). Five kernels (four when T
- * is too short to split into chunks, six on the tensor-core path); dL Wr^T is
- * computed inside the last, the combine. */
+ * is too short to split into chunks); dL Wr^T is computed inside the last, the
+ * combine. On the tensor-core path (E % 128 == 0, T % 1024 == 0, d % 256 == 0)
+ * six kernels, or, with K >= 2, nine: dL Wr^T too is a tensor-core GEMM (Wr
+ * split like dL; fp32 out, in the first T * d floats of the gathered-rows
+ * region, the split operands after it), added by the combine. */
 moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,
                                  const int32_t *topk_idx, const float *dS,
                                  const int32_t *row_of_slot, int T, int d, int E, int K,

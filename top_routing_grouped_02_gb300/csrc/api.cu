@@ -363,11 +363,16 @@ moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float
     const size_t need = L.xg + (size_t)T * d * sizeof(float);
     if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((s = check_arch()) != MOE_OK) return s;
+    // the region after the gathered rows serves as a second scratch (the
+    // tensor-core path's split operands) when the first one, T * d floats, ends
+    // before it (K >= 2)
+    const bool s2 = ws_bytes > L.z && L.z >= need;
     return from_cuda(launch_backward_router(
         reinterpret_cast<const __nv_bfloat16 *>(X), Wr, logits, topk_idx, dS, row_of_slot, T, d, E,
         K, renorm, reinterpret_cast<const __nv_bfloat16 *>(dXg), dL, dWr, dbias,
-        at<float>(ws, L.xg), reinterpret_cast<__nv_bfloat16 *>(dX), at<uint32_t>(ws, L.err),
-        as_stream(stream)));
+        at<float>(ws, L.xg), s2 ? at<char>(ws, L.z) : nullptr, s2 ? ws_bytes - L.z : 0,
+        reinterpret_cast<__nv_bfloat16 *>(dX),
+        at<uint32_t>(ws, L.err), as_stream(stream)));
 }
 
 size_t moe_backward_dw_scratch_bytes(int T, int d, int E, int K) {

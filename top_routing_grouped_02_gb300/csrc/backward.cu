@@ -294,6 +294,82 @@ router_split_kernel(const float *__restrict__ dL, int64_t n, int E, __nv_bfloat1
     dLc[t * 2 * E + E + e] = lo;
 }
 
+// Wr split the same way for the router's share on the tensor cores:
+// WrA[j] = [high | high], WrB[j] = [low | low] ([d, 2E] bf16), so that the
+// 4E-long reduction over [dLh | dLl] gives (dLh + dLl)(high + low). Block 0
+// also writes the one-group offsets {0, T}.
+__global__ void __launch_bounds__(256)
+wr_split_kernel(const float *__restrict__ Wr, int d, int E, int T, __nv_bfloat16 *__restrict__ WrA,
+                __nv_bfloat16 *__restrict__ WrB, int32_t *__restrict__ off2) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (blockIdx.x == 0 && threadIdx.x < 2) off2[threadIdx.x] = threadIdx.x == 0 ? 0 : T;
+    if (i >= (int64_t)d * E) return;
+    const int64_t j = i / E;
+    const int e = (int)(i - j * E);
+    const float v = __ldg(Wr + i);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi)));
+    WrA[j * 2 * E + e] = hi;
+    WrA[j * 2 * E + E + e] = hi;
+    WrB[j * 2 * E + e] = lo;
+    WrB[j * 2 * E + E + e] = lo;
+}
+
+// dX[t, :] = bf16( sum over k ascending of dXg[row_of_slot[t*K+k], :] (fp32) +
+// dXr[t, :] ), one rounding: a warp per token, 8 columns per lane and step.
+constexpr int kCThreads = 256;
+__global__ void __launch_bounds__(kCThreads)
+combine_add_kernel(const __nv_bfloat16 *__restrict__ dXg, const int32_t *__restrict__ row_of_slot,
+                   const float *__restrict__ dXr, int T, int K, int d, int64_t R,
+                   __nv_bfloat16 *__restrict__ dX) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t t = (int64_t)blockIdx.x * (kCThreads / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    int rows[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        rows[k] = -1;
+        if (k < K) {
+            const int r = __ldg(row_of_slot + t * K + k);
+            rows[k] = (r >= 0 && r < R) ? r : -1;
+        }
+    }
+    for (int c = lane; c < d / 8; c += 32) {
+        uint4 raw[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k)
+            raw[k] = rows[k] >= 0
+                         ? __ldg(reinterpret_cast<const uint4 *>(dXg + (int64_t)rows[k] * d) + c)
+                         : make_uint4(0, 0, 0, 0);
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(dXr + t * d) + 2 * c);
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(dXr + t * d) + 2 * c + 1);
+        float acc[8] = {};
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (rows[k] < 0) continue;
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw[k]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                acc[2 * u] = __fadd_rn(acc[2 * u], f.x);
+                acc[2 * u + 1] = __fadd_rn(acc[2 * u + 1], f.y);
+            }
+        }
+        const float add[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint4 out;
+        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            o2[u] = __floats2bfloat162_rn(__fadd_rn(acc[2 * u], add[2 * u]),
+                                          __fadd_rn(acc[2 * u + 1], add[2 * u + 1]));
+        reinterpret_cast<uint4 *>(dX + t * d)[c] = out;
+    }
+}
+
 // dWr[j][e] = sum over chunks c ascending of (P[c][j][e] + P[c][j][E + e]): the
 // token chunks' partial products with the high and low parts, fixed order.
 __global__ void __launch_bounds__(256)
@@ -565,7 +641,8 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                                    const int32_t *idx, const float *dS,
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
-                                   float *dbias, float *scratch, __nv_bfloat16 *dX, uint32_t *err,
+                                   float *dbias, float *scratch, char *scratch2,
+                                   size_t scratch2_bytes, __nv_bfloat16 *dX, uint32_t *err,
                                    cudaStream_t s) {
     const int64_t R = (int64_t)T * K;
     const unsigned tb = (unsigned)((T + kDlThreads / 32 - 1) / (kDlThreads / 32));
@@ -579,18 +656,26 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
     e = launch_k(col_sum_kernel, dim3(E), dim3(kColThreads), 0, s, static_cast<const float *>(dL), T,
                  E, dbias);
     if (e != cudaSuccess) return e;
-    // dWr on the tensor cores where the shape allows: chunks of 1024 tokens as the
-    // grouped GEMM's groups (the weight-gradient mode), partials [chunk][d][2E]
-    // fp32, then dL's split [T][2E] bf16 and the chunk offsets, all in the scratch
+    // On the tensor cores where the shape allows: dWr with chunks of 1024 tokens as
+    // the weight-gradient GEMM's groups (partials [chunk][d][2E] fp32, then dL's
+    // split [T][2E] bf16 and the chunk offsets); and, given the second scratch
+    // region, the router's share dXr = dL Wr^T (fp32 [T, d] in the first scratch,
+    // Wr's split and the offsets {0, T} in the second) for a combine that adds it.
     const int tc_chunk = 1024;
     const int tc_chunks = T / tc_chunk;
     const size_t tc_part = (size_t)tc_chunks * d * 2 * E * 4;
     const size_t tc_split = (size_t)T * 2 * E * 2;
-    if (E % 128 == 0 && T % tc_chunk == 0 && d % 256 == 0 && tc_chunks >= 1 && tc_chunks <= 255 &&
-        tc_part + tc_split + 4 * (size_t)(tc_chunks + 1) <= (size_t)T * d * 4) {
-        float *P = scratch;
-        __nv_bfloat16 *dLc = reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<char *>(scratch) + tc_part);
-        int32_t *coff = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dLc) + tc_split);
+    const size_t tc_off = 16 * (size_t)((tc_chunks + 1 + 3) / 4);
+    const size_t tc_wr = (size_t)d * 2 * E * 2;
+    const bool tc_shape = E % 128 == 0 && T % tc_chunk == 0 && d % 256 == 0 && tc_chunks >= 1 &&
+                          tc_chunks <= 255;
+    const bool tc_dx = tc_shape && scratch2 != nullptr &&
+                       tc_part + tc_split + tc_off + 2 * tc_wr + 16 <= scratch2_bytes;
+    if (tc_shape && (tc_dx || tc_part + tc_split + tc_off <= (size_t)T * d * 4)) {
+        char *base = tc_dx ? scratch2 : reinterpret_cast<char *>(scratch);
+        float *P = reinterpret_cast<float *>(base);
+        __nv_bfloat16 *dLc = reinterpret_cast<__nv_bfloat16 *>(base + tc_part);
+        int32_t *coff = reinterpret_cast<int32_t *>(base + tc_part + tc_split);
         const int64_t n = (int64_t)T * E;
         e = launch_k(router_split_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
                      static_cast<const float *>(dL), n, E, dLc, coff, tc_chunks, tc_chunk);
@@ -601,7 +686,19 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
         e = launch_k(dwr_reduce_halves_kernel, dim3((unsigned)((m + 255) / 256)), dim3(256), 0, s,
                      static_cast<const float *>(P), d, E, tc_chunks, dWr);
         if (e != cudaSuccess) return e;
-        return launch_combine_router(dXg, row_of_slot, dL, Wr, T, K, d, E, R, dX, s);
+        if (!tc_dx) return launch_combine_router(dXg, row_of_slot, dL, Wr, T, K, d, E, R, dX, s);
+        __nv_bfloat16 *WrA = reinterpret_cast<__nv_bfloat16 *>(base + tc_part + tc_split + tc_off);
+        __nv_bfloat16 *WrB = WrA + (size_t)d * 2 * E;
+        int32_t *off2 = reinterpret_cast<int32_t *>(WrB + (size_t)d * 2 * E);
+        e = launch_k(wr_split_kernel, dim3((unsigned)((m + 255) / 256)), dim3(256), 0, s, Wr, d, E,
+                     T, WrA, WrB, off2);
+        if (e != cudaSuccess) return e;
+        e = launch_router_dx_tc(dLc, WrA, WrB, off2, T, d, E, scratch, err, s);
+        if (e != cudaSuccess) return e;
+        return launch_k(combine_add_kernel,
+                        dim3((unsigned)((T + kCThreads / 32 - 1) / (kCThreads / 32))),
+                        dim3(kCThreads), 0, s, dXg, row_of_slot, static_cast<const float *>(scratch),
+                        T, K, d, R, dX);
     }
     // dWr on the FP32 pipe: chunks of TC tokens, their partials in the scratch
     // region (T * d floats; TC grows until the chunks' d x E partials fit), then

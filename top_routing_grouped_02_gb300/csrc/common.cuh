@@ -134,16 +134,24 @@ cudaError_t launch_backward_dx(const __nv_bfloat16 *dA1, const __nv_bfloat16 *dA
                                __nv_bfloat16 *dX, uint32_t *err, cudaStream_t s);
 // Router backward (backward.cu): dL [T, E], dbias [E], dWr [d, E] (fp32) and
 // dX [T, d] = bf16(sum_k dXg[row_of_slot[t*K+k]] + dL Wr^T), with `scratch`
-// (T * d floats) for the partial sums of dWr.
+// (T * d floats) for the partial sums of dWr and, on the tensor-core path with
+// a second scratch region (nullable), the fp32 router share dL Wr^T.
 cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, const float *L,
                                    const int32_t *idx, const float *dS,
                                    const int32_t *row_of_slot, int T, int d, int E, int K,
                                    int renorm, const __nv_bfloat16 *dXg, float *dL, float *dWr,
-                                   float *dbias, float *scratch, __nv_bfloat16 *dX, uint32_t *err,
+                                   float *dbias, float *scratch, char *scratch2,
+                                   size_t scratch2_bytes, __nv_bfloat16 *dX, uint32_t *err,
                                    cudaStream_t s);
 // dWr partials on the tensor cores: P[c][j][col] = sum over the tokens t of chunk c
 // of X[t][j] dLc[t][col] (fp32 [nchunks*d, 2E]), chunk c = tokens offsets[c] ..
 // offsets[c+1] - 1 (multiples of 64); dLc [T, 2E] bf16. E % 128 == 0, d % 128 == 0.
+// The router's share dXr [T, d] fp32 = (dLh + dLl)(Wrh + Wrl)^T on the tensor
+// cores: dLc = [dLh | dLl] [T, 2E], WrA = [Wrh | Wrh], WrB = [Wrl | Wrl] [d, 2E]
+// bf16; offsets = {0, T}. 2E % 64 == 0, d % 256 == 0.
+cudaError_t launch_router_dx_tc(const __nv_bfloat16 *dLc, const __nv_bfloat16 *WrA,
+                                const __nv_bfloat16 *WrB, const int32_t *offsets, int T, int d,
+                                int E, float *dXr, uint32_t *err, cudaStream_t s);
 cudaError_t launch_router_dwr_tc(const __nv_bfloat16 *X, const __nv_bfloat16 *dLc,
                                  const int32_t *offsets, int T, int d, int E, int nchunks,
                                  float *P, uint32_t *err, cudaStream_t s);

@@ -239,6 +239,8 @@ struct GemmArgs {
     int out2_ld;
     uint32_t *dep;
     int gap_rounds;
+    float *outf;  // kDX with f32_out: fp32 outputs [rows, out_ld] (tmOut is an fp32 map)
+    int f32_out;
     // kGateUpPre: the pre-activation outputs A1, A3 [R, n] fp32; kDH: dA3 (dA1
     // goes to out)
     float *pre_out1;
@@ -1140,6 +1142,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         }
                     }
                 }
+            } else if (MODE == kDX && args.f32_out) {
+                // fp32 outputs (the router's share dL Wr^T): 16-column TMA boxes for
+                // whole 32-row warps, else direct stores of the valid rows
+                float *dst = args.outf + p * args.out_ld + nb * BN;
+#pragma unroll 1
+                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(taddr + c * 32, v);
+                    if (whole) {
+                        uint32_t lo[16], hi[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            lo[i] = v[i];
+                            hi[i] = v[16 + i];
+                        }
+                        store_box(lo, nb * BN + c * 32, row0 + q * 32, omap);
+                        store_box(hi, nb * BN + c * 32 + 16, row0 + q * 32, omap);
+                    } else if (valid) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                    }
+                }
             } else {
                 float w = 0.f;
                 if (MODE == kDX) {
@@ -1618,6 +1645,33 @@ cudaError_t launch_router_dwr_tc(const __nv_bfloat16 *X, const __nv_bfloat16 *dL
     b.wout_rows = d;
     b.err = err;
     return launch_ew<kDW2, false, 4>(ta, tb, tb, to, ta, to, b, nchunks * b.MT * b.NB, s);
+}
+
+cudaError_t launch_router_dx_tc(const __nv_bfloat16 *dLc, const __nv_bfloat16 *WrA,
+                                const __nv_bfloat16 *WrB, const int32_t *offsets, int T, int d,
+                                int E, float *dXr, uint32_t *err, cudaStream_t s) {
+    // the dX GEMM mode over the tokens as one group: A = dLc [T, 2E] in both
+    // halves of the 4E reduction, B = WrA then WrB ([d, 2E], K-major); fp32 out
+    CUtensorMap ta, tb0, tb1, to;
+    if (!make_map(&ta, dLc, 2 * (uint64_t)E, T, 64, BM) ||
+        !make_map(&tb0, WrA, 2 * (uint64_t)E, d, 64, 64) ||
+        !make_map(&tb1, WrB, 2 * (uint64_t)E, d, 64, 64) ||
+        !make_map_f32(&to, dXr, d, T, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    GemmArgs a{};
+    a.offsets = offsets;
+    a.E = 1;
+    a.R = T;
+    a.Kdim = 4 * E;
+    a.NB = d / BN;
+    a.out_ld = d;
+    a.outf = dXr;
+    a.f32_out = 1;
+    a.err = err;
+    a.bn_rows = d;
+    a.kb_half = 2 * E / BK;
+    const int tiles = T / BM + 1;
+    return launch_ew_auto<kDX, false>(ta, tb0, tb1, to, ta, to, a, tiles * a.NB, s);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t *err, cudaStream_t s) {
