@@ -16,7 +16,7 @@
 // and over the batch: dbias = sum_t dL[t,:], dWr = X^T dL, and the router's
 // share of dX is dL Wr^T, added to the experts' share in the final combine.
 //
-// Four or five kernels, all deterministic (fixed summation orders, no atomics):
+// All deterministic (fixed summation orders, no atomics):
 //  1. dl:       one warp per token (lane l holds experts l, l+32, ...).
 //  2. dbias:    one block per expert, a fixed-shape tree over the tokens.
 //  3. dWr:      per chunk of tokens, fp32 fma chains over the chunk's tokens in
@@ -25,6 +25,11 @@
 //  4. combine:  dX[t,:] = bf16( sum over k ascending of dXg[row_of_slot[t,k],:]
 //               (fp32) + (dL Wr^T)[t,:] ), one rounding, with dL Wr^T one fma
 //               chain over e ascending per element, computed in the kernel.
+// For E % 128 == 0, T % 1024 == 0 and d % 256 == 0, steps 3 and 4 run on the
+// tensor cores instead: dL (and Wr) split into bf16 high and low parts, dWr as
+// the weight-gradient GEMM over 1024-token chunks plus a fixed-order reduce,
+// and (given a second scratch region) dL Wr^T as the dX GEMM with fp32
+// outputs, which combine_add_kernel adds to the experts' rows.
 #include <algorithm>
 
 #include <cuda_bf16.h>
