@@ -325,7 +325,9 @@ moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float
  * wait that runs out sets MOE_DEVERR_TIMEOUT). On the SonicMoE-shaped layer the
  * fused launch measured slower than the two (0.183-0.191 against 0.170 ms).
  * ws: workspace of this shape, zeroed once before first use and not shared by
- * calls that overlap on the GPU. */
+ * calls that overlap on the GPU. Takes no tile list: the GEMMs decode their
+ * work units from offsets in their own order (expert-major, groups of tiles,
+ * few-tile experts interleaved), which moe_permute's flat list cannot express. */
 moe_status_t moe_expert_mlp(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W3,
                             const moe_bf16 *W2, const float *topk_w,
                             const int32_t *perm_token, const int32_t *perm_slot,
