@@ -46,6 +46,9 @@ def _check(idx: np.ndarray, E: int):
     (1, 4, 4, 0.0),         # one token, every expert
     (33, 256, 8, 3.0),      # most experts empty
     (1000, 5, 1, 0.5),
+    (20000, 64, 4, 0.5),    # one kernel, 10 chunks a block: warps take two chunks each
+    (65536, 32, 2, 0.0),    # one kernel at its limit: 64 blocks of 32 chunks
+    (65537, 32, 2, 0.0),    # one token more: the three kernels
     (70000, 16, 2, 0.0),    # many chunks (> 2048)
 ])
 def test_permute_matches_oracle(T, E, K, skew):
