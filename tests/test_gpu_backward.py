@@ -118,6 +118,7 @@ def test_backward_dh_matches_oracle_in_full(pair, monkeypatch):
     (300, 256, 8, 256),   # E = 256: T too short for chunks, dWr written directly
     (4100, 8, 2, 256),    # 129 chunks of 32 tokens, the last one ragged
     (2048, 128, 4, 256),  # dWr on the tensor cores: 2 chunks of 1024 tokens
+    (2048, 128, 1, 256),  # the same with K = 1: no second scratch, dL Wr^T in the combine
     (1024, 256, 8, 768),  # the same with E = 256 (two 256-column blocks) and 6 row tiles
 ])
 def test_router_backward_matches_oracle(T, E, K, d):
