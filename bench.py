@@ -15,7 +15,8 @@ Prints ONE JSON line on rank 0:
   roofline    the dominant kernel (gate/up GEMM) against the measured bf16 peak; its
               duration comes from a second region of K forwards right after the
               timed one, with an event between every two stages
-  gpu_launches  kernels per step (8, or 9 with the CTA-pair row gather) x K
+  gpu_launches  kernels per step x K, as the library counts them (moe_forward_launches:
+              6 on the Mixtral-shaped layer with its CTA-pair row gather, 5 on the tiny one)
   cpu_baseline  the CPU oracle on a bounded token sample (rank 0, N=1 only)
   clocks      nvidia-smi SM clocks / throttle reasons sampled during the timed region
   extra       tokens/s, per-stage times (from the second region), router and combine
