@@ -40,7 +40,7 @@ def test_route_logits_router_only_workload(T, renorm):
     _check_routing(idx, w, counts, idx_r, w_r, synth.ROUTER_E)
 
 
-@pytest.mark.parametrize("T,E,K", [(2049, 8, 2), (70000, 8, 2), (5000, 16, 4), (3001, 5, 3),
+@pytest.mark.parametrize("T,E,K", [(2049, 8, 2), (70000, 8, 2), (400000, 8, 2), (5000, 16, 4), (3001, 5, 3),
                                    (1 << 20, 8, 2)])
 @pytest.mark.parametrize("renorm", [True, False])
 def test_route_logits_many_blocks_thread_per_token(T, E, K, renorm):

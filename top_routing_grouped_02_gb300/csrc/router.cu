@@ -130,8 +130,8 @@ struct RouteCfg {
 // counts the choices in the shared histogram.
 template <int EP>
 __device__ __forceinline__ void select_token(const float (&v)[EP], int E, int K, int renorm,
-                                             int64_t t, int32_t *__restrict__ idx_out,
-                                             float *__restrict__ w_out, int *hist) {
+                                                 int64_t t, int32_t *__restrict__ idx_out,
+                                                 float *__restrict__ w_out, int *hist) {
     float m = v[0];
 #pragma unroll
     for (int e = 1; e < EP; ++e)
@@ -833,10 +833,11 @@ select_thread_kernel(const float *__restrict__ logits, int T, int E, int K, int 
     __shared__ int hist[EP];
     for (int e = threadIdx.x; e < EP; e += blockDim.x) hist[e] = 0;
     __syncthreads();
+    // multi-block: a grid-stride loop over a grid of a few blocks per SM, so that
+    // the blocks' histograms reach the E global counters in few atomics
     const int64_t t0 = SINGLE ? threadIdx.x : (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t tstep = SINGLE ? blockDim.x : T;  // multi-block: one token per thread
-    for (int64_t t = t0; t < T; t += tstep) {
-        float v[EP];
+    const int64_t tstep = SINGLE ? blockDim.x : (int64_t)gridDim.x * blockDim.x;
+    auto load = [&](int64_t t, float (&v)[EP]) {
         if constexpr (VEC) {
             const float4 *src = reinterpret_cast<const float4 *>(logits + t * EP);
 #pragma unroll
@@ -851,6 +852,10 @@ select_thread_kernel(const float *__restrict__ logits, int T, int E, int K, int 
 #pragma unroll
             for (int e = 0; e < EP; ++e) v[e] = (e < E) ? __ldg(logits + t * E + e) : -INFINITY;
         }
+    };
+    for (int64_t t = t0; t < T; t += tstep) {
+        float v[EP];
+        load(t, v);
         select_token<EP>(v, E, K, renorm, t, idx_out, w_out, hist);
     }
     __syncthreads();
@@ -886,7 +891,14 @@ cudaError_t launch_select(const float *logits, int T, int E, int K, int renorm, 
                                   : select_thread_kernel<8, false, false>)
                            : (vec ? select_thread_kernel<16, false, true>
                                   : select_thread_kernel<16, false, false>);
-        const unsigned blocks = (unsigned)((T + kSelThreadBlock - 1) / kSelThreadBlock);
+        // as many blocks as are resident at once
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSelThreadBlock, 0) !=
+                cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        const int64_t need = (T + kSelThreadBlock - 1) / kSelThreadBlock;
+        const unsigned blocks =
+            (unsigned)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)per_sm * sm_count()));
         return launch_k(kern, dim3(blocks), dim3(kSelThreadBlock), 0, s, logits, T, E, K, renorm,
                         idx, w, counts);
     }
