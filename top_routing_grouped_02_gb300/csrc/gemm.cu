@@ -259,6 +259,9 @@ struct GemmArgs {
     int wout_rows;
     float *dspart;
     int ds_ld;
+    // nonzero: the output's TMA stores carry an L2 evict-first hint (outputs no
+    // later kernel reads soon, such as the weight gradients)
+    int out_evict_first;
 };
 
 // Counter words of the fused kernel: the launch's epoch in the high 24 bits, the
@@ -998,7 +1001,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::tma_store_2d(map, buf, x, y);
+                    if (args.out_evict_first)
+                        ptx::tma_store_2d_hint(map, buf, x, y, ptx::policy_evict_first());
+                    else
+                        ptx::tma_store_2d(map, buf, x, y);
                     ptx::bulk_commit_group();
                 }
                 ++epi_groups;
@@ -1600,6 +1606,7 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     a.MT = d / BM;
     a.wout_rows = d;
     a.err = err;
+    a.out_evict_first = 1;  // 4 d n E bytes that nothing reads back here
     // CTA pairs (256 output rows a unit) where the forward uses them
     const bool pair13 = use_pair(R, E) && a.MT % 2 == 0;
     e = pair13 ? launch_ew<kDW13, true, 4>(tx, t1, t3, to1, tx, to3, a, E * (a.MT / 2) * a.NB, s)
@@ -1621,6 +1628,7 @@ cudaError_t launch_backward_dw(const __nv_bfloat16 *X, const __nv_bfloat16 *dY,
     b.MT = n / BM;
     b.wout_rows = n;
     b.err = err;
+    b.out_evict_first = 1;
     const bool pair2 = use_pair(R, E) && b.MT % 2 == 0;
     return pair2 ? launch_ew<kDW2, true, 4>(th, ty, ty, to2, th, to2, b, E * (b.MT / 2) * b.NB, s)
                  : launch_ew<kDW2, false, 4>(th, ty, ty, to2, th, to2, b, E * b.MT * b.NB, s);
