@@ -299,13 +299,15 @@ moe_status_t moe_backward_dw(const moe_bf16 *X, const moe_bf16 *dY, const moe_bf
  * t ascending; for E % 128 == 0, T % 1024 == 0 and d % 256 == 0 a tensor-core
  * GEMM over 1024-token chunks with dL split into bf16 high and low parts, fp32
  * accumulation) and the chunks' partials in ascending order; dL Wr^T is one
- * fp32 fma chain over e ascending per element; dbias a fixed tree: all
+ * fp32 fma chain over e ascending per element; dbias column sums over chunks
+ * of about 128 tokens (t ascending), then the chunks in ascending order: all
  * deterministic. ws: at least moe_workspace_bytes(T, d, E, K, 0) bytes (a
  * workspace of the layer's shape serves); T * d floats from its gathered-rows
- * region on hold the dWr partials (and the split dL). Five kernels (four when T
- * is too short to split into chunks); dL Wr^T is computed inside the last, the
+ * region on hold the dbias and dWr partials (and the split dL), and one of its
+ * control words the column sums' ticket. Five kernels (four when T is too
+ * short to split into chunks); dL Wr^T is computed inside the last, the
  * combine. On the tensor-core path (E % 128 == 0, T % 1024 == 0, d % 256 == 0)
- * six kernels, or, with K >= 2, nine: dL Wr^T too is a tensor-core GEMM (Wr
+ * also five, or, with K >= 2, seven: dL Wr^T too is a tensor-core GEMM (Wr
  * split like dL; fp32 out, in the first T * d floats of the gathered-rows
  * region, the split operands after it), added by the combine. */
 moe_status_t moe_backward_router(const moe_bf16 *X, const float *Wr, const float *logits,

@@ -17,8 +17,10 @@
 // share of dX is dL Wr^T, added to the experts' share in the final combine.
 //
 // All deterministic (fixed summation orders, no atomics):
-//  1. dl:       one warp per token (lane l holds experts l, l+32, ...).
-//  2. dbias:    one block per expert, a fixed-shape tree over the tokens.
+//  1. dl:       one warp per token (lane l holds experts l, l+32, ...); on the
+//               tensor-core path it also writes dL's bf16 split.
+//  2. dbias:    column sums per chunk of tokens (t ascending, coalesced rows),
+//               then the chunks in ascending order by the last block.
 //  3. dWr:      per chunk of tokens, fp32 fma chains over the chunk's tokens in
 //               ascending order; then the chunks' partials added in ascending
 //               order (no second kernel when a single chunk covers T).
@@ -43,14 +45,23 @@ namespace {
 
 constexpr int kDlThreads = 256;
 
+// Also zeroes the column sums' ticket and, given dLc, writes dL's bf16 high and
+// low parts beside it (dLc[t][e] = bf16(dL), dLc[t][E + e] = bf16(dL - high))
+// and the token chunks' offsets c * chunk (c <= nchunks) for the tensor-core dWr.
 template <int NPL>
 __global__ void __launch_bounds__(kDlThreads)
 router_dl_kernel(const float *__restrict__ L, const int32_t *__restrict__ idx,
                  const float *__restrict__ dS, const int32_t *__restrict__ row_of_slot, int T,
-                 int E, int K, int renorm, int64_t R, float *__restrict__ dL) {
+                 int E, int K, int renorm, int64_t R, float *__restrict__ dL,
+                 uint32_t *__restrict__ ticket, __nv_bfloat16 *__restrict__ dLc,
+                 int32_t *__restrict__ coff, int nchunks, int chunk) {
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) *ticket = 0u;
+        if (dLc != nullptr && (int)threadIdx.x <= nchunks) coff[threadIdx.x] = threadIdx.x * chunk;
+    }
     const int64_t t = (int64_t)blockIdx.x * (kDlThreads / 32) + warp;
     if (t >= T) return;
     const float *lt = L + t * E;
@@ -114,28 +125,61 @@ router_dl_kernel(const float *__restrict__ L, const int32_t *__restrict__ idx,
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) out[e] = p[i] * (g[i] - mean);
+        if (e < E) {
+            const float v = p[i] * (g[i] - mean);
+            out[e] = v;
+            if (dLc != nullptr) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                dLc[t * 2 * E + e] = hi;
+                dLc[t * 2 * E + E + e] = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi)));
+            }
+        }
     }
 }
 
-// dbias[e] = sum over t of dL[t, e]: thread i adds tokens i, i + 256, ...
-// (ascending), then a fixed tree over the block's threads.
+// dbias[e] = sum over t of dL[t, e] in a fixed order. Block (g, c) takes
+// columns 32g..32g+31 of token chunk c: warp w adds the chunk's tokens w, w + 8,
+// ... in ascending order (a warp reads 32 neighbouring columns of a row at once),
+// then the 8 warps are added in order into part[c][e]. With one chunk that is
+// dbias itself; otherwise the last block to finish (a ticket, zeroed by the
+// kernel before this one) adds the chunks in ascending c. Either way the
+// result does not depend on which block finishes when.
 constexpr int kColThreads = 256;
 __global__ void __launch_bounds__(kColThreads)
-col_sum_kernel(const float *__restrict__ dL, int T, int E, float *__restrict__ dbias) {
+col_sum_kernel(const float *__restrict__ dL, int T, int E, int tc, float *__restrict__ part,
+               uint32_t *__restrict__ ticket, float *__restrict__ dbias) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float part[kColThreads];
-    const int e = blockIdx.x;
+    __shared__ float ws[kColThreads / 32][32];
+    __shared__ bool last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 32 + lane;
+    const int64_t t0 = (int64_t)blockIdx.y * tc, t1 = std::min<int64_t>(T, t0 + tc);
     float s = 0.f;
-    for (int64_t t = threadIdx.x; t < T; t += kColThreads) s += __ldg(dL + t * E + e);
-    part[threadIdx.x] = s;
+    if (e < E)
+        for (int64_t t = t0 + warp; t < t1; t += kColThreads / 32) s += __ldg(dL + t * E + e);
+    ws[warp][lane] = s;
     __syncthreads();
-    for (int w = kColThreads / 2; w > 0; w >>= 1) {
-        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-        __syncthreads();
+    if (warp == 0 && e < E) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kColThreads / 32; ++w) v += ws[w][lane];
+        if (gridDim.y == 1) dbias[e] = v;
+        else part[(int64_t)blockIdx.y * E + e] = v;
     }
-    if (threadIdx.x == 0) dbias[e] = part[0];
+    if (gridDim.y == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x * gridDim.y - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int ee = threadIdx.x; ee < E; ee += kColThreads) {
+        float v = 0.f;
+        for (int c = 0; c < (int)gridDim.y; ++c) v += __ldcg(part + (int64_t)c * E + ee);
+        dbias[ee] = v;
+    }
+    if (threadIdx.x == 0) *ticket = 0u;
 }
 
 // dWr[j, e] = sum over t of x[t, j] dL[t, e], in two fixed orders: chunk c of
@@ -275,28 +319,6 @@ dwr_reduce_kernel(const float *__restrict__ P, int64_t n, int chunks, float *__r
     float s = 0.f;
     for (int c = 0; c < chunks; ++c) s = __fadd_rn(s, __ldg(P + c * n + i));
     dWr[i] = s;
-}
-
-// Tensor-core dWr (E % 128 == 0, T % 1024 == 0): dL as bf16 high and low parts
-// side by side, dLc[t][e] = bf16(dL[t][e]) and dLc[t][E + e] = bf16(dL[t][e] -
-// high), so that x dL = x high + x low to within 2^-16 of |x dL| (x is bf16
-// already, so each product is exact in the fp32 accumulators). Block 0 also
-// writes the token chunks' offsets c * chunk for the grouped GEMM.
-__global__ void __launch_bounds__(256)
-router_split_kernel(const float *__restrict__ dL, int64_t n, int E, __nv_bfloat16 *__restrict__ dLc,
-                    int32_t *__restrict__ offsets, int nchunks, int chunk) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
-    if (blockIdx.x == 0 && (int)threadIdx.x <= nchunks) offsets[threadIdx.x] = threadIdx.x * chunk;
-    if (i >= n) return;
-    const int64_t t = i / E;
-    const int e = (int)(i - t * E);
-    const float v = __ldg(dL + i);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi)));
-    dLc[t * 2 * E + e] = hi;
-    dLc[t * 2 * E + E + e] = lo;
 }
 
 // Wr split the same way for the router's share on the tensor cores:
@@ -650,22 +672,12 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                                    size_t scratch2_bytes, __nv_bfloat16 *dX, uint32_t *err,
                                    cudaStream_t s) {
     const int64_t R = (int64_t)T * K;
-    const unsigned tb = (unsigned)((T + kDlThreads / 32 - 1) / (kDlThreads / 32));
-    auto dl = E <= 32    ? router_dl_kernel<1>
-              : E <= 64  ? router_dl_kernel<2>
-              : E <= 128 ? router_dl_kernel<4>
-                         : router_dl_kernel<8>;
-    cudaError_t e = launch_k(dl, dim3(tb), dim3(kDlThreads), 0, s, L, idx, dS, row_of_slot, T, E, K,
-                             renorm, R, dL);
-    if (e != cudaSuccess) return e;
-    e = launch_k(col_sum_kernel, dim3(E), dim3(kColThreads), 0, s, static_cast<const float *>(dL), T,
-                 E, dbias);
-    if (e != cudaSuccess) return e;
     // On the tensor cores where the shape allows: dWr with chunks of 1024 tokens as
     // the weight-gradient GEMM's groups (partials [chunk][d][2E] fp32, then dL's
-    // split [T][2E] bf16 and the chunk offsets); and, given the second scratch
-    // region, the router's share dXr = dL Wr^T (fp32 [T, d] in the first scratch,
-    // Wr's split and the offsets {0, T} in the second) for a combine that adds it.
+    // split [T][2E] bf16, written with dL, and the chunk offsets); and, given the
+    // second scratch region, the router's share dXr = dL Wr^T (fp32 [T, d] in the
+    // first scratch, Wr's split and the offsets {0, T} in the second) for a
+    // combine that adds it.
     const int tc_chunk = 1024;
     const int tc_chunks = T / tc_chunk;
     const size_t tc_part = (size_t)tc_chunks * d * 2 * E * 4;
@@ -676,15 +688,30 @@ cudaError_t launch_backward_router(const __nv_bfloat16 *X, const float *Wr, cons
                           tc_chunks <= 255;
     const bool tc_dx = tc_shape && scratch2 != nullptr &&
                        tc_part + tc_split + tc_off + 2 * tc_wr + 16 <= scratch2_bytes;
-    if (tc_shape && (tc_dx || tc_part + tc_split + tc_off <= (size_t)T * d * 4)) {
-        char *base = tc_dx ? scratch2 : reinterpret_cast<char *>(scratch);
-        float *P = reinterpret_cast<float *>(base);
-        __nv_bfloat16 *dLc = reinterpret_cast<__nv_bfloat16 *>(base + tc_part);
-        int32_t *coff = reinterpret_cast<int32_t *>(base + tc_part + tc_split);
-        const int64_t n = (int64_t)T * E;
-        e = launch_k(router_split_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
-                     static_cast<const float *>(dL), n, E, dLc, coff, tc_chunks, tc_chunk);
-        if (e != cudaSuccess) return e;
+    const bool tc = tc_shape && (tc_dx || tc_part + tc_split + tc_off <= (size_t)T * d * 4);
+    char *base = tc_dx ? scratch2 : reinterpret_cast<char *>(scratch);
+    float *P = reinterpret_cast<float *>(base);
+    __nv_bfloat16 *dLc = tc ? reinterpret_cast<__nv_bfloat16 *>(base + tc_part) : nullptr;
+    int32_t *coff = reinterpret_cast<int32_t *>(base + tc_part + tc_split);
+    uint32_t *ticket = err + kWordColTicket;
+
+    const unsigned tb = (unsigned)((T + kDlThreads / 32 - 1) / (kDlThreads / 32));
+    auto dl = E <= 32    ? router_dl_kernel<1>
+              : E <= 64  ? router_dl_kernel<2>
+              : E <= 128 ? router_dl_kernel<4>
+                         : router_dl_kernel<8>;
+    cudaError_t e = launch_k(dl, dim3(tb), dim3(kDlThreads), 0, s, L, idx, dS, row_of_slot, T, E, K,
+                             renorm, R, dL, ticket, dLc, coff, tc_chunks, tc_chunk);
+    if (e != cudaSuccess) return e;
+    // dbias: chunks of about 128 tokens (at most 256, their partials in the
+    // scratch region while the column sums run)
+    const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(256, (int64_t)T * d / E));
+    const int cch = (int)std::min<int64_t>(cmax, (T + 127) / 128);
+    const int ctc = (T + cch - 1) / cch;
+    e = launch_k(col_sum_kernel, dim3((unsigned)((E + 31) / 32), (unsigned)cch), dim3(kColThreads),
+                 0, s, static_cast<const float *>(dL), T, E, ctc, scratch, ticket, dbias);
+    if (e != cudaSuccess) return e;
+    if (tc) {
         e = launch_router_dwr_tc(X, dLc, coff, T, d, E, tc_chunks, P, err, s);
         if (e != cudaSuccess) return e;
         const int64_t m = (int64_t)d * E;

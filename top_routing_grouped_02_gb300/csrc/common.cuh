@@ -65,10 +65,11 @@ struct WsLayout {
 };
 
 // Control words at the start of the workspace (uint32 each): the error word,
-// the grouping scan's ticket, and the fused expert MLP's launch epoch and
-// ticket (its row-tile counters carry the epoch, so they need no clearing).
+// the grouping scan's ticket, the fused expert MLP's launch epoch and
+// ticket (its row-tile counters carry the epoch, so they need no clearing),
+// and the router backward's column-sum ticket (zeroed by the kernel before it).
 enum : int { kWordErr = 0, kWordDone = 1, kWordEpoch = 2, kWordTicket = 3, kWordGroupEpoch = 4,
-             kWordGroupTicket = 5 };
+             kWordGroupTicket = 5, kWordColTicket = 6 };
 
 WsLayout ws_layout(int T, int d, int E, int K, int n);
 // Layout for the Token Rounding forward: grouped buffers sized for the largest
