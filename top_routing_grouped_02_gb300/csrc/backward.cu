@@ -156,8 +156,11 @@ col_sum_kernel(const float *__restrict__ dL, int T, int E, int tc, float *__rest
     const int e = blockIdx.x * 32 + lane;
     const int64_t t0 = (int64_t)blockIdx.y * tc, t1 = std::min<int64_t>(T, t0 + tc);
     float s = 0.f;
-    if (e < E)
+    if (e < E) {
+        // (unrolled so that several rows' loads are in flight; the adds keep their order)
+#pragma unroll 8
         for (int64_t t = t0 + warp; t < t1; t += kColThreads / 32) s += __ldg(dL + t * E + e);
+    }
     ws[warp][lane] = s;
     __syncthreads();
     if (warp == 0 && e < E) {
@@ -567,7 +570,9 @@ pad_offsets_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restri
 // dst[q] for padded rows q < poff[E]: the source row of grouped row
 // p = offsets[e] + (q - poff[e]) (src[perm_token[p]], times w[perm_slot[p]]
 // when w is given, rounded to bf16 once), or zeros past the expert's rows. One
-// warp per row; indices out of range give a zero row.
+// warp per row; indices out of range give a zero row. The block first copies
+// poff into shared memory, so each warp's search over the experts costs no
+// global round trips.
 __global__ void __launch_bounds__(256)
 gather_pad_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restrict__ perm_token,
                   int T, const int32_t *__restrict__ offsets, const int32_t *__restrict__ poff,
@@ -575,15 +580,18 @@ gather_pad_kernel(const __nv_bfloat16 *__restrict__ src, const int32_t *__restri
                   int64_t R, int64_t cap, __nv_bfloat16 *__restrict__ dst) {
     pdl_wait();
     pdl_trigger();
+    __shared__ int32_t spoff[kMaxE + 1];
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) spoff[i] = __ldg(poff + i);
+    __syncthreads();
     const int64_t q = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (q >= cap || q >= __ldg(poff + E)) return;
+    if (q >= cap || q >= spoff[E]) return;
     int lo = 0, hi = E - 1;  // the last expert whose padded rows start at or before q
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(poff + mid) <= q) lo = mid; else hi = mid - 1;
+        if (spoff[mid] <= q) lo = mid; else hi = mid - 1;
     }
-    const int64_t local = q - __ldg(poff + lo);
+    const int64_t local = q - spoff[lo];
     const int64_t p = (int64_t)__ldg(offsets + lo) + local;
     bool ok = local < (int64_t)__ldg(offsets + lo + 1) - __ldg(offsets + lo) && p >= 0 && p < R;
     int64_t t = ok ? __ldg(perm_token + p) : -1;
