@@ -3,6 +3,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 
 namespace moe {
@@ -91,6 +94,56 @@ bool pdl_enabled() {
         return !(v != nullptr && v[0] == '0');
     }();
     return on;
+}
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+}  // namespace
+
+bool current_context_id(unsigned long long *id) {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes) {
+    struct Done {
+        const void *kernel;
+        unsigned long long ctx;
+        int bytes;
+    };
+    static std::mutex m;
+    static std::vector<Done> done;
+    unsigned long long id = 0;
+    bool known = current_context_id(&id);
+    if (known) {
+        std::lock_guard<std::mutex> lock(m);
+        for (const Done &x : done)
+            if (x.kernel == kernel && x.ctx == id && x.bytes >= bytes) return cudaSuccess;
+    }
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (!known) known = current_context_id(&id);  // the call made the context current
+    if (known) {
+        std::lock_guard<std::mutex> lock(m);
+        done.push_back({kernel, id, bytes});
+    }
+    return cudaSuccess;
 }
 
 int sm_count() {

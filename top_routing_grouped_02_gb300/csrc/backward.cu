@@ -627,14 +627,10 @@ template <int EB>
 cudaError_t launch_dwr_part(const __nv_bfloat16 *X, const float *dL, int T, int d, int E, int TC,
                             int chunks, float *part, cudaStream_t s) {
     using C = DwrCfg<EB>;
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(router_dwr_part_kernel<EB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    {
+        const cudaError_t e =
+            ensure_dynamic_smem(reinterpret_cast<const void *>(router_dwr_part_kernel<EB>), C::SMEM);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
     }
     return launch_k(router_dwr_part_kernel<EB>,
                     dim3((d + C::JB - 1) / C::JB, chunks, (E + EB - 1) / EB), dim3(kPThreads),
@@ -643,14 +639,10 @@ cudaError_t launch_dwr_part(const __nv_bfloat16 *X, const float *dL, int T, int 
 cudaError_t launch_combine_router(const __nv_bfloat16 *dXg, const int32_t *row_of_slot,
                                   const float *dL, const float *Wr, int T, int K, int d, int E,
                                   int64_t R, __nv_bfloat16 *dX, cudaStream_t s) {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(combine_router_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+    {
+        const cudaError_t e =
+            ensure_dynamic_smem(reinterpret_cast<const void *>(combine_router_kernel), kFSmem);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
     }
     return launch_k(combine_router_kernel,
                     dim3((unsigned)((T + kFTok - 1) / kFTok), (d + kFCols - 1) / kFCols),

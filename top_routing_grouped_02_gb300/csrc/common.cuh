@@ -245,6 +245,13 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// Unique id of the CUDA context current on this thread (never reused, unlike a
+// context handle); false when there is none yet or the driver cannot say.
+bool current_context_id(unsigned long long *id);
+// Raises the kernel's dynamic shared-memory limit to `bytes` in the current
+// context. Remembered per (kernel, context), so each context gets it once;
+// safe to call from several host threads.
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
 // MOE_OK when the current device is sm_103 (cached per device), MOE_ERR_ARCH
 // otherwise, MOE_ERR_CUDA when the device cannot be queried. Clears a CUDA error
 // left pending by an earlier, unrelated call first.

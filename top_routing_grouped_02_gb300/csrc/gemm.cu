@@ -1263,15 +1263,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (fn == nullptr) {
+    // looked up once (a function-local static is initialised thread-safely)
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1312,14 +1313,10 @@ cudaError_t launch_ew(const CUtensorMap &a, const CUtensorMap &b0, const CUtenso
                       const GemmArgs &args, int max_units, cudaStream_t s) {
     constexpr size_t kSmem = smem_bytes<PAIR>();
     constexpr int kThreads = threads_of<EW>();
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, PAIR, EW>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    {
+        const cudaError_t e = ensure_dynamic_smem(
+            reinterpret_cast<const void *>(grouped_gemm_kernel<MODE, PAIR, EW>), (int)kSmem);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
     }
     if constexpr (!PAIR) {
         const int grid = max(1, min(sm_count(), max_units));

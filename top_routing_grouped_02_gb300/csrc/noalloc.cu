@@ -36,30 +36,6 @@ struct ScratchSlot {
 };
 ScratchSlot g_slots[64];
 
-using CtxGetCurrentFn = CUresult (*)(CUcontext *);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
-
-template <typename Fn>
-Fn driver_fn(const char *name) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-        return nullptr;
-    return reinterpret_cast<Fn>(p);
-}
-
-// Unique id of the context current on this thread; false when there is none
-// yet (or the driver cannot say).
-bool current_context_id(unsigned long long *id) {
-    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
-    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
-    if (get_current == nullptr || get_id == nullptr) return false;
-    CUcontext ctx = nullptr;
-    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
-    return get_id(ctx, id) == CUDA_SUCCESS;
-}
-
 moe_status_t scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;

@@ -931,15 +931,12 @@ cudaError_t launch_route_chain(const __nv_bfloat16 *X, const float *Wr, const fl
     const int tg = route_token_groups(T, d, C::TPW);
     const int warps = std::min(kRouteWarps, tg * nb);
     const size_t smem = (size_t)warps * C::WARP_SMEM + (size_t)tg * nb * C::PART;
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    {
+        // the most any call of this kernel asks for, so the limit is set once
         const size_t most = (size_t)kRouteWarps * C::WARP_SMEM + (size_t)kRouteMaxBlocks * C::PART;
-        cudaError_t e = cudaFuncSetAttribute(route_chain_kernel<EP>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+        const cudaError_t e =
+            ensure_dynamic_smem(reinterpret_cast<const void *>(route_chain_kernel<EP>), (int)most);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
     }
     const unsigned grid = (unsigned)(((int64_t)T + (int64_t)tg * C::TPW - 1) / ((int64_t)tg * C::TPW));
     return launch_k(route_chain_kernel<EP>, dim3(grid), dim3(32 * warps), smem, s, X, Wr, bias, T,
@@ -949,14 +946,10 @@ cudaError_t launch_route_chain(const __nv_bfloat16 *X, const float *Wr, const fl
 template <int PA, int PB>
 cudaError_t launch_big(const __nv_bfloat16 *X, const float *Wr, const float *bias, int T, int d,
                        int E, float *L, cudaStream_t s) {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(logits_big_kernel<PA, PB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmem);
+    {
+        const cudaError_t e =
+            ensure_dynamic_smem(reinterpret_cast<const void *>(logits_big_kernel<PA, PB>), kBSmem);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
     }
     constexpr int kTok = 16 * (PA + PB);
     const dim3 grid((unsigned)((T + kTok - 1) / kTok), (unsigned)((E + kBE - 1) / kBE));
