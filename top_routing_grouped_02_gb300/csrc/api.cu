@@ -3,6 +3,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -15,8 +16,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Per device, filled on first use under a mutex and published with a
+// release store, so host threads calling at once see either nothing or all of it.
 struct DeviceInfo {
-    bool init = false;
+    std::atomic<bool> init{false};
+    std::mutex m;
     bool arch_ok = false;
     int sms = 0;
 };
@@ -26,15 +30,18 @@ const DeviceInfo *device_info() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     DeviceInfo &di = g_dev[dev];
-    if (!di.init) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return nullptr;
-        di.arch_ok = (major == 10 && minor == 3);
-        di.sms = sms;
-        di.init = true;
+    if (!di.init.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(di.m);
+        if (!di.init.load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return nullptr;
+            di.arch_ok = (major == 10 && minor == 3);
+            di.sms = sms;
+            di.init.store(true, std::memory_order_release);
+        }
     }
     return &di;
 }
