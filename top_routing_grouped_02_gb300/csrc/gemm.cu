@@ -51,9 +51,9 @@
 //               back to the producer and, after the last stage, the
 //               accumulator to the epilogue.
 //   warp 2      allocates / frees 512 TMEM columns (2 accumulators x 256).
-//   warps 4..    epilogue, EW = 4 or 8 warps: warp w reads TMEM lanes
-//               32(w%4)..+31 (= tile rows); with 8 the two warps of each lane
-//               quadrant take half of the columns: tcgen05.ld of the lanes,
+//   warps 4..    epilogue, EW = 4, 8 or 12 warps: warp w reads TMEM lanes
+//               32(w%4)..+31 (= tile rows); with 8 or 12 the 2 or 3 warps of
+//               each lane quadrant split the columns: tcgen05.ld of the lanes,
 //               activation or scaling in fp32, bf16 packing; each 32 x 32
 //               chunk goes through a swizzled shared-memory buffer and one TMA
 //               store (whole 64-byte row segments instead of 32 half-sector
@@ -95,7 +95,7 @@ namespace {
 
 // Epilogue warps: 4, or 8 when a tile's main loop is short (see choose_ew).
 // A launch has 128 + 32 * EW threads.
-constexpr int kMaxThreads = 128 + 32 * 8;
+constexpr int kMaxThreads = 128 + 32 * 12;
 template <int EW>
 constexpr int threads_of() { return 128 + 32 * EW; }
 constexpr int BM = kTileM;  // 128 rows per CTA
@@ -206,14 +206,15 @@ struct Ctl {
 };
 
 // Epilogue staging: 32-row x 32-column bf16 buffers (64-byte rows, 64-byte
-// swizzle) that TMA stores write out; 8 of them, two per warp with 4 epilogue
-// warps and one per warp with 8.
+// swizzle) that TMA stores write out: two per warp with 4 epilogue warps, one
+// per warp with 8 or 12.
 constexpr uint32_t kEpiBuf = 32 * 32 * 2;
-constexpr uint32_t kEpiBytes = 8 * kEpiBuf;
-
-template <bool PAIR>
+template <int EW>
+constexpr int epi_bufs() { return EW > 8 ? EW : 8; }
+template <bool PAIR, int EW>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes + kEpiBytes + sizeof(Ctl);
+    return 1024 + (size_t)Geo<PAIR>::kStages * Geo<PAIR>::kStageBytes +
+           (size_t)epi_bufs<EW>() * kEpiBuf + sizeof(Ctl);
 }
 
 struct GemmArgs {
@@ -430,7 +431,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int kThreads = threads_of<EW>();
     // epilogue warps signalling an accumulator release (both CTAs of a pair)
     constexpr uint32_t kTemptyCount = PAIR ? 2 * EW : EW;
-    constexpr int kNBuf = 8 / EW;  // staging buffers per epilogue warp
+    constexpr int kNBuf = epi_bufs<EW>() / EW;  // staging buffers per epilogue warp
     // fused: both GEMMs' units in one launch (single CTA only); the maps are
     // tmA = H (A of down units), tmB0/tmB1 = W1/W3, tmOut = H (stores),
     // tmB2 = W2, tmOut2 = Z (stores)
@@ -443,7 +444,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)S * G::kStageBytes + kEpiBytes);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + (size_t)S * G::kStageBytes +
+                                       (size_t)epi_bufs<EW>() * kEpiBuf);
     const uint32_t smem_base = ptx::smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = args.E;
@@ -940,8 +942,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp >= 4) {
         // -------------------------------------------------------- epilogue --
         // TMEM lanes 32q..32q+31 (= tile rows) belong to warps with warp % 4 == q;
-        // with 8 epilogue warps the two warps of a quadrant split the tile's
-        // 32-column chunks
+        // with 8 or 12 epilogue warps the warps of a quadrant split the tile's
+        // 32-column chunks (warp `half` of nhalf takes chunks half*C/nhalf ..)
         const int q = warp & 3, half = (warp - 4) >> 2, nhalf = EW / 4;
         const int r = q * 32 + lane;
         const uint32_t tempty0 = PAIR ? ptx::mapa(ptx::smem_addr(&ctl->tempty[0]), 0)
@@ -963,7 +965,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int64_t p = (int64_t)row0 + r;
             // kDH: the row's stored pre-activations, one 32-column chunk ahead of
             // their use; the first chunk's loads go out before the accumulator wait
-            const int c_lo = half * (BN / 32 / nhalf), c_hi = (half + 1) * (BN / 32 / nhalf);
+            const int c_lo = half * (BN / 32) / nhalf, c_hi = (half + 1) * (BN / 32) / nhalf;
             float4 x1[8], x3[8];
             auto load_pre = [&](int c, float4 (&l1)[8], float4 (&l3)[8]) {
                 const int64_t off = p * args.out_ld + nb * BN + c * 32;
@@ -1028,7 +1030,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // its gradient is written as zeros.
                 const int oy = un.e * args.wout_rows + un.row0 + q * 32;
 #pragma unroll 1
-                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                for (int c = half * (BN / 32) / nhalf; c < (half + 1) * (BN / 32) / nhalf; ++c) {
                     uint32_t v[32], lo[16], hi[16];
                     if (un.kbs > 0) {
                         ptx::tmem_ld32(taddr + c * 32, v);
@@ -1098,7 +1100,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else if (!dn) {
                 __nv_bfloat16 *dst = args.out + p * args.out_ld + nb * 128;
 #pragma unroll 1
-                for (int c = half * (4 / nhalf); c < (half + 1) * (4 / nhalf); ++c) {
+                for (int c = half * 4 / nhalf; c < (half + 1) * 4 / nhalf; ++c) {
                     uint32_t g[32], v[32];
                     ptx::tmem_ld32(taddr + c * 32, g);
                     ptx::tmem_ld32(taddr + 128 + c * 32, v);
@@ -1153,7 +1155,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // whole 32-row warps, else direct stores of the valid rows
                 float *dst = args.outf + p * args.out_ld + nb * BN;
 #pragma unroll 1
-                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                for (int c = half * (BN / 32) / nhalf; c < (half + 1) * (BN / 32) / nhalf; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld32(taddr + c * 32, v);
                     if (whole) {
@@ -1185,7 +1187,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 __nv_bfloat16 *dst = FUSED ? args.out2 + p * args.out2_ld + nb * BN
                                            : args.out + p * args.out_ld + nb * BN;
 #pragma unroll 1
-                for (int c = half * (BN / 32 / nhalf); c < (half + 1) * (BN / 32 / nhalf); ++c) {
+                for (int c = half * (BN / 32) / nhalf; c < (half + 1) * (BN / 32) / nhalf; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld32(taddr + c * 32, v);
                     uint32_t packed[16];
@@ -1311,7 +1313,7 @@ template <int MODE, bool PAIR, int EW>
 cudaError_t launch_ew(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                       const CUtensorMap &out, const CUtensorMap &b2, const CUtensorMap &out2,
                       const GemmArgs &args, int max_units, cudaStream_t s) {
-    constexpr size_t kSmem = smem_bytes<PAIR>();
+    constexpr size_t kSmem = smem_bytes<PAIR, EW>();
     constexpr int kThreads = threads_of<EW>();
     {
         const cudaError_t e = ensure_dynamic_smem(
@@ -1346,12 +1348,18 @@ cudaError_t launch_ew(const CUtensorMap &a, const CUtensorMap &b0, const CUtenso
 
 // Eight epilogue warps when a tile's main loop is at most 8 k-blocks (the
 // epilogue then dominates: measured on the SonicMoE-shaped down GEMM, n = 256,
-// 0.082 -> 0.072 ms); four otherwise (with longer main loops the extra warps
-// cost slightly: DeepSeek-V3-shaped GEMMs about 1% slower).
+// 0.082 -> 0.072 ms), twelve for the single-CTA down GEMM there (0.0764 ->
+// 0.0708 ms; the backward's dX GEMM measured no faster with them); four
+// otherwise (with longer main loops the extra warps cost slightly: DeepSeek-V3-
+// shaped GEMMs about 1% slower).
 template <int MODE, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                            const CUtensorMap &out, const GemmArgs &args, int max_units,
                            cudaStream_t s) {
+    if constexpr (MODE == kDown && !PAIR) {
+        if (args.Kdim / BK <= 8)
+            return launch_ew<MODE, PAIR, 12>(a, b0, b1, out, b0, out, args, max_units, s);
+    }
     if (args.Kdim / BK <= 8)
         return launch_ew<MODE, PAIR, 8>(a, b0, b1, out, b0, out, args, max_units, s);
     return launch_ew<MODE, PAIR, 4>(a, b0, b1, out, b0, out, args, max_units, s);
